@@ -1,0 +1,361 @@
+"""Pins of the oracle's schedules against what the pages and the mathematics
+fix (no GPU): brute-force results, page-derived trees, closed-form step and
+byte counts, the generalized algorithm's extra-cost statements, special cases
+that reduce to textbook schedules, and the AHC example."""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.chunking import ceil_log2, split
+from oracle.direct import direct_int
+from oracle.elementops import Arith, Symbolic, leaf_buffers, tree_leaves, tree_str
+from oracle.schedules import ahc_holder, ahc_layout, generalized_plan
+
+
+def _pow2(P):
+    return P & (P - 1) == 0
+
+
+def _cases(Ps=range(1, 17)):
+    """(algo, P, params) for every schedule and parameter valid at each P."""
+    for P in Ps:
+        L = ceil_log2(P)
+        yield "ring", P, {}
+        yield "binomial", P, {}
+        for r in range(L + 1):
+            yield "generalized", P, {"group": "cyclic", "r": r}
+        if _pow2(P):
+            yield "rd", P, {}
+            yield "rh", P, {}
+            for k1 in range(L + 1):
+                yield "hybrid", P, {"k1": k1}
+            for r in range(L + 1):
+                yield "generalized", P, {"group": "xor", "r": r}
+        for sizes in _partitions(P):
+            yield "ahc", P, {"group_sizes": sizes}
+
+
+def _partitions(P):
+    """A few contiguous groupings of P ranks for AHC."""
+    out = [[P]]
+    if P >= 2:
+        out.append([1] * P)
+        out.append([P // 2, P - P // 2])
+    if P >= 5:
+        out.append([2, P - 2])
+    if P >= 6:
+        out.append([1, 2, P - 3])
+    uniq = []
+    for s in out:
+        if s not in uniq and min(s) >= 1:
+            uniq.append(s)
+    return uniq
+
+
+def _expected_steps(algo, P, p):
+    L = ceil_log2(P)
+    if algo == "ring":
+        return 2 * (P - 1)
+    if algo == "binomial":
+        return 2 * L
+    if algo == "rd":
+        return L
+    if algo == "rh":
+        return 2 * L
+    if algo == "hybrid":
+        return L + p["k1"]
+    if algo == "generalized":
+        return 2 * L - p["r"]
+    if algo == "ahc":
+        g = p["group_sizes"]
+        return 2 * (max(g) - 1) + 2 * (len(g) - 1)
+    raise AssertionError(algo)
+
+
+@pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
+def test_int32_every_schedule_equals_direct_reduction(op):
+    rng = np.random.default_rng(11)
+    for algo, P, p in _cases():
+        for n in sorted({0, 1, P - 1, P, P + 1, 2 * P + 3, 40}):
+            if n < 0:
+                continue
+            bufs = [rng.integers(-1000, 1001, n).astype(np.int32) for _ in range(P)]
+            if op == "prod":
+                bufs = [rng.integers(-3, 4, n).astype(np.int32) for _ in range(P)]
+            res = oracle.run(algo, bufs, Arith(op, "int32"), **p)
+            want = direct_int(bufs, op)
+            for r in range(P):
+                assert np.array_equal(res.bufs[r], want), (algo, P, p, n, r)
+            assert res.steps == _expected_steps(algo, P, p), (algo, P, p)
+
+
+def test_int32_sum_exhaustive_lengths_small_P():
+    rng = np.random.default_rng(12)
+    for algo, P, p in _cases(range(1, 9)):
+        for n in range(0, 41):
+            bufs = [rng.integers(-1000, 1001, n).astype(np.int32) for _ in range(P)]
+            res = oracle.run(algo, bufs, Arith("sum", "int32"), **p)
+            want = direct_int(bufs, "sum")
+            assert all(np.array_equal(b, want) for b in res.bufs), (algo, P, p, n)
+
+
+def test_every_rank_gets_a_complete_tree():
+    """Each element of each rank is a reduction of every rank exactly once."""
+    for algo, P, p in _cases():
+        n = 2 * P + 1
+        res = oracle.run(algo, leaf_buffers(P, n), Symbolic(), **p)
+        for r in range(P):
+            for e in range(n):
+                assert sorted(tree_leaves(res.bufs[r][e])) == list(range(P)), (algo, P, p, r, e)
+
+
+def test_ring_trees_match_page(golden):
+    g = golden("ring_trees.json")
+    for case in g["cases"]:
+        P = case["P"]
+        K = 3
+        res = oracle.run("ring", leaf_buffers(P, P * K), Symbolic())
+        for k, want in enumerate(case["chunk_trees"]):
+            for r in range(P):
+                for e in range(k * K, (k + 1) * K):
+                    assert tree_str(res.bufs[r][e]) == want
+
+
+def test_binomial_trees_match_page(golden):
+    for case in golden("binomial_trees.json")["cases"]:
+        P = case["P"]
+        res = oracle.run("binomial", leaf_buffers(P, 3), Symbolic())
+        for r in range(P):
+            assert all(tree_str(x) == case["tree"] for x in res.bufs[r])
+
+
+def test_ring_traffic_closed_forms():
+    # every rank sends one chunk per round: 2(N - 1) S / N per rank when N | n
+    for P in range(1, 17):
+        n = 12 * P
+        res = oracle.run("ring", [np.zeros(n, np.int32)] * P, Arith("sum", "int32"))
+        assert res.steps == 2 * (P - 1)
+        assert res.sent_per_rank() == [2 * (P - 1) * n // P] * P
+        assert sum(res.sent_per_rank()) == 2 * (P - 1) * n
+        assert all(s == [n // P] * P for s in res.sent)
+
+
+def test_ring_ceil_split_ragged():
+    assert split(1024, 3) == [(0, 342), (342, 684), (684, 1024)]
+    assert split(10, 4) == [(0, 3), (3, 6), (6, 9), (9, 10)]
+    assert split(2, 4) == [(0, 1), (1, 2), (2, 2), (2, 2)]
+    assert split(0, 3) == [(0, 0)] * 3
+
+
+def test_rd_and_rh_traffic():
+    for P in (2, 4, 8, 16):
+        n = 8 * P
+        L = ceil_log2(P)
+        z = [np.zeros(n, np.int32)] * P
+        rdr = oracle.run("rd", z, Arith("sum", "int32"))
+        assert rdr.sent_per_rank() == [L * n] * P            # whole vector each round
+        rhr = oracle.run("rh", z, Arith("sum", "int32"))
+        assert rhr.sent_per_rank() == [2 * (P - 1) * n // P] * P   # same as the ring
+        halves = [s[0] for s in rhr.sent[:L]]
+        assert halves == [n >> (i + 1) for i in range(L)]
+
+
+def test_bandwidth_optimal_generalized_sends_like_ring():
+    """Bandwidth-optimal version: same transferred data as the ring,
+    2 ceil(log P) steps."""
+    for P in range(1, 20):
+        n = 5 * P
+        res = oracle.run("generalized", [np.zeros(n, np.int32)] * P,
+                         Arith("sum", "int32"), group="cyclic", r=0)
+        L = ceil_log2(P)
+        assert res.steps == 2 * L
+        assert res.sent_per_rank() == [2 * (P - 1) * 5] * P
+        assert res.combines == (P - 1) * n
+
+
+def test_generalized_p7_tree_and_sends(golden):
+    g = golden("generalized_p7.json")
+    P, K = 7, 2
+    res = oracle.run("generalized", leaf_buffers(P, P * K), Symbolic(), group="cyclic", r=0)
+    want0 = g["tree_chunk0_r0"]
+    for c in range(P):
+        shifted = "".join(str((int(ch) + c) % P) if ch.isdigit() else ch for ch in want0)
+        for r in range(P):
+            for e in range(c * K, (c + 1) * K):
+                assert tree_str(res.bufs[r][e]) == shifted
+    for r_key, want in g["sends_per_rank_in_u"].items():
+        if r_key == "comment":
+            continue
+        res = oracle.run("generalized", [np.zeros(P * K, np.int32)] * P,
+                         Arith("sum", "int32"), group="cyclic", r=int(r_key))
+        assert [s[0] // K for s in res.sent] == want
+        assert all(len(set(s)) == 1 for s in res.sent)
+
+
+def _reduction_counts(P, r):
+    n = P
+    res = oracle.run("generalized", [np.zeros(n, np.int32)] * P,
+                     Arith("sum", "int32"), group="cyclic", r=r)
+    L = res.info["L"]
+    sends = [res.sent[i][0] for i in range(L)]
+    combs = [t["combines"] for t in res.info["trace"][:L]]
+    return L, sends, combs, res
+
+
+def test_generalized_extra_cost_one_more_result(golden):
+    """r = 1: u more data per reduction step; 2u more computation on a step
+    with N_i even, u otherwise, the last step (N = 2) counting u."""
+    g = golden("generalized_p7.json")
+    _, _, c0, _ = _reduction_counts(7, 0)
+    _, _, c1, _ = _reduction_counts(7, 1)
+    assert [b - a for a, b in zip(c0, c1)] == g["extra_combines_r1_per_step"]["values"]
+    for P in range(3, 70):
+        L, s0, c0, res0 = _reduction_counts(P, 0)
+        _, s1, c1, _ = _reduction_counts(P, 1)
+        assert [b - a for a, b in zip(s0, s1)] == [1] * L, P
+        Ns = res0.info["Ns"]
+        want = [2 if (Ns[i] % 2 == 0 and Ns[i] > 2) else 1 for i in range(L)]
+        got = [b - a for a, b in zip(c0, c1)]
+        # the statement is the worst case: sharing can only save combines
+        assert all(x <= y for x, y in zip(got, want)), (P, got, want)
+        if P == 2 ** L - 1:
+            assert got == want, P
+
+
+@pytest.mark.parametrize("P", [7, 15, 31, 63, 127])
+def test_generalized_extra_cost_worst_case_exact(P):
+    """(2^r - 1) ceil(log P) u extra data and (2^r - 1)(2 ceil(log P) - 2) u
+    extra computation, exact in the worst case (N_i even in ceil(log P) - 2
+    steps, i.e. P = 2^k - 1, the experiments' P = 127 among them)."""
+    L, s0, c0, _ = _reduction_counts(P, 0)
+    for r in range(1, L):
+        _, s, c, res = _reduction_counts(P, r)
+        assert sum(s) - sum(s0) == (2 ** r - 1) * L, (P, r)
+        assert sum(c) - sum(c0) == (2 ** r - 1) * (2 * L - 2), (P, r)
+        assert max(t["max_live_per_position"] for t in res.info["trace"]) <= 2
+
+
+def test_generalized_extra_cost_bounds_any_P():
+    for P in range(3, 40):
+        L, s0, c0, _ = _reduction_counts(P, 0)
+        for r in range(1, L):
+            _, s, c, _ = _reduction_counts(P, r)
+            assert sum(s) - sum(s0) <= (2 ** r - 1) * L
+            assert sum(c) - sum(c0) <= (2 ** r - 1) * (2 * L - 2)
+
+
+def test_latency_optimal_sends_everything_each_step():
+    for P in range(2, 20):
+        L, s, _, res = _reduction_counts(P, ceil_log2(P))
+        assert res.steps == L
+        assert s == [P] * L
+
+
+@pytest.mark.parametrize("P", [2, 4, 8, 16])
+def test_xor_group_is_recursive_halving_and_doubling(P):
+    """With P = 2^k and the self-inverse group the bandwidth-optimal version
+    is recursive halving and the latency-optimal one recursive doubling."""
+    n = 2 * P + 1
+    L = ceil_log2(P)
+    a = oracle.run("generalized", leaf_buffers(P, n), Symbolic(), group="xor", r=0)
+    b = oracle.run("rh", leaf_buffers(P, n), Symbolic())
+    assert [[tree_str(x) for x in buf] for buf in a.bufs] == \
+           [[tree_str(x) for x in buf] for buf in b.bufs]
+    assert a.sent == b.sent
+    c = oracle.run("generalized", leaf_buffers(P, n), Symbolic(), group="xor", r=L)
+    d = oracle.schedules.rd(leaf_buffers(P, n), Symbolic(), first="high")
+    assert [[tree_str(x) for x in buf] for buf in c.bufs] == \
+           [[tree_str(x) for x in buf] for buf in d.bufs]
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_hybrid_endpoints(P):
+    L = ceil_log2(P)
+    n = 3 * P + 2
+    h0 = oracle.run("hybrid", leaf_buffers(P, n), Symbolic(), k1=0)
+    rd_ = oracle.run("rd", leaf_buffers(P, n), Symbolic())
+    assert [[tree_str(x) for x in b] for b in h0.bufs] == [[tree_str(x) for x in b] for b in rd_.bufs]
+    hL = oracle.run("hybrid", leaf_buffers(P, n), Symbolic(), k1=L)
+    assert hL.steps == 2 * L
+
+
+def test_rd_partner_distance_order():
+    res = oracle.run("rd", leaf_buffers(4, 1), Symbolic())
+    assert tree_str(res.bufs[0][0]) == "((0+1)+(2+3))"
+    assert tree_str(res.bufs[3][0]) == "((3+2)+(1+0))"
+
+
+def test_ahc_example(golden):
+    g = golden("ahc_example.json")
+    sizes = g["group_sizes"]
+    M, G, nch, offs = ahc_layout(sizes)
+    assert (M, G, nch) == (g["lcm"], g["groups"], g["chunks"])
+    holders = [tuple(ahc_holder(sizes, offs, M, gm, k) for gm in range(G)) for k in range(M)]
+    segs = []
+    for k, hs in enumerate(holders):
+        if segs and segs[-1][1] == hs:
+            segs[-1][0][1] = (k + 1) * G
+        else:
+            segs.append([[k * G, (k + 1) * G], hs])
+    assert [s[0] for s in segs] == g["segments"]
+    res = oracle.run("ahc", leaf_buffers(5, 24), Symbolic(), group_sizes=sizes)
+    assert res.steps == g["steps"]
+
+
+def test_ahc_special_cases_reduce_to_ring():
+    """One group is the ring (its LCM x G chunks are the ring's P chunks);
+    groups of one rank each make the inter-group ring over P chunks."""
+    for P in range(1, 9):
+        n = 3 * P + 1
+        ring = oracle.run("ring", leaf_buffers(P, n), Symbolic())
+        want = [[tree_str(x) for x in b] for b in ring.bufs]
+        one = oracle.run("ahc", leaf_buffers(P, n), Symbolic(), group_sizes=[P])
+        assert [[tree_str(x) for x in b] for b in one.bufs] == want
+        singles = oracle.run("ahc", leaf_buffers(P, n), Symbolic(), group_sizes=[1] * P)
+        assert [[tree_str(x) for x in b] for b in singles.bufs] == want
+
+
+def test_identity_cases():
+    x = [np.arange(5, dtype=np.int32)]
+    for algo in ("ring", "binomial", "rd", "rh", "generalized"):
+        res = oracle.run(algo, x, Arith("sum", "int32"))
+        assert res.steps == 0 and np.array_equal(res.bufs[0], x[0])
+    res = oracle.run("ahc", x, Arith("sum", "int32"), group_sizes=[1])
+    assert res.steps == 0
+    z = [np.zeros(0, np.float32)] * 6
+    res = oracle.run("ring", z, Arith("sum", "float32"))
+    assert all(b.size == 0 for b in res.bufs)
+
+
+def test_invalid_parameters_rejected():
+    z = [np.zeros(4, np.int32)] * 6
+    a = Arith("sum", "int32")
+    with pytest.raises(ValueError):
+        oracle.run("rd", z, a)
+    with pytest.raises(ValueError):
+        oracle.run("generalized", z, a, group="xor")
+    with pytest.raises(ValueError):
+        oracle.run("generalized", z, a, r=4)
+    with pytest.raises(ValueError):
+        oracle.run("ahc", z, a, group_sizes=[2, 3])
+    with pytest.raises(ValueError):
+        generalized_plan(12, "xor", 0)
+
+
+def test_float_order_is_the_schedule_order():
+    """fp32: the ring's chunk-0 value equals the chain evaluated by hand in
+    the order the page fixes; other chunks equal their rotated chains."""
+    rng = np.random.default_rng(3)
+    P, K = 5, 7
+    bufs = [rng.standard_normal(P * K).astype(np.float32) for _ in range(P)]
+    res = oracle.run("ring", bufs, Arith("sum", "float32"))
+    for k in range(P):
+        sl = slice(k * K, (k + 1) * K)
+        acc = bufs[k][sl].copy()
+        for j in range(1, P):
+            acc = (bufs[(k + j) % P][sl] + acc).astype(np.float32)
+        for r in range(P):
+            assert np.array_equal(res.bufs[r][sl], acc)
