@@ -1,0 +1,523 @@
+"""Benchmark of the GB300 allreduce schedule engine.
+
+One step = one allreduce call (ar_execute) over P virtual-rank buffers already
+resident in HBM.  The default workload is the large gradient-sync point:
+ring schedule, fused single pass, order-faithful, P = 8 ranks x 256 MiB of
+fp32 per rank, op = sum.  Buffers (2 GiB) are far larger than the 129 MB L2,
+so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--P 8] [--mib 256] [--dtype float32] [--algo ring]
+                    [--form fused] [--order faithful] [--sweep out.jsonl]
+
+Prints ONE JSON line (rank 0).  value = allreduced bytes (P x S per call,
+summed over all ranks' GPUs) per second, in GB/s.  Under torchrun each rank
+runs the same per-GPU workload on its own GPU (no data-path collective; the
+only collective is the timing max over ranks).
+
+--impl reference times the CPU oracle (the plain simulation that defines
+the schedules' results) on a bounded sample of the same workload, on the
+host cores, and prints the same line with "impl": "reference".
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "allreduced bytes/s (P x S per call)"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+KERNEL_SRC = os.path.join(ROOT, "collective_reduction_gb300", "csrc", "kernels.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--P", type=int, default=8)
+    ap.add_argument("--mib", type=float, default=256.0, help="MiB per rank")
+    ap.add_argument("--dtype", default="float32", choices=["float32", "bfloat16", "int32"])
+    ap.add_argument("--op", default="sum")
+    ap.add_argument("--algo", default="ring")
+    ap.add_argument("--form", default="fused")
+    ap.add_argument("--order", default="faithful")
+    ap.add_argument("--r", type=int, default=0)
+    ap.add_argument("--k1", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", default=None, help="write the size sweep as JSON lines to this file")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def esize(dtype):
+    return 2 if dtype == "bfloat16" else 4
+
+
+def workload_name(a):
+    return (f"{a.algo} allreduce, {a.form} {a.order}, P={a.P} x {a.mib:g} MiB {a.dtype} per rank, "
+            f"op={a.op}" + (f", r={a.r}" if a.algo == "generalized" else "")
+            + (f", k1={a.k1}" if a.algo == "hybrid" else ""))
+
+
+def dtype_tag(dtype):
+    return {"float32": "f32", "bfloat16": "bf16", "int32": "int32"}[dtype]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(P, mib, dtype, algo, form, order):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing, is for another workload, or predates the kernel."""
+    try:
+        rec = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("kernel_sha256_16") != kernel_hash():
+            return None
+        key = f"P={P} mib={mib:g} dtype={dtype} algo={algo} form={form} order={order}"
+        if rec.get("workload") != key:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in self.rows:
+            try:
+                sm.append(float(row[0]))
+                mx = float(row[1])
+                for nm, v in zip(names, row[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except Exception:
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier_sync(world):
+    import torch
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        torch.cuda.synchronize()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def gather_sample(dev, P, n, K, chunks):
+    """K elements from each of the schedule's `chunks` base chunks of every rank
+    buffer, laid out so a ceil split of the sample into `chunks` parts puts
+    each chunk's elements into the same part."""
+    import numpy as np
+    import torch
+    size = -(-n // chunks)
+    idx = []
+    for c in range(chunks):
+        lo, hi = min(n, c * size), min(n, (c + 1) * size)
+        if hi - lo < K:
+            raise ValueError("chunk shorter than the sample")
+        idx.extend(np.linspace(lo, hi - 1, K).astype(np.int64).tolist())
+    it = torch.tensor(idx, dtype=torch.int64, device="cuda")
+    out = []
+    for t in dev:
+        s = t.index_select(0, it)
+        if t.dtype == torch.bfloat16:
+            out.append(s.view(torch.int16).cpu().numpy().view(np.uint16))
+        else:
+            out.append(s.cpu().numpy())
+    return out, it
+
+
+def base_chunks(a):
+    if a.algo == "ahc":
+        raise ValueError("the bench's sampled check covers ring / generalized / binomial / rd / rh")
+    return a.P
+
+
+def cpu_baseline_and_check(a, sample_in, sample_out_engine):
+    """The oracle, as it stands, timed on host cores on a bounded sample of
+    the workload; also checks the engine's output on that sample."""
+    import numpy as np
+
+    import oracle
+    from oracle.elementops import Arith
+    kw = {}
+    if a.algo == "generalized":
+        kw = {"r": a.r}
+    if a.algo == "hybrid":
+        kw = {"k1": a.k1}
+    t0 = time.perf_counter()
+    reps = 0
+    res = None
+    while True:
+        res = oracle.run(a.algo, sample_in, Arith(a.op, a.dtype), **kw)
+        reps += 1
+        if time.perf_counter() - t0 >= a.cpu_seconds:
+            break
+    dt = time.perf_counter() - t0
+    nbytes = a.P * sample_in[0].size * esize(a.dtype)
+    ok = None
+    if sample_out_engine is not None and a.order == "faithful":
+        def bits(x):
+            x = np.ascontiguousarray(x)
+            return x if x.dtype == np.uint16 else x.view(np.uint32)
+        ok = all(np.array_equal(bits(res.bufs[r]), bits(sample_out_engine[r])) for r in range(a.P))
+    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{sample_in[0].size} elements per rank ({sample_in[0].size // a.P} from each of the "
+                      f"{a.P} chunks of the benchmark buffers), {reps} oracle runs in {dt:.1f} s, "
+                      f"NumPy single-threaded"}, ok
+
+
+def run_ours(a):
+    import numpy as np
+    import torch
+
+    import ar_synth
+    import collective_reduction_gb300 as ar
+
+    world, rank, local = dist_setup()
+    es = esize(a.dtype)
+    n = int(a.mib * (1 << 20)) // es
+    S = n * es
+    params = dict(form=a.form, order=a.order)
+    if a.algo == "generalized":
+        params["r"] = a.r
+    if a.algo == "hybrid":
+        params["k1"] = a.k1
+    if a.dtype == "int32":
+        dev = [torch.randint(-1000, 1001, (n,), dtype=torch.int32, device="cuda",
+                             generator=torch.Generator("cuda").manual_seed(r)) for r in range(a.P)]
+    else:
+        dev = ar_synth.device_inputs(a.P, n, a.dtype, sigma=1e-3, seed=rank)
+    plan = ar.Plan(a.P, n, a.dtype, a.op, a.algo, **params)
+    info = plan.info()
+    stream = torch.cuda.current_stream()
+
+    # sampled check + CPU baseline (rank 0 only): sample before the first call
+    sample_k = 1 << 17 if a.dtype != "bfloat16" else 1 << 18
+    sample_k = max(1, min(sample_k // a.P, n // a.P))
+    sample_in, idx = (None, None)
+    if rank == 0:
+        sample_in, idx = gather_sample(dev, a.P, n, sample_k, base_chunks(a))
+    plan.execute(dev, stream)
+    plan.check()
+    sample_out = None
+    if rank == 0:
+        sample_out = []
+        for t in dev:
+            s = t.index_select(0, idx)
+            sample_out.append(s.view(torch.int16).cpu().numpy().view(np.uint16) if t.dtype == torch.bfloat16
+                              else s.cpu().numpy())
+
+    for _ in range(a.warmup):
+        plan.execute(dev, stream)
+    clocks = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    clocks.start()
+    time.sleep(0.3)
+    barrier_sync(world)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(a.steps):
+        ev[i][0].record(stream)
+        plan.execute(dev, stream)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    barrier_sync(world)
+    clk = clocks.stop()
+    plan.check()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world)
+    per_launch = [s.elapsed_time(e) for s, e in ev]
+    kernel_ms = statistics.mean(per_launch)
+
+    bytes_per_call = a.P * S
+    value = bytes_per_call * a.steps * world / (total_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    alg_bytes = info["hbm_bytes"]
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    traffic = recorded_traffic(a.P, a.mib, a.dtype, a.algo, a.form, a.order)
+
+    # end to end through the C ABI with pinned host buffers
+    host = [torch.empty(n, dtype=dev[0].dtype).pin_memory() for _ in range(a.P)]
+    for h, d in zip(host, dev):
+        h.copy_(d)
+    plan.execute_host(host, dev, stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(a.e2e_steps):
+        plan.execute_host(host, dev, stream)
+    e2e_s = (time.perf_counter() - t0) / a.e2e_steps
+    e2e_s = max_over_ranks(e2e_s, world)
+    plan.check()
+
+    cpu, verified = (None, None)
+    if rank == 0 and world == 1 or rank == 0:
+        cpu, verified = cpu_baseline_and_check(a, sample_in, sample_out)
+        if world > 1:
+            cpu = None if rank != 0 else cpu
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": a.steps,
+        "warmup": a.warmup,
+        "ms_per_step": round(total_ms / a.steps, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype_tag(a.dtype),
+        "data": "synthetic",
+        "config": {"workload": workload_name(a), "P": a.P, "bytes_per_rank": S, "elements_per_rank": n,
+                   "algo": a.algo, "form": a.form, "order": a.order, "op": a.op,
+                   "l2": "inputs larger than L2 (P x S = %.1f GiB vs 129 MB)" % (a.P * S / 2 ** 30),
+                   "busbw_GBps": round(S / (total_ms / a.steps / 1e3) * 2 * (a.P - 1) / a.P / 1e9, 2),
+                   "algbw_GBps": round(S / (total_ms / a.steps / 1e3) / 1e9, 2),
+                   "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernel_ms": round(kernel_ms, 6), "kernel": "staged_kernel"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(bytes_per_call / e2e_s / 1e9, 3) * world, "unit": "GB/s",
+                "h2d_bytes_per_step": bytes_per_call, "d2h_bytes_per_step": bytes_per_call},
+        "clocks": clk,
+        "gpu_launches": info["launches"] * a.steps,
+        "verified_sample_vs_oracle": verified,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(a):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import ar_synth
+    import oracle
+    from oracle.elementops import Arith
+    # bounded sample of the workload: up to 2^20 elements per rank (chunk structure
+    # kept: a ceil split of the sample gives the same P chunks)
+    n = max(a.P, min(int(a.mib * (1 << 20)) // esize(a.dtype), 1 << 20) // a.P * a.P)
+    dist = "uniform_int" if a.dtype == "int32" else "normal"
+    bufs = ar_synth.rank_inputs(a.P, n, a.dtype, dist, sigma=1e-3)
+    kw = {"r": a.r} if a.algo == "generalized" else ({"k1": a.k1} if a.algo == "hybrid" else {})
+    for _ in range(a.warmup):
+        oracle.run(a.algo, bufs, Arith(a.op, a.dtype), **kw)
+    times = []
+    for _ in range(a.steps):
+        t0 = time.perf_counter()
+        oracle.run(a.algo, bufs, Arith(a.op, a.dtype), **kw)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    nbytes = a.P * n * esize(a.dtype)
+    value = nbytes * a.steps / total / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(total / a.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_tag(a.dtype), "data": "synthetic",
+        "config": {"workload": workload_name(a), "P": a.P, "bytes_per_rank": int(a.mib * (1 << 20)),
+                   "algo": a.algo, "form": a.form, "order": a.order, "op": a.op,
+                   "sample_elements_per_rank": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} elements per rank (of {int(a.mib * (1 << 20)) // esize(a.dtype)}), "
+                                   f"one oracle run per step, NumPy single-threaded"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- sweep
+
+def run_sweep(a, path):
+    """Configuration 5: ring fused (faithful, fp32acc) and ring step form over
+    P in {2, 8, 16, 64} and 1 KiB .. 256 MiB per rank, fp32 and bf16; one
+    JSON line per point.  Points up to 64 KiB are timed as a CUDA graph of
+    100 calls."""
+    import torch
+
+    import ar_synth
+    import collective_reduction_gb300 as ar
+    torch.cuda.set_device(0)
+    free = torch.cuda.mem_get_info()[0]
+    peak, _ = measured_peak()
+    with open(path, "w") as out:
+        for dtype in ("float32", "bfloat16"):
+            for P in (2, 8, 16, 64):
+                for lg in range(10, 29):
+                    S = 1 << lg
+                    if P * S * 1.2 > free:
+                        continue
+                    n = S // esize(dtype)
+                    dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
+                    for form, order in (("fused", "faithful"), ("fused", "fp32acc"), ("step", "faithful")):
+                        if form == "step" and S > (1 << 26) and P == 64:
+                            continue
+                        plan = ar.Plan(P, n, dtype, "sum", "ring", form=form, order=order)
+                        info = plan.info()
+                        for _ in range(3):
+                            plan.execute(dev)
+                        torch.cuda.synchronize()
+                        if S <= 65536:
+                            g = torch.cuda.CUDAGraph()
+                            s = torch.cuda.Stream()
+                            s.wait_stream(torch.cuda.current_stream())
+                            with torch.cuda.stream(s):
+                                with torch.cuda.graph(g, stream=s):
+                                    for _ in range(100):
+                                        plan.execute(dev)
+                            torch.cuda.synchronize()
+                            reps = []
+                            for _ in range(5):
+                                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                                e0.record()
+                                g.replay()
+                                e1.record()
+                                torch.cuda.synchronize()
+                                reps.append(e0.elapsed_time(e1) / 100)
+                            ms = statistics.median(reps)
+                            del g
+                        else:
+                            reps = []
+                            for _ in range(20):
+                                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                                e0.record()
+                                plan.execute(dev)
+                                e1.record()
+                                torch.cuda.synchronize()
+                                reps.append(e0.elapsed_time(e1))
+                            ms = statistics.median(reps)
+                        plan.check()
+                        row = {"dtype": dtype, "P": P, "bytes_per_rank": S, "form": form, "order": order,
+                               "ms": ms, "allreduced_GBps": P * S / (ms / 1e3) / 1e9,
+                               "busbw_GBps": S / (ms / 1e3) * 2 * (P - 1) / P / 1e9,
+                               "hbm_GBps": info["hbm_bytes"] / (ms / 1e3) / 1e9,
+                               "frac_of_measured": info["hbm_bytes"] / (ms / 1e3) / 1e9 / peak,
+                               "launches": info["launches"]}
+                        out.write(json.dumps(row) + "\n")
+                        out.flush()
+                        plan.close()
+                    del dev
+                    torch.cuda.empty_cache()
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+        return
+    if a.sweep:
+        run_sweep(a, a.sweep)
+        return
+    run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

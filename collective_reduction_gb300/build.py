@@ -1,0 +1,70 @@
+"""Builds libar.so, the engine's C-ABI shared library, in the package folder.
+
+    python -m collective_reduction_gb300.build
+
+Every translation unit is compiled by nvcc for sm_103a in parallel and linked
+with the static CUDA runtime.  Float code is compiled without contraction
+(-fmad=false) and without flushing subnormals, so the kernels perform exactly
+the adds and multiplies the schedules name.
+"""
+
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(PKG, "libar.so")
+SOURCES = ["kernels.cu", "schedule.cpp", "lower.cpp", "api.cpp"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc():
+    for cand in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda"):
+        p = os.path.join(cand, "bin", "nvcc") if cand else ""
+        if p and os.path.exists(p):
+            return p
+    p = shutil.which("nvcc")
+    if not p:
+        raise RuntimeError("nvcc not found: the engine needs the CUDA toolkit to build")
+    return p
+
+
+def build(verbose=False):
+    nv = nvcc()
+    common = ["-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    with tempfile.TemporaryDirectory(prefix="ar_build_") as tmp:
+        procs, objs = [], []
+        for src in SOURCES:
+            obj = os.path.join(tmp, src + ".o")
+            cmd = [nv, "-c", os.path.join(CSRC, src), "-o", obj] + common
+            if src.endswith(".cu"):
+                cmd += ARCH + ["-lineinfo", "-fmad=false", "-ftz=false", "-prec-div=true",
+                               "-prec-sqrt=true", "-Xptxas", "-v" if verbose else "-O3"]
+            procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+            objs.append(obj)
+        failed = []
+        for src, p in procs:
+            out, _ = p.communicate()
+            text = out.decode(errors="replace")
+            if p.returncode != 0:
+                failed.append(f"--- {src} ---\n{text}")
+            elif verbose and text.strip():
+                sys.stderr.write(text)
+        if failed:
+            raise RuntimeError("libar build failed:\n" + "\n".join(failed))
+        tmp_lib = os.path.join(tmp, "libar.so")
+        link = [nv, "-shared", "-o", tmp_lib] + objs + ARCH + ["-cudart", "static"]
+        r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+        if r.returncode != 0:
+            raise RuntimeError("libar link failed:\n" + r.stdout.decode(errors="replace"))
+        shutil.move(tmp_lib, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose="-v" in sys.argv))

@@ -1,0 +1,352 @@
+// C ABI of the allreduce engine: argument checks, plan construction (compile,
+// lower, upload) and launch dispatch.  No arithmetic of the allreduce happens
+// here; every element is combined by the CUDA kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <stdexcept>
+#include <vector>
+
+#include "ar.h"
+#include "kernels.hpp"
+#include "lower.hpp"
+#include "schedule.hpp"
+
+struct ar_schedule_s {
+    ar::Schedule S;
+};
+
+struct ar_plan_s {
+    ar::Schedule S;
+    ar::Lowered L;
+    int device = 0;
+    int num_sms = 0;
+    int smem_staged = 0;
+    int smem_elem = 0;
+    char* d_tables = nullptr;
+    char* d_scratch = nullptr;
+    uint64_t slot_stride = 0;
+    uint64_t scratch_bytes = 0;
+    int* d_status = nullptr;
+    struct Set {
+        const ar::WorkItem* bulk;
+        const ar::WorkItem* edge;
+        const ar::WorkItem* fallback;
+        uint32_t n_bulk, n_edge, n_fallback;
+    };
+    std::vector<Set> sets;
+    const ar::DevProg* d_progs = nullptr;
+    const uint16_t* d_refs = nullptr;
+    const uint32_t* d_ins = nullptr;
+};
+
+namespace {
+
+ar_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return AR_OK;
+    return e == cudaErrorMemoryAllocation ? AR_ERR_NOMEM : AR_ERR_CUDA;
+}
+
+void fill_info(const ar::Schedule& S, ar_plan_info* info) {
+    std::memset(info, 0, sizeof(*info));
+    const int es = ar::esize_of(S.dtype);
+    info->P = S.P;
+    info->dtype = S.dtype;
+    info->op = S.op;
+    info->algo = S.algo;
+    info->form = S.params.form;
+    info->order = S.params.order;
+    info->n = static_cast<uint64_t>(S.n);
+    info->steps = static_cast<int>(S.rounds.size());
+    std::vector<uint64_t> per(S.P, 0);
+    for (auto& rd : S.rounds)
+        for (int r = 0; r < S.P; ++r) per[r] += static_cast<uint64_t>(rd.sent[r]) * es;
+    for (uint64_t b : per) {
+        info->sent_bytes_total += b;
+        info->sent_bytes_max = std::max(info->sent_bytes_max, b);
+    }
+    info->combines = static_cast<uint64_t>(S.combines);
+    info->max_slots = S.max_slots;
+    info->n_segments = S.nseg();
+}
+
+template <class T>
+size_t put(std::vector<char>& blob, const std::vector<T>& v) {
+    size_t off = (blob.size() + 255) / 256 * 256;
+    blob.resize(off + v.size() * sizeof(T));
+    if (!v.empty()) std::memcpy(blob.data() + off, v.data(), v.size() * sizeof(T));
+    return off;
+}
+
+void destroy_plan(ar_plan_s* p) {
+    if (!p) return;
+    if (p->d_tables) cudaFree(p->d_tables);
+    if (p->d_scratch) cudaFree(p->d_scratch);
+    if (p->d_status) cudaFree(p->d_status);
+    delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ar_status_string(ar_status s) {
+    switch (s) {
+        case AR_OK: return "AR_OK: success";
+        case AR_ERR_INVALID_ARG: return "AR_ERR_INVALID_ARG: invalid argument";
+        case AR_ERR_UNSUPPORTED: return "AR_ERR_UNSUPPORTED: request not supported";
+        case AR_ERR_CUDA: return "AR_ERR_CUDA: CUDA runtime error";
+        case AR_ERR_NOMEM: return "AR_ERR_NOMEM: out of memory";
+        case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT: a bounded wait in a kernel gave up";
+    }
+    return "unknown ar_status";
+}
+
+ar_status ar_schedule_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo, const ar_params* params,
+                             ar_schedule_t* out) {
+    if (!out) return AR_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n > (uint64_t(1) << 40)) return AR_ERR_UNSUPPORTED;
+    try {
+        auto* s = new ar_schedule_s();
+        ar_status st = ar::compile_schedule(P, static_cast<int64_t>(n), dtype, op, algo, params, s->S);
+        if (st != AR_OK) {
+            delete s;
+            return st;
+        }
+        *out = s;
+        return AR_OK;
+    } catch (const std::bad_alloc&) {
+        return AR_ERR_NOMEM;
+    }
+}
+
+ar_status ar_schedule_destroy(ar_schedule_t s) {
+    delete s;
+    return AR_OK;
+}
+
+ar_status ar_schedule_query(ar_schedule_t s, ar_plan_info* info) {
+    if (!s || !info) return AR_ERR_INVALID_ARG;
+    fill_info(s->S, info);
+    return AR_OK;
+}
+
+ar_status ar_schedule_step_sent(ar_schedule_t s, int step, uint64_t* elems_per_rank) {
+    if (!s || !elems_per_rank || step < 0 || step >= static_cast<int>(s->S.rounds.size()))
+        return AR_ERR_INVALID_ARG;
+    for (int r = 0; r < s->S.P; ++r) elems_per_rank[r] = static_cast<uint64_t>(s->S.rounds[step].sent[r]);
+    return AR_OK;
+}
+
+ar_status ar_schedule_tree(ar_schedule_t s, int rank, uint64_t elem, char* buf, size_t cap, size_t* needed) {
+    if (!s || rank < 0 || rank >= s->S.P || elem >= static_cast<uint64_t>(s->S.n)) return AR_ERR_INVALID_ARG;
+    try {
+        const int seg = s->S.seg_of(static_cast<int64_t>(elem));
+        std::string t = s->S.dag.text(s->S.final_at(rank, seg));
+        if (needed) *needed = t.size() + 1;
+        if (!buf || cap < t.size() + 1) return AR_ERR_INVALID_ARG;
+        std::memcpy(buf, t.c_str(), t.size() + 1);
+        return AR_OK;
+    } catch (const std::bad_alloc&) {
+        return AR_ERR_NOMEM;
+    }
+}
+
+ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo, const ar_params* params,
+                         ar_plan_t* out) {
+    if (!out) return AR_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n > (uint64_t(1) << 40)) return AR_ERR_UNSUPPORTED;
+    ar_plan_s* p = nullptr;
+    try {
+        p = new ar_plan_s();
+        ar_status st = ar::compile_schedule(P, static_cast<int64_t>(n), dtype, op, algo, params, p->S);
+        if (st != AR_OK) {
+            delete p;
+            return st;
+        }
+        try {
+            ar::lower(p->S, p->L);
+        } catch (const std::length_error&) {
+            delete p;
+            return AR_ERR_UNSUPPORTED;
+        }
+        cudaError_t e = cudaGetDevice(&p->device);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+        int optin = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
+        if (e == cudaSuccess) e = ar::prepare_kernels(dtype, op);
+        if (e != cudaSuccess) {
+            delete p;
+            return cuda_status(e);
+        }
+        const ar::Lowered& L = p->L;
+        p->smem_staged = ar::staged_smem_bytes(L);
+        p->smem_elem = (L.max_in_all + L.max_tmp_all) * ar::kElemThreads * 4;
+        if (p->smem_staged > optin || p->smem_elem > optin) {
+            delete p;
+            return AR_ERR_UNSUPPORTED;
+        }
+        // one device blob: programs, refs, instructions, then every item list
+        std::vector<char> blob;
+        size_t o_progs = put(blob, L.progs), o_refs = put(blob, L.refs), o_ins = put(blob, L.ins);
+        std::vector<size_t> o_sets;
+        for (auto& s : L.sets) {
+            o_sets.push_back(put(blob, s.bulk));
+            o_sets.push_back(put(blob, s.edge));
+            o_sets.push_back(put(blob, s.fallback));
+        }
+        blob.resize(std::max<size_t>(blob.size(), 256));
+        e = cudaMalloc(&p->d_tables, blob.size());
+        if (e == cudaSuccess) e = cudaMemcpy(p->d_tables, blob.data(), blob.size(), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess) e = cudaMalloc(&p->d_status, 256);
+        if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, 256);
+        const int es = ar::esize_of(dtype);
+        if (e == cudaSuccess && p->S.params.form == AR_FORM_STEP && p->S.max_slots > 1) {
+            p->slot_stride = (static_cast<uint64_t>(n) * es + 255) / 256 * 256;
+            p->scratch_bytes = static_cast<uint64_t>(p->S.max_slots - 1) * P * p->slot_stride;
+            e = cudaMalloc(&p->d_scratch, p->scratch_bytes);
+        }
+        if (e != cudaSuccess) {
+            destroy_plan(p);
+            return cuda_status(e);
+        }
+        p->d_progs = reinterpret_cast<const ar::DevProg*>(p->d_tables + o_progs);
+        p->d_refs = reinterpret_cast<const uint16_t*>(p->d_tables + o_refs);
+        p->d_ins = reinterpret_cast<const uint32_t*>(p->d_tables + o_ins);
+        for (size_t i = 0; i < L.sets.size(); ++i) {
+            ar_plan_s::Set s;
+            s.bulk = reinterpret_cast<const ar::WorkItem*>(p->d_tables + o_sets[3 * i]);
+            s.edge = reinterpret_cast<const ar::WorkItem*>(p->d_tables + o_sets[3 * i + 1]);
+            s.fallback = reinterpret_cast<const ar::WorkItem*>(p->d_tables + o_sets[3 * i + 2]);
+            s.n_bulk = static_cast<uint32_t>(L.sets[i].bulk.size());
+            s.n_edge = static_cast<uint32_t>(L.sets[i].edge.size());
+            s.n_fallback = static_cast<uint32_t>(L.sets[i].fallback.size());
+            p->sets.push_back(s);
+        }
+        *out = p;
+        return AR_OK;
+    } catch (const std::bad_alloc&) {
+        destroy_plan(p);
+        return AR_ERR_NOMEM;
+    }
+}
+
+ar_status ar_plan_destroy(ar_plan_t plan) {
+    if (!plan) return AR_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    destroy_plan(plan);
+    return cuda_status(e);
+}
+
+ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info) {
+    if (!plan || !info) return AR_ERR_INVALID_ARG;
+    fill_info(plan->S, info);
+    info->hbm_bytes = plan->L.hbm_bytes;
+    info->scratch_bytes = plan->scratch_bytes;
+    info->launches = plan->L.launches;
+    info->tile_bytes = plan->L.tile_bytes;
+    info->n_programs = static_cast<int>(plan->L.progs.size());
+    info->n_items = plan->L.n_items;
+    return AR_OK;
+}
+
+ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
+    if (!plan || !rank_bufs) return AR_ERR_INVALID_ARG;
+    const ar::Schedule& S = plan->S;
+    const int P = S.P;
+    const uint64_t es = ar::esize_of(S.dtype);
+    const uint64_t bytes = static_cast<uint64_t>(S.n) * es;
+    if (S.n == 0) return AR_OK;  // nothing to touch: any pointers are accepted
+    std::vector<std::pair<uintptr_t, int>> addr;
+    bool aligned = true;
+    for (int r = 0; r < P; ++r) {
+        uintptr_t a = reinterpret_cast<uintptr_t>(rank_bufs[r]);
+        if (!a || a % es) return AR_ERR_INVALID_ARG;
+        aligned = aligned && a % 16 == 0;
+        addr.emplace_back(a, r);
+    }
+    std::sort(addr.begin(), addr.end());
+    for (int r = 0; r + 1 < P; ++r)
+        if (addr[r].first == addr[r + 1].first || addr[r].first + bytes > addr[r + 1].first) return AR_ERR_INVALID_ARG;
+    if (P == 1 || S.n == 0) return AR_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ar::KernelArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int r = 0; r < P; ++r) a.bufs[r] = rank_bufs[r];
+    a.scratch = plan->d_scratch;
+    a.slot_stride = plan->slot_stride;
+    a.progs = plan->d_progs;
+    a.refs = plan->d_refs;
+    a.ins = plan->d_ins;
+    a.status = plan->d_status;
+    a.P = P;
+    for (const auto& s : plan->sets) {
+        cudaError_t e = cudaSuccess;
+        if (aligned) {
+            if (s.n_bulk) {
+                a.items = s.bulk;
+                a.n_items = s.n_bulk;
+                a.tile_bytes = plan->L.tile_bytes;
+                a.stages = plan->L.stages;
+                a.max_in = plan->L.max_in;
+                a.max_tmp = plan->L.max_tmp;
+                e = ar::launch_staged(S.dtype, S.op, a, static_cast<int>(std::min<uint32_t>(s.n_bulk, plan->num_sms)),
+                                      plan->smem_staged, st);
+            }
+            if (e == cudaSuccess && s.n_edge) {
+                a.items = s.edge;
+                a.n_items = s.n_edge;
+                a.max_in = plan->L.max_in_all;
+                a.max_tmp = plan->L.max_tmp_all;
+                e = ar::launch_elementwise(S.dtype, S.op, a, plan->smem_elem, st);
+            }
+        } else if (s.n_fallback) {
+            a.items = s.fallback;
+            a.n_items = s.n_fallback;
+            a.max_in = plan->L.max_in_all;
+            a.max_tmp = plan->L.max_tmp_all;
+            e = ar::launch_elementwise(S.dtype, S.op, a, plan->smem_elem, st);
+        }
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return AR_OK;
+}
+
+ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* dev_bufs, void* stream) {
+    if (!plan || !host_bufs || !dev_bufs) return AR_ERR_INVALID_ARG;
+    const int P = plan->S.P;
+    const size_t bytes = static_cast<size_t>(plan->S.n) * ar::esize_of(plan->S.dtype);
+    for (int r = 0; r < P; ++r)
+        if (!host_bufs[r]) return AR_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int r = 0; r < P; ++r) {
+        cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_bufs[r], bytes, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    ar_status s = ar_execute(plan, dev_bufs, stream);
+    if (s != AR_OK) return s;
+    for (int r = 0; r < P; ++r) {
+        cudaError_t e = cudaMemcpyAsync(host_bufs[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return cuda_status(cudaStreamSynchronize(st));
+}
+
+ar_status ar_plan_check(ar_plan_t plan) {
+    if (!plan) return AR_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    int word = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&word, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (word != 0) {
+        cudaMemset(plan->d_status, 0, sizeof(int));
+        return AR_ERR_TIMEOUT;
+    }
+    return AR_OK;
+}
+
+}  // extern "C"

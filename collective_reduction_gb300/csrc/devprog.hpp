@@ -1,0 +1,69 @@
+// Tile programs: the device-side form of a compiled schedule.
+//
+// A work item is an element range of every rank buffer with one program.
+// The program lists the buffers to load (inputs, in order), then either
+//   CHAIN_R  acc = in[0]; acc = in[i] (+) acc for i = 1..n_in-1   (ring order)
+//   CHAIN_L  acc = in[0]; acc = acc (+) in[i]
+//   ACC      fp32 accumulation of all inputs in the kernel's fixed order
+// followed by storing acc to every output buffer, or
+//   DAG      a straight-line list of instructions over inputs, temporaries
+//            and one accumulator register: OP d = a (+) b, STORE buf <- v.
+// All inputs of an item are loaded before any output is stored, so a
+// program may overwrite buffers it reads (the step form relies on this).
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define AR_HD __host__ __device__
+#else
+#define AR_HD
+#endif
+
+namespace ar {
+
+enum ProgKind : uint16_t { PK_CHAIN_R = 0, PK_CHAIN_L = 1, PK_DAG = 2, PK_ACC = 3 };
+
+// value references inside DAG instructions (10 bits)
+constexpr uint32_t REF_TMP = 0x200;  // bit 9 set: temporary index in bits 0..8
+constexpr uint32_t REF_ACC = 0x3FF;  // the accumulator register
+constexpr uint32_t MAX_IN = 256;     // inputs per program
+constexpr uint32_t MAX_TMP = 511;    // temporaries per program
+
+// instruction word: bits 30..31 kind
+//   OP:    a = bits 0..9, b = bits 10..19, d = bits 20..29
+//   STORE: v = bits 0..9, buffer id = bits 10..25
+constexpr uint32_t INS_OP = 0u;
+constexpr uint32_t INS_STORE = 1u;
+
+AR_HD inline uint32_t ins_op(uint32_t a, uint32_t b, uint32_t d) {
+    return (INS_OP << 30) | a | (b << 10) | (d << 20);
+}
+AR_HD inline uint32_t ins_store(uint32_t v, uint32_t buf) {
+    return (INS_STORE << 30) | v | (buf << 10);
+}
+
+// Buffer id: (slot << 6) | rank.  Slot 0 is the rank's own buffer; slot s >= 1
+// lives in the plan's scratch at ((s - 1) * P + rank) * slot_stride bytes.
+AR_HD inline uint32_t buf_id(int slot, int rank) {
+    return (static_cast<uint32_t>(slot) << 6) | static_cast<uint32_t>(rank);
+}
+
+struct DevProg {
+    uint16_t kind;
+    uint16_t n_in;
+    uint16_t n_tmp;
+    uint16_t n_out;     // CHAIN / ACC: number of output buffers
+    uint32_t n_ins;     // DAG: number of instruction words
+    uint32_t in_off;    // refs[in_off ..): input buffer ids
+    uint32_t out_off;   // refs[out_off ..): output buffer ids (CHAIN / ACC)
+    uint32_t ins_off;   // ins[ins_off ..): instruction words (DAG)
+};
+
+struct WorkItem {
+    int64_t elem;       // first element of the range
+    uint32_t count;     // elements in the range
+    uint32_t prog;      // program index
+};
+
+}  // namespace ar

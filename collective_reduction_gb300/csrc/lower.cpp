@@ -1,0 +1,366 @@
+// Lowering: compiled schedule -> tile programs -> work items.
+//
+// Fused form: every segment's program reads the P contributions once and
+// evaluates the DAG of trees the P ranks end with.  For sum / prod (and every
+// int32 op) a (+) b and b (+) a are bit-identical on the GPU (IEEE add / mul
+// are commutative and NaN results are canonical), so the DAG is first
+// canonicalised under commutation, which lets identical trees that differ only
+// in operand order share one evaluation.  max / min keep the operand order
+// (they differ on +-0 and NaN).
+//
+// Step form: every round's program reads each source and destination once and
+// applies the round's transfers (receiver on the left).
+#include "lower.hpp"
+
+#include <algorithm>
+#include <map>
+#include <stdexcept>
+
+namespace ar {
+namespace {
+
+struct Prog {
+    uint16_t kind = PK_DAG;
+    uint16_t n_tmp = 0;
+    std::vector<uint16_t> in, out;
+    std::vector<uint32_t> ins;
+    int stores() const {
+        if (kind != PK_DAG) return static_cast<int>(out.size());
+        int s = 0;
+        for (uint32_t w : ins) s += (w >> 30) == INS_STORE;
+        return s;
+    }
+};
+
+class Builder {
+public:
+    explicit Builder(Lowered& lw) : lw_(lw) {}
+    uint32_t add(const Prog& p) {
+        if (p.in.size() > MAX_IN || p.n_tmp > MAX_TMP) throw std::length_error("program too large");
+        std::vector<uint32_t> key{p.kind, p.n_tmp, static_cast<uint32_t>(p.in.size()),
+                                  static_cast<uint32_t>(p.out.size())};
+        key.insert(key.end(), p.in.begin(), p.in.end());
+        key.insert(key.end(), p.out.begin(), p.out.end());
+        key.insert(key.end(), p.ins.begin(), p.ins.end());
+        auto it = index_.find(key);
+        if (it != index_.end()) return it->second;
+        DevProg d{};
+        d.kind = p.kind;
+        d.n_in = static_cast<uint16_t>(p.in.size());
+        d.n_tmp = p.n_tmp;
+        d.n_out = static_cast<uint16_t>(p.out.size());
+        d.n_ins = static_cast<uint32_t>(p.ins.size());
+        d.in_off = static_cast<uint32_t>(lw_.refs.size());
+        lw_.refs.insert(lw_.refs.end(), p.in.begin(), p.in.end());
+        d.out_off = static_cast<uint32_t>(lw_.refs.size());
+        lw_.refs.insert(lw_.refs.end(), p.out.begin(), p.out.end());
+        d.ins_off = static_cast<uint32_t>(lw_.ins.size());
+        lw_.ins.insert(lw_.ins.end(), p.ins.begin(), p.ins.end());
+        uint32_t id = static_cast<uint32_t>(lw_.progs.size());
+        lw_.progs.push_back(d);
+        stores_.push_back(p.stores());
+        index_.emplace(std::move(key), id);
+        return id;
+    }
+    int stores(uint32_t id) const { return stores_[id]; }
+
+private:
+    Lowered& lw_;
+    std::map<std::vector<uint32_t>, uint32_t> index_;
+    std::vector<int> stores_;
+};
+
+// Canonical DAG: same trees, children of commutative combines ordered.
+struct Canon {
+    Dag c;
+    std::vector<int32_t> memo;
+    const Dag& src;
+    bool commute;
+    Canon(const Dag& s, bool cm) : c(s.P()), memo(s.size(), -1), src(s), commute(cm) {}
+    int32_t get(int32_t x) {
+        if (src.leaf(x)) return x;
+        if (memo[x] >= 0) return memo[x];
+        int32_t a = get(src.left(x)), b = get(src.right(x));
+        if (commute && a > b) std::swap(a, b);
+        return memo[x] = c.combine(a, b);
+    }
+};
+
+bool right_chain(const Dag& d, int32_t x, std::vector<int32_t>& leaves) {
+    leaves.clear();
+    while (!d.leaf(x)) {
+        if (!d.leaf(d.left(x))) return false;
+        leaves.push_back(d.left(x));
+        x = d.right(x);
+    }
+    leaves.push_back(x);
+    std::reverse(leaves.begin(), leaves.end());
+    return true;
+}
+
+bool left_chain(const Dag& d, int32_t x, std::vector<int32_t>& leaves) {
+    leaves.clear();
+    while (!d.leaf(x)) {
+        if (!d.leaf(d.right(x))) return false;
+        leaves.push_back(d.right(x));
+        x = d.left(x);
+    }
+    leaves.push_back(x);
+    std::reverse(leaves.begin(), leaves.end());
+    return true;
+}
+
+// Straight-line code for the trees outs[r] (one per rank) of a DAG.
+Prog dag_program(const Dag& d, const std::vector<int32_t>& outs) {
+    const int P = d.P();
+    Prog p;
+    p.kind = PK_DAG;
+    // post-order of the internal nodes reachable from the outputs
+    std::vector<int32_t> topo;
+    std::map<int32_t, int> uses;  // operand uses by internal nodes
+    std::map<int32_t, std::vector<int>> stores_of;
+    std::vector<char> seen(d.size(), 0);
+    std::vector<char> leaf_used(P, 0);
+    for (int r = 0; r < P; ++r) {
+        stores_of[outs[r]].push_back(r);
+        std::vector<std::pair<int32_t, int>> st{{outs[r], 0}};
+        while (!st.empty()) {
+            auto& top = st.back();
+            int32_t x = top.first;
+            if (d.leaf(x)) {
+                leaf_used[x] = 1;
+                st.pop_back();
+                continue;
+            }
+            if (seen[x] == 2) {
+                st.pop_back();
+                continue;
+            }
+            if (top.second == 0) {
+                top.second = 1;
+                seen[x] = 1;
+                st.push_back({d.left(x), 0});
+            } else if (top.second == 1) {
+                top.second = 2;
+                st.push_back({d.right(x), 0});
+            } else {
+                seen[x] = 2;
+                topo.push_back(x);
+                st.pop_back();
+            }
+        }
+    }
+    for (int32_t x : topo) {
+        uses[d.left(x)]++;
+        uses[d.right(x)]++;
+    }
+    std::map<int32_t, uint32_t> loc;
+    for (int r = 0; r < P; ++r)
+        if (leaf_used[r]) {
+            loc[r] = static_cast<uint32_t>(p.in.size());
+            p.in.push_back(static_cast<uint16_t>(buf_id(0, r)));
+        }
+    for (int32_t leaf = 0; leaf < P; ++leaf)
+        if (stores_of.count(leaf))
+            for (int r : stores_of[leaf]) p.ins.push_back(ins_store(loc[leaf], buf_id(0, r)));
+    std::vector<char> tmp_busy;
+    auto alloc = [&]() -> uint32_t {
+        size_t k = 0;
+        while (k < tmp_busy.size() && tmp_busy[k]) ++k;
+        if (k == tmp_busy.size()) tmp_busy.push_back(0);
+        tmp_busy[k] = 1;
+        p.n_tmp = std::max<uint16_t>(p.n_tmp, static_cast<uint16_t>(tmp_busy.size()));
+        return REF_TMP | static_cast<uint32_t>(k);
+    };
+    std::map<int32_t, int> left_uses = uses;
+    for (size_t k = 0; k < topo.size(); ++k) {
+        int32_t x = topo[k];
+        int32_t l = d.left(x), r = d.right(x);
+        uint32_t a = loc.at(l), b = loc.at(r);
+        for (int32_t o : {l, r}) {
+            if (d.leaf(o)) continue;
+            if (--left_uses[o] == 0) {
+                uint32_t ref = loc[o];
+                if (ref != REF_ACC && (ref & REF_TMP)) tmp_busy[ref & 0x1FF] = 0;
+            }
+        }
+        bool next_uses = k + 1 < topo.size() && (d.left(topo[k + 1]) == x || d.right(topo[k + 1]) == x);
+        uint32_t dest;
+        if (uses[x] == 0 || (uses[x] == 1 && next_uses))
+            dest = REF_ACC;
+        else
+            dest = alloc();
+        p.ins.push_back(ins_op(a, b, dest));
+        loc[x] = dest;
+        if (stores_of.count(x))
+            for (int rr : stores_of[x]) p.ins.push_back(ins_store(dest, buf_id(0, rr)));
+    }
+    return p;
+}
+
+Prog fused_program(Canon& cn, const Schedule& S, int seg) {
+    const int P = S.P;
+    std::vector<int32_t> outs(P);
+    for (int r = 0; r < P; ++r) outs[r] = cn.get(S.final_at(r, seg));
+    bool same = std::all_of(outs.begin(), outs.end(), [&](int32_t x) { return x == outs[0]; });
+    std::vector<int32_t> leaves;
+    if (same && (right_chain(cn.c, outs[0], leaves) || left_chain(cn.c, outs[0], leaves))) {
+        Prog p;
+        p.kind = right_chain(cn.c, outs[0], leaves) ? PK_CHAIN_R : PK_CHAIN_L;
+        if (p.kind == PK_CHAIN_L) left_chain(cn.c, outs[0], leaves);
+        for (int32_t x : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, x)));
+        for (int r = 0; r < P; ++r) p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
+        return p;
+    }
+    return dag_program(cn.c, outs);
+}
+
+Prog acc_program(int P) {
+    Prog p;
+    p.kind = PK_ACC;
+    for (int r = 0; r < P; ++r) {
+        p.in.push_back(static_cast<uint16_t>(buf_id(0, r)));
+        p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
+    }
+    return p;
+}
+
+Prog round_program(std::vector<const Transfer*> xs) {
+    std::sort(xs.begin(), xs.end(), [](const Transfer* a, const Transfer* b) {
+        return std::make_pair(a->dst, a->dst_out) < std::make_pair(b->dst, b->dst_out);
+    });
+    Prog p;
+    if (xs.size() == 1) {  // one transfer: acc = src, then dst_in (+) acc
+        const Transfer& x = *xs[0];
+        p.kind = PK_CHAIN_R;
+        p.in.push_back(static_cast<uint16_t>(buf_id(x.src_slot, x.src)));
+        if (x.combine) p.in.push_back(static_cast<uint16_t>(buf_id(x.dst_in, x.dst)));
+        p.out.push_back(static_cast<uint16_t>(buf_id(x.dst_out, x.dst)));
+        return p;
+    }
+    p.kind = PK_DAG;
+    std::map<uint16_t, uint32_t> idx;
+    auto input = [&](int slot, int rank) {
+        uint16_t b = static_cast<uint16_t>(buf_id(slot, rank));
+        auto it = idx.find(b);
+        if (it != idx.end()) return it->second;
+        uint32_t k = static_cast<uint32_t>(p.in.size());
+        p.in.push_back(b);
+        idx[b] = k;
+        return k;
+    };
+    for (const Transfer* x : xs) {
+        if (x->combine) input(x->dst_in, x->dst);
+        input(x->src_slot, x->src);
+    }
+    for (const Transfer* x : xs) {
+        uint32_t out = buf_id(x->dst_out, x->dst);
+        if (x->combine) {
+            p.ins.push_back(ins_op(idx[static_cast<uint16_t>(buf_id(x->dst_in, x->dst))],
+                                   idx[static_cast<uint16_t>(buf_id(x->src_slot, x->src))], REF_ACC));
+            p.ins.push_back(ins_store(REF_ACC, out));
+        } else {
+            p.ins.push_back(ins_store(idx[static_cast<uint16_t>(buf_id(x->src_slot, x->src))], out));
+        }
+    }
+    return p;
+}
+
+struct Range {
+    uint32_t prog;
+    int64_t lo, hi;
+};
+
+void push_range(std::vector<Range>& v, uint32_t prog, int64_t lo, int64_t hi) {
+    if (hi <= lo) return;
+    if (!v.empty() && v.back().prog == prog && v.back().hi == lo)
+        v.back().hi = hi;
+    else
+        v.push_back({prog, lo, hi});
+}
+
+}  // namespace
+
+int staged_smem_bytes(const Lowered& lw) {
+    // 2 mbarriers per stage, padded to 128 bytes, then the stage tiles and the
+    // temporaries
+    return 128 + lw.tile_bytes * (lw.stages * lw.max_in + lw.max_tmp);
+}
+
+void lower(const Schedule& S, Lowered& lw) {
+    lw = Lowered();
+    const int es = esize_of(S.dtype);
+    const int V = 16 / es;  // elements per 16-byte vector
+    Builder b(lw);
+    std::vector<std::vector<Range>> sets;
+    if (S.P > 1 && S.n > 0) {
+        if (S.params.form == AR_FORM_FUSED) {
+            std::vector<Range> rs;
+            if (S.params.order == AR_ORDER_FP32ACC) {
+                push_range(rs, b.add(acc_program(S.P)), 0, S.n);
+            } else {
+                bool commute = S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD;
+                Canon cn(S.dag, commute);
+                for (int s = 0; s < S.nseg(); ++s)
+                    push_range(rs, b.add(fused_program(cn, S, s)), S.bounds[s], S.bounds[s + 1]);
+            }
+            sets.push_back(rs);
+        } else {
+            for (const Round& rd : S.rounds) {
+                std::map<int, std::vector<const Transfer*>> by_seg;
+                for (const Transfer& x : rd.xfers) {
+                    int s0 = S.seg_of(x.lo), s1 = S.seg_of(x.hi - 1) + 1;
+                    for (int s = s0; s < s1; ++s) by_seg[s].push_back(&x);
+                }
+                std::vector<Range> rs;
+                for (auto& kv : by_seg)
+                    push_range(rs, b.add(round_program(kv.second)), S.bounds[kv.first], S.bounds[kv.first + 1]);
+                sets.push_back(rs);
+            }
+        }
+    }
+    // tile size from the programs that own an aligned body
+    lw.max_in = 1;
+    lw.max_tmp = 0;
+    for (auto& rs : sets)
+        for (auto& r : rs) {
+            const DevProg& d = lw.progs[r.prog];
+            lw.max_in_all = std::max<int>(lw.max_in_all, d.n_in);
+            lw.max_tmp_all = std::max<int>(lw.max_tmp_all, d.n_tmp);
+            int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
+            if (a < e) {
+                lw.max_in = std::max<int>(lw.max_in, d.n_in);
+                lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
+            }
+        }
+    lw.stages = kStages;
+    int64_t t = (kSmemBudget - 128) / (lw.stages * lw.max_in + lw.max_tmp);
+    t = std::min<int64_t>(t, kMaxTileBytes);
+    t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
+    lw.tile_bytes = static_cast<int>(t);
+    const int64_t tile_elems = t / es;
+    for (auto& rs : sets) {
+        LaunchSet ls;
+        for (auto& r : rs) {
+            int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
+            if (a < e) {
+                if (r.lo < a) ls.edge.push_back({r.lo, static_cast<uint32_t>(a - r.lo), r.prog});
+                for (int64_t x = a; x < e; x += tile_elems)
+                    ls.bulk.push_back({x, static_cast<uint32_t>(std::min(tile_elems, e - x)), r.prog});
+                if (e < r.hi) ls.edge.push_back({e, static_cast<uint32_t>(r.hi - e), r.prog});
+            } else {
+                ls.edge.push_back({r.lo, static_cast<uint32_t>(r.hi - r.lo), r.prog});
+            }
+            for (int64_t x = r.lo; x < r.hi; x += 4096)
+                ls.fallback.push_back({x, static_cast<uint32_t>(std::min<int64_t>(4096, r.hi - x)), r.prog});
+            const DevProg& d = lw.progs[r.prog];
+            ls.bytes += static_cast<uint64_t>(d.n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
+        }
+        lw.hbm_bytes += ls.bytes;
+        lw.n_items += ls.bulk.size() + ls.edge.size();
+        lw.launches += (!ls.bulk.empty()) + (!ls.edge.empty());
+        lw.sets.push_back(std::move(ls));
+    }
+}
+
+}  // namespace ar

@@ -1,0 +1,198 @@
+/*
+ * ar.h -- C ABI of the single-GPU allreduce schedule engine (sm_103a).
+ *
+ * P "virtual ranks" are P buffers of n elements resident in one GPU's HBM.
+ * An allreduce combines them elementwise with one associative operator and
+ * leaves the result in every buffer ("A Generalization of the Allreduce
+ * Operation", introduction: a combination of the processes' vectors that is
+ * distributed back to every process).  The call shape follows the in-place,
+ * stream-asynchronous, status-returning collective of "All-Reduce, in
+ * depth" (The APIs): arguments in, an error code out, work enqueued on a
+ * stream.
+ *
+ * The engine follows a named schedule exactly: it compiles the schedule into
+ * rounds of transfers and into each element's reduction tree, then either
+ *   - AR_FORM_FUSED: one pass that reads every contribution once, evaluates
+ *     the schedule's reduction trees in registers / shared memory and writes
+ *     every rank's result (2 P S bytes of HBM traffic, the minimum), or
+ *   - AR_FORM_STEP: one kernel launch per round of the schedule, moving and
+ *     combining exactly the chunks that round moves.
+ * In AR_ORDER_FAITHFUL mode both forms give bit-identical results to the
+ * schedule run literally (bf16: every combine rounded to bf16).  In
+ * AR_ORDER_FP32ACC mode (fused only) the kernel accumulates all P
+ * contributions in fp32 in its own fixed order and rounds once.
+ *
+ * Conventions common to every function:
+ *   - Every function returns ar_status; AR_OK is 0.  Nothing aborts.
+ *   - Sizes are element counts unless the name says bytes.
+ *   - Pointers named *_bufs are host arrays of P pointers; the pointers are
+ *     device (or host, for ar_execute_host) addresses owned by the caller.
+ *   - Functions whose comment says "host only" make no CUDA call and may be
+ *     used on a machine without a GPU.
+ */
+#ifndef AR_H
+#define AR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AR_MAX_RANKS 64
+
+typedef enum {
+    AR_OK = 0,
+    AR_ERR_INVALID_ARG = 1, /* null / aliased / overlapping pointers, bad sizes */
+    AR_ERR_UNSUPPORTED = 2, /* valid request this engine does not implement   */
+    AR_ERR_CUDA = 3,        /* a CUDA runtime call failed                      */
+    AR_ERR_NOMEM = 4,       /* host or device allocation failed                */
+    AR_ERR_TIMEOUT = 5      /* a bounded wait inside a kernel gave up          */
+} ar_status;
+
+typedef enum { AR_INT32 = 0, AR_FLOAT32 = 1, AR_BFLOAT16 = 2 } ar_dtype;
+
+/* Element operations (elementwise operator of "還元演算子" (Reduction operator),
+ * binomial-tree section).  The receiving rank's own value is always the left
+ * operand.  int32 sum / prod wrap modulo 2^32.  fp32 is IEEE round-to-
+ * nearest-even with subnormals.  bf16 widens both operands to fp32, applies
+ * the fp32 op and rounds to bf16 (nearest even) after every op.
+ * max = a > b ? a : b, min = a < b ? a : b (ties and NaN keep b). */
+typedef enum { AR_SUM = 0, AR_PROD = 1, AR_MAX = 2, AR_MIN = 3 } ar_op;
+
+/* Schedules.
+ *  AR_RING        ring reduce-scatter + all-gather over P chunks; rank r
+ *                 sends to r + 1 ("All-Reduce, in depth", The ring
+ *                 algorithm; "A Generalization of the Allreduce Operation",
+ *                 ring as the cyclic-group straightforward algorithm, Fig. 5).
+ *                 2(P-1) rounds.
+ *  AR_BINOMIAL    binomial-tree reduce to rank 0 (x_i <- x_i (+) x_{i+2^k})
+ *                 then broadcast ("還元演算子", binomial tree).  2 ceil(log2 P).
+ *  AR_RH          recursive halving reduce-scatter + doubling all-gather,
+ *                 distance P/2 first; the bandwidth-optimal generalized
+ *                 algorithm with the XOR group ("A Generalization ...",
+ *                 remark after eq. 25, Table 1.b).  P = 2^k.  2 log2 P.
+ *  AR_RD          recursive doubling, whole vectors, distance 1 first.
+ *                 P = 2^k.  log2 P rounds.
+ *  AR_HYBRID      k1 halving rounds, recursive doubling on the block each rank
+ *                 then owns, k1 doubling rounds ("A Generalization ...",
+ *                 introduction, the classic hybrid).  P = 2^k.  log2 P + k1.
+ *  AR_GENERALIZED the group-theoretic generalized allreduce for any P
+ *                 ("A Generalization ...", eqs. 17-44): cyclic group (any P)
+ *                 or XOR group (P = 2^k); r distribution steps removed,
+ *                 0 <= r <= ceil(log2 P); 2 ceil(log2 P) - r rounds.
+ *  AR_AHC         asymmetric hierarchical allreduce (AHC, HCCL, Description):
+ *                 contiguous groups of the given sizes, LCM x G chunks, ring
+ *                 reduce-scatter inside each group, ring allreduce between the
+ *                 logical devices with identical IDs, ring all-gather inside
+ *                 each group. */
+typedef enum {
+    AR_RING = 0, AR_BINOMIAL = 1, AR_RH = 2, AR_RD = 3,
+    AR_HYBRID = 4, AR_GENERALIZED = 5, AR_AHC = 6
+} ar_algo;
+
+enum { AR_FORM_FUSED = 0, AR_FORM_STEP = 1 };
+enum { AR_ORDER_FAITHFUL = 0, AR_ORDER_FP32ACC = 1 };
+enum { AR_GROUP_CYCLIC = 0, AR_GROUP_XOR = 1 };
+
+typedef struct {
+    int form;               /* AR_FORM_FUSED or AR_FORM_STEP                      */
+    int order;              /* AR_ORDER_FAITHFUL or AR_ORDER_FP32ACC (fused only) */
+    int group;              /* AR_GENERALIZED: AR_GROUP_CYCLIC or AR_GROUP_XOR    */
+    int r;                  /* AR_GENERALIZED: removed distribution steps         */
+    int k1;                 /* AR_HYBRID: halving steps, 0..log2 P                */
+    int n_groups;           /* AR_AHC: number of groups G                         */
+    const int* group_sizes; /* AR_AHC: G sizes adding up to P (copied at create)  */
+} ar_params;
+
+typedef struct {
+    int P;
+    int dtype, op, algo, form, order;
+    uint64_t n;                  /* elements per rank                              */
+    int steps;                   /* rounds of the schedule                         */
+    uint64_t sent_bytes_max;     /* max over ranks of bytes sent, all rounds       */
+    uint64_t sent_bytes_total;   /* bytes sent by all ranks, all rounds            */
+    uint64_t combines;           /* element combines the schedule performs         */
+    int max_slots;               /* partials a rank holds per chunk at once (>= 1) */
+    int n_segments;              /* element ranges with one reduction tree each    */
+    /* Filled for plans (ar_plan_query); zero for schedules. */
+    uint64_t hbm_bytes;          /* algorithmic HBM bytes moved by one execute     */
+    uint64_t scratch_bytes;      /* device scratch the plan owns                   */
+    int launches;                /* kernel launches per execute (aligned buffers)  */
+    int tile_bytes;              /* bytes per input tile in the staged kernel      */
+    int n_programs;              /* distinct tile programs                         */
+    uint64_t n_items;            /* work items over all launches                   */
+} ar_plan_info;
+
+typedef struct ar_schedule_s* ar_schedule_t;
+typedef struct ar_plan_s* ar_plan_t;
+
+/* ---- schedule compiler (host only) ---------------------------------------
+ * ar_schedule_create compiles (P, n, dtype, op, algo, params) into rounds of
+ * transfers and per-element reduction trees.  P in 1..AR_MAX_RANKS (larger P:
+ * AR_ERR_UNSUPPORTED).  params may be NULL for the defaults (fused, faithful,
+ * cyclic, r = 0, k1 = 0).  On success *out owns host memory released by
+ * ar_schedule_destroy.  Errors: AR_ERR_INVALID_ARG (P < 1, unknown enum, null
+ * out, AHC sizes not adding up to P, r or k1 out of range),
+ * AR_ERR_UNSUPPORTED (P > AR_MAX_RANKS, XOR / RD / RH / hybrid with P not a
+ * power of two, AHC with more than 4096 chunks, FP32ACC with the step form),
+ * AR_ERR_NOMEM. */
+ar_status ar_schedule_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo,
+                             const ar_params* params, ar_schedule_t* out);
+ar_status ar_schedule_destroy(ar_schedule_t s);
+/* Counters of the compiled schedule (hbm / plan fields left zero). */
+ar_status ar_schedule_query(ar_schedule_t s, ar_plan_info* info);
+/* Elements each rank sends in round `step` (0-based): writes P counts to
+ * elems_per_rank.  AR_ERR_INVALID_ARG if step is out of range. */
+ar_status ar_schedule_step_sent(ar_schedule_t s, int step, uint64_t* elems_per_rank);
+/* The reduction tree the schedule leaves in element `elem` of rank `rank`, as
+ * text: a leaf is a rank number, "(a+b)" is a combine whose left operand a is
+ * the receiver's value.  Writes at most cap bytes including the terminating
+ * NUL; *needed receives the full length + 1.  AR_ERR_INVALID_ARG when the
+ * buffer is too small (nothing useful written) or indices are out of range. */
+ar_status ar_schedule_tree(ar_schedule_t s, int rank, uint64_t elem, char* buf, size_t cap,
+                           size_t* needed);
+
+/* ---- plans (need a CUDA device) -------------------------------------------
+ * ar_plan_create compiles the schedule, lowers it to tile programs for the
+ * chosen form and uploads them to the current device; it allocates the
+ * plan's device tables and, for the step form of schedules that keep two
+ * partials per chunk, scratch.  No kernel runs.  Errors as
+ * ar_schedule_create plus AR_ERR_CUDA / AR_ERR_NOMEM. */
+ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo,
+                         const ar_params* params, ar_plan_t* out);
+/* Frees the plan's host and device memory.  Synchronises the device first. */
+ar_status ar_plan_destroy(ar_plan_t plan);
+/* Counters of the schedule and of its lowering. */
+ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info);
+/* Enqueues the allreduce on `stream` (0 = legacy default stream) and returns.
+ * rank_bufs: host array of P device pointers, each to n elements of the
+ * plan's dtype on the plan's device, distinct, non-overlapping and aligned
+ * to the element size (AR_ERR_INVALID_ARG otherwise).  With n = 0 the call
+ * is a no-op and the pointers are not inspected.  Every buffer is both input
+ * and output.
+ * 16-byte aligned buffers use the staged kernels; any other alignment is
+ * valid and takes a slower element-wise path.  Executes of one plan must be
+ * ordered on one stream (they share the plan's scratch).  The launch itself
+ * is checked (AR_ERR_CUDA); kernel-side failures are reported by
+ * ar_plan_check. */
+ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream);
+/* End-to-end variant: copies P host buffers to the P device buffers, runs the
+ * allreduce and copies every device buffer back to its host buffer, all
+ * enqueued on `stream` (one cudaMemcpyAsync per buffer and direction), then
+ * synchronises the stream.  host_bufs should be pinned for full speed. */
+ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* dev_bufs,
+                          void* stream);
+/* Synchronises the device and reads the plan's device status word: AR_OK, or
+ * AR_ERR_TIMEOUT if a bounded wait in a kernel gave up since the last check
+ * (the word is then cleared).  AR_ERR_CUDA if synchronisation fails. */
+ar_status ar_plan_check(ar_plan_t plan);
+
+/* Static text for a status code (never NULL). */
+const char* ar_status_string(ar_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AR_H */

@@ -74,6 +74,10 @@ class Arith:
         self.combines = 0  # element operations performed
 
     def _f32_op(self, a, b):
+        with np.errstate(over="ignore", invalid="ignore", under="ignore"):
+            return self._f32_op_raw(a, b)
+
+    def _f32_op_raw(self, a, b):
         if self.op == "sum":
             return np.add(a, b, dtype=np.float32)
         if self.op == "prod":

@@ -1,0 +1,266 @@
+"""GPU parity: the engine's CUDA path against the CPU oracle, element by
+element, through the C ABI.  Order-faithful results must be bit-identical to
+the oracle's literal simulation (every dtype, every schedule); fp32-
+accumulated results must stay within the normwise relative error the engine
+promises (1e-6 fp32, 4e-3 bf16) of a float64 direct reduction."""
+
+import numpy as np
+import pytest
+
+import ar_synth
+import oracle
+from oracle.chunking import ceil_log2
+from oracle.direct import direct_f64, direct_int, normwise_rel_err
+from oracle.elementops import Arith
+
+from gpu_util import assert_bit_equal, engine, ensure_built, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+FORMS = ["fused", "step"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ensure_built()
+    import torch
+    assert torch.cuda.is_available()
+
+
+def check_faithful(bufs, dtype, op, algo, form, **kw):
+    want = oracle.run(algo, bufs, Arith(op, dtype), **kw).bufs
+    got = engine(bufs, dtype, op, algo, form=form, **kw)
+    for r in range(len(bufs)):
+        assert_bit_equal(got[r], want[r], dtype, f"{algo} {op} {dtype} {form} {kw} rank {r}")
+    return got
+
+
+# ---- configuration 1: ring, P = 3, 1024 int32 -------------------------------------------
+
+@pytest.mark.parametrize("form", FORMS)
+def test_config1_ring_int32(form):
+    bufs = ar_synth.rank_inputs(3, 1024, "int32", "uniform_int")
+    got = check_faithful(bufs, "int32", "sum", "ring", form)
+    want = direct_int(bufs, "sum")
+    for g in got:
+        assert np.array_equal(g, want)
+
+
+# ---- configuration 2: RH, RD, hybrid, binomial, P = 8, 2^20 fp32 -------------------------
+
+CONFIG2 = [("rh", {}), ("rd", {}), ("binomial", {})] + [("hybrid", {"k1": k}) for k in range(4)]
+
+
+@pytest.fixture(scope="module")
+def config2_inputs():
+    return ar_synth.rank_inputs(8, 1 << 20, "float32", "normal", sigma=1.0)
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("op", ["sum", "max"])
+@pytest.mark.parametrize("algo,kw", CONFIG2)
+def test_config2_power_of_two_schedules(config2_inputs, algo, kw, op, form):
+    check_faithful(config2_inputs, "float32", op, algo, form, **kw)
+
+
+# ---- configuration 3: generalized, P = 7 and 12 ----------------------------------------
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("n", [106, 1 << 20])
+@pytest.mark.parametrize("P", [7, 12])
+def test_config3_generalized_every_step_count(P, n, form):
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2)
+    L = ceil_log2(P)
+    for r in range(L + 1):
+        check_faithful(bufs, "float32", "sum", "generalized", form, group="cyclic", r=r)
+
+
+def test_config3_xor_group_rejected_for_p12():
+    import collective_reduction_gb300 as ar
+    with pytest.raises(ar.ArError) as e:
+        ar.Plan(12, 106, "float32", "sum", "generalized", group="xor")
+    assert e.value.name == "AR_ERR_UNSUPPORTED"
+
+
+# ---- configuration 4: AHC, groups {2, 3}, 2^24 bf16 -------------------------------------
+
+@pytest.fixture(scope="module")
+def config4_inputs():
+    return ar_synth.rank_inputs(5, 1 << 24, "bfloat16", "normal", sigma=1e-3)
+
+
+@pytest.mark.parametrize("form", FORMS)
+def test_config4_ahc_bf16(config4_inputs, form):
+    check_faithful(config4_inputs, "bfloat16", "sum", "ahc", form, group_sizes=[2, 3])
+
+
+def test_config4_ahc_fp32acc_within_tolerance(config4_inputs):
+    got = engine(config4_inputs, "bfloat16", "sum", "ahc", group_sizes=[2, 3], order="fp32acc")
+    ref = direct_f64(config4_inputs, "sum", "bfloat16")
+    from oracle.elementops import bf16_to_f32
+    for g in got:
+        assert normwise_rel_err(bf16_to_f32(g), ref) <= 4e-3
+
+
+# ---- configuration 5 (small points, full check) -----------------------------------------
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("P", [2, 8, 16, 64])
+@pytest.mark.parametrize("nbytes", [1024, 65536, 1 << 20])
+def test_config5_ring_small_sizes(P, nbytes, dtype):
+    n = nbytes // (4 if dtype == "float32" else 2)
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-3, seed=P)
+    check_faithful(bufs, dtype, "sum", "ring", "fused")
+    if nbytes <= 65536:
+        check_faithful(bufs, dtype, "sum", "ring", "step")
+    got = engine(bufs, dtype, "sum", "ring", order="fp32acc")
+    ref = direct_f64(bufs, "sum", dtype)
+    tol = 1e-6 if dtype == "float32" else 4e-3
+    from oracle.elementops import bf16_to_f32
+    for g in got:
+        y = bf16_to_f32(g) if dtype == "bfloat16" else g
+        assert normwise_rel_err(y, ref) <= tol
+
+
+# ---- every (dtype, op) through a chain and a DAG program -------------------------------
+
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+@pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
+@pytest.mark.parametrize("algo,kw", [("ring", {}), ("rd", {}), ("generalized", {"r": 2}), ("binomial", {})])
+def test_every_dtype_and_op(dtype, op, algo, kw):
+    P = 4 if algo == "rd" else 5
+    n = 4099
+    dist = "small_int" if (dtype == "int32" and op == "prod") else ("uniform_int" if dtype == "int32" else "normal")
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.5, seed=3)
+    for form in FORMS:
+        check_faithful(bufs, dtype, op, algo, form, **kw)
+
+
+def test_special_values_bf16_and_fp32():
+    """Ties, subnormals, infinities, NaN and signed zeros: P = 2 ring makes
+    chunk 0 compute x1 (+) x0 and chunk 1 x0 (+) x1."""
+    f32 = np.array([0.0, -0.0, 1e-40, -1e-40, 1.0, 1.0 + 2 ** -8, np.inf, -np.inf, np.nan, 3.4e38,
+                    2 ** -126, 1.5, -2.5, 1e-45, 7.0, 0.1], dtype=np.float32)
+    rng = np.random.default_rng(5)
+    a = rng.permutation(np.concatenate([f32, -f32]))
+    b = rng.permutation(np.concatenate([f32, f32[::-1]]))
+    a = np.concatenate([a, b]).astype(np.float32)
+    b = np.concatenate([b, a[:b.size]]).astype(np.float32)
+    for op in ("sum", "prod", "max", "min"):
+        check_faithful([a.copy(), b.copy()], "float32", op, "ring", "fused")
+        from oracle.elementops import f32_to_bf16_rne
+        check_faithful([f32_to_bf16_rne(a), f32_to_bf16_rne(b)], "bfloat16", op, "ring", "fused")
+
+
+def test_bf16_rounding_edge_grid():
+    """bf16 sums whose fp32 results sit exactly on, just above and just below
+    bf16 rounding ties, including subnormal and overflow ranges."""
+    rng = np.random.default_rng(9)
+    hi = rng.integers(1, 0x7F7F, 4096, dtype=np.uint32).astype(np.uint16)
+    lo = (hi.astype(np.uint32) - rng.integers(1, 24, 4096) * 0x80).clip(1, 0x7F7F).astype(np.uint16)
+    sub = rng.integers(1, 0x80, 1024, dtype=np.uint32).astype(np.uint16)
+    x = np.concatenate([hi, sub, hi | 0x8000]).astype(np.uint16)
+    y = np.concatenate([lo, sub[::-1], lo]).astype(np.uint16)
+    for op in ("sum", "prod"):
+        check_faithful([x, y], "bfloat16", op, "ring", "fused")
+        check_faithful([x, y], "bfloat16", op, "ring", "step")
+
+
+# ---- edge cases ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [0, 1, 3, 7, 1001, 4097])
+@pytest.mark.parametrize("P", [1, 2, 7, 13])
+def test_ragged_and_tiny_lengths(P, n):
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1.0, seed=n)
+    for form in FORMS:
+        check_faithful(bufs, "float32", "sum", "ring", form)
+        check_faithful(bufs, "float32", "sum", "generalized", form, r=min(1, ceil_log2(P)))
+
+
+def test_unaligned_buffers_take_elementwise_path():
+    import torch
+    import collective_reduction_gb300 as ar
+    P, n = 6, 3001
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", seed=4)
+    want = oracle.run("generalized", bufs, Arith("sum", "float32"), r=1).bufs
+    big = [torch.zeros(n + 1, dtype=torch.float32, device="cuda") for _ in range(P)]
+    views = [big[r][1:] for r in range(P)]  # 4-byte offset: not 16-byte aligned
+    for r in range(P):
+        views[r].copy_(torch.from_numpy(bufs[r]))
+    for form in FORMS:
+        for r in range(P):
+            views[r].copy_(torch.from_numpy(bufs[r]))
+        plan = ar.Plan(P, n, "float32", "sum", "generalized", r=1, form=form)
+        plan.execute(views)
+        plan.check()
+        for r in range(P):
+            assert_bit_equal(views[r].cpu().numpy(), want[r], "float32", f"unaligned {form} rank {r}")
+        plan.close()
+
+
+@pytest.mark.parametrize("form", FORMS)
+def test_p64_latency_optimal_max(form):
+    """P = 64, r = ceil(log2 P): a rank-specific tree per rank (max keeps the
+    operand order, so no tree merges)."""
+    P, n = 64, 640
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", seed=64)
+    check_faithful(bufs, "float32", "max", "generalized", form, r=6)
+    check_faithful(bufs, "float32", "sum", "generalized", form, r=6, group="xor")
+
+
+def test_invalid_buffers_rejected():
+    import torch
+    import collective_reduction_gb300 as ar
+    t = [torch.zeros(100, device="cuda") for _ in range(3)]
+    plan = ar.Plan(3, 100, "float32", "sum", "ring")
+    for bad in ([t[0], t[0], t[1]], [t[0], t[1], t[0][10:]]):
+        with pytest.raises(ar.ArError) as e:
+            plan.execute(bad)
+        assert e.value.name == "AR_ERR_INVALID_ARG"
+    with pytest.raises(ar.ArError):
+        plan.execute([t[0], t[1], 0])
+    plan.close()
+
+
+def test_execute_host_end_to_end():
+    import torch
+    import collective_reduction_gb300 as ar
+    P, n = 8, 1 << 16
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", seed=8)
+    want = oracle.run("ring", bufs, Arith("sum", "float32")).bufs
+    host = [torch.from_numpy(b.copy()).pin_memory() for b in bufs]
+    dev = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(P)]
+    plan = ar.Plan(P, n, "float32", "sum", "ring")
+    plan.execute_host(host, dev)
+    plan.check()
+    for r in range(P):
+        assert_bit_equal(host[r].numpy(), want[r], "float32", f"e2e rank {r}")
+        assert_bit_equal(dev[r].cpu().numpy(), want[r], "float32", f"e2e dev rank {r}")
+    plan.close()
+
+
+def test_repeated_execute_and_streams():
+    """Back-to-back executes on a side stream, then on the default stream."""
+    import torch
+    import collective_reduction_gb300 as ar
+    P, n = 8, 1 << 18
+    bufs = ar_synth.rank_inputs(P, n, "int32", "small_int", seed=2)
+    plan = ar.Plan(P, n, "int32", "sum", "ring")
+    dev = [to_dev(b, "int32") for b in bufs]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            plan.execute(dev)
+    torch.cuda.current_stream().wait_stream(s)
+    plan.execute(dev)
+    torch.cuda.synchronize()
+    plan.check()
+    # four allreduces: each multiplies the sum by P
+    x = direct_int(bufs, "sum").astype(np.int64)
+    for _ in range(3):
+        x = (x * P)
+    want = (x.astype(np.int64) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
+    for t in dev:
+        assert np.array_equal(to_host(t, "int32"), want)
+    plan.close()

@@ -1,0 +1,148 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+function ``include/ar.h`` declares, and the schedule compiler behind
+``ar_schedule_*`` builds exactly the reduction trees and per-round traffic of
+the oracle's independent simulation."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.chunking import ceil_log2
+from oracle.elementops import Symbolic, leaf_buffers, tree_str
+
+ar = pytest.importorskip("collective_reduction_gb300")
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ar.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ar.LIB_PATH):
+        from collective_reduction_gb300 import build
+        build.build()
+    return ar.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ar_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ("ar_plan_create", "ar_execute", "ar_plan_destroy", "ar_plan_query", "ar_status_string",
+                 "ar_schedule_create", "ar_schedule_tree", "ar_execute_host", "ar_plan_check"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.ar_status_string(s).decode().startswith(ar.STATUS[s])
+    assert lib.ar_status_string(99)
+
+
+def _cases():
+    for P in (1, 2, 3, 4, 5, 7, 8, 12, 16):
+        L = ceil_log2(P)
+        yield "ring", P, {}
+        yield "binomial", P, {}
+        for r in range(L + 1):
+            yield "generalized", P, {"group": "cyclic", "r": r}
+        if P & (P - 1) == 0:
+            yield "rd", P, {}
+            yield "rh", P, {}
+            for k1 in range(L + 1):
+                yield "hybrid", P, {"k1": k1}
+            for r in range(L + 1):
+                yield "generalized", P, {"group": "xor", "r": r}
+        for sizes in ([P], [1] * P, [P // 2, P - P // 2] if P > 1 else [1], [2, P - 2] if P >= 4 else [P]):
+            yield "ahc", P, {"group_sizes": sizes}
+
+
+@pytest.mark.parametrize("op", ["max", "sum"])
+def test_compiler_trees_and_traffic_match_oracle(lib, op):
+    for algo, P, kw in _cases():
+        for n in (2 * P + 3, P - 1 if P > 1 else 1):
+            s = ar.Schedule(P, n, "float32", op, algo, **kw)
+            res = oracle.run(algo, leaf_buffers(P, n), Symbolic(), **kw)
+            info = s.info()
+            assert info["steps"] == res.steps, (algo, P, kw)
+            for i in range(res.steps):
+                assert s.step_sent(i) == res.sent[i], (algo, P, kw, i)
+            for r in range(P):
+                for e in range(n):
+                    assert s.tree(r, e) == tree_str(res.bufs[r][e]), (algo, P, kw, r, e)
+            assert info["combines"] == res.combines, (algo, P, kw)
+            s.close()
+
+
+def test_compiler_counters_large_P(lib):
+    # P = 64 ring and P = 63 generalized: steps and traffic closed forms
+    s = ar.Schedule(64, 64 * 1000, "float32", "sum", "ring")
+    i = s.info()
+    assert i["steps"] == 126 and i["sent_bytes_max"] == 2 * 63 * 1000 * 4
+    g = ar.Schedule(63, 63 * 10, "float32", "sum", "generalized", r=3)
+    assert g.info()["steps"] == 2 * 6 - 3
+    assert g.info()["max_slots"] == 2
+
+
+def test_ahc_twelve_chunks(lib):
+    s = ar.Schedule(5, 24, "bfloat16", "sum", "ahc", group_sizes=[2, 3])
+    i = s.info()
+    assert i["steps"] == 6
+    # 12 chunks of 2 elements; segments split at chunk boundaries only
+    assert i["n_segments"] == 12
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 8, "float32", "sum", "ring", {}), "AR_ERR_INVALID_ARG"),
+    ((65, 8, "float32", "sum", "ring", {}), "AR_ERR_UNSUPPORTED"),
+    ((6, 8, "float32", "sum", "rd", {}), "AR_ERR_UNSUPPORTED"),
+    ((6, 8, "float32", "sum", "rh", {}), "AR_ERR_UNSUPPORTED"),
+    ((6, 8, "float32", "sum", "hybrid", {"k1": 1}), "AR_ERR_UNSUPPORTED"),
+    ((8, 8, "float32", "sum", "hybrid", {"k1": 4}), "AR_ERR_INVALID_ARG"),
+    ((12, 8, "float32", "sum", "generalized", {"group": "xor"}), "AR_ERR_UNSUPPORTED"),
+    ((7, 8, "float32", "sum", "generalized", {"r": 4}), "AR_ERR_INVALID_ARG"),
+    ((5, 8, "float32", "sum", "ahc", {"group_sizes": [2, 2]}), "AR_ERR_INVALID_ARG"),
+    ((5, 8, "float32", "sum", "ahc", {"group_sizes": [0, 5]}), "AR_ERR_INVALID_ARG"),
+    ((5, 8, "float32", "sum", "ahc", {}), "AR_ERR_INVALID_ARG"),
+    ((5, 8, "float32", "sum", "ring", {"form": "step", "order": "fp32acc"}), "AR_ERR_UNSUPPORTED"),
+    ((60, 8, "float32", "sum", "ahc", {"group_sizes": [7, 8, 9, 11, 13, 12]}), "AR_ERR_UNSUPPORTED"),
+])
+def test_invalid_requests_rejected(lib, args, status):
+    P, n, dt, op, algo, kw = args
+    with pytest.raises(ar.ArError) as e:
+        ar.Schedule(P, n, dt, op, algo, **kw)
+    assert e.value.name == status
+
+
+def test_raw_abi_null_checks(lib):
+    assert lib.ar_schedule_create(4, 8, 1, 0, 0, None, None) == 1
+    assert lib.ar_schedule_query(None, None) == 1
+    assert lib.ar_execute(None, None, None) == 1
+    assert lib.ar_plan_query(None, None) == 1
+    assert lib.ar_plan_destroy(None) == 1
+    assert lib.ar_plan_check(None) == 1
+    bad_dtype = ctypes.c_void_p()
+    assert lib.ar_schedule_create(4, 8, 7, 0, 0, None, ctypes.byref(bad_dtype)) == 1
+    assert lib.ar_schedule_create(4, 8, 1, 9, 0, None, ctypes.byref(bad_dtype)) == 1
+    assert lib.ar_schedule_create(4, 8, 1, 0, 42, None, ctypes.byref(bad_dtype)) == 1
+
+
+def test_tree_buffer_too_small(lib):
+    s = ar.Schedule(4, 8, "float32", "sum", "ring")
+    need = ctypes.c_size_t(0)
+    buf = ctypes.create_string_buffer(2)
+    assert lib.ar_schedule_tree(s._h, 0, 0, buf, 2, ctypes.byref(need)) == 1
+    assert need.value == len("(3+(2+(1+0)))") + 1
+    assert lib.ar_schedule_tree(s._h, 4, 0, buf, 2, ctypes.byref(need)) == 1
+    assert lib.ar_schedule_tree(s._h, 0, 8, buf, 2, ctypes.byref(need)) == 1
