@@ -34,9 +34,11 @@ def nvcc():
     return p
 
 
-def build(verbose=False):
+def build(verbose=False, defines=(), out=None):
+    """Compile and link; `defines` are extra -D macros, `out` another path."""
     nv = nvcc()
     common = ["-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    common += [f"-D{d}" for d in defines]
     with tempfile.TemporaryDirectory(prefix="ar_build_") as tmp:
         procs, objs = [], []
         for src in SOURCES:
@@ -49,8 +51,8 @@ def build(verbose=False):
             objs.append(obj)
         failed = []
         for src, p in procs:
-            out, _ = p.communicate()
-            text = out.decode(errors="replace")
+            log, _ = p.communicate()
+            text = log.decode(errors="replace")
             if p.returncode != 0:
                 failed.append(f"--- {src} ---\n{text}")
             elif verbose and text.strip():
@@ -62,8 +64,9 @@ def build(verbose=False):
         r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("libar link failed:\n" + r.stdout.decode(errors="replace"))
-        shutil.move(tmp_lib, LIB)
-    return LIB
+        dest = out or LIB
+        shutil.move(tmp_lib, dest)
+    return dest
 
 
 if __name__ == "__main__":

@@ -24,6 +24,7 @@ struct ar_plan_s {
     int device = 0;
     int num_sms = 0;
     int smem_staged = 0;
+    int smem_stream = 0;
     int smem_elem = 0;
     char* d_tables = nullptr;
     char* d_scratch = nullptr;
@@ -35,6 +36,7 @@ struct ar_plan_s {
         const ar::WorkItem* edge;
         const ar::WorkItem* fallback;
         uint32_t n_bulk, n_edge, n_fallback;
+        bool stream;
     };
     std::vector<Set> sets;
     const ar::DevProg* d_progs = nullptr;
@@ -185,8 +187,9 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
         }
         const ar::Lowered& L = p->L;
         p->smem_staged = ar::staged_smem_bytes(L);
+        p->smem_stream = ar::stream_smem_bytes(L);
         p->smem_elem = (L.max_in_all + L.max_tmp_all) * ar::kElemThreads * 4;
-        if (p->smem_staged > optin || p->smem_elem > optin) {
+        if (p->smem_staged > optin || p->smem_stream > optin || p->smem_elem > optin) {
             delete p;
             return AR_ERR_UNSUPPORTED;
         }
@@ -225,6 +228,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             s.n_bulk = static_cast<uint32_t>(L.sets[i].bulk.size());
             s.n_edge = static_cast<uint32_t>(L.sets[i].edge.size());
             s.n_fallback = static_cast<uint32_t>(L.sets[i].fallback.size());
+            s.stream = L.sets[i].stream;
             p->sets.push_back(s);
         }
         *out = p;
@@ -290,12 +294,20 @@ ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
             if (s.n_bulk) {
                 a.items = s.bulk;
                 a.n_items = s.n_bulk;
-                a.tile_bytes = plan->L.tile_bytes;
-                a.stages = plan->L.stages;
-                a.max_in = plan->L.max_in;
-                a.max_tmp = plan->L.max_tmp;
-                e = ar::launch_staged(S.dtype, S.op, a, static_cast<int>(std::min<uint32_t>(s.n_bulk, plan->num_sms)),
-                                      plan->smem_staged, st);
+                const int grid = static_cast<int>(std::min<uint32_t>(s.n_bulk, plan->num_sms));
+                if (s.stream) {
+                    a.tile_bytes = plan->L.stream_tile;
+                    a.stages = plan->L.stream_stages;
+                    a.max_in = 1;
+                    a.max_tmp = 0;
+                    e = ar::launch_stream(S.dtype, S.op, a, grid, plan->smem_stream, st);
+                } else {
+                    a.tile_bytes = plan->L.tile_bytes;
+                    a.stages = plan->L.stages;
+                    a.max_in = plan->L.max_in;
+                    a.max_tmp = plan->L.max_tmp;
+                    e = ar::launch_staged(S.dtype, S.op, a, grid, plan->smem_staged, st);
+                }
             }
             if (e == cudaSuccess && s.n_edge) {
                 a.items = s.edge;

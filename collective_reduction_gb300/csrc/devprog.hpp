@@ -22,13 +22,28 @@
 
 namespace ar {
 
-enum ProgKind : uint16_t { PK_CHAIN_R = 0, PK_CHAIN_L = 1, PK_DAG = 2, PK_ACC = 3 };
+enum ProgKind : uint8_t { PK_CHAIN_R = 0, PK_CHAIN_L = 1, PK_DAG = 2, PK_ACC = 3 };
+// DevProg::flags: the outputs are every rank's own buffer in rank order, so a
+// kernel can take output o's address straight from the rank-pointer array
+constexpr uint8_t PF_OUT_ALL = 1;
 
 // value references inside DAG instructions (10 bits)
 constexpr uint32_t REF_TMP = 0x200;  // bit 9 set: temporary index in bits 0..8
 constexpr uint32_t REF_ACC = 0x3FF;  // the accumulator register
 constexpr uint32_t MAX_IN = 256;     // inputs per program
 constexpr uint32_t MAX_TMP = 511;    // temporaries per program
+constexpr int kBarrierBytes = 512;   // mbarrier area at the start of a kernel's shared memory
+
+// Kernel geometry the lowering must agree with: consumer warps per CTA of the
+// staged / rank-streaming kernels, 16-byte vectors each consumer thread takes
+// per item tile (staged: up to kStagedVpt) or per rank tile (streaming).
+constexpr int kConsumerWarps = 8;
+constexpr int kStagedVpt = 8;
+constexpr int kStreamVpt = 8;        // rank-streaming kernel, chains and fp32 / int32 accumulation
+constexpr int kStreamVptNarrow = 4;  // rank-streaming kernel, bf16 fp32 accumulation (16 fp32 per vector)
+constexpr int kMaxStagedTile = 32 * kConsumerWarps * 16 * kStagedVpt;          // 32 KB
+constexpr int kStreamTileBytes = 32 * kConsumerWarps * 16 * kStreamVpt;        // 32 KB
+constexpr int kStreamTileNarrow = 32 * kConsumerWarps * 16 * kStreamVptNarrow; // 16 KB
 
 // instruction word: bits 30..31 kind
 //   OP:    a = bits 0..9, b = bits 10..19, d = bits 20..29
@@ -50,7 +65,8 @@ AR_HD inline uint32_t buf_id(int slot, int rank) {
 }
 
 struct DevProg {
-    uint16_t kind;
+    uint8_t kind;
+    uint8_t flags;
     uint16_t n_in;
     uint16_t n_tmp;
     uint16_t n_out;     // CHAIN / ACC: number of output buffers

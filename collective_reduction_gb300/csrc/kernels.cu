@@ -1,15 +1,23 @@
 // CUDA kernels of the allreduce engine (sm_103a).
 //
-// staged_kernel: persistent, one CTA per SM, warp-specialised.  Lane 0 of
-// warp 0 is the producer: for every work item it waits for a free pipeline
-// stage and issues one cp.async.bulk (TMA bulk copy) per input buffer of the
-// item's program into that stage, completing on the stage's mbarrier.  Eight
-// consumer warps wait for the stage, evaluate the tile program from shared
-// memory (chains and DAG instructions on 16-byte vectors, one accumulator
-// register per vector) and store the results to global memory with 128-bit
-// streaming stores, then release the stage.  Every wait is bounded: after two
-// seconds the waiter sets a bit in the plan's status word and the CTA winds
-// down (the producer first waits, again bounded, for its copies in flight).
+// stream_kernel: the hot path (ring fused pass and rounds, every fp32-
+// accumulate pass).  Persistent, one CTA per SM, warp-specialised: warp 0
+// resolves source addresses and its lane 0 issues one cp.async.bulk (TMA bulk
+// copy, L2 evict-first) per rank tile into a ring of shared-memory stages,
+// each completing on its own mbarrier; eight consumer warps fold every rank
+// tile into per-thread register accumulators in program order and, after the
+// item's last input, store the result to every output with 128-bit streaming
+// stores.  Rank tiles are 32 KB whatever P is, so all consumer threads stay
+// busy and the pipeline depth stays ~200 KB per SM.
+//
+// staged_kernel: for DAG programs (trees, rank-specific results).  Same
+// structure, but a stage holds all input tiles of one item, which the
+// consumers evaluate as straight-line instructions with shared-memory
+// temporaries.
+//
+// Every wait is bounded: after two seconds the waiter sets a bit in the
+// status word and the CTA winds down (a failing producer first waits, again
+// bounded, for its copies in flight).
 //
 // elementwise_kernel: one CTA per work item, one element per thread; used for
 // the unaligned heads / tails of ranges and for buffers that are not 16-byte
@@ -28,7 +36,7 @@ namespace ar {
 namespace {
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits give up after 2 s
-constexpr int kVpt = 8;                      // 16-byte vectors per consumer thread per item
+constexpr int kVpt = kStagedVpt;             // 16-byte vectors per consumer thread per item
 constexpr int kConsumers = 32 * kConsumerWarps;
 
 // ---------------------------------------------------------------- arithmetic
@@ -87,19 +95,6 @@ struct Acc {
     int32_t i[4];
 };
 
-template <int DT, int OP>
-__device__ __forceinline__ void acc_identity(Acc<DT>& x) {
-    if (DT == AR_INT32) {
-        const int32_t id = OP == AR_SUM ? 0 : OP == AR_PROD ? 1 : OP == AR_MAX ? INT32_MIN : INT32_MAX;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) x.i[q] = id;
-    } else {
-        const float id = OP == AR_SUM ? -0.0f : OP == AR_PROD ? 1.0f : OP == AR_MAX ? -INFINITY : INFINITY;
-#pragma unroll
-        for (int q = 0; q < Acc<DT>::W; ++q) x.f[q] = id;
-    }
-}
-
 template <int DT>
 __device__ __forceinline__ void acc_widen(Acc<DT>& x, uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -141,34 +136,44 @@ __device__ __forceinline__ uint4 acc_narrow(const Acc<DT>& x) {
                       pack_bf16x2(x.f[6], x.f[7]));
 }
 
-// FP32ACC order over n inputs: blocks of 8 consecutive inputs reduced as a
-// balanced pairwise tree (missing inputs are the op's identity), block
-// results folded left to right.  load(i) yields input i as a 16-byte vector.
+// FP32ACC order over inputs 0..n-1 (the kernels' own fixed order, identical
+// in every kernel and for every rank): blocks of 8 consecutive inputs are
+// each folded left to right, then the block results are folded left to
+// right; fp32 / bf16 accumulate in fp32 and round once at the end.  Inputs are
+// fed one at a time, so the order can be followed while inputs stream in.
+template <int DT, int OP>
+struct AccStream {
+    Acc<DT> acc, blk;
+    __device__ __forceinline__ void feed(uint32_t i, uint4 x) {
+        Acc<DT> w;
+        acc_widen<DT>(w, x);
+        if ((i & 7u) == 0)
+            blk = w;
+        else
+            acc_combine<DT, OP>(blk, w);
+        if ((i & 7u) == 7u) {
+            if (i == 7u)
+                acc = blk;
+            else
+                acc_combine<DT, OP>(acc, blk);
+        }
+    }
+    __device__ __forceinline__ uint4 finish(uint32_t n) {
+        if (n & 7u) {
+            if (n < 8u)
+                acc = blk;
+            else
+                acc_combine<DT, OP>(acc, blk);
+        }
+        return acc_narrow<DT>(acc);
+    }
+};
+
 template <int DT, int OP, class Load>
 __device__ __forceinline__ uint4 acc_reduce(uint32_t n, Load load) {
-    Acc<DT> acc;
-    for (uint32_t g = 0; g < n; g += 8) {
-        Acc<DT> s[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (g + q < n)
-                acc_widen<DT>(s[q], load(g + q));
-            else
-                acc_identity<DT, OP>(s[q]);
-        }
-        acc_combine<DT, OP>(s[0], s[1]);
-        acc_combine<DT, OP>(s[2], s[3]);
-        acc_combine<DT, OP>(s[4], s[5]);
-        acc_combine<DT, OP>(s[6], s[7]);
-        acc_combine<DT, OP>(s[0], s[2]);
-        acc_combine<DT, OP>(s[4], s[6]);
-        acc_combine<DT, OP>(s[0], s[4]);
-        if (g == 0)
-            acc = s[0];
-        else
-            acc_combine<DT, OP>(acc, s[0]);
-    }
-    return acc_narrow<DT>(acc);
+    AccStream<DT, OP> s;
+    for (uint32_t i = 0; i < n; ++i) s.feed(i, load(i));
+    return s.finish(n);
 }
 
 // ------------------------------------------------------------- memory access
@@ -197,10 +202,20 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+#ifndef AR_STORE_CS
+#define AR_STORE_CS 1
+#endif
+
+// results are never re-read by the kernel: streaming (evict-first) stores
 __device__ __forceinline__ void stg128(char* p, uint4 v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
+    if (AR_STORE_CS)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                     "r"(v.w)
+                     : "memory");
+    else
+        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                     "r"(v.w)
+                     : "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -246,11 +261,31 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
+// loads are read once: ask L2 to evict them first
+#ifndef AR_L2_EVICT_FIRST
+#define AR_L2_EVICT_FIRST 1
+#endif
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    if (AR_L2_EVICT_FIRST) {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+            "%4;" ::"r"(dst),
+            "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+            "l"(src), "r"(bytes), "r"(bar)
+            : "memory");
+    }
 }
 
 // ------------------------------------------------------------ staged kernel
@@ -264,6 +299,7 @@ struct Stage {
 
 template <int ES>
 __device__ void produce(const KernelArgs& a, const Stage& sm) {
+    const uint64_t policy = AR_L2_EVICT_FIRST ? evict_first_policy() : 0;
     uint32_t k = 0;
     bool ok = true;
     for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x, ++k) {
@@ -281,7 +317,7 @@ __device__ void produce(const KernelArgs& a, const Stage& sm) {
         const uint32_t dst = sm.tiles + s * sm.stage_bytes;
         for (uint32_t i = 0; i < pg.n_in; ++i) {
             const char* src = buf_addr(a, a.refs[pg.in_off + i]) + w.elem * ES;
-            bulk_load(dst + i * a.tile_bytes, src, nb, bar);
+            bulk_load(dst + i * a.tile_bytes, src, nb, bar, policy);
         }
     }
     if (!ok) {
@@ -403,7 +439,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) staged_kernel(const __grid_
     Stage sm;
     sm.full = smem_addr(smem);
     sm.empty = sm.full + 8 * a.stages;
-    sm.tiles = sm.full + 128;
+    sm.tiles = sm.full + kBarrierBytes;
     sm.stage_bytes = static_cast<uint32_t>(a.tile_bytes) * a.max_in;
     sm.tmps = sm.tiles + a.stages * sm.stage_bytes;
     if (threadIdx.x == 0) {
@@ -419,6 +455,164 @@ __global__ void __launch_bounds__(kStagedThreads, 1) staged_kernel(const __grid_
         return;
     }
     consume<DT, OP>(a, sm, threadIdx.x - 32);
+}
+
+// ---------------------------------------------------- rank-streaming kernel
+//
+// For programs that are a chain or an fp32 accumulation (the ring's fused
+// pass and rounds, every FP32ACC pass) the inputs are consumed strictly in
+// order, so an item's tiles need not be resident together: the producer
+// streams one rank tile (kStreamVpt vectors per consumer thread) per stage
+// through a deep ring of stages, and each consumer thread keeps its vectors'
+// accumulators in registers across the item's inputs.  Tile size and thread
+// utilisation no longer shrink with P.
+
+template <int ES>
+__device__ void stream_produce(const KernelArgs& a, const Stage& sm) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t policy = AR_L2_EVICT_FIRST ? evict_first_policy() : 0;
+    uint32_t g = 0;  // rank tiles issued so far
+    bool ok = true;
+    for (uint32_t it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        const uint32_t nb = w.count * ES;
+        const int64_t off = w.elem * ES;
+        for (uint32_t i0 = 0; i0 < pg.n_in && ok; i0 += 32) {
+            // the warp resolves 32 source addresses at once; lane 0 issues
+            const char* mine = nullptr;
+            if (i0 + lane < pg.n_in) mine = buf_addr(a, a.refs[pg.in_off + i0 + lane]) + off;
+            const uint32_t cnt = min(32u, pg.n_in - i0);
+            for (uint32_t j = 0; j < cnt; ++j) {
+                const char* src = reinterpret_cast<const char*>(
+                    __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(mine), j));
+                int issued = 0;
+                if (lane == 0) {
+                    const uint32_t s = g % a.stages, ph = (g / a.stages) & 1u;
+                    if (mbar_wait(sm.empty + 8 * s, ph ^ 1u)) {
+                        const uint32_t bar = sm.full + 8 * s;
+                        mbar_expect_tx(bar, nb);
+                        bulk_load(sm.tiles + s * a.tile_bytes, src, nb, bar, policy);
+                        issued = 1;
+                    }
+                }
+                issued = __shfl_sync(0xFFFFFFFFu, issued, 0);
+                if (!issued) {
+                    ok = false;
+                    break;
+                }
+                ++g;
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        atomicOr(a.status, kStatusWaitEmpty);
+        const uint32_t first = g > static_cast<uint32_t>(a.stages) ? g - a.stages : 0;
+        for (uint32_t j = first; j < g; ++j)
+            if (!mbar_wait(sm.full + 8 * (j % a.stages), (j / a.stages) & 1u)) atomicOr(a.status, kStatusDrain);
+    }
+}
+
+// Waits for rank tile g, hands its shared address to use(t), releases it.
+template <class Use>
+__device__ __forceinline__ bool stream_tile(const KernelArgs& a, const Stage& sm, uint32_t g, int ct, Use use) {
+    const uint32_t s = g % a.stages, ph = (g / a.stages) & 1u;
+    if (!mbar_wait(sm.full + 8 * s, ph)) {
+        atomicOr(a.status, kStatusWaitFull);
+        return false;
+    }
+    use(sm.tiles + s * a.tile_bytes);
+    __syncwarp();
+    if ((ct & 31) == 0) mbar_arrive(sm.empty + 8 * s);
+    return true;
+}
+
+__device__ __forceinline__ char* out_addr(const KernelArgs& a, const DevProg& pg, uint32_t o) {
+    if (pg.flags & PF_OUT_ALL) return static_cast<char*>(a.bufs[o]);
+    return buf_addr(a, a.refs[pg.out_off + o]);
+}
+
+template <int DT, int OP, int VPT>
+__device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    // bf16 fp32 accumulation holds 16 floats per vector: only the narrow
+    // instantiation runs it (the lowering picks the narrow tile for it)
+    constexpr bool kAccOk = !(DT == AR_BFLOAT16 && VPT > kStreamVptNarrow);
+    uint32_t g = 0;
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        const uint32_t nvec = (w.count * ES) >> 4;
+        const int64_t off = w.elem * ES;
+        uint4 res[VPT];
+        if (pg.kind == PK_ACC) {
+            if (!kAccOk) {
+                atomicOr(a.status, kStatusBadProgram);
+                return;
+            }
+            AccStream<DT, OP> acc[kAccOk ? VPT : 1];
+            for (uint32_t i = 0; i < pg.n_in; ++i, ++g) {
+                const bool ok = stream_tile(a, sm, g, ct, [&](uint32_t t) {
+#pragma unroll
+                    for (int j = 0; j < (kAccOk ? VPT : 1); ++j) {
+                        const uint32_t v = ct + j * kConsumers;
+                        if (v < nvec) acc[j].feed(i, lds128(t + v * 16));
+                    }
+                });
+                if (!ok) return;
+            }
+#pragma unroll
+            for (int j = 0; j < (kAccOk ? VPT : 1); ++j) res[j] = acc[j].finish(pg.n_in);
+        } else {
+            const bool right = pg.kind == PK_CHAIN_R;
+            for (uint32_t i = 0; i < pg.n_in; ++i, ++g) {
+                const bool ok = stream_tile(a, sm, g, ct, [&](uint32_t t) {
+#pragma unroll
+                    for (int j = 0; j < VPT; ++j) {
+                        const uint32_t v = ct + j * kConsumers;
+                        if (v < nvec) {
+                            const uint4 x = lds128(t + v * 16);
+                            res[j] = i == 0 ? x : right ? vop<DT, OP>(x, res[j]) : vop<DT, OP>(res[j], x);
+                        }
+                    }
+                });
+                if (!ok) return;
+            }
+        }
+        for (uint32_t o = 0; o < pg.n_out; ++o) {
+            char* dst = out_addr(a, pg, o) + off;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint32_t v = ct + j * kConsumers;
+                if (v < nvec) stg128(dst + v * 16, res[j]);
+            }
+        }
+    }
+}
+
+template <int DT, int OP, int VPT>
+__global__ void __launch_bounds__(kStagedThreads, 1) stream_kernel(const __grid_constant__ KernelArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    Stage sm;
+    sm.full = smem_addr(smem);
+    sm.empty = sm.full + 8 * a.stages;
+    sm.tiles = sm.full + kBarrierBytes;
+    sm.stage_bytes = a.tile_bytes;
+    sm.tmps = 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(sm.full + 8 * s, 1);
+            mbar_init(sm.empty + 8 * s, kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        stream_produce<ES>(a, sm);
+        return;
+    }
+    stream_consume<DT, OP, VPT>(a, sm, threadIdx.x - 32);
 }
 
 // --------------------------------------------------------- element kernel
@@ -500,27 +694,31 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
 
 using KernelFn = void (*)(KernelArgs);
 
+enum Which { K_STAGED = 0, K_STREAM = 1, K_STREAM_NARROW = 2, K_ELEM = 3 };
+
 template <int DT, int OP>
-struct Table {
-    static constexpr KernelFn staged = staged_kernel<DT, OP>;
-    static constexpr KernelFn elem = elementwise_kernel<DT, OP>;
-};
+KernelFn table(int which) {
+    if (which == K_STAGED) return staged_kernel<DT, OP>;
+    if (which == K_STREAM) return stream_kernel<DT, OP, kStreamVpt>;
+    if (which == K_STREAM_NARROW) return stream_kernel<DT, OP, kStreamVptNarrow>;
+    return elementwise_kernel<DT, OP>;
+}
 
 template <int DT>
-KernelFn pick(int op, bool staged) {
+KernelFn pick(int op, int which) {
     switch (op) {
-        case AR_SUM: return staged ? Table<DT, AR_SUM>::staged : Table<DT, AR_SUM>::elem;
-        case AR_PROD: return staged ? Table<DT, AR_PROD>::staged : Table<DT, AR_PROD>::elem;
-        case AR_MAX: return staged ? Table<DT, AR_MAX>::staged : Table<DT, AR_MAX>::elem;
-        default: return staged ? Table<DT, AR_MIN>::staged : Table<DT, AR_MIN>::elem;
+        case AR_SUM: return table<DT, AR_SUM>(which);
+        case AR_PROD: return table<DT, AR_PROD>(which);
+        case AR_MAX: return table<DT, AR_MAX>(which);
+        default: return table<DT, AR_MIN>(which);
     }
 }
 
-KernelFn kernel_for(int dtype, int op, bool staged) {
+KernelFn kernel_for(int dtype, int op, int which) {
     switch (dtype) {
-        case AR_INT32: return pick<AR_INT32>(op, staged);
-        case AR_FLOAT32: return pick<AR_FLOAT32>(op, staged);
-        default: return pick<AR_BFLOAT16>(op, staged);
+        case AR_INT32: return pick<AR_INT32>(op, which);
+        case AR_FLOAT32: return pick<AR_FLOAT32>(op, which);
+        default: return pick<AR_BFLOAT16>(op, which);
     }
 }
 
@@ -533,8 +731,8 @@ cudaError_t prepare_kernels(int dtype, int op) {
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    for (bool staged : {true, false}) {
-        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel_for(dtype, op, staged)),
+    for (int which : {K_STAGED, K_STREAM, K_STREAM_NARROW, K_ELEM}) {
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel_for(dtype, op, which)),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
     }
@@ -542,13 +740,21 @@ cudaError_t prepare_kernels(int dtype, int op) {
 }
 
 cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
-    KernelFn f = kernel_for(dtype, op, true);
+    KernelFn f = kernel_for(dtype, op, K_STAGED);
+    f<<<grid, kStagedThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
+    // the rank tile fixes the vectors per consumer thread
+    if (a.tile_bytes != kStreamTileBytes && a.tile_bytes != kStreamTileNarrow) return cudaErrorInvalidValue;
+    KernelFn f = kernel_for(dtype, op, a.tile_bytes == kStreamTileBytes ? K_STREAM : K_STREAM_NARROW);
     f<<<grid, kStagedThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem, cudaStream_t st) {
-    KernelFn f = kernel_for(dtype, op, false);
+    KernelFn f = kernel_for(dtype, op, K_ELEM);
     f<<<a.n_items, kElemThreads, smem, st>>>(a);
     return cudaGetLastError();
 }

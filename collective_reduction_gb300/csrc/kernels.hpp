@@ -32,8 +32,8 @@ struct KernelArgs {
 constexpr int kStatusWaitFull = 1;   // a consumer gave up waiting for a stage
 constexpr int kStatusWaitEmpty = 2;  // the producer gave up waiting for a free stage
 constexpr int kStatusDrain = 4;      // a failing producer gave up draining its copies
+constexpr int kStatusBadProgram = 8; // a program kind the launched kernel does not run
 
-constexpr int kConsumerWarps = 8;
 constexpr int kStagedThreads = 32 * (1 + kConsumerWarps);
 constexpr int kElemThreads = 64;
 
@@ -41,6 +41,8 @@ constexpr int kElemThreads = 64;
 cudaError_t prepare_kernels(int dtype, int op);
 // Persistent staged kernel over a.items (all 16-byte aligned), grid CTAs.
 cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st);
+// Persistent rank-streaming kernel over a.items (chain / FP32ACC programs only).
+cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st);
 // One CTA per item, one element per thread.
 cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem, cudaStream_t st);
 

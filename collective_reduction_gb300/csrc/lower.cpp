@@ -20,7 +20,8 @@ namespace ar {
 namespace {
 
 struct Prog {
-    uint16_t kind = PK_DAG;
+    uint8_t kind = PK_DAG;
+    uint8_t flags = 0;
     uint16_t n_tmp = 0;
     std::vector<uint16_t> in, out;
     std::vector<uint32_t> ins;
@@ -37,7 +38,7 @@ public:
     explicit Builder(Lowered& lw) : lw_(lw) {}
     uint32_t add(const Prog& p) {
         if (p.in.size() > MAX_IN || p.n_tmp > MAX_TMP) throw std::length_error("program too large");
-        std::vector<uint32_t> key{p.kind, p.n_tmp, static_cast<uint32_t>(p.in.size()),
+        std::vector<uint32_t> key{p.kind, p.flags, p.n_tmp, static_cast<uint32_t>(p.in.size()),
                                   static_cast<uint32_t>(p.out.size())};
         key.insert(key.end(), p.in.begin(), p.in.end());
         key.insert(key.end(), p.out.begin(), p.out.end());
@@ -46,6 +47,7 @@ public:
         if (it != index_.end()) return it->second;
         DevProg d{};
         d.kind = p.kind;
+        d.flags = p.flags;
         d.n_in = static_cast<uint16_t>(p.in.size());
         d.n_tmp = p.n_tmp;
         d.n_out = static_cast<uint16_t>(p.out.size());
@@ -208,6 +210,7 @@ Prog fused_program(Canon& cn, const Schedule& S, int seg) {
         Prog p;
         p.kind = right_chain(cn.c, outs[0], leaves) ? PK_CHAIN_R : PK_CHAIN_L;
         if (p.kind == PK_CHAIN_L) left_chain(cn.c, outs[0], leaves);
+        p.flags = PF_OUT_ALL;
         for (int32_t x : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, x)));
         for (int r = 0; r < P; ++r) p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
         return p;
@@ -218,6 +221,7 @@ Prog fused_program(Canon& cn, const Schedule& S, int seg) {
 Prog acc_program(int P) {
     Prog p;
     p.kind = PK_ACC;
+    p.flags = PF_OUT_ALL;
     for (int r = 0; r < P; ++r) {
         p.in.push_back(static_cast<uint16_t>(buf_id(0, r)));
         p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
@@ -282,10 +286,11 @@ void push_range(std::vector<Range>& v, uint32_t prog, int64_t lo, int64_t hi) {
 }  // namespace
 
 int staged_smem_bytes(const Lowered& lw) {
-    // 2 mbarriers per stage, padded to 128 bytes, then the stage tiles and the
-    // temporaries
-    return 128 + lw.tile_bytes * (lw.stages * lw.max_in + lw.max_tmp);
+    // the mbarrier area, then the stage tiles and the temporaries
+    return kBarrierBytes + lw.tile_bytes * (lw.stages * lw.max_in + lw.max_tmp);
 }
+
+int stream_smem_bytes(const Lowered& lw) { return kBarrierBytes + lw.stream_tile * lw.stream_stages; }
 
 void lower(const Schedule& S, Lowered& lw) {
     lw = Lowered();
@@ -319,29 +324,47 @@ void lower(const Schedule& S, Lowered& lw) {
             }
         }
     }
-    // tile size from the programs that own an aligned body
+    // A set whose programs are all chains / fp32 accumulations streams one
+    // rank tile at a time (rank-streaming kernel); sets with a DAG program
+    // stage all of an item's input tiles at once (staged kernel).
+    std::vector<bool> stream(sets.size(), true);
+    for (size_t k = 0; k < sets.size(); ++k)
+        for (auto& r : sets[k])
+            if (lw.progs[r.prog].kind == PK_DAG) stream[k] = false;
+    // staged-kernel geometry from the programs that own an aligned body
     lw.max_in = 1;
     lw.max_tmp = 0;
-    for (auto& rs : sets)
-        for (auto& r : rs) {
+    for (size_t k = 0; k < sets.size(); ++k)
+        for (auto& r : sets[k]) {
             const DevProg& d = lw.progs[r.prog];
             lw.max_in_all = std::max<int>(lw.max_in_all, d.n_in);
             lw.max_tmp_all = std::max<int>(lw.max_tmp_all, d.n_tmp);
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
-            if (a < e) {
+            if (a < e && !stream[k]) {
                 lw.max_in = std::max<int>(lw.max_in, d.n_in);
                 lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
             }
         }
-    lw.stages = kStages;
-    int64_t t = (kSmemBudget - 128) / (lw.stages * lw.max_in + lw.max_tmp);
+    // deepest pipeline (up to kStages) that keeps tiles >= 6 KB, else 2 stages
+    int64_t t = 0;
+    lw.stages = 2;
+    for (int st = std::max(kStages, 2); st >= 2; --st) {
+        t = (kSmemBudget - kBarrierBytes) / (st * lw.max_in + lw.max_tmp);
+        lw.stages = st;
+        if (t >= 6144) break;
+    }
+    t = (kSmemBudget - kBarrierBytes) / (lw.stages * lw.max_in + lw.max_tmp);
     t = std::min<int64_t>(t, kMaxTileBytes);
     t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
     lw.tile_bytes = static_cast<int>(t);
-    const int64_t tile_elems = t / es;
-    for (auto& rs : sets) {
+    lw.stream_tile = (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC) ? kStreamTileNarrow
+                                                                                    : kStreamTileBytes;
+    lw.stream_stages = std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile);
+    for (size_t k = 0; k < sets.size(); ++k) {
         LaunchSet ls;
-        for (auto& r : rs) {
+        ls.stream = stream[k];
+        const int64_t tile_elems = (stream[k] ? lw.stream_tile : lw.tile_bytes) / es;
+        for (auto& r : sets[k]) {
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
             if (a < e) {
                 if (r.lo < a) ls.edge.push_back({r.lo, static_cast<uint32_t>(a - r.lo), r.prog});

@@ -15,6 +15,7 @@ struct LaunchSet {
     std::vector<WorkItem> edge;      // unaligned heads / tails, element kernel
     std::vector<WorkItem> fallback;  // whole ranges for unaligned buffers
     uint64_t bytes = 0;              // algorithmic HBM bytes of the set
+    bool stream = false;             // bulk items run on the rank-streaming kernel
 };
 
 struct Lowered {
@@ -24,6 +25,8 @@ struct Lowered {
     std::vector<LaunchSet> sets;
     int tile_bytes = 0;   // bytes per input tile of the staged kernel
     int stages = 0;       // pipeline depth of the staged kernel
+    int stream_tile = 0;  // bytes per rank tile of the rank-streaming kernel
+    int stream_stages = 0;
     int max_in = 0;       // largest n_in of a program used by bulk items
     int max_tmp = 0;      // largest n_tmp of such a program
     int max_in_all = 0;   // largest n_in / n_tmp over all programs
@@ -33,15 +36,31 @@ struct Lowered {
     int launches = 0;     // launches per execute on aligned buffers
 };
 
-// Staged-kernel shared-memory budget (bytes) shared by lowering and launch.
-constexpr int kSmemBudget = 200 * 1024;
-constexpr int kMaxTileBytes = 32 * 1024;
-constexpr int kStages = 3;
+// Staged-kernel geometry shared by lowering and launch: shared-memory budget
+// per CTA, largest input tile, pipeline depth.
+#ifndef AR_SMEM_BUDGET
+#define AR_SMEM_BUDGET (200 * 1024)
+#endif
+#ifndef AR_MAX_TILE
+#define AR_MAX_TILE kMaxStagedTile
+#endif
+#ifndef AR_STAGES
+#define AR_STAGES 3
+#endif
+constexpr int kSmemBudget = AR_SMEM_BUDGET;
+constexpr int kMaxTileBytes = AR_MAX_TILE;
+constexpr int kStages = AR_STAGES;        // staged kernel: preferred pipeline depth
+// the rank-streaming kernel keeps no temporaries: its stages may use the
+// whole opt-in shared memory of a GB300 SM (227 KB)
+constexpr int kStreamSmemBudget = 227 * 1024;
+static_assert(kMaxTileBytes <= kMaxStagedTile, "staged tiles beyond what the consumers cover");
+constexpr int kMaxStages = kBarrierBytes / 16;
 
 // Builds the fused pass (one set) or the rounds (one set per round).
 void lower(const Schedule& S, Lowered& out);
 
-// Dynamic shared memory the staged kernel needs for a lowering.
+// Dynamic shared memory the staged / rank-streaming kernels need.
 int staged_smem_bytes(const Lowered& lw);
+int stream_smem_bytes(const Lowered& lw);
 
 }  // namespace ar

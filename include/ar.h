@@ -192,6 +192,7 @@ ar_status ar_plan_check(ar_plan_t plan);
 /* Static text for a status code (never NULL). */
 const char* ar_status_string(ar_status s);
 
+
 #ifdef __cplusplus
 }
 #endif
