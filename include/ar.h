@@ -192,6 +192,39 @@ ar_status ar_plan_check(ar_plan_t plan);
 /* Static text for a status code (never NULL). */
 const char* ar_status_string(ar_status s);
 
+/* ---- allreduce without device allocation ----------------------------------
+ * The pages have no counterpart to this call; it exists for callers that must
+ * not allocate device memory: a process whose GPU memory is already reserved
+ * in full by another allocator (a framework's caching pool), a service with a
+ * device-memory budget fixed at start-up, or a hot path that cannot pay for
+ * cudaMalloc / cudaFree's implicit device-wide synchronisation.  Such a caller
+ * cannot create a plan, because ar_plan_create allocates the plan's tables,
+ * status word and scratch.
+ *
+ * ar_allreduce_static compiles the schedule on the host (as ar_plan_create
+ * does) and runs the same kernels on the same rank buffers (same arguments,
+ * layout and result as ar_plan_create + ar_execute), but puts every byte of
+ * device scratch -- the status word, the tile-program tables and, for the step
+ * form, the second partial of a chunk -- in one file-scope static device array
+ * of AR_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine;
+ * host memory is used only while the schedule is compiled.
+ *   - Set-up: the first call made with a given device current resolves the
+ *     array's device address (cudaGetSymbolAddress) for that device; make that
+ *     first call before any stream capture.
+ *   - Limits: AR_ERR_UNSUPPORTED when the schedule's tables need more than
+ *     AR_STATIC_TABLE_BYTES or its partial slots more than what is left of the
+ *     array (AR_STATIC_SCRATCH_BYTES - AR_STATIC_TABLE_BYTES - 256 bytes).
+ *   - Sharing: every call reuses the one array and overwrites the previous
+ *     call's contents (the status word is cleared, the tables rewritten, on
+ *     `stream`).  Calls that can overlap on the GPU race with each other:
+ *     issue them on one stream, or order them with events.
+ *   - Errors as ar_plan_create + ar_execute; the bounded waits of the kernels
+ *     are not reported by this call. */
+#define AR_STATIC_SCRATCH_BYTES (32u << 20)
+#define AR_STATIC_TABLE_BYTES (1u << 20)
+ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo,
+                              const ar_params* params, void* const* rank_bufs, void* stream);
 
 #ifdef __cplusplus
 }
