@@ -292,6 +292,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 struct Stage {
     uint32_t full, empty;  // mbarrier arrays (shared addresses)
+    uint32_t ready;        // rank-streaming kernel: per stage, an item's result is in it
     uint32_t tiles;        // stage 0 tiles
     uint32_t tmps;         // temporaries
     uint32_t stage_bytes;
@@ -513,72 +514,98 @@ __device__ void stream_produce(const KernelArgs& a, const Stage& sm) {
     }
 }
 
-// Waits for rank tile g, hands its shared address to use(t), releases it.
-template <class Use>
-__device__ __forceinline__ bool stream_tile(const KernelArgs& a, const Stage& sm, uint32_t g, int ct, Use use) {
-    const uint32_t s = g % a.stages, ph = (g / a.stages) & 1u;
-    if (!mbar_wait(sm.full + 8 * s, ph)) {
-        atomicOr(a.status, kStatusWaitFull);
-        return false;
-    }
-    use(sm.tiles + s * a.tile_bytes);
-    __syncwarp();
-    if ((ct & 31) == 0) mbar_arrive(sm.empty + 8 * s);
-    return true;
-}
+#ifndef AR_TMA_STORE
+#define AR_TMA_STORE 1
+#endif
+constexpr bool kTmaStore = AR_TMA_STORE != 0;
+// warp 0 produces; with TMA stores warp 1 stores; the rest consume
+constexpr int kStreamLead = kTmaStore ? 2 : 1;
+constexpr int kStreamThreads = 32 * (kStreamLead + kConsumerWarps);
 
 __device__ __forceinline__ char* out_addr(const KernelArgs& a, const DevProg& pg, uint32_t o) {
     if (pg.flags & PF_OUT_ALL) return static_cast<char*>(a.bufs[o]);
     return buf_addr(a, a.refs[pg.out_off + o]);
 }
 
-template <int DT, int OP, int VPT>
-__device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
-    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
-    // bf16 fp32 accumulation holds 16 floats per vector: only the narrow
-    // instantiation runs it (the lowering picks the narrow tile for it)
-    constexpr bool kAccOk = !(DT == AR_BFLOAT16 && VPT > kStreamVptNarrow);
-    uint32_t g = 0;
+__device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// global <- shared bulk copy (TMA store), tracked by the issuing thread's
+// bulk async-groups
+__device__ __forceinline__ void bulk_store(char* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// Storer (lane 0 of warp 1): once the consumers have written an item's
+// result into the stage of its last rank tile, copy that tile to every
+// output buffer, and release the stage when the copies have read it.
+//
+// There is one `ready` barrier per stage: a stage holding an item's last tile
+// is refilled only after the storer has released it, so no consumer warp can
+// arrive twice within one phase of that stage's barrier.  ready_parity keeps
+// the phase parity of every stage's barrier.
+template <int ES>
+__device__ void stream_store(const KernelArgs& a, const Stage& sm) {
+    uint32_t g = 0, ready_parity = 0;
     for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
         const WorkItem w = a.items[it];
         const DevProg pg = a.progs[w.prog];
-        const uint32_t nvec = (w.count * ES) >> 4;
-        const int64_t off = w.elem * ES;
-        uint4 res[VPT];
-        if (pg.kind == PK_ACC) {
-            if (!kAccOk) {
-                atomicOr(a.status, kStatusBadProgram);
-                return;
-            }
-            AccStream<DT, OP> acc[kAccOk ? VPT : 1];
-            for (uint32_t i = 0; i < pg.n_in; ++i, ++g) {
-                const bool ok = stream_tile(a, sm, g, ct, [&](uint32_t t) {
-#pragma unroll
-                    for (int j = 0; j < (kAccOk ? VPT : 1); ++j) {
-                        const uint32_t v = ct + j * kConsumers;
-                        if (v < nvec) acc[j].feed(i, lds128(t + v * 16));
-                    }
-                });
-                if (!ok) return;
-            }
-#pragma unroll
-            for (int j = 0; j < (kAccOk ? VPT : 1); ++j) res[j] = acc[j].finish(pg.n_in);
-        } else {
-            const bool right = pg.kind == PK_CHAIN_R;
-            for (uint32_t i = 0; i < pg.n_in; ++i, ++g) {
-                const bool ok = stream_tile(a, sm, g, ct, [&](uint32_t t) {
-#pragma unroll
-                    for (int j = 0; j < VPT; ++j) {
-                        const uint32_t v = ct + j * kConsumers;
-                        if (v < nvec) {
-                            const uint4 x = lds128(t + v * 16);
-                            res[j] = i == 0 ? x : right ? vop<DT, OP>(x, res[j]) : vop<DT, OP>(res[j], x);
-                        }
-                    }
-                });
-                if (!ok) return;
-            }
+        g += pg.n_in;
+        const uint32_t s = (g - 1) % a.stages;
+        if (!mbar_wait(sm.ready + 8 * s, (ready_parity >> s) & 1u)) {
+            atomicOr(a.status, kStatusWaitFull);
+            break;
         }
+        ready_parity ^= 1u << s;
+        const uint32_t src = sm.tiles + s * a.tile_bytes;
+        const uint32_t nb = w.count * ES;
+        const int64_t off = w.elem * ES;
+        for (uint32_t o = 0; o < pg.n_out; ++o) bulk_store(out_addr(a, pg, o) + off, src, nb);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        mbar_arrive_count(sm.empty + 8 * s, kConsumerWarps);
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Waits for rank tile g; its shared address, or 0 after the bounded wait.
+__device__ __forceinline__ uint32_t stream_acquire(const KernelArgs& a, const Stage& sm, uint32_t g) {
+    const uint32_t s = g % a.stages, ph = (g / a.stages) & 1u;
+    if (!mbar_wait(sm.full + 8 * s, ph)) {
+        atomicOr(a.status, kStatusWaitFull);
+        return 0;
+    }
+    return sm.tiles + s * a.tile_bytes;
+}
+
+// After a tile that is not an item's last input: give the stage back.
+__device__ __forceinline__ void stream_release(const KernelArgs& a, const Stage& sm, uint32_t g, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.empty + 8 * (g % a.stages));
+}
+
+// After an item's last input: with TMA stores, write the result over this
+// thread's own vectors of the tile and hand the stage to the storer (which
+// copies it to every output and then gives the stage back); otherwise give
+// the stage back and store the result directly.
+template <int VPT>
+__device__ __forceinline__ void stream_finish(const KernelArgs& a, const Stage& sm, uint32_t g, uint32_t t,
+                                              const DevProg& pg, int64_t off, uint32_t nvec, int ct,
+                                              const uint4 (&res)[VPT]) {
+    const int lane = ct & 31;
+    if (kTmaStore) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const uint32_t v = ct + j * kConsumers;
+            if (v < nvec) sts128(t + v * 16, res[j]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.ready + 8 * (g % a.stages));
+    } else {
+        stream_release(a, sm, g, lane);
         for (uint32_t o = 0; o < pg.n_out; ++o) {
             char* dst = out_addr(a, pg, o) + off;
 #pragma unroll
@@ -591,12 +618,83 @@ __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
 }
 
 template <int DT, int OP, int VPT>
-__global__ void __launch_bounds__(kStagedThreads, 1) stream_kernel(const __grid_constant__ KernelArgs a) {
+__device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    // bf16 fp32 accumulation holds 16 floats per vector: only the narrow
+    // instantiation runs it (the lowering picks the narrow tile for it)
+    constexpr bool kAccOk = !(DT == AR_BFLOAT16 && VPT > kStreamVptNarrow);
+    constexpr int NA = kAccOk ? VPT : 1;
+    const int lane = ct & 31;
+    uint32_t g = 0;
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        const uint32_t nvec = (w.count * ES) >> 4;
+        const int64_t off = w.elem * ES;
+        uint4 res[VPT];
+        if (pg.kind == PK_ACC) {
+            if (!kAccOk) {
+                atomicOr(a.status, kStatusBadProgram);
+                return;
+            }
+            AccStream<DT, OP> acc[NA];
+            for (uint32_t i = 0; i < pg.n_in; ++i, ++g) {
+                const uint32_t t = stream_acquire(a, sm, g);
+                if (!t) return;
+#pragma unroll
+                for (int j = 0; j < NA; ++j) {
+                    const uint32_t v = ct + j * kConsumers;
+                    if (v < nvec) acc[j].feed(i, lds128(t + v * 16));
+                }
+                if (i + 1 < pg.n_in) {
+                    stream_release(a, sm, g, lane);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NA; ++j) res[j] = acc[j].finish(pg.n_in);
+                    stream_finish<VPT>(a, sm, g, t, pg, off, nvec, ct, res);
+                }
+            }
+        } else {
+            const bool right = pg.kind == PK_CHAIN_R;
+            for (uint32_t i = 0; i < pg.n_in; ++i, ++g) {
+                const uint32_t t = stream_acquire(a, sm, g);
+                if (!t) return;
+                if (i == 0) {
+#pragma unroll
+                    for (int j = 0; j < VPT; ++j) {
+                        const uint32_t v = ct + j * kConsumers;
+                        if (v < nvec) res[j] = lds128(t + v * 16);
+                    }
+                } else if (right) {
+#pragma unroll
+                    for (int j = 0; j < VPT; ++j) {
+                        const uint32_t v = ct + j * kConsumers;
+                        if (v < nvec) res[j] = vop<DT, OP>(lds128(t + v * 16), res[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VPT; ++j) {
+                        const uint32_t v = ct + j * kConsumers;
+                        if (v < nvec) res[j] = vop<DT, OP>(res[j], lds128(t + v * 16));
+                    }
+                }
+                if (i + 1 < pg.n_in)
+                    stream_release(a, sm, g, lane);
+                else
+                    stream_finish<VPT>(a, sm, g, t, pg, off, nvec, ct, res);
+            }
+        }
+    }
+}
+
+template <int DT, int OP, int VPT>
+__global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
     Stage sm;
     sm.full = smem_addr(smem);
     sm.empty = sm.full + 8 * a.stages;
+    sm.ready = sm.empty + 8 * a.stages;
     sm.tiles = sm.full + kBarrierBytes;
     sm.stage_bytes = a.tile_bytes;
     sm.tmps = 0;
@@ -604,15 +702,21 @@ __global__ void __launch_bounds__(kStagedThreads, 1) stream_kernel(const __grid_
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(sm.full + 8 * s, 1);
             mbar_init(sm.empty + 8 * s, kConsumerWarps);
+            mbar_init(sm.ready + 8 * s, kConsumerWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
         stream_produce<ES>(a, sm);
         return;
     }
-    stream_consume<DT, OP, VPT>(a, sm, threadIdx.x - 32);
+    if (kTmaStore && warp == 1) {
+        if (threadIdx.x == 32) stream_store<ES>(a, sm);
+        return;
+    }
+    stream_consume<DT, OP, VPT>(a, sm, threadIdx.x - 32 * kStreamLead);
 }
 
 // --------------------------------------------------------- element kernel
@@ -748,8 +852,9 @@ cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int 
 cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
     // the rank tile fixes the vectors per consumer thread
     if (a.tile_bytes != kStreamTileBytes && a.tile_bytes != kStreamTileNarrow) return cudaErrorInvalidValue;
+    if (a.stages < 1 || a.stages > 32 || 24 * a.stages > kBarrierBytes) return cudaErrorInvalidValue;
     KernelFn f = kernel_for(dtype, op, a.tile_bytes == kStreamTileBytes ? K_STREAM : K_STREAM_NARROW);
-    f<<<grid, kStagedThreads, smem, st>>>(a);
+    f<<<grid, kStreamThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 

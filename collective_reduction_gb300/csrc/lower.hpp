@@ -54,7 +54,8 @@ constexpr int kStages = AR_STAGES;        // staged kernel: preferred pipeline d
 // whole opt-in shared memory of a GB300 SM (227 KB)
 constexpr int kStreamSmemBudget = 227 * 1024;
 static_assert(kMaxTileBytes <= kMaxStagedTile, "staged tiles beyond what the consumers cover");
-constexpr int kMaxStages = kBarrierBytes / 16;
+// full, empty and ready barriers (8 bytes each) per stage in the barrier area
+constexpr int kMaxStages = kBarrierBytes / 24;
 
 // Builds the fused pass (one set) or the rounds (one set per round).
 void lower(const Schedule& S, Lowered& out);

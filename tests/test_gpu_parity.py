@@ -122,6 +122,23 @@ def test_config5_ring_small_sizes(P, nbytes, dtype):
         assert normwise_rel_err(y, ref) <= tol
 
 
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("P", [2, 3, 7])
+def test_many_items_per_cta(P, dtype):
+    """Tens of rank-streaming items per CTA at small P, where consumer warps
+    can drift a whole item apart: the pipeline's barriers must keep every
+    item's result intact (full oracle comparison, plus the status word)."""
+    n = (1 << 23) + 5
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=P + 100)
+    check_faithful(bufs, dtype, "sum", "ring", "fused")
+    got = engine(bufs, dtype, "sum", "ring", order="fp32acc")
+    ref = direct_f64(bufs, "sum", dtype)
+    from oracle.elementops import bf16_to_f32
+    tol = 1e-6 if dtype == "float32" else 4e-3
+    for g in got:
+        assert normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) <= tol
+
+
 # ---- every (dtype, op) through a chain and a DAG program -------------------------------
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
