@@ -39,6 +39,18 @@ struct ar_plan_s {
         bool stream;
     };
     std::vector<Set> sets;
+    // element windows of a fused plan for the pipelined host path: window w
+    // covers elements [lo, hi), bulk items [b0, b1) and edge items [e0, e1)
+    struct Window {
+        int64_t lo, hi;
+        uint32_t b0, b1, e0, e1;
+    };
+    std::vector<Window> windows;
+    // copy streams of the pipelined host path, created on first use: the
+    // copies of rank r go to stream r mod kCopyStreams in each direction
+    static constexpr int kCopyStreams = 1;  // more streams measured slower on GB300
+    cudaStream_t s_in[kCopyStreams] = {}, s_out[kCopyStreams] = {};
+    std::vector<cudaEvent_t> events;  // (2 kCopyStreams + 1) per window + 1
     const ar::DevProg* d_progs = nullptr;
     const uint16_t* d_refs = nullptr;
     const uint32_t* d_ins = nullptr;
@@ -84,10 +96,108 @@ size_t put(std::vector<char>& blob, const std::vector<T>& v) {
 
 void destroy_plan(ar_plan_s* p) {
     if (!p) return;
+    for (cudaEvent_t e : p->events) cudaEventDestroy(e);
+    for (int k = 0; k < ar_plan_s::kCopyStreams; ++k) {
+        if (p->s_in[k]) cudaStreamDestroy(p->s_in[k]);
+        if (p->s_out[k]) cudaStreamDestroy(p->s_out[k]);
+    }
     if (p->d_tables) cudaFree(p->d_tables);
     if (p->d_scratch) cudaFree(p->d_scratch);
     if (p->d_status) cudaFree(p->d_status);
     delete p;
+}
+
+// Checks P device pointers: non-null, element-aligned, pairwise disjoint.
+ar_status validate_bufs(const ar_plan_s* plan, void* const* bufs, bool* aligned16) {
+    const ar::Schedule& S = plan->S;
+    const uint64_t es = ar::esize_of(S.dtype);
+    const uint64_t bytes = static_cast<uint64_t>(S.n) * es;
+    std::vector<std::pair<uintptr_t, int>> addr;
+    bool aligned = true;
+    for (int r = 0; r < S.P; ++r) {
+        uintptr_t a = reinterpret_cast<uintptr_t>(bufs[r]);
+        if (!a || a % es) return AR_ERR_INVALID_ARG;
+        aligned = aligned && a % 16 == 0;
+        addr.emplace_back(a, r);
+    }
+    std::sort(addr.begin(), addr.end());
+    for (int r = 0; r + 1 < S.P; ++r)
+        if (addr[r].first == addr[r + 1].first || addr[r].first + bytes > addr[r + 1].first) return AR_ERR_INVALID_ARG;
+    *aligned16 = aligned;
+    return AR_OK;
+}
+
+void base_args(const ar_plan_s* plan, void* const* bufs, ar::KernelArgs& a) {
+    std::memset(&a, 0, sizeof(a));
+    for (int r = 0; r < plan->S.P; ++r) a.bufs[r] = bufs[r];
+    a.scratch = plan->d_scratch;
+    a.slot_stride = plan->slot_stride;
+    a.progs = plan->d_progs;
+    a.refs = plan->d_refs;
+    a.ins = plan->d_ins;
+    a.status = plan->d_status;
+    a.P = plan->S.P;
+}
+
+// Launches bulk items [b0, b1) and edge items [e0, e1) of one set.
+cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan_s::Set& s, uint32_t b0, uint32_t b1,
+                         uint32_t e0, uint32_t e1, cudaStream_t st) {
+    const ar::Schedule& S = plan->S;
+    cudaError_t e = cudaSuccess;
+    if (b1 > b0) {
+        a.items = s.bulk + b0;
+        a.n_items = b1 - b0;
+        const int grid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms));
+        if (s.stream) {
+            a.tile_bytes = plan->L.stream_tile;
+            a.stages = plan->L.stream_stages;
+            a.flags = plan->L.stream_tma_store ? ar::kArgTmaStore : 0;
+            a.max_in = 1;
+            a.max_tmp = 0;
+            e = ar::launch_stream(S.dtype, S.op, a, grid, plan->smem_stream, st);
+        } else {
+            a.tile_bytes = plan->L.tile_bytes;
+            a.stages = plan->L.stages;
+            a.max_in = plan->L.max_in;
+            a.max_tmp = plan->L.max_tmp;
+            e = ar::launch_staged(S.dtype, S.op, a, grid, plan->smem_staged, st);
+        }
+    }
+    if (e == cudaSuccess && e1 > e0) {
+        a.items = s.edge + e0;
+        a.n_items = e1 - e0;
+        a.max_in = plan->L.max_in_all;
+        a.max_tmp = plan->L.max_tmp_all;
+        e = ar::launch_elementwise(S.dtype, S.op, a, plan->smem_elem, st);
+    }
+    return e;
+}
+
+// Element windows for the pipelined host path (fused plans): about 128 MB of
+// rank data per window, at most 32 windows, cut at bulk-item boundaries.
+void make_windows(ar_plan_s* p) {
+    p->windows.clear();
+    if (p->L.sets.size() != 1) return;
+    const ar::LaunchSet& ls = p->L.sets[0];
+    const uint64_t nb = ls.bulk.size();
+    const uint64_t total = static_cast<uint64_t>(p->S.P) * p->S.n * ar::esize_of(p->S.dtype);
+    uint64_t W = std::min<uint64_t>({total / (128ull << 20), 32, nb});
+    if (W < 2) return;
+    auto first_edge_at = [&](int64_t x) {
+        uint32_t k = 0;
+        while (k < ls.edge.size() && ls.edge[k].elem < x) ++k;
+        return k;
+    };
+    for (uint64_t w = 0; w < W; ++w) {
+        ar_plan_s::Window win;
+        win.b0 = static_cast<uint32_t>(nb * w / W);
+        win.b1 = static_cast<uint32_t>(nb * (w + 1) / W);
+        win.lo = w == 0 ? 0 : ls.bulk[win.b0].elem;
+        win.hi = w + 1 == W ? p->S.n : ls.bulk[win.b1].elem;
+        win.e0 = first_edge_at(win.lo);
+        win.e1 = w + 1 == W ? static_cast<uint32_t>(ls.edge.size()) : first_edge_at(win.hi);
+        p->windows.push_back(win);
+    }
 }
 
 }  // namespace
@@ -231,6 +341,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             s.stream = L.sets[i].stream;
             p->sets.push_back(s);
         }
+        make_windows(p);
         *out = p;
         return AR_OK;
     } catch (const std::bad_alloc&) {
@@ -261,61 +372,18 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info) {
 ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
     if (!plan || !rank_bufs) return AR_ERR_INVALID_ARG;
     const ar::Schedule& S = plan->S;
-    const int P = S.P;
-    const uint64_t es = ar::esize_of(S.dtype);
-    const uint64_t bytes = static_cast<uint64_t>(S.n) * es;
     if (S.n == 0) return AR_OK;  // nothing to touch: any pointers are accepted
-    std::vector<std::pair<uintptr_t, int>> addr;
-    bool aligned = true;
-    for (int r = 0; r < P; ++r) {
-        uintptr_t a = reinterpret_cast<uintptr_t>(rank_bufs[r]);
-        if (!a || a % es) return AR_ERR_INVALID_ARG;
-        aligned = aligned && a % 16 == 0;
-        addr.emplace_back(a, r);
-    }
-    std::sort(addr.begin(), addr.end());
-    for (int r = 0; r + 1 < P; ++r)
-        if (addr[r].first == addr[r + 1].first || addr[r].first + bytes > addr[r + 1].first) return AR_ERR_INVALID_ARG;
-    if (P == 1 || S.n == 0) return AR_OK;
+    bool aligned = false;
+    ar_status v = validate_bufs(plan, rank_bufs, &aligned);
+    if (v != AR_OK) return v;
+    if (S.P == 1) return AR_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ar::KernelArgs a;
-    std::memset(&a, 0, sizeof(a));
-    for (int r = 0; r < P; ++r) a.bufs[r] = rank_bufs[r];
-    a.scratch = plan->d_scratch;
-    a.slot_stride = plan->slot_stride;
-    a.progs = plan->d_progs;
-    a.refs = plan->d_refs;
-    a.ins = plan->d_ins;
-    a.status = plan->d_status;
-    a.P = P;
+    base_args(plan, rank_bufs, a);
     for (const auto& s : plan->sets) {
         cudaError_t e = cudaSuccess;
         if (aligned) {
-            if (s.n_bulk) {
-                a.items = s.bulk;
-                a.n_items = s.n_bulk;
-                const int grid = static_cast<int>(std::min<uint32_t>(s.n_bulk, plan->num_sms));
-                if (s.stream) {
-                    a.tile_bytes = plan->L.stream_tile;
-                    a.stages = plan->L.stream_stages;
-                    a.max_in = 1;
-                    a.max_tmp = 0;
-                    e = ar::launch_stream(S.dtype, S.op, a, grid, plan->smem_stream, st);
-                } else {
-                    a.tile_bytes = plan->L.tile_bytes;
-                    a.stages = plan->L.stages;
-                    a.max_in = plan->L.max_in;
-                    a.max_tmp = plan->L.max_tmp;
-                    e = ar::launch_staged(S.dtype, S.op, a, grid, plan->smem_staged, st);
-                }
-            }
-            if (e == cudaSuccess && s.n_edge) {
-                a.items = s.edge;
-                a.n_items = s.n_edge;
-                a.max_in = plan->L.max_in_all;
-                a.max_tmp = plan->L.max_tmp_all;
-                e = ar::launch_elementwise(S.dtype, S.op, a, plan->smem_elem, st);
-            }
+            e = launch_range(plan, a, s, 0, s.n_bulk, 0, s.n_edge, st);
         } else if (s.n_fallback) {
             a.items = s.fallback;
             a.n_items = s.n_fallback;
@@ -330,22 +398,94 @@ ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
 
 ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* dev_bufs, void* stream) {
     if (!plan || !host_bufs || !dev_bufs) return AR_ERR_INVALID_ARG;
-    const int P = plan->S.P;
-    const size_t bytes = static_cast<size_t>(plan->S.n) * ar::esize_of(plan->S.dtype);
+    const ar::Schedule& S = plan->S;
+    const int P = S.P;
+    const size_t es = ar::esize_of(S.dtype);
+    const size_t bytes = static_cast<size_t>(S.n) * es;
     for (int r = 0; r < P; ++r)
         if (!host_bufs[r]) return AR_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    for (int r = 0; r < P; ++r) {
-        cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_bufs[r], bytes, cudaMemcpyHostToDevice, st);
+    bool aligned = false;
+    if (S.n > 0) {
+        ar_status v = validate_bufs(plan, dev_bufs, &aligned);
+        if (v != AR_OK) return v;
+    }
+    if (!aligned || plan->windows.size() < 2 || P == 1) {
+        // one pass: every copy in, the allreduce, every copy out
+        for (int r = 0; r < P; ++r) {
+            cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_bufs[r], bytes, cudaMemcpyHostToDevice, st);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        ar_status s = ar_execute(plan, dev_bufs, stream);
+        if (s != AR_OK) return s;
+        for (int r = 0; r < P; ++r) {
+            cudaError_t e = cudaMemcpyAsync(host_bufs[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, st);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        return cuda_status(cudaStreamSynchronize(st));
+    }
+    // Pipelined: every element's reduction depends only on that element of
+    // every rank, so the buffers are processed in windows.  Window w's copies
+    // in run on the s_in streams, its reduction on `stream`, its copies out on
+    // the s_out streams; copies of neighbouring windows overlap the reduction
+    // of window w, and the per-rank copies of a window spread over several
+    // streams (copy engines) in each direction.
+    constexpr int K = ar_plan_s::kCopyStreams;
+    const size_t W = plan->windows.size();
+    const size_t per_win = 2 * K + 1;
+    cudaError_t e = cudaSuccess;
+    if (plan->events.size() != per_win * W + 1) {
+        for (int k = 0; k < K && e == cudaSuccess; ++k) {
+            if (!plan->s_in[k]) e = cudaStreamCreateWithFlags(&plan->s_in[k], cudaStreamNonBlocking);
+            if (e == cudaSuccess && !plan->s_out[k]) e = cudaStreamCreateWithFlags(&plan->s_out[k], cudaStreamNonBlocking);
+        }
+        for (cudaEvent_t x : plan->events) cudaEventDestroy(x);
+        plan->events.clear();
+        for (size_t k = 0; e == cudaSuccess && k < per_win * W + 1; ++k) {
+            cudaEvent_t ev;
+            e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e == cudaSuccess) plan->events.push_back(ev);
+        }
         if (e != cudaSuccess) return cuda_status(e);
     }
-    ar_status s = ar_execute(plan, dev_bufs, stream);
-    if (s != AR_OK) return s;
-    for (int r = 0; r < P; ++r) {
-        cudaError_t e = cudaMemcpyAsync(host_bufs[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, st);
-        if (e != cudaSuccess) return cuda_status(e);
+    cudaEvent_t* ev = plan->events.data();
+    cudaEvent_t start = ev[per_win * W];
+    auto chk = [&](cudaError_t x) {
+        if (e == cudaSuccess) e = x;
+    };
+    chk(cudaEventRecord(start, st));
+    for (int k = 0; k < K; ++k) {
+        chk(cudaStreamWaitEvent(plan->s_in[k], start, 0));
+        chk(cudaStreamWaitEvent(plan->s_out[k], start, 0));
     }
-    return cuda_status(cudaStreamSynchronize(st));
+    ar::KernelArgs a;
+    base_args(plan, dev_bufs, a);
+    const ar_plan_s::Set& set = plan->sets[0];
+    for (size_t w = 0; w < W && e == cudaSuccess; ++w) {
+        const ar_plan_s::Window& win = plan->windows[w];
+        cudaEvent_t* in_done = ev + per_win * w;      // K events
+        cudaEvent_t reduced = ev[per_win * w + K];
+        cudaEvent_t* out_done = ev + per_win * w + K + 1;  // K events
+        const size_t off = static_cast<size_t>(win.lo) * es, len = static_cast<size_t>(win.hi - win.lo) * es;
+        for (int r = 0; r < P; ++r)
+            chk(cudaMemcpyAsync(static_cast<char*>(dev_bufs[r]) + off, static_cast<const char*>(host_bufs[r]) + off,
+                                len, cudaMemcpyHostToDevice, plan->s_in[r % K]));
+        for (int k = 0; k < K; ++k) {
+            chk(cudaEventRecord(in_done[k], plan->s_in[k]));
+            chk(cudaStreamWaitEvent(st, in_done[k], 0));
+        }
+        if (e == cudaSuccess) e = launch_range(plan, a, set, win.b0, win.b1, win.e0, win.e1, st);
+        chk(cudaEventRecord(reduced, st));
+        for (int k = 0; k < K; ++k) chk(cudaStreamWaitEvent(plan->s_out[k], reduced, 0));
+        for (int r = 0; r < P; ++r)
+            chk(cudaMemcpyAsync(static_cast<char*>(host_bufs[r]) + off, static_cast<const char*>(dev_bufs[r]) + off,
+                                len, cudaMemcpyDeviceToHost, plan->s_out[r % K]));
+        for (int k = 0; k < K; ++k) chk(cudaEventRecord(out_done[k], plan->s_out[k]));
+    }
+    if (e == cudaSuccess)
+        for (int k = 0; k < K; ++k) chk(cudaStreamWaitEvent(st, ev[per_win * (W - 1) + K + 1 + k], 0));
+    chk(cudaStreamSynchronize(st));
+    return cuda_status(e);
 }
 
 ar_status ar_plan_check(ar_plan_t plan) {

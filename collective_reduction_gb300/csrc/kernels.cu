@@ -514,12 +514,8 @@ __device__ void stream_produce(const KernelArgs& a, const Stage& sm) {
     }
 }
 
-#ifndef AR_TMA_STORE
-#define AR_TMA_STORE 1
-#endif
-constexpr bool kTmaStore = AR_TMA_STORE != 0;
-// warp 0 produces; with TMA stores warp 1 stores; the rest consume
-constexpr int kStreamLead = kTmaStore ? 2 : 1;
+// warp 0 produces, warp 1 stores (TMA-store epilogue only), the rest consume
+constexpr int kStreamLead = 2;
 constexpr int kStreamThreads = 32 * (kStreamLead + kConsumerWarps);
 
 __device__ __forceinline__ char* out_addr(const KernelArgs& a, const DevProg& pg, uint32_t o) {
@@ -595,7 +591,7 @@ __device__ __forceinline__ void stream_finish(const KernelArgs& a, const Stage& 
                                               const DevProg& pg, int64_t off, uint32_t nvec, int ct,
                                               const uint4 (&res)[VPT]) {
     const int lane = ct & 31;
-    if (kTmaStore) {
+    if (a.flags & kArgTmaStore) {
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const uint32_t v = ct + j * kConsumers;
@@ -712,8 +708,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_
         stream_produce<ES>(a, sm);
         return;
     }
-    if (kTmaStore && warp == 1) {
-        if (threadIdx.x == 32) stream_store<ES>(a, sm);
+    if (warp == 1) {
+        if (threadIdx.x == 32 && (a.flags & kArgTmaStore)) stream_store<ES>(a, sm);
         return;
     }
     stream_consume<DT, OP, VPT>(a, sm, threadIdx.x - 32 * kStreamLead);

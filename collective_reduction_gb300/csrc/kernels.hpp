@@ -26,7 +26,12 @@ struct KernelArgs {
     int stages;                // staged kernel: pipeline depth
     int max_in;                // staged: input tiles per stage; element kernel: value rows
     int max_tmp;               // staged: temporary tiles; element kernel: temp rows
+    int flags;                 // kArg* bits
 };
+
+// KernelArgs::flags: the rank-streaming kernel writes results back to shared
+// memory and copies them out with TMA bulk stores (else 128-bit stores)
+constexpr int kArgTmaStore = 1;
 
 // Status word bits written by the kernels.
 constexpr int kStatusWaitFull = 1;   // a consumer gave up waiting for a stage

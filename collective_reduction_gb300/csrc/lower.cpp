@@ -360,6 +360,15 @@ void lower(const Schedule& S, Lowered& lw) {
     lw.stream_tile = (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC) ? kStreamTileNarrow
                                                                                     : kStreamTileBytes;
     lw.stream_stages = std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile);
+    // The TMA-store epilogue holds an item's last stage until its outputs are
+    // copied out: measured faster with few outputs per item (and for bf16
+    // fp32 accumulation, whose direct stores are costly), slower with many.
+    int max_out = 0;
+    for (size_t k = 0; k < sets.size(); ++k)
+        if (stream[k])
+            for (auto& r : sets[k]) max_out = std::max<int>(max_out, lw.progs[r.prog].n_out);
+    lw.stream_tma_store =
+        max_out <= 4 || (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC);
     for (size_t k = 0; k < sets.size(); ++k) {
         LaunchSet ls;
         ls.stream = stream[k];

@@ -27,6 +27,7 @@ struct Lowered {
     int stages = 0;       // pipeline depth of the staged kernel
     int stream_tile = 0;  // bytes per rank tile of the rank-streaming kernel
     int stream_stages = 0;
+    bool stream_tma_store = false;  // rank-streaming kernel: TMA bulk-store epilogue
     int max_in = 0;       // largest n_in of a program used by bulk items
     int max_tmp = 0;      // largest n_tmp of such a program
     int max_in_all = 0;   // largest n_in / n_tmp over all programs

@@ -179,9 +179,15 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info);
  * ar_plan_check. */
 ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream);
 /* End-to-end variant: copies P host buffers to the P device buffers, runs the
- * allreduce and copies every device buffer back to its host buffer, all
- * enqueued on `stream` (one cudaMemcpyAsync per buffer and direction), then
- * synchronises the stream.  host_bufs should be pinned for full speed. */
+ * allreduce and copies every device buffer back to its host buffer, then
+ * synchronises `stream`.  Large fused plans on 16-byte-aligned device buffers
+ * are processed in element windows of about 128 MB: the copies in of window
+ * w+1 and out of window w-1 run on two internal streams of the plan while
+ * window w is reduced on `stream` (every element's result depends only on
+ * that element of every rank).  Otherwise: all copies in, the allreduce, all
+ * copies out, on `stream`.  One cudaMemcpyAsync per buffer, window and
+ * direction.  host_bufs should be pinned for full speed.  Calls on one plan
+ * must not overlap (they share the internal streams). */
 ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* dev_bufs,
                           void* stream);
 /* Synchronises the device and reads the plan's device status word: AR_OK, or

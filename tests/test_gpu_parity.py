@@ -256,6 +256,35 @@ def test_execute_host_end_to_end():
     plan.close()
 
 
+@pytest.mark.parametrize("order", ["faithful", "fp32acc"])
+def test_execute_host_pipelined_windows(order):
+    """Large enough for the windowed host path (copies overlapped with the
+    reduction, several windows), ragged so windows also carry edge items."""
+    import torch
+    import collective_reduction_gb300 as ar
+    P, n = 7, 10_000_003
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2, seed=77)
+    host = [torch.from_numpy(b.copy()).pin_memory() for b in bufs]
+    dev = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(P)]
+    plan = ar.Plan(P, n, "float32", "sum", "ring", order=order)
+    for _ in range(2):  # second call reuses the plan's streams and events
+        for r in range(P):
+            host[r].copy_(torch.from_numpy(bufs[r]))
+        plan.execute_host(host, dev)
+        plan.check()
+        if order == "faithful":
+            want = oracle.run("ring", bufs, Arith("sum", "float32")).bufs
+            for r in range(P):
+                assert_bit_equal(host[r].numpy(), want[r], "float32", f"host rank {r}")
+                assert_bit_equal(dev[r].cpu().numpy(), want[r], "float32", f"dev rank {r}")
+        else:
+            ref = direct_f64(bufs, "sum", "float32")
+            for r in range(P):
+                assert normwise_rel_err(host[r].numpy(), ref) <= 1e-6
+                assert np.array_equal(host[r].numpy(), dev[r].cpu().numpy())
+    plan.close()
+
+
 def test_repeated_execute_and_streams():
     """Back-to-back executes on a side stream, then on the default stream."""
     import torch
