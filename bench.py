@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", default=None, help="write the size sweep as JSON lines to this file")
+    ap.add_argument("--configs", default=None,
+                    help="time every schedule of the parity configurations, JSON lines to this file")
     return ap.parse_args()
 
 
@@ -507,13 +509,14 @@ def run_sweep(a, path):
                             del g
                         else:
                             reps = []
-                            for _ in range(20):
+                            for _ in range(5):
                                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                                 e0.record()
-                                plan.execute(dev)
+                                for _ in range(10):
+                                    plan.execute(dev)
                                 e1.record()
                                 torch.cuda.synchronize()
-                                reps.append(e0.elapsed_time(e1))
+                                reps.append(e0.elapsed_time(e1) / 10)
                             ms = statistics.median(reps)
                         plan.check()
                         row = {"dtype": dtype, "P": P, "bytes_per_rank": S, "form": form, "order": order,
@@ -529,6 +532,104 @@ def run_sweep(a, path):
                     torch.cuda.empty_cache()
 
 
+def config_cases():
+    """The schedules of the four parity configurations, each in every form."""
+    cases = []
+    for form in ("fused", "step"):
+        cases.append(("config1", 3, 1024, "int32", "sum", "ring", {"form": form}, ("uniform_int", 1.0)))
+    for op in ("sum", "max"):
+        for algo, kw in [("rh", {}), ("rd", {}), ("binomial", {})] + [("hybrid", {"k1": k}) for k in range(4)]:
+            for form in ("fused", "step"):
+                cases.append(("config2", 8, 1 << 20, "float32", op, algo, dict(kw, form=form), ("normal", 1.0)))
+    for P in (7, 12):
+        L = (P - 1).bit_length()
+        for n in (106, 1 << 20):
+            for r in range(L + 1):
+                for form in ("fused", "step"):
+                    cases.append(("config3", P, n, "float32", "sum", "generalized", {"r": r, "form": form},
+                                  ("normal", 1e-2)))
+    for kw in ({"form": "fused"}, {"form": "fused", "order": "fp32acc"}, {"form": "step"}):
+        cases.append(("config4", 5, 1 << 24, "bfloat16", "sum", "ahc", dict(kw, group_sizes=[2, 3]),
+                      ("normal", 1e-3)))
+    return cases
+
+
+def run_configs(a, path):
+    """Times every schedule of configurations 1-4 on the GPU (10 back-to-back
+    calls, median of 5 CUDA-event measurements, launch overhead included) and
+    the oracle on the same inputs on the host, and checks the GPU result
+    against the oracle's bit for bit (fp32-accumulate: within tolerance)."""
+    import numpy as np
+    import torch
+
+    import ar_synth
+    import collective_reduction_gb300 as ar
+    import oracle
+    from oracle.direct import direct_f64, normwise_rel_err
+    from oracle.elementops import Arith, bf16_to_f32
+    torch.cuda.set_device(0)
+    peak, _ = measured_peak()
+    inputs = {}
+    with open(path, "w") as out:
+        for cfg, P, n, dtype, op, algo, kw, (dist, sigma) in config_cases():
+            key = (P, n, dtype, dist, sigma)
+            if key not in inputs:
+                inputs = {key: ar_synth.rank_inputs(P, n, dtype, dist, sigma=sigma)}
+            host = inputs[key]
+            tdt = {"int32": torch.int32, "float32": torch.float32, "bfloat16": torch.int16}[dtype]
+            dev0 = [torch.from_numpy(h.view(np.int16) if dtype == "bfloat16" else h).to("cuda") for h in host]
+            dev = [t.clone() for t in dev0]
+            if dtype == "bfloat16":
+                dev = [t.view(torch.bfloat16) for t in dev]
+            plan = ar.Plan(P, n, dtype, op, algo, **kw)
+            info = plan.info()
+            plan.execute(dev)
+            torch.cuda.synchronize()
+            plan.check()
+            got = [t.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bfloat16" else t.cpu().numpy()
+                   for t in dev]
+            okw = {k: v for k, v in kw.items() if k in ("r", "k1", "group_sizes")}
+            t0 = time.perf_counter()
+            want = oracle.run(algo, host, Arith(op, dtype), **okw)
+            oracle_s = time.perf_counter() - t0
+            if kw.get("order") == "fp32acc":
+                ref = direct_f64(host, op, dtype)
+                err = max(normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) for g in got)
+                ok = err <= (1e-6 if dtype == "float32" else 4e-3)
+            else:
+                def bits(x):
+                    x = np.ascontiguousarray(x)
+                    return x if x.dtype == np.uint16 else x.view(np.uint32)
+                ok = all(np.array_equal(bits(g), bits(w)) for g, w in zip(got, want.bufs))
+            for _ in range(3):
+                plan.execute(dev)
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(10):
+                    plan.execute(dev)
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / 10)
+            plan.check()
+            ms = statistics.median(ts)
+            S = n * esize(dtype)
+            row = {"config": cfg, "P": P, "n": n, "dtype": dtype, "op": op, "algo": algo,
+                   "params": {k: v for k, v in kw.items()}, "verified": bool(ok),
+                   "steps": info["steps"], "launches": info["launches"], "us_per_call": round(ms * 1e3, 2),
+                   "allreduced_GBps": round(P * S / (ms / 1e3) / 1e9, 2),
+                   "hbm_bytes_per_call": info["hbm_bytes"],
+                   "hbm_GBps": round(info["hbm_bytes"] / (ms / 1e3) / 1e9, 1),
+                   "frac_of_measured": round(info["hbm_bytes"] / (ms / 1e3) / 1e9 / peak, 4),
+                   "oracle_s": round(oracle_s, 4),
+                   "oracle_GBps": round(P * S / oracle_s / 1e9, 4)}
+            out.write(json.dumps(row) + "\n")
+            out.flush()
+            plan.close()
+
+
 def main():
     a = parse()
     if a.impl == "reference":
@@ -536,6 +637,9 @@ def main():
         return
     if a.sweep:
         run_sweep(a, a.sweep)
+        return
+    if a.configs:
+        run_configs(a, a.configs)
         return
     run_ours(a)
 

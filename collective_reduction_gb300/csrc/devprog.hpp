@@ -5,7 +5,11 @@
 //   CHAIN_R  acc = in[0]; acc = in[i] (+) acc for i = 1..n_in-1   (ring order)
 //   CHAIN_L  acc = in[0]; acc = acc (+) in[i]
 //   ACC      fp32 accumulation of all inputs in the kernel's fixed order
-// followed by storing acc to every output buffer, or
+//   TREE     one tree evaluated in post-order on a stack: push in[i], then
+//            c_i times replace the two top entries a, b by a (+) b, where c_i
+//            is bits 2(i mod 16)..+1 of ins[i / 16]
+// followed by storing acc (the tree: the last stack entry) to every output
+// buffer, or
 //   DAG      a straight-line list of instructions over inputs, temporaries
 //            and one accumulator register: OP d = a (+) b, STORE buf <- v.
 // All inputs of an item are loaded before any output is stored, so a
@@ -22,7 +26,7 @@
 
 namespace ar {
 
-enum ProgKind : uint8_t { PK_CHAIN_R = 0, PK_CHAIN_L = 1, PK_DAG = 2, PK_ACC = 3 };
+enum ProgKind : uint8_t { PK_CHAIN_R = 0, PK_CHAIN_L = 1, PK_DAG = 2, PK_ACC = 3, PK_TREE = 4 };
 // DevProg::flags: the outputs are every rank's own buffer in rank order, so a
 // kernel can take output o's address straight from the rank-pointer array
 constexpr uint8_t PF_OUT_ALL = 1;
@@ -38,12 +42,14 @@ constexpr int kBarrierBytes = 512;   // mbarrier area at the start of a kernel's
 // staged / rank-streaming kernels, 16-byte vectors each consumer thread takes
 // per item tile (staged: up to kStagedVpt) or per rank tile (streaming).
 constexpr int kConsumerWarps = 8;
-constexpr int kStagedVpt = 8;
+constexpr int kStagedVpt = 4;
 constexpr int kStreamVpt = 8;        // rank-streaming kernel, chains and fp32 / int32 accumulation
 constexpr int kStreamVptNarrow = 4;  // rank-streaming kernel, bf16 fp32 accumulation (16 fp32 per vector)
-constexpr int kMaxStagedTile = 32 * kConsumerWarps * 16 * kStagedVpt;          // 32 KB
+constexpr int kMaxStagedTile = 32 * kConsumerWarps * 16 * kStagedVpt;          // 16 KB
 constexpr int kStreamTileBytes = 32 * kConsumerWarps * 16 * kStreamVpt;        // 32 KB
 constexpr int kStreamTileNarrow = 32 * kConsumerWarps * 16 * kStreamVptNarrow; // 16 KB
+constexpr int kTreeDepth = 4;        // deepest TREE stack (a balanced 8-leaf tree needs 4)
+constexpr int kTreeMaxLeaves = 64;   // TREE combine counts: 2 bits per leaf in 4 words
 
 // instruction word: bits 30..31 kind
 //   OP:    a = bits 0..9, b = bits 10..19, d = bits 20..29

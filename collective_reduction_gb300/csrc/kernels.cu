@@ -184,6 +184,11 @@ __device__ __forceinline__ char* buf_addr(const KernelArgs& a, uint32_t id) {
     return a.scratch + (static_cast<uint64_t>(slot - 1) * a.P + rank) * a.slot_stride;
 }
 
+__device__ __forceinline__ char* out_addr(const KernelArgs& a, const DevProg& pg, uint32_t o) {
+    if (pg.flags & PF_OUT_ALL) return static_cast<char*>(a.bufs[o]);
+    return buf_addr(a, a.refs[pg.out_off + o]);
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -404,6 +409,62 @@ __device__ __forceinline__ void dag_item(const KernelArgs& a, const DevProg& pg,
     }
 }
 
+// Tree stack in registers: kTreeDepth entries of kVpt vectors per thread.
+// The stack pointer is uniform across the CTA but only known at run time;
+// these recursive helpers turn each access into a chain of uniform branches,
+// one per possible depth, so every stack entry keeps fixed registers.
+template <int K = 0>
+__device__ __forceinline__ void tree_push(uint4 (&stk)[kTreeDepth][kVpt], int sp, uint32_t t, uint32_t nvec,
+                                          int ct) {
+    if (sp == K) {
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            const uint32_t v = ct + j * kConsumers;
+            if (v < nvec) stk[K][j] = lds128(t + v * 16);
+        }
+    } else if constexpr (K + 1 < kTreeDepth) {
+        tree_push<K + 1>(stk, sp, t, nvec, ct);
+    }
+}
+
+// stk[sp-2] = stk[sp-2] (+) stk[sp-1]: the left subtree sits deeper
+template <int DT, int OP, int K = 2>
+__device__ __forceinline__ void tree_combine(uint4 (&stk)[kTreeDepth][kVpt], int sp, uint32_t nvec, int ct) {
+    if (sp == K) {
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            const uint32_t v = ct + j * kConsumers;
+            if (v < nvec) stk[K - 2][j] = vop<DT, OP>(stk[K - 2][j], stk[K - 1][j]);
+        }
+    } else if constexpr (K < kTreeDepth) {
+        tree_combine<DT, OP, K + 1>(stk, sp, nvec, ct);
+    }
+}
+
+// A single tree every rank receives, evaluated in post-order from the item's
+// resident leaf tiles, all of this thread's vectors at once.
+template <int DT, int OP>
+__device__ __forceinline__ void tree_item(const KernelArgs& a, const DevProg& pg, uint32_t st, uint32_t nvec,
+                                          int64_t off, int ct) {
+    uint32_t counts[kTreeMaxLeaves / 16];
+#pragma unroll
+    for (int q = 0; q < kTreeMaxLeaves / 16; ++q) counts[q] = a.ins[pg.ins_off + q];
+    uint4 stk[kTreeDepth][kVpt];
+    int sp = 0;
+    for (uint32_t i = 0; i < pg.n_in; ++i) {
+        tree_push(stk, sp++, st + i * a.tile_bytes, nvec, ct);
+        for (uint32_t c = (counts[i >> 4] >> (2 * (i & 15))) & 3u; c > 0; --c, --sp) tree_combine<DT, OP>(stk, sp, nvec, ct);
+    }
+    for (uint32_t o = 0; o < pg.n_out; ++o) {
+        char* dst = out_addr(a, pg, o) + off;
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            const uint32_t v = ct + j * kConsumers;
+            if (v < nvec) stg128(dst + v * 16, stk[0][j]);
+        }
+    }
+}
+
 template <int DT, int OP>
 __device__ void consume(const KernelArgs& a, const Stage& sm, int ct) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
@@ -426,6 +487,8 @@ __device__ void consume(const KernelArgs& a, const Stage& sm, int ct) {
             chain_item<DT, OP, false>(a, pg, st, nvec, off, ct);
         else if (pg.kind == PK_ACC)
             acc_item<DT, OP>(a, pg, st, nvec, off, ct);
+        else if (pg.kind == PK_TREE)
+            tree_item<DT, OP>(a, pg, st, nvec, off, ct);
         else
             dag_item<DT, OP>(a, pg, st, sm.tmps, nvec, off, ct);
         __syncwarp();
@@ -517,11 +580,6 @@ __device__ void stream_produce(const KernelArgs& a, const Stage& sm) {
 // warp 0 produces, warp 1 stores (TMA-store epilogue only), the rest consume
 constexpr int kStreamLead = 2;
 constexpr int kStreamThreads = 32 * (kStreamLead + kConsumerWarps);
-
-__device__ __forceinline__ char* out_addr(const KernelArgs& a, const DevProg& pg, uint32_t o) {
-    if (pg.flags & PF_OUT_ALL) return static_cast<char*>(a.bufs[o]);
-    return buf_addr(a, a.refs[pg.out_off + o]);
-}
 
 __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -759,10 +817,19 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
                 acc = pg.kind == PK_CHAIN_R ? eop<DT, OP>(x, acc) : eop<DT, OP>(acc, x);
             }
             for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, acc);
+        } else if (pg.kind == PK_TREE) {
+            // post-order on a small stack (local memory is fine on this path)
+            uint32_t stk[kTreeDepth];
+            int sp = 0;
+            for (uint32_t i = 0; i < pg.n_in; ++i) {
+                stk[sp++] = vals[i * kElemThreads + t];
+                for (uint32_t q = (a.ins[pg.ins_off + (i >> 4)] >> (2 * (i & 15))) & 3u; q > 0; --q, --sp)
+                    stk[sp - 2] = eop<DT, OP>(stk[sp - 2], stk[sp - 1]);
+            }
+            for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, stk[0]);
         } else if (pg.kind == PK_ACC) {
-            // same order as the staged kernel: the element sits in lane 0 of a
-            // vector whose other lanes hold the op's identity-free zeros; only
-            // lane 0 of the result is kept
+            // the same order as the other kernels: the element rides in lane 0
+            // of a vector (the other lanes carry zeros and are dropped)
             const uint4 r = acc_reduce<DT, OP>(pg.n_in, [&](uint32_t i) {
                 return make_uint4(vals[i * kElemThreads + t], 0u, 0u, 0u);
             });
@@ -847,9 +914,12 @@ cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int 
 
 cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
     // the rank tile fixes the vectors per consumer thread
-    if (a.tile_bytes != kStreamTileBytes && a.tile_bytes != kStreamTileNarrow) return cudaErrorInvalidValue;
+    const int which = a.tile_bytes == kStreamTileBytes    ? K_STREAM
+                      : a.tile_bytes == kStreamTileNarrow ? K_STREAM_NARROW
+                                                          : -1;
+    if (which < 0) return cudaErrorInvalidValue;
     if (a.stages < 1 || a.stages > 32 || 24 * a.stages > kBarrierBytes) return cudaErrorInvalidValue;
-    KernelFn f = kernel_for(dtype, op, a.tile_bytes == kStreamTileBytes ? K_STREAM : K_STREAM_NARROW);
+    KernelFn f = kernel_for(dtype, op, which);
     f<<<grid, kStreamThreads, smem, st>>>(a);
     return cudaGetLastError();
 }

@@ -29,7 +29,7 @@ struct Prog {
         if (kind != PK_DAG) return static_cast<int>(out.size());
         int s = 0;
         for (uint32_t w : ins) s += (w >> 30) == INS_STORE;
-        return s;
+        return s;  // (TREE programs store to their outputs like CHAIN / ACC)
     }
 };
 
@@ -200,6 +200,37 @@ Prog dag_program(const Dag& d, const std::vector<int32_t>& outs) {
     return p;
 }
 
+// Post-order of a single tree: leaves left to right, and after each leaf the
+// number of combines that follow it; false if the stack gets deeper than
+// kTreeDepth.
+bool tree_program(const Dag& d, int32_t root, std::vector<int32_t>& leaves, std::vector<uint32_t>& combines) {
+    leaves.clear();
+    combines.clear();
+    int depth = 0, max_depth = 0;
+    std::vector<std::pair<int32_t, int>> st{{root, 0}};
+    while (!st.empty()) {
+        auto& top = st.back();
+        const int32_t x = top.first;
+        if (d.leaf(x)) {
+            leaves.push_back(x);
+            combines.push_back(0);
+            max_depth = std::max(max_depth, ++depth);
+            st.pop_back();
+        } else if (top.second == 0) {
+            top.second = 1;
+            st.push_back({d.left(x), 0});
+        } else if (top.second == 1) {
+            top.second = 2;
+            st.push_back({d.right(x), 0});
+        } else {
+            ++combines.back();
+            --depth;
+            st.pop_back();
+        }
+    }
+    return max_depth <= kTreeDepth && leaves.size() <= static_cast<size_t>(kTreeMaxLeaves);
+}
+
 Prog fused_program(Canon& cn, const Schedule& S, int seg) {
     const int P = S.P;
     std::vector<int32_t> outs(P);
@@ -212,6 +243,18 @@ Prog fused_program(Canon& cn, const Schedule& S, int seg) {
         if (p.kind == PK_CHAIN_L) left_chain(cn.c, outs[0], leaves);
         p.flags = PF_OUT_ALL;
         for (int32_t x : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, x)));
+        for (int r = 0; r < P; ++r) p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
+        return p;
+    }
+    std::vector<uint32_t> combines;
+    if (same && tree_program(cn.c, outs[0], leaves, combines)) {
+        Prog p;
+        p.kind = PK_TREE;
+        p.flags = PF_OUT_ALL;
+        for (int32_t x : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, x)));
+        // combine counts (< kTreeDepth <= 4), 2 bits per leaf, 16 per word
+        p.ins.assign(kTreeMaxLeaves / 16, 0);
+        for (size_t i = 0; i < combines.size(); ++i) p.ins[i / 16] |= combines[i] << (2 * (i % 16));
         for (int r = 0; r < P; ++r) p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
         return p;
     }
@@ -325,12 +368,12 @@ void lower(const Schedule& S, Lowered& lw) {
         }
     }
     // A set whose programs are all chains / fp32 accumulations streams one
-    // rank tile at a time (rank-streaming kernel); sets with a DAG program
-    // stage all of an item's input tiles at once (staged kernel).
+    // rank tile at a time (rank-streaming kernel); sets with a tree or DAG
+    // program stage all of an item's input tiles at once (staged kernel).
     std::vector<bool> stream(sets.size(), true);
     for (size_t k = 0; k < sets.size(); ++k)
         for (auto& r : sets[k])
-            if (lw.progs[r.prog].kind == PK_DAG) stream[k] = false;
+            if (lw.progs[r.prog].kind == PK_DAG || lw.progs[r.prog].kind == PK_TREE) stream[k] = false;
     // staged-kernel geometry from the programs that own an aligned body
     lw.max_in = 1;
     lw.max_tmp = 0;
@@ -357,8 +400,9 @@ void lower(const Schedule& S, Lowered& lw) {
     t = std::min<int64_t>(t, kMaxTileBytes);
     t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
     lw.tile_bytes = static_cast<int>(t);
-    lw.stream_tile = (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC) ? kStreamTileNarrow
-                                                                                    : kStreamTileBytes;
+    // bf16 fp32 accumulation holds 16 fp32 per vector: 16 KB rank tiles
+    const bool narrow = S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC;
+    lw.stream_tile = narrow ? kStreamTileNarrow : kStreamTileBytes;
     lw.stream_stages = std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile);
     // The TMA-store epilogue holds an item's last stage until its outputs are
     // copied out: measured faster with few outputs per item (and for bf16
