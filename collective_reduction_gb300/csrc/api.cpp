@@ -37,6 +37,7 @@ struct ar_plan_s {
         const ar::WorkItem* fallback;
         uint32_t n_bulk, n_edge, n_fallback;
         bool stream;
+        bool small;
     };
     std::vector<Set> sets;
     // element windows of a fused plan for the pipelined host path: window w
@@ -339,6 +340,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             s.n_edge = static_cast<uint32_t>(L.sets[i].edge.size());
             s.n_fallback = static_cast<uint32_t>(L.sets[i].fallback.size());
             s.stream = L.sets[i].stream;
+            s.small = L.sets[i].small;
             p->sets.push_back(s);
         }
         make_windows(p);
@@ -382,7 +384,7 @@ ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
     base_args(plan, rank_bufs, a);
     for (const auto& s : plan->sets) {
         cudaError_t e = cudaSuccess;
-        if (aligned) {
+        if (aligned && !s.small) {
             e = launch_range(plan, a, s, 0, s.n_bulk, 0, s.n_edge, st);
         } else if (s.n_fallback) {
             a.items = s.fallback;

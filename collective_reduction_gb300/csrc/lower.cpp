@@ -432,9 +432,12 @@ void lower(const Schedule& S, Lowered& lw) {
             const DevProg& d = lw.progs[r.prog];
             ls.bytes += static_cast<uint64_t>(d.n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
         }
+        // a tiny set that would need a staged launch and an edge launch runs
+        // as one element-wise launch instead (launch latency dominates there)
+        ls.small = !ls.bulk.empty() && !ls.edge.empty() && ls.bytes <= (256u << 10);
         lw.hbm_bytes += ls.bytes;
-        lw.n_items += ls.bulk.size() + ls.edge.size();
-        lw.launches += (!ls.bulk.empty()) + (!ls.edge.empty());
+        lw.n_items += ls.small ? ls.fallback.size() : ls.bulk.size() + ls.edge.size();
+        lw.launches += ls.small ? 1 : (!ls.bulk.empty()) + (!ls.edge.empty());
         lw.sets.push_back(std::move(ls));
     }
 }

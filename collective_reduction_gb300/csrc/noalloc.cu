@@ -164,7 +164,7 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
             const ar::WorkItem* edge = reinterpret_cast<const ar::WorkItem*>(tables + o_sets[3 * i + 1]);
             const ar::WorkItem* fb = reinterpret_cast<const ar::WorkItem*>(tables + o_sets[3 * i + 2]);
             cudaError_t e = cudaSuccess;
-            if (aligned) {
+            if (aligned && !s.small) {
                 if (!s.bulk.empty()) {
                     a.items = bulk;
                     a.n_items = static_cast<uint32_t>(s.bulk.size());

@@ -80,12 +80,13 @@ int mod(int64_t a, int64_t m) { return static_cast<int>(((a % m) + m) % m); }
 
 struct Gen {
     Schedule& S;
-    int P;
+    int P;        // ranks taking part (0..P-1)
     int64_t n;
+    int P_total;  // ranks of the whole schedule (size of the sent counters)
 
     Round& new_round() {
         S.rounds.emplace_back();
-        S.rounds.back().sent.assign(P, 0);
+        S.rounds.back().sent.assign(P_total, 0);
         return S.rounds.back();
     }
     // A plain message: one transfer whose bytes count as sent by src.
@@ -191,6 +192,36 @@ void gen_hybrid(Gen& g, int k1) {
             nxt[r] = {std::min(own[r].first, own[r ^ d].first), std::max(own[r].second, own[r ^ d].second)};
         own = nxt;
     }
+}
+
+int pow2_floor(int P) {
+    int Pp = 1;
+    while (Pp * 2 <= P) Pp *= 2;
+    return Pp;
+}
+
+// Any P for a power-of-two schedule ("A Generalization of the Allreduce
+// Operation", introduction: reduce the process count to the largest power of
+// two P' with a preparation and a finalization step).  Preparation: excess
+// rank P' + i sends its vector to rank i, which combines it.  The inner
+// schedule then runs on ranks 0..P'-1 (chunked over P').  Finalization: rank
+// i sends the result back to rank P' + i.
+template <class Inner>
+void gen_fold(Gen& g, Inner inner) {
+    const int Pp = pow2_floor(g.P);
+    if (Pp == g.P) {
+        inner(g);
+        return;
+    }
+    const int e = g.P - Pp;
+    {
+        Round& rd = g.new_round();
+        for (int i = 0; i < e; ++i) g.msg(rd, Pp + i, i, 0, g.n, true);
+    }
+    Gen h{g.S, Pp, g.n, g.P_total};
+    inner(h);
+    Round& rd = g.new_round();
+    for (int i = 0; i < e; ++i) g.msg(rd, i, Pp + i, 0, g.n, false);
 }
 
 // Generalized allreduce ("A Generalization of the Allreduce Operation",
@@ -442,13 +473,9 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
     const int L = ceil_log2(P);
     const bool pow2 = is_pow2(P);
     switch (algo) {
-        case AR_RH:
-        case AR_RD:
-            if (!pow2) return AR_ERR_UNSUPPORTED;
-            break;
         case AR_HYBRID:
-            if (!pow2) return AR_ERR_UNSUPPORTED;
-            if (pr.k1 < 0 || pr.k1 > L) return AR_ERR_INVALID_ARG;
+            // any P: the halving steps run among the largest power of two
+            if (pr.k1 < 0 || pr.k1 > ceil_log2(pow2_floor(P))) return AR_ERR_INVALID_ARG;
             break;
         case AR_GENERALIZED:
             if (pr.r < 0 || pr.r > L) return AR_ERR_INVALID_ARG;
@@ -476,14 +503,14 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
     S.op = op;
     S.algo = algo;
     S.params = pr;
-    Gen g{S, P, n};
+    Gen g{S, P, n, P};
     try {
         switch (algo) {
             case AR_RING: gen_ring(g); break;
             case AR_BINOMIAL: gen_binomial(g); break;
-            case AR_RH: gen_generalized(g, true, 0); break;
-            case AR_RD: gen_hybrid(g, 0); break;
-            case AR_HYBRID: gen_hybrid(g, pr.k1); break;
+            case AR_RH: gen_fold(g, [](Gen& h) { gen_generalized(h, true, 0); }); break;
+            case AR_RD: gen_fold(g, [](Gen& h) { gen_hybrid(h, 0); }); break;
+            case AR_HYBRID: gen_fold(g, [&](Gen& h) { gen_hybrid(h, pr.k1); }); break;
             case AR_GENERALIZED: gen_generalized(g, pr.group == AR_GROUP_XOR, pr.r); break;
             case AR_AHC: gen_ahc(g, pr.group_sizes); break;
         }

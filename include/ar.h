@@ -72,12 +72,18 @@ typedef enum { AR_SUM = 0, AR_PROD = 1, AR_MAX = 2, AR_MIN = 3 } ar_op;
  *  AR_RH          recursive halving reduce-scatter + doubling all-gather,
  *                 distance P/2 first; the bandwidth-optimal generalized
  *                 algorithm with the XOR group ("A Generalization ...",
- *                 remark after eq. 25, Table 1.b).  P = 2^k.  2 log2 P.
+ *                 remark after eq. 25, Table 1.b).  2 log2 P rounds.
  *  AR_RD          recursive doubling, whole vectors, distance 1 first.
- *                 P = 2^k.  log2 P rounds.
+ *                 log2 P rounds.
  *  AR_HYBRID      k1 halving rounds, recursive doubling on the block each rank
  *                 then owns, k1 doubling rounds ("A Generalization ...",
- *                 introduction, the classic hybrid).  P = 2^k.  log2 P + k1.
+ *                 introduction, the classic hybrid).  log2 P + k1 rounds.
+ *                 RH, RD and the hybrid take any P: with P' the largest power
+ *                 of two <= P, a preparation round folds rank P'+i into rank i,
+ *                 the schedule runs on ranks 0..P'-1 and a finalization round
+ *                 copies rank i's result to rank P'+i ("A Generalization ...",
+ *                 introduction, the workaround for non-power-of-two counts):
+ *                 two more rounds; k1 <= log2 P'.
  *  AR_GENERALIZED the group-theoretic generalized allreduce for any P
  *                 ("A Generalization ...", eqs. 17-44): cyclic group (any P)
  *                 or XOR group (P = 2^k); r distribution steps removed,
@@ -135,8 +141,8 @@ typedef struct ar_plan_s* ar_plan_t;
  * cyclic, r = 0, k1 = 0).  On success *out owns host memory released by
  * ar_schedule_destroy.  Errors: AR_ERR_INVALID_ARG (P < 1, unknown enum, null
  * out, AHC sizes not adding up to P, r or k1 out of range),
- * AR_ERR_UNSUPPORTED (P > AR_MAX_RANKS, XOR / RD / RH / hybrid with P not a
- * power of two, AHC with more than 4096 chunks, FP32ACC with the step form),
+ * AR_ERR_UNSUPPORTED (P > AR_MAX_RANKS, the XOR group with P not a power of
+ * two, AHC with more than 4096 chunks, FP32ACC with the step form),
  * AR_ERR_NOMEM. */
 ar_status ar_schedule_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo,
                              const ar_params* params, ar_schedule_t* out);

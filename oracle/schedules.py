@@ -154,16 +154,38 @@ def binomial(bufs, arith):
     return sim.result()
 
 
-def rd(bufs, arith, first="low"):
-    """Recursive doubling: log P rounds, x_r <- x_r (+) x_{r xor d}.
-
-    first='low' takes distances 1, 2, 4, ... (the classic order); 'high' takes
-    P/2, P/4, ..., 1.  P must be a power of two.
+def fold_to_pow2(bufs, arith, inner):
+    """Any P by reduction to the largest power of two P' <= P (A Generalization
+    of the Allreduce Operation, introduction, the straightforward workaround
+    for non-power-of-two process counts): a preparation round in which each
+    excess process sends its vector to a process that takes part, the
+    power-of-two schedule on the P' taking part, and a finalization round in
+    which the result goes back.  Excess process P' + i pairs with process i
+    (the pages leave the pairing open).  inner(bufs) runs the schedule on P'
+    buffers and returns its Result.  A power-of-two P runs inner directly.
     """
+    P = len(bufs)
+    Pp = 1
+    while Pp * 2 <= P:
+        Pp *= 2
+    if Pp == P:
+        return inner(bufs)
+    n = len(bufs[0])
+    e = P - Pp
+    pre = RankSim(bufs, arith)
+    pre.round([(Pp + i, i, 0, n, "add") for i in range(e)])
+    res = inner(pre.buf[:Pp])
+    post = RankSim(list(res.bufs) + [pre.buf[Pp + i] for i in range(e)], arith)
+    post.round([(i, Pp + i, 0, n, "copy") for i in range(e)])
+    sent = [pre.sent[0]] + [list(s) + [0] * e for s in res.sent] + [post.sent[0]]
+    # one counter serves all three parts: everything since the preparation
+    combines = arith.combines - pre.start
+    return Result(post.buf, sent, combines, {"P_pow2": Pp, "excess": e})
+
+
+def _rd_pow2(bufs, arith, first):
     sim = RankSim(bufs, arith)
     P, n = sim.P, sim.n
-    if not _is_pow2(P):
-        raise ValueError("recursive doubling needs a power-of-two P")
     L = ceil_log2(P)
     dists = [1 << k for k in range(L)]
     if first == "high":
@@ -171,6 +193,15 @@ def rd(bufs, arith, first="low"):
     for d in dists:
         sim.round([(r ^ d, r, 0, n, "add") for r in range(P)])
     return sim.result()
+
+
+def rd(bufs, arith, first="low"):
+    """Recursive doubling: log P rounds, x_r <- x_r (+) x_{r xor d}.
+
+    first='low' takes distances 1, 2, 4, ... (the classic order); 'high' takes
+    P/2, P/4, ..., 1.  Other P: fold_to_pow2 around it (log P' + 2 rounds).
+    """
+    return fold_to_pow2(bufs, arith, lambda b: _rd_pow2(b, arith, first))
 
 
 def _chunk_span(ch, c0, c1):
@@ -208,12 +239,20 @@ def _doubling_rounds(sim, ch, own, steps):
                   for r in range(P)]
 
 
+def pow2_floor(P):
+    Pp = 1
+    while Pp * 2 <= P:
+        Pp *= 2
+    return Pp
+
+
 def rh(bufs, arith):
     """Recursive halving reduce-scatter + recursive doubling all-gather.
 
-    2 log P rounds; rank r ends the reduce-scatter with chunk r.  P = 2^k.
+    2 log P rounds; rank r ends the reduce-scatter with chunk r.  Other P:
+    fold_to_pow2 around it (2 log P' + 2 rounds).
     """
-    return hybrid(bufs, arith, ceil_log2(len(bufs)))
+    return hybrid(bufs, arith, ceil_log2(pow2_floor(len(bufs))))
 
 
 def hybrid(bufs, arith, k1):
@@ -221,15 +260,17 @@ def hybrid(bufs, arith, k1):
     first) on the block each rank then owns, k1 doubling rounds.
 
     k1 = 0 is recursive doubling, k1 = log P is recursive halving; log P + k1
-    rounds.  P must be a power of two.
+    rounds.  Other P: fold_to_pow2 around it, k1 in 0..log P'.
     """
+    if not 0 <= k1 <= ceil_log2(pow2_floor(len(bufs))):
+        raise ValueError("k1 must lie in 0..log P'")
+    return fold_to_pow2(bufs, arith, lambda b: _hybrid_pow2(b, arith, k1))
+
+
+def _hybrid_pow2(bufs, arith, k1):
     sim = RankSim(bufs, arith)
     P, n = sim.P, sim.n
-    if not _is_pow2(P):
-        raise ValueError("the hybrid needs a power-of-two P")
     L = ceil_log2(P)
-    if not 0 <= k1 <= L:
-        raise ValueError("k1 must lie in 0..log P")
     ch = split(n, P)
     own = [(0, P)] * P
     _halving_rounds(sim, ch, own, L, k1)

@@ -63,6 +63,17 @@ def test_config2_power_of_two_schedules(config2_inputs, algo, kw, op, form):
     check_faithful(config2_inputs, "float32", op, algo, form, **kw)
 
 
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("P", [3, 6, 12, 13])
+def test_non_power_of_two_folded_schedules(P, form):
+    """RD, RH and the hybrid on any P through the preparation / finalization
+    rounds around the largest power of two."""
+    bufs = ar_synth.rank_inputs(P, 40003, "float32", "normal", sigma=1.0, seed=P)
+    for algo, kw in (("rd", {}), ("rh", {}), ("hybrid", {"k1": 1})):
+        for op in ("sum", "max"):
+            check_faithful(bufs, "float32", op, algo, form, **kw)
+
+
 # ---- configuration 3: generalized, P = 7 and 12 ----------------------------------------
 
 @pytest.mark.parametrize("form", FORMS)

@@ -53,15 +53,16 @@ def test_status_strings(lib):
 def _cases():
     for P in (1, 2, 3, 4, 5, 7, 8, 12, 16):
         L = ceil_log2(P)
+        Lp = ceil_log2(1 << (P.bit_length() - 1))
         yield "ring", P, {}
         yield "binomial", P, {}
         for r in range(L + 1):
             yield "generalized", P, {"group": "cyclic", "r": r}
+        yield "rd", P, {}
+        yield "rh", P, {}
+        for k1 in range(Lp + 1):
+            yield "hybrid", P, {"k1": k1}
         if P & (P - 1) == 0:
-            yield "rd", P, {}
-            yield "rh", P, {}
-            for k1 in range(L + 1):
-                yield "hybrid", P, {"k1": k1}
             for r in range(L + 1):
                 yield "generalized", P, {"group": "xor", "r": r}
         for sizes in ([P], [1] * P, [P // 2, P - P // 2] if P > 1 else [1], [2, P - 2] if P >= 4 else [P]):
@@ -106,10 +107,9 @@ def test_ahc_twelve_chunks(lib):
 @pytest.mark.parametrize("args,status", [
     ((0, 8, "float32", "sum", "ring", {}), "AR_ERR_INVALID_ARG"),
     ((65, 8, "float32", "sum", "ring", {}), "AR_ERR_UNSUPPORTED"),
-    ((6, 8, "float32", "sum", "rd", {}), "AR_ERR_UNSUPPORTED"),
-    ((6, 8, "float32", "sum", "rh", {}), "AR_ERR_UNSUPPORTED"),
-    ((6, 8, "float32", "sum", "hybrid", {"k1": 1}), "AR_ERR_UNSUPPORTED"),
+    ((6, 8, "float32", "sum", "hybrid", {"k1": 3}), "AR_ERR_INVALID_ARG"),
     ((8, 8, "float32", "sum", "hybrid", {"k1": 4}), "AR_ERR_INVALID_ARG"),
+    ((8, 8, "float32", "sum", "hybrid", {"k1": -1}), "AR_ERR_INVALID_ARG"),
     ((12, 8, "float32", "sum", "generalized", {"group": "xor"}), "AR_ERR_UNSUPPORTED"),
     ((7, 8, "float32", "sum", "generalized", {"r": 4}), "AR_ERR_INVALID_ARG"),
     ((5, 8, "float32", "sum", "ahc", {"group_sizes": [2, 2]}), "AR_ERR_INVALID_ARG"),

@@ -19,19 +19,27 @@ def _pow2(P):
     return P & (P - 1) == 0
 
 
+def _pow2_floor(P):
+    q = 1
+    while q * 2 <= P:
+        q *= 2
+    return q
+
+
 def _cases(Ps=range(1, 17)):
     """(algo, P, params) for every schedule and parameter valid at each P."""
     for P in Ps:
         L = ceil_log2(P)
+        Lp = ceil_log2(_pow2_floor(P))
         yield "ring", P, {}
         yield "binomial", P, {}
         for r in range(L + 1):
             yield "generalized", P, {"group": "cyclic", "r": r}
+        yield "rd", P, {}
+        yield "rh", P, {}
+        for k1 in range(Lp + 1):
+            yield "hybrid", P, {"k1": k1}
         if _pow2(P):
-            yield "rd", P, {}
-            yield "rh", P, {}
-            for k1 in range(L + 1):
-                yield "hybrid", P, {"k1": k1}
             for r in range(L + 1):
                 yield "generalized", P, {"group": "xor", "r": r}
         for sizes in _partitions(P):
@@ -57,16 +65,18 @@ def _partitions(P):
 
 def _expected_steps(algo, P, p):
     L = ceil_log2(P)
+    Lp = ceil_log2(_pow2_floor(P))
+    fold = 0 if _pow2(P) else 2   # preparation + finalization rounds
     if algo == "ring":
         return 2 * (P - 1)
     if algo == "binomial":
         return 2 * L
     if algo == "rd":
-        return L
+        return Lp + fold
     if algo == "rh":
-        return 2 * L
+        return 2 * Lp + fold
     if algo == "hybrid":
-        return L + p["k1"]
+        return Lp + p["k1"] + fold
     if algo == "generalized":
         return 2 * L - p["r"]
     if algo == "ahc":
@@ -334,7 +344,7 @@ def test_invalid_parameters_rejected():
     z = [np.zeros(4, np.int32)] * 6
     a = Arith("sum", "int32")
     with pytest.raises(ValueError):
-        oracle.run("rd", z, a)
+        oracle.run("hybrid", z, a, k1=3)      # log P' = 2 for P = 6
     with pytest.raises(ValueError):
         oracle.run("generalized", z, a, group="xor")
     with pytest.raises(ValueError):
@@ -359,3 +369,37 @@ def test_float_order_is_the_schedule_order():
             acc = (bufs[(k + j) % P][sl] + acc).astype(np.float32)
         for r in range(P):
             assert np.array_equal(res.bufs[r][sl], acc)
+
+
+@pytest.mark.parametrize("P", [3, 5, 6, 7, 9, 12, 13, 15])
+def test_non_power_of_two_fold_costs(P):
+    """Reducing P to the largest power of two P' with a preparation and a
+    finalization step costs 2m more data per excess process (m = its vector)
+    and two more steps, which makes recursive doubling slower than the
+    ceil(log P) steps of the latency-optimal generalized version."""
+    n = 4 * P
+    Pp = _pow2_floor(P)
+    e = P - Pp
+    z = [np.zeros(n, np.int32)] * P
+    for algo in ("rd", "rh"):
+        folded = oracle.run(algo, z, Arith("sum", "int32"))
+        inner = oracle.run(algo, [np.zeros(n, np.int32)] * Pp, Arith("sum", "int32"))
+        assert sum(folded.sent_per_rank()) - sum(inner.sent_per_rank()) == 2 * e * n
+        assert folded.steps == inner.steps + 2
+        assert folded.sent[0] == [0] * Pp + [n] * e          # excess ranks send in
+        assert folded.sent[-1] == [n] * e + [0] * (P - e)    # first e ranks send back
+    rd = oracle.run("rd", z, Arith("sum", "int32"))
+    lat = oracle.run("generalized", z, Arith("sum", "int32"), r=ceil_log2(P))
+    assert rd.steps > lat.steps == ceil_log2(P)
+
+
+def test_non_power_of_two_fold_tree():
+    """P = 6: rank 4 and 5 fold into ranks 0 and 1; recursive doubling on
+    ranks 0..3 (distance 1, then 2); ranks 4 and 5 receive ranks 0 and 1's
+    results."""
+    res = oracle.run("rd", leaf_buffers(6, 1), Symbolic())
+    want = {0: "(((0+4)+(1+5))+(2+3))", 1: "(((1+5)+(0+4))+(3+2))", 2: "((2+3)+((0+4)+(1+5)))",
+            3: "((3+2)+((1+5)+(0+4)))"}
+    for r, t in want.items():
+        assert tree_str(res.bufs[r][0]) == t
+    assert tree_str(res.bufs[4][0]) == want[0] and tree_str(res.bufs[5][0]) == want[1]
