@@ -588,7 +588,7 @@ def run_configs(a, path):
             plan.check()
             got = [t.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bfloat16" else t.cpu().numpy()
                    for t in dev]
-            okw = {k: v for k, v in kw.items() if k in ("r", "k1", "group_sizes")}
+            okw = {k: v for k, v in kw.items() if k in ("r", "k1", "group_sizes", "blocks")}
             t0 = time.perf_counter()
             want = oracle.run(algo, host, Arith(op, dtype), **okw)
             oracle_s = time.perf_counter() - t0

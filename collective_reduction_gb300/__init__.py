@@ -16,7 +16,7 @@ import os
 
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
-ALGOS = {"ring": 0, "binomial": 1, "rh": 2, "rd": 3, "hybrid": 4, "generalized": 5, "ahc": 6}
+ALGOS = {"ring": 0, "binomial": 1, "rh": 2, "rd": 3, "hybrid": 4, "generalized": 5, "ahc": 6, "pipeline": 7}
 FORMS = {"fused": 0, "step": 1}
 ORDERS = {"faithful": 0, "fp32acc": 1}
 GROUPS = {"cyclic": 0, "xor": 1}
@@ -39,7 +39,7 @@ class ArError(RuntimeError):
 class Params(ctypes.Structure):
     _fields_ = [("form", ctypes.c_int), ("order", ctypes.c_int), ("group", ctypes.c_int),
                 ("r", ctypes.c_int), ("k1", ctypes.c_int), ("n_groups", ctypes.c_int),
-                ("group_sizes", ctypes.POINTER(ctypes.c_int))]
+                ("group_sizes", ctypes.POINTER(ctypes.c_int)), ("blocks", ctypes.c_int)]
 
 
 class Info(ctypes.Structure):
@@ -105,8 +105,8 @@ def _check(status, where):
         raise ArError(status, where)
 
 
-def _params(form="fused", order="faithful", group="cyclic", r=0, k1=0, group_sizes=None):
-    p = Params(FORMS[form], ORDERS[order], GROUPS[group], int(r), int(k1), 0, None)
+def _params(form="fused", order="faithful", group="cyclic", r=0, k1=0, group_sizes=None, blocks=1):
+    p = Params(FORMS[form], ORDERS[order], GROUPS[group], int(r), int(k1), 0, None, int(blocks))
     keep = None
     if group_sizes is not None:
         keep = (ctypes.c_int * len(group_sizes))(*[int(g) for g in group_sizes])

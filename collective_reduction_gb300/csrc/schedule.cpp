@@ -386,6 +386,27 @@ void gen_ahc(Gen& g, const std::vector<int>& sizes) {
     intra(false);
 }
 
+// Pipelined chain reduce ("還元演算子", pipelined algorithm): m blocks; round
+// t has unit i pass block t - i to unit i + 1, which combines it, so the last
+// unit has every block after p + m - 2 rounds; the broadcast mirrors it (unit
+// i passes block t - (p - 1 - i) to unit i - 1, which overwrites).
+void gen_pipeline(Gen& g, int m) {
+    if (g.P < 2) return;
+    auto blk = ceil_split(g.n, m);
+    for (int t = 0; t < g.P + m - 2; ++t) {
+        Round& rd = g.new_round();
+        for (int i = 0; i + 1 < g.P; ++i)
+            if (t - i >= 0 && t - i < m) g.msg(rd, i, i + 1, blk[t - i].first, blk[t - i].second, true);
+    }
+    for (int t = 0; t < g.P + m - 2; ++t) {
+        Round& rd = g.new_round();
+        for (int i = 1; i < g.P; ++i) {
+            const int b = t - (g.P - 1 - i);
+            if (b >= 0 && b < m) g.msg(rd, i, i - 1, blk[b].first, blk[b].second, false);
+        }
+    }
+}
+
 // Runs the rounds on tree ids: every transfer reads the pre-round state, a
 // round may write each (rank, slot, segment) once, combines intern
 // (receiver, incoming) in the DAG.
@@ -450,7 +471,7 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
     if (P < 1 || n < 0) return AR_ERR_INVALID_ARG;
     if (dtype < AR_INT32 || dtype > AR_BFLOAT16) return AR_ERR_INVALID_ARG;
     if (op < AR_SUM || op > AR_MIN) return AR_ERR_INVALID_ARG;
-    if (algo < AR_RING || algo > AR_AHC) return AR_ERR_INVALID_ARG;
+    if (algo < AR_RING || algo > AR_PIPELINE) return AR_ERR_INVALID_ARG;
     if (P > AR_MAX_RANKS) return AR_ERR_UNSUPPORTED;
     Params pr;
     if (p) {
@@ -459,6 +480,7 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
         pr.group = p->group;
         pr.r = p->r;
         pr.k1 = p->k1;
+        pr.blocks = p->blocks == 0 ? 1 : p->blocks;
         if (algo == AR_AHC) {
             if (p->n_groups < 1 || !p->group_sizes) return AR_ERR_INVALID_ARG;
             pr.group_sizes.assign(p->group_sizes, p->group_sizes + p->n_groups);
@@ -476,6 +498,9 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
         case AR_HYBRID:
             // any P: the halving steps run among the largest power of two
             if (pr.k1 < 0 || pr.k1 > ceil_log2(pow2_floor(P))) return AR_ERR_INVALID_ARG;
+            break;
+        case AR_PIPELINE:
+            if (pr.blocks < 1 || pr.blocks > 4096) return AR_ERR_INVALID_ARG;
             break;
         case AR_GENERALIZED:
             if (pr.r < 0 || pr.r > L) return AR_ERR_INVALID_ARG;
@@ -513,6 +538,7 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
             case AR_HYBRID: gen_fold(g, [&](Gen& h) { gen_hybrid(h, pr.k1); }); break;
             case AR_GENERALIZED: gen_generalized(g, pr.group == AR_GROUP_XOR, pr.r); break;
             case AR_AHC: gen_ahc(g, pr.group_sizes); break;
+            case AR_PIPELINE: gen_pipeline(g, pr.blocks); break;
         }
         run_symbolic(S);
     } catch (const std::bad_alloc&) {

@@ -55,6 +55,7 @@ struct Params {
     int r = 0;
     int k1 = 0;
     std::vector<int> group_sizes;
+    int blocks = 1;
 };
 
 struct Schedule {

@@ -92,10 +92,16 @@ typedef enum { AR_SUM = 0, AR_PROD = 1, AR_MAX = 2, AR_MIN = 3 } ar_op;
  *                 contiguous groups of the given sizes, LCM x G chunks, ring
  *                 reduce-scatter inside each group, ring allreduce between the
  *                 logical devices with identical IDs, ring all-gather inside
- *                 each group. */
+ *                 each group.
+ *  AR_PIPELINE    pipelined chain reduce over `blocks` blocks (ceil split):
+ *                 in round t unit i passes block t - i to unit i + 1, which
+ *                 combines it; the last unit holds every block after
+ *                 p + blocks - 2 rounds ("還元演算子" (Reduction operator),
+ *                 pipelined algorithm); then the mirror-image pipelined
+ *                 broadcast.  2 (p + blocks - 2) rounds. */
 typedef enum {
     AR_RING = 0, AR_BINOMIAL = 1, AR_RH = 2, AR_RD = 3,
-    AR_HYBRID = 4, AR_GENERALIZED = 5, AR_AHC = 6
+    AR_HYBRID = 4, AR_GENERALIZED = 5, AR_AHC = 6, AR_PIPELINE = 7
 } ar_algo;
 
 enum { AR_FORM_FUSED = 0, AR_FORM_STEP = 1 };
@@ -110,6 +116,7 @@ typedef struct {
     int k1;                 /* AR_HYBRID: halving steps, 0..log2 P                */
     int n_groups;           /* AR_AHC: number of groups G                         */
     const int* group_sizes; /* AR_AHC: G sizes adding up to P (copied at create)  */
+    int blocks;             /* AR_PIPELINE: blocks m, 1..4096 (0 means 1)         */
 } ar_params;
 
 typedef struct {

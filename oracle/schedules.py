@@ -32,6 +32,8 @@ Schedules and where they are defined:
                t_k(x) = x + k mod P, Fig. 2; or the self-inverse XOR group of
                Table 1.b for P = 2^k), r removed distribution steps
   ahc          AHC (HCCL), Description steps 1-3
+  pipeline     "還元演算子" (Reduction operator), pipelined algorithm: a chain
+               reduce over m blocks, then the mirror-image broadcast
 """
 
 import math
@@ -40,7 +42,7 @@ import numpy as np
 
 from .chunking import ceil_div, ceil_log2, split
 
-ALGOS = ("ring", "binomial", "rd", "rh", "hybrid", "generalized", "ahc")
+ALGOS = ("ring", "binomial", "rd", "rh", "hybrid", "generalized", "ahc", "pipeline")
 
 
 class Result:
@@ -442,6 +444,31 @@ def generalized(bufs, arith, group="cyclic", r=0):
     return Result(out, sent, arith.combines - start, info)
 
 
+def pipeline(bufs, arith, m):
+    """Pipelined chain reduce + broadcast ("還元演算子" (Reduction operator),
+    pipelined algorithm).  The vector is cut into m blocks (ceil split).
+    Reduce: in round t unit i < p-1 passes block t - i (when 0 <= t - i < m)
+    to unit i + 1, which combines it into its own; the last unit holds every
+    block after p + m - 2 rounds (p - 1 until it receives the first block,
+    m - 1 more for the rest).  Allreduce adds the mirror image: in round t
+    unit i > 0 passes block t - (p - 1 - i) to unit i - 1, which overwrites.
+    2 (p + m - 2) rounds for p >= 2.
+    """
+    sim = RankSim(bufs, arith)
+    P, n = sim.P, sim.n
+    if m < 1:
+        raise ValueError("m must be at least 1")
+    if P == 1:
+        return sim.result()
+    blocks = split(n, m)
+    for t in range(P + m - 2):
+        sim.round([(i, i + 1, *blocks[t - i], "add") for i in range(P - 1) if 0 <= t - i < m])
+    for t in range(P + m - 2):
+        sim.round([(i, i - 1, *blocks[t - (P - 1 - i)], "copy") for i in range(1, P)
+                   if 0 <= t - (P - 1 - i) < m])
+    return sim.result()
+
+
 def ahc_layout(group_sizes):
     """AHC chunking: LCM of the group sizes, G groups, LCM x G chunks; group
     offsets (groups are contiguous rank ranges in the given order)."""
@@ -528,7 +555,7 @@ def ahc(bufs, arith, group_sizes):
     return sim.result(info)
 
 
-def run(algo, bufs, arith, group="cyclic", r=0, k1=0, group_sizes=None):
+def run(algo, bufs, arith, group="cyclic", r=0, k1=0, group_sizes=None, blocks=1):
     """Run one schedule by name."""
     if algo == "ring":
         return ring(bufs, arith)
@@ -544,4 +571,6 @@ def run(algo, bufs, arith, group="cyclic", r=0, k1=0, group_sizes=None):
         return generalized(bufs, arith, group, r)
     if algo == "ahc":
         return ahc(bufs, arith, group_sizes)
+    if algo == "pipeline":
+        return pipeline(bufs, arith, blocks)
     raise ValueError(f"unknown algorithm {algo!r}")

@@ -74,6 +74,14 @@ def test_non_power_of_two_folded_schedules(P, form):
             check_faithful(bufs, "float32", op, algo, form, **kw)
 
 
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("P,m", [(2, 1), (5, 4), (8, 16), (13, 7)])
+def test_pipelined_chain(P, m, form):
+    bufs = ar_synth.rank_inputs(P, 100003, "bfloat16", "normal", sigma=1e-2, seed=m)
+    for op in ("sum", "min"):
+        check_faithful(bufs, "bfloat16", op, "pipeline", form, blocks=m)
+
+
 # ---- configuration 3: generalized, P = 7 and 12 ----------------------------------------
 
 @pytest.mark.parametrize("form", FORMS)

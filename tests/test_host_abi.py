@@ -67,6 +67,8 @@ def _cases():
                 yield "generalized", P, {"group": "xor", "r": r}
         for sizes in ([P], [1] * P, [P // 2, P - P // 2] if P > 1 else [1], [2, P - 2] if P >= 4 else [P]):
             yield "ahc", P, {"group_sizes": sizes}
+        for m in (1, 3):
+            yield "pipeline", P, {"blocks": m}
 
 
 @pytest.mark.parametrize("op", ["max", "sum"])
@@ -116,6 +118,8 @@ def test_ahc_twelve_chunks(lib):
     ((5, 8, "float32", "sum", "ahc", {"group_sizes": [0, 5]}), "AR_ERR_INVALID_ARG"),
     ((5, 8, "float32", "sum", "ahc", {}), "AR_ERR_INVALID_ARG"),
     ((5, 8, "float32", "sum", "ring", {"form": "step", "order": "fp32acc"}), "AR_ERR_UNSUPPORTED"),
+    ((5, 8, "float32", "sum", "pipeline", {"blocks": -1}), "AR_ERR_INVALID_ARG"),
+    ((5, 8, "float32", "sum", "pipeline", {"blocks": 4097}), "AR_ERR_INVALID_ARG"),
     ((60, 8, "float32", "sum", "ahc", {"group_sizes": [7, 8, 9, 11, 13, 12]}), "AR_ERR_UNSUPPORTED"),
 ])
 def test_invalid_requests_rejected(lib, args, status):

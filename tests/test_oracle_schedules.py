@@ -44,6 +44,8 @@ def _cases(Ps=range(1, 17)):
                 yield "generalized", P, {"group": "xor", "r": r}
         for sizes in _partitions(P):
             yield "ahc", P, {"group_sizes": sizes}
+        for m in (1, 2, 3, 5):
+            yield "pipeline", P, {"blocks": m}
 
 
 def _partitions(P):
@@ -82,6 +84,8 @@ def _expected_steps(algo, P, p):
     if algo == "ahc":
         g = p["group_sizes"]
         return 2 * (max(g) - 1) + 2 * (len(g) - 1)
+    if algo == "pipeline":
+        return 0 if P == 1 else 2 * (P + p["blocks"] - 2)
     raise AssertionError(algo)
 
 
@@ -403,3 +407,33 @@ def test_non_power_of_two_fold_tree():
     for r, t in want.items():
         assert tree_str(res.bufs[r][0]) == t
     assert tree_str(res.bufs[4][0]) == want[0] and tree_str(res.bufs[5][0]) == want[1]
+
+
+def test_pipeline_reduce_phase_matches_page(golden):
+    """p + m - 2 parallel steps until the last unit holds every block; each
+    block reaches it as the chain x_{p-1} (+) (... (+) (x_1 (+) x_0))."""
+    g = golden("pipeline_reduce.json")
+    for c in g["reduce_steps"]:
+        p, m = c["p"], c["m"]
+        n = 3 * m
+        res = oracle.run("pipeline", leaf_buffers(p, n), Symbolic(), blocks=m)
+        assert res.steps == 2 * c["steps"]
+        # the reduce phase: rounds in which some unit sends towards p - 1
+        first_half = res.sent[:c["steps"]]
+        assert all(sum(s) > 0 for s in first_half)
+        assert all(s[p - 1] == 0 for s in first_half)
+        chain = "0"
+        for i in range(1, p):
+            chain = f"({i}+{chain})"
+        assert all(tree_str(x) == chain for b in res.bufs for x in b)
+
+
+def test_pipeline_optimal_block_count(golden):
+    """The page's optimal m minimises its own runtime model."""
+    for c in golden("pipeline_reduce.json")["optimal_m"]:
+        n, p, tb, ts = c["n"], c["p"], c["T_byte"], c["T_start"]
+        def T(m):
+            return (ts + n / m * tb) * (p + m - 2)
+        m_star = (n * (p - 2) * tb / ts) ** 0.5
+        assert T(m_star) <= T(m_star * 0.9) and T(m_star) <= T(m_star * 1.1)
+        assert T(m_star) <= min(T(m) for m in range(1, 4 * int(m_star) + 10)) * (1 + 1e-9) or m_star < 1
