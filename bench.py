@@ -533,7 +533,10 @@ def run_sweep(a, path):
 
 
 def config_cases():
-    """The schedules of the four parity configurations, each in every form."""
+    """The schedules of the four parity configurations, each in every form,
+    then the widened ones: RD / RH / hybrid on a non-power-of-two P through
+    the preparation and finalization rounds, the pipelined chain, and the
+    reduce-scatter and all-gather halves on their own."""
     cases = []
     for form in ("fused", "step"):
         cases.append(("config1", 3, 1024, "int32", "sum", "ring", {"form": form}, ("uniform_int", 1.0)))
@@ -551,6 +554,18 @@ def config_cases():
     for kw in ({"form": "fused"}, {"form": "fused", "order": "fp32acc"}, {"form": "step"}):
         cases.append(("config4", 5, 1 << 24, "bfloat16", "sum", "ahc", dict(kw, group_sizes=[2, 3]),
                       ("normal", 1e-3)))
+    for algo, kw in (("rd", {}), ("rh", {}), ("hybrid", {"k1": 1})):
+        for form in ("fused", "step"):
+            cases.append(("fold_p12", 12, 1 << 20, "float32", "sum", algo, dict(kw, form=form), ("normal", 1.0)))
+    for m in (1, 16):
+        for form in ("fused", "step"):
+            cases.append(("pipeline_p8", 8, 1 << 20, "bfloat16", "sum", "pipeline", {"blocks": m, "form": form},
+                          ("normal", 1e-2)))
+    for phase in ("reduce_scatter", "all_gather"):
+        for algo, kw in (("ring", {}), ("rh", {}), ("generalized", {})):
+            for form in ("fused", "step"):
+                cases.append(("halves_p8", 8, 1 << 24, "float32", "sum", algo, dict(kw, form=form, phase=phase),
+                              ("normal", 1.0)))
     return cases
 
 
@@ -588,7 +603,7 @@ def run_configs(a, path):
             plan.check()
             got = [t.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bfloat16" else t.cpu().numpy()
                    for t in dev]
-            okw = {k: v for k, v in kw.items() if k in ("r", "k1", "group_sizes", "blocks")}
+            okw = {k: v for k, v in kw.items() if k in ("r", "k1", "group_sizes", "blocks", "phase")}
             t0 = time.perf_counter()
             want = oracle.run(algo, host, Arith(op, dtype), **okw)
             oracle_s = time.perf_counter() - t0
@@ -600,7 +615,12 @@ def run_configs(a, path):
                 def bits(x):
                     x = np.ascontiguousarray(x)
                     return x if x.dtype == np.uint16 else x.view(np.uint32)
-                ok = all(np.array_equal(bits(g), bits(w)) for g, w in zip(got, want.bufs))
+                if kw.get("phase") == "reduce_scatter":
+                    # only the owners' chunks are defined after a reduce-scatter
+                    ok = all(np.array_equal(bits(got[r][lo:hi]), bits(want.bufs[r][lo:hi]))
+                             for r, lo, hi in want.info["owner"])
+                else:
+                    ok = all(np.array_equal(bits(g), bits(w)) for g, w in zip(got, want.bufs))
             for _ in range(3):
                 plan.execute(dev)
             torch.cuda.synchronize()

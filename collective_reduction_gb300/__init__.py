@@ -20,6 +20,7 @@ ALGOS = {"ring": 0, "binomial": 1, "rh": 2, "rd": 3, "hybrid": 4, "generalized":
 FORMS = {"fused": 0, "step": 1}
 ORDERS = {"faithful": 0, "fp32acc": 1}
 GROUPS = {"cyclic": 0, "xor": 1}
+PHASES = {"allreduce": 0, "reduce_scatter": 1, "all_gather": 2}
 ESIZE = {"int32": 4, "float32": 4, "bfloat16": 2}
 MAX_RANKS = 64
 
@@ -39,12 +40,13 @@ class ArError(RuntimeError):
 class Params(ctypes.Structure):
     _fields_ = [("form", ctypes.c_int), ("order", ctypes.c_int), ("group", ctypes.c_int),
                 ("r", ctypes.c_int), ("k1", ctypes.c_int), ("n_groups", ctypes.c_int),
-                ("group_sizes", ctypes.POINTER(ctypes.c_int)), ("blocks", ctypes.c_int)]
+                ("group_sizes", ctypes.POINTER(ctypes.c_int)), ("blocks", ctypes.c_int),
+                ("phase", ctypes.c_int)]
 
 
 class Info(ctypes.Structure):
     _fields_ = [("P", ctypes.c_int), ("dtype", ctypes.c_int), ("op", ctypes.c_int), ("algo", ctypes.c_int),
-                ("form", ctypes.c_int), ("order", ctypes.c_int), ("n", ctypes.c_uint64),
+                ("form", ctypes.c_int), ("order", ctypes.c_int), ("phase", ctypes.c_int), ("n", ctypes.c_uint64),
                 ("steps", ctypes.c_int), ("sent_bytes_max", ctypes.c_uint64),
                 ("sent_bytes_total", ctypes.c_uint64), ("combines", ctypes.c_uint64),
                 ("max_slots", ctypes.c_int), ("n_segments", ctypes.c_int),
@@ -105,8 +107,9 @@ def _check(status, where):
         raise ArError(status, where)
 
 
-def _params(form="fused", order="faithful", group="cyclic", r=0, k1=0, group_sizes=None, blocks=1):
-    p = Params(FORMS[form], ORDERS[order], GROUPS[group], int(r), int(k1), 0, None, int(blocks))
+def _params(form="fused", order="faithful", group="cyclic", r=0, k1=0, group_sizes=None, blocks=1,
+            phase="allreduce"):
+    p = Params(FORMS[form], ORDERS[order], GROUPS[group], int(r), int(k1), 0, None, int(blocks), PHASES[phase])
     keep = None
     if group_sizes is not None:
         keep = (ctypes.c_int * len(group_sizes))(*[int(g) for g in group_sizes])

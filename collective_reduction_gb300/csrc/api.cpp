@@ -73,6 +73,7 @@ void fill_info(const ar::Schedule& S, ar_plan_info* info) {
     info->algo = S.algo;
     info->form = S.params.form;
     info->order = S.params.order;
+    info->phase = S.params.phase;
     info->n = static_cast<uint64_t>(S.n);
     info->steps = static_cast<int>(S.rounds.size());
     std::vector<uint64_t> per(S.P, 0);

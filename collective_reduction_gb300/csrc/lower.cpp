@@ -112,8 +112,9 @@ bool left_chain(const Dag& d, int32_t x, std::vector<int32_t>& leaves) {
     return true;
 }
 
-// Straight-line code for the trees outs[r] (one per rank) of a DAG.
-Prog dag_program(const Dag& d, const std::vector<int32_t>& outs) {
+// Straight-line code for the trees outs[k].second that ranks outs[k].first
+// must end with.
+Prog dag_program(const Dag& d, const std::vector<std::pair<int, int32_t>>& outs) {
     const int P = d.P();
     Prog p;
     p.kind = PK_DAG;
@@ -123,9 +124,9 @@ Prog dag_program(const Dag& d, const std::vector<int32_t>& outs) {
     std::map<int32_t, std::vector<int>> stores_of;
     std::vector<char> seen(d.size(), 0);
     std::vector<char> leaf_used(P, 0);
-    for (int r = 0; r < P; ++r) {
-        stores_of[outs[r]].push_back(r);
-        std::vector<std::pair<int32_t, int>> st{{outs[r], 0}};
+    for (const auto& ro : outs) {
+        stores_of[ro.second].push_back(ro.first);
+        std::vector<std::pair<int32_t, int>> st{{ro.second, 0}};
         while (!st.empty()) {
             auto& top = st.back();
             int32_t x = top.first;
@@ -231,44 +232,52 @@ bool tree_program(const Dag& d, int32_t root, std::vector<int32_t>& leaves, std:
     return max_depth <= kTreeDepth && leaves.size() <= static_cast<size_t>(kTreeMaxLeaves);
 }
 
-Prog fused_program(Canon& cn, const Schedule& S, int seg) {
-    const int P = S.P;
-    std::vector<int32_t> outs(P);
-    for (int r = 0; r < P; ++r) outs[r] = cn.get(S.final_at(r, seg));
-    bool same = std::all_of(outs.begin(), outs.end(), [&](int32_t x) { return x == outs[0]; });
+// The ranks a fused pass writes in a segment (every rank for an allreduce).
+std::vector<int> defined_ranks(const Schedule& S, int seg) {
+    std::vector<int> out;
+    for (int r = 0; r < S.P; ++r)
+        if (S.defined_at(r, seg)) out.push_back(r);
+    return out;
+}
+
+void set_outputs(Prog& p, const std::vector<int>& ranks, int P) {
+    for (int r : ranks) p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
+    if (static_cast<int>(ranks.size()) == P) p.flags = PF_OUT_ALL;  // ranks are 0..P-1 in order
+}
+
+Prog fused_program(Canon& cn, const Schedule& S, int seg, const std::vector<int>& ranks) {
+    std::vector<std::pair<int, int32_t>> outs;
+    for (int r : ranks) outs.push_back({r, cn.get(S.final_at(r, seg))});
+    const int32_t x = outs[0].second;
+    bool same = std::all_of(outs.begin(), outs.end(), [&](const std::pair<int, int32_t>& o) { return o.second == x; });
     std::vector<int32_t> leaves;
-    if (same && (right_chain(cn.c, outs[0], leaves) || left_chain(cn.c, outs[0], leaves))) {
+    if (same && (right_chain(cn.c, x, leaves) || left_chain(cn.c, x, leaves))) {
         Prog p;
-        p.kind = right_chain(cn.c, outs[0], leaves) ? PK_CHAIN_R : PK_CHAIN_L;
-        if (p.kind == PK_CHAIN_L) left_chain(cn.c, outs[0], leaves);
-        p.flags = PF_OUT_ALL;
-        for (int32_t x : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, x)));
-        for (int r = 0; r < P; ++r) p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
+        p.kind = right_chain(cn.c, x, leaves) ? PK_CHAIN_R : PK_CHAIN_L;
+        if (p.kind == PK_CHAIN_L) left_chain(cn.c, x, leaves);
+        for (int32_t l : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, l)));
+        set_outputs(p, ranks, S.P);
         return p;
     }
     std::vector<uint32_t> combines;
-    if (same && tree_program(cn.c, outs[0], leaves, combines)) {
+    if (same && tree_program(cn.c, x, leaves, combines)) {
         Prog p;
         p.kind = PK_TREE;
-        p.flags = PF_OUT_ALL;
-        for (int32_t x : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, x)));
+        for (int32_t l : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, l)));
         // combine counts (< kTreeDepth <= 4), 2 bits per leaf, 16 per word
         p.ins.assign(kTreeMaxLeaves / 16, 0);
         for (size_t i = 0; i < combines.size(); ++i) p.ins[i / 16] |= combines[i] << (2 * (i % 16));
-        for (int r = 0; r < P; ++r) p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
+        set_outputs(p, ranks, S.P);
         return p;
     }
     return dag_program(cn.c, outs);
 }
 
-Prog acc_program(int P) {
+Prog acc_program(int P, const std::vector<int>& ranks) {
     Prog p;
     p.kind = PK_ACC;
-    p.flags = PF_OUT_ALL;
-    for (int r = 0; r < P; ++r) {
-        p.in.push_back(static_cast<uint16_t>(buf_id(0, r)));
-        p.out.push_back(static_cast<uint16_t>(buf_id(0, r)));
-    }
+    for (int r = 0; r < P; ++r) p.in.push_back(static_cast<uint16_t>(buf_id(0, r)));
+    set_outputs(p, ranks, P);
     return p;
 }
 
@@ -344,13 +353,15 @@ void lower(const Schedule& S, Lowered& lw) {
     if (S.P > 1 && S.n > 0) {
         if (S.params.form == AR_FORM_FUSED) {
             std::vector<Range> rs;
-            if (S.params.order == AR_ORDER_FP32ACC) {
-                push_range(rs, b.add(acc_program(S.P)), 0, S.n);
-            } else {
-                bool commute = S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD;
-                Canon cn(S.dag, commute);
-                for (int s = 0; s < S.nseg(); ++s)
-                    push_range(rs, b.add(fused_program(cn, S, s)), S.bounds[s], S.bounds[s + 1]);
+            const bool commute = S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD;
+            Canon cn(S.dag, commute);
+            for (int s = 0; s < S.nseg(); ++s) {
+                if (S.bounds[s + 1] <= S.bounds[s]) continue;
+                const std::vector<int> ranks = defined_ranks(S, s);
+                if (ranks.empty()) continue;  // (an all-gather owner-only segment)
+                const Prog p = S.params.order == AR_ORDER_FP32ACC ? acc_program(S.P, ranks)
+                                                                  : fused_program(cn, S, s, ranks);
+                push_range(rs, b.add(p), S.bounds[s], S.bounds[s + 1]);
             }
             sets.push_back(rs);
         } else {

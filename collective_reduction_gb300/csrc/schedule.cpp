@@ -83,6 +83,9 @@ struct Gen {
     int P;        // ranks taking part (0..P-1)
     int64_t n;
     int P_total;  // ranks of the whole schedule (size of the sent counters)
+    int phase;    // AR_PHASE_*: both halves, or the reduce-scatter / all-gather half
+    bool rs() const { return phase != AR_PHASE_ALL_GATHER; }
+    bool ag() const { return phase != AR_PHASE_REDUCE_SCATTER; }
 
     Round& new_round() {
         S.rounds.emplace_back();
@@ -102,14 +105,14 @@ struct Gen {
 // pass chunk (r + 1 - t) mod P on, overwriting.
 void gen_ring(Gen& g) {
     auto ch = ceil_split(g.n, g.P);
-    for (int t = 0; t + 1 < g.P; ++t) {
+    for (int t = 0; g.rs() && t + 1 < g.P; ++t) {
         Round& rd = g.new_round();
         for (int r = 0; r < g.P; ++r) {
             auto c = ch[mod(r - t, g.P)];
             g.msg(rd, r, (r + 1) % g.P, c.first, c.second, true);
         }
     }
-    for (int t = 0; t + 1 < g.P; ++t) {
+    for (int t = 0; g.ag() && t + 1 < g.P; ++t) {
         Round& rd = g.new_round();
         for (int r = 0; r < g.P; ++r) {
             auto c = ch[mod(r + 1 - t, g.P)];
@@ -214,14 +217,16 @@ void gen_fold(Gen& g, Inner inner) {
         return;
     }
     const int e = g.P - Pp;
-    {
+    if (g.rs()) {
         Round& rd = g.new_round();
         for (int i = 0; i < e; ++i) g.msg(rd, Pp + i, i, 0, g.n, true);
     }
-    Gen h{g.S, Pp, g.n, g.P_total};
+    Gen h{g.S, Pp, g.n, g.P_total, g.phase};
     inner(h);
-    Round& rd = g.new_round();
-    for (int i = 0; i < e; ++i) g.msg(rd, i, Pp + i, 0, g.n, false);
+    if (g.ag()) {
+        Round& rd = g.new_round();
+        for (int i = 0; i < e; ++i) g.msg(rd, i, Pp + i, 0, g.n, false);
+    }
 }
 
 // Generalized allreduce ("A Generalization of the Allreduce Operation",
@@ -258,7 +263,7 @@ void gen_generalized(Gen& g, bool xr, int r) {
         throw std::logic_error("generalized: partial not resident");
     };
 
-    for (int i = 0; i < L; ++i) {
+    for (int i = 0; g.rs() && i < L; ++i) {
         const int N = Ns[i], h = N / 2, lo = N - 2 * h;
         std::set<std::pair<int, int32_t>> msgs;
         // (a_dst, t_new) -> (t_dst, a_src, t_src)
@@ -319,7 +324,7 @@ void gen_generalized(Gen& g, bool xr, int r) {
     // found the old slots dead); the distribution copies slot 0 to slot 0
     for (int a = 0; a < T; ++a)
         if (slot_of(a, cur[a][0]) != 0) throw std::logic_error("generalized: result not in slot 0");
-    for (int i = L - r - 1; i >= 0; --i) {
+    for (int i = L - r - 1; g.ag() && i >= 0; --i) {
         const int N = Ns[i], h = N / 2, lo = N - 2 * h;
         Round& rd = g.new_round();
         for (int a = lo; a < lo + h; ++a) {
@@ -455,13 +460,31 @@ void run_symbolic(Schedule& S) {
         for (auto& w : writes) state[w.first] = w.second;
     }
     S.final_node.assign(static_cast<size_t>(P) * nseg, -1);
-    for (int r = 0; r < P; ++r)
-        for (int s = 0; s < nseg; ++s) {
-            int32_t v = at(r, 0, s);
-            if (S.bounds[s + 1] > S.bounds[s] && !S.dag.complete(v))
-                throw std::logic_error("schedule leaves an incomplete reduction");
-            S.final_node[static_cast<size_t>(r) * nseg + s] = v;
+    S.defined.assign(static_cast<size_t>(P) * nseg, 0);
+    const int phase = S.params.phase;
+    for (int s = 0; s < nseg; ++s) {
+        const bool empty = S.bounds[s + 1] <= S.bounds[s];
+        int owners = 0;
+        for (int r = 0; r < P; ++r) {
+            const int32_t v = at(r, 0, s);
+            const size_t k = static_cast<size_t>(r) * nseg + s;
+            S.final_node[k] = v;
+            if (phase == AR_PHASE_ALLREDUCE) {
+                if (!empty && !S.dag.complete(v)) throw std::logic_error("schedule leaves an incomplete reduction");
+                S.defined[k] = 1;
+            } else if (phase == AR_PHASE_REDUCE_SCATTER) {
+                S.defined[k] = S.dag.complete(v);
+                owners += S.defined[k];
+            } else {
+                // all-gather: every rank ends with the owner's own value
+                if (!empty && (!S.dag.leaf(v) || v != at(0, 0, s)))
+                    throw std::logic_error("all-gather leaves ranks disagreeing");
+                S.defined[k] = v != r;
+            }
         }
+        if (phase == AR_PHASE_REDUCE_SCATTER && !empty && owners == 0)
+            throw std::logic_error("reduce-scatter leaves a chunk without an owner");
+    }
 }
 
 }  // namespace
@@ -481,6 +504,7 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
         pr.r = p->r;
         pr.k1 = p->k1;
         pr.blocks = p->blocks == 0 ? 1 : p->blocks;
+        pr.phase = p->phase;
         if (algo == AR_AHC) {
             if (p->n_groups < 1 || !p->group_sizes) return AR_ERR_INVALID_ARG;
             pr.group_sizes.assign(p->group_sizes, p->group_sizes + p->n_groups);
@@ -492,6 +516,14 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
     if (pr.order != AR_ORDER_FAITHFUL && pr.order != AR_ORDER_FP32ACC) return AR_ERR_INVALID_ARG;
     if (pr.group != AR_GROUP_CYCLIC && pr.group != AR_GROUP_XOR) return AR_ERR_INVALID_ARG;
     if (pr.form == AR_FORM_STEP && pr.order == AR_ORDER_FP32ACC) return AR_ERR_UNSUPPORTED;
+    if (pr.phase < AR_PHASE_ALLREDUCE || pr.phase > AR_PHASE_ALL_GATHER) return AR_ERR_INVALID_ARG;
+    // the halves exist for the schedules that split into a reduce-scatter and
+    // an all-gather: the ring, RH and the bandwidth-optimal generalized one
+    if (pr.phase != AR_PHASE_ALLREDUCE) {
+        const bool split = algo == AR_RING || algo == AR_RH || (algo == AR_GENERALIZED && pr.r == 0);
+        if (!split) return AR_ERR_UNSUPPORTED;
+        if (pr.phase == AR_PHASE_ALL_GATHER && pr.order == AR_ORDER_FP32ACC) return AR_ERR_UNSUPPORTED;
+    }
     const int L = ceil_log2(P);
     const bool pow2 = is_pow2(P);
     switch (algo) {
@@ -528,7 +560,7 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
     S.op = op;
     S.algo = algo;
     S.params = pr;
-    Gen g{S, P, n, P};
+    Gen g{S, P, n, P, pr.phase};
     try {
         switch (algo) {
             case AR_RING: gen_ring(g); break;

@@ -56,6 +56,7 @@ struct Params {
     int k1 = 0;
     std::vector<int> group_sizes;
     int blocks = 1;
+    int phase = AR_PHASE_ALLREDUCE;
 };
 
 struct Schedule {
@@ -71,8 +72,13 @@ struct Schedule {
     std::vector<int64_t> bounds;
     Dag dag;
     std::vector<int32_t> final_node;  // [rank * nseg + seg]
+    // Whether the schedule defines rank's result in a segment: every rank for
+    // an allreduce; the owners (complete trees) after a reduce-scatter; the
+    // ranks that receive a copy in an all-gather.
+    std::vector<char> defined;        // [rank * nseg + seg]
     int nseg() const { return static_cast<int>(bounds.size()) - 1; }
     int32_t final_at(int rank, int seg) const { return final_node[rank * nseg() + seg]; }
+    bool defined_at(int rank, int seg) const { return defined[rank * nseg() + seg] != 0; }
     int seg_of(int64_t elem) const;  // segment containing elem (elem < n)
 };
 

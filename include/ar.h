@@ -107,6 +107,16 @@ typedef enum {
 enum { AR_FORM_FUSED = 0, AR_FORM_STEP = 1 };
 enum { AR_ORDER_FAITHFUL = 0, AR_ORDER_FP32ACC = 1 };
 enum { AR_GROUP_CYCLIC = 0, AR_GROUP_XOR = 1 };
+/* Which part of the schedule runs ("All-Reduce, in depth", The APIs: FSDP and
+ * ZeRO use the reduce-scatter for gradients and the all-gather for
+ * parameters).  Available for AR_RING, AR_RH and AR_GENERALIZED with r = 0.
+ *  REDUCE_SCATTER: afterwards every chunk's owner holds its full reduction
+ *    (ring: chunk k on rank k-1 mod P; RH / generalized: chunk k on rank k;
+ *    RH with P not a power of two: ranks 0..P'-1 over P' chunks); the other
+ *    chunks of every buffer are unspecified.
+ *  ALL_GATHER: the owners' chunks (same ownership) are copied to every rank;
+ *    the other chunks' inputs are ignored. */
+enum { AR_PHASE_ALLREDUCE = 0, AR_PHASE_REDUCE_SCATTER = 1, AR_PHASE_ALL_GATHER = 2 };
 
 typedef struct {
     int form;               /* AR_FORM_FUSED or AR_FORM_STEP                      */
@@ -117,11 +127,12 @@ typedef struct {
     int n_groups;           /* AR_AHC: number of groups G                         */
     const int* group_sizes; /* AR_AHC: G sizes adding up to P (copied at create)  */
     int blocks;             /* AR_PIPELINE: blocks m, 1..4096 (0 means 1)         */
+    int phase;              /* AR_PHASE_*; 0 = the whole allreduce               */
 } ar_params;
 
 typedef struct {
     int P;
-    int dtype, op, algo, form, order;
+    int dtype, op, algo, form, order, phase;
     uint64_t n;                  /* elements per rank                              */
     int steps;                   /* rounds of the schedule                         */
     uint64_t sent_bytes_max;     /* max over ranks of bytes sent, all rounds       */

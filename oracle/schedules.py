@@ -34,6 +34,14 @@ Schedules and where they are defined:
   ahc          AHC (HCCL), Description steps 1-3
   pipeline     "還元演算子" (Reduction operator), pipelined algorithm: a chain
                reduce over m blocks, then the mirror-image broadcast
+
+The ring, rh and the generalized schedule with r = 0 split into a
+reduce-scatter and an all-gather ("All-Reduce, in depth", The APIs: the two
+halves are the collectives FSDP and ZeRO call on their own).  phase =
+"reduce_scatter" runs the first half only, "all_gather" the second half only
+on buffers whose owned chunks hold the values to spread; ``Result.info
+["owner"]`` lists (rank, lo, hi): who holds the full reduction of [lo, hi)
+after the first half, and so who supplies it to the second.
 """
 
 import math
@@ -43,6 +51,14 @@ import numpy as np
 from .chunking import ceil_div, ceil_log2, split
 
 ALGOS = ("ring", "binomial", "rd", "rh", "hybrid", "generalized", "ahc", "pipeline")
+PHASES = ("allreduce", "reduce_scatter", "all_gather")
+
+
+def _halves(phase):
+    """(run the reduce-scatter half, run the all-gather half)."""
+    if phase not in PHASES:
+        raise ValueError(f"unknown phase {phase!r}")
+    return phase != "all_gather", phase != "reduce_scatter"
 
 
 class Result:
@@ -108,7 +124,7 @@ def _is_pow2(P):
     return P >= 1 and (P & (P - 1)) == 0
 
 
-def ring(bufs, arith):
+def ring(bufs, arith, phase="allreduce"):
     """Ring reduce-scatter + all-gather over P chunks (ceil split).
 
     Reduce-scatter round t: rank r passes chunk (r - t) mod P to rank r + 1,
@@ -117,14 +133,15 @@ def ring(bufs, arith):
     (r + 1 - t) mod P to rank r + 1, which overwrites its copy.
     2(P - 1) rounds.
     """
+    do_rs, do_ag = _halves(phase)
     sim = RankSim(bufs, arith)
     P, n = sim.P, sim.n
     ch = split(n, P)
-    for t in range(P - 1):
+    for t in range(P - 1 if do_rs else 0):
         sim.round([(r, (r + 1) % P, *ch[(r - t) % P], "add") for r in range(P)])
-    for t in range(P - 1):
+    for t in range(P - 1 if do_ag else 0):
         sim.round([(r, (r + 1) % P, *ch[(r + 1 - t) % P], "copy") for r in range(P)])
-    return sim.result()
+    return sim.result({"owner": [((c - 1) % P, *ch[c]) for c in range(P)]})
 
 
 def binomial(bufs, arith):
@@ -156,7 +173,7 @@ def binomial(bufs, arith):
     return sim.result()
 
 
-def fold_to_pow2(bufs, arith, inner):
+def fold_to_pow2(bufs, arith, inner, phase="allreduce"):
     """Any P by reduction to the largest power of two P' <= P (A Generalization
     of the Allreduce Operation, introduction, the straightforward workaround
     for non-power-of-two process counts): a preparation round in which each
@@ -165,7 +182,10 @@ def fold_to_pow2(bufs, arith, inner):
     which the result goes back.  Excess process P' + i pairs with process i
     (the pages leave the pairing open).  inner(bufs) runs the schedule on P'
     buffers and returns its Result.  A power-of-two P runs inner directly.
+    A reduce-scatter keeps the preparation round and an all-gather the
+    finalization round; the excess processes own no chunk.
     """
+    do_rs, do_ag = _halves(phase)
     P = len(bufs)
     Pp = 1
     while Pp * 2 <= P:
@@ -175,14 +195,16 @@ def fold_to_pow2(bufs, arith, inner):
     n = len(bufs[0])
     e = P - Pp
     pre = RankSim(bufs, arith)
-    pre.round([(Pp + i, i, 0, n, "add") for i in range(e)])
+    if do_rs:
+        pre.round([(Pp + i, i, 0, n, "add") for i in range(e)])
     res = inner(pre.buf[:Pp])
     post = RankSim(list(res.bufs) + [pre.buf[Pp + i] for i in range(e)], arith)
-    post.round([(i, Pp + i, 0, n, "copy") for i in range(e)])
-    sent = [pre.sent[0]] + [list(s) + [0] * e for s in res.sent] + [post.sent[0]]
+    if do_ag:
+        post.round([(i, Pp + i, 0, n, "copy") for i in range(e)])
+    sent = pre.sent + [list(s) + [0] * e for s in res.sent] + post.sent
     # one counter serves all three parts: everything since the preparation
     combines = arith.combines - pre.start
-    return Result(post.buf, sent, combines, {"P_pow2": Pp, "excess": e})
+    return Result(post.buf, sent, combines, dict(res.info, P_pow2=Pp, excess=e))
 
 
 def _rd_pow2(bufs, arith, first):
@@ -248,39 +270,60 @@ def pow2_floor(P):
     return Pp
 
 
-def rh(bufs, arith):
+def rh(bufs, arith, phase="allreduce"):
     """Recursive halving reduce-scatter + recursive doubling all-gather.
 
     2 log P rounds; rank r ends the reduce-scatter with chunk r.  Other P:
     fold_to_pow2 around it (2 log P' + 2 rounds).
     """
-    return hybrid(bufs, arith, ceil_log2(pow2_floor(len(bufs))))
+    return hybrid(bufs, arith, ceil_log2(pow2_floor(len(bufs))), phase)
 
 
-def hybrid(bufs, arith, k1):
+def hybrid(bufs, arith, k1, phase="allreduce"):
     """Classic hybrid: k1 halving rounds, recursive doubling (distance 1
     first) on the block each rank then owns, k1 doubling rounds.
 
     k1 = 0 is recursive doubling, k1 = log P is recursive halving; log P + k1
     rounds.  Other P: fold_to_pow2 around it, k1 in 0..log P'.
     """
-    if not 0 <= k1 <= ceil_log2(pow2_floor(len(bufs))):
+    Lp = ceil_log2(pow2_floor(len(bufs)))
+    if not 0 <= k1 <= Lp:
         raise ValueError("k1 must lie in 0..log P'")
-    return fold_to_pow2(bufs, arith, lambda b: _hybrid_pow2(b, arith, k1))
+    if phase != "allreduce" and k1 != Lp:
+        raise ValueError("only recursive halving (k1 = log P') splits into halves")
+    return fold_to_pow2(bufs, arith, lambda b: _hybrid_pow2(b, arith, k1, phase), phase)
 
 
-def _hybrid_pow2(bufs, arith, k1):
+def _hybrid_pow2(bufs, arith, k1, phase="allreduce"):
+    do_rs, do_ag = _halves(phase)
     sim = RankSim(bufs, arith)
     P, n = sim.P, sim.n
     L = ceil_log2(P)
     ch = split(n, P)
     own = [(0, P)] * P
-    _halving_rounds(sim, ch, own, L, k1)
+    if do_rs:
+        _halving_rounds(sim, ch, own, L, k1)
+    else:
+        # the ranges the halving would leave (no messages): rank r, chunk r
+        _halving_rounds(_Dry(P), ch, own, L, k1)
+    owner = [(r, *_chunk_span(ch, *own[r])) for r in range(P)] if k1 == L else []
     for k in range(L - k1):
         d = 1 << k
         sim.round([(r ^ d, r, *_chunk_span(ch, *own[r]), "add") for r in range(P)])
-    _doubling_rounds(sim, ch, own, k1)
-    return sim.result()
+    if do_ag:
+        _doubling_rounds(sim, ch, own, k1)
+    return sim.result({"owner": owner})
+
+
+class _Dry:
+    """Stands in for a RankSim where only the ownership bookkeeping of
+    _halving_rounds is wanted: it accepts and drops every round."""
+
+    def __init__(self, P):
+        self.P = P
+
+    def round(self, msgs):
+        pass
 
 
 class _Trees:
@@ -317,7 +360,7 @@ def generalized_plan(P, group, r):
     return Ns, L, Ns[L - r]
 
 
-def generalized(bufs, arith, group="cyclic", r=0):
+def generalized(bufs, arith, group="cyclic", r=0, phase="allreduce"):
     """The group-theoretic generalized allreduce.
 
     Positions model.  The group T_P acts on ranks: cyclic t_a(c) = (a + c)
@@ -338,10 +381,19 @@ def generalized(bufs, arith, group="cyclic", r=0):
     Distribution, steps i = L-r-1 down to 0: positions lo..lo+h-1 copy to +h.
     With r = L (latency-optimal) there is none, and every rank keeps its own
     target's result.
+
+    With r = 0 the reduction steps are a reduce-scatter (position 0 ends with
+    the result, so rank t_0(c) = c holds chunk c) and the distribution an
+    all-gather of position 0's vector.  A reduce-scatter leaves every rank's
+    other chunks as they came in; an all-gather takes position 0's vector from
+    the input.
     """
+    do_rs, do_ag = _halves(phase)
     P = len(bufs)
     n = len(bufs[0])
     Ns, L, T = generalized_plan(P, group, r)
+    if phase != "allreduce" and r != 0:
+        raise ValueError("only r = 0 splits into halves")
     ch = split(n, P)
     cyc = group == "cyclic"
 
@@ -382,7 +434,7 @@ def generalized(bufs, arith, group="cyclic", r=0):
         cur.append(row)
 
     sent, trace = [], []
-    for i in range(L):
+    for i in range(L if do_rs else 0):
         N = Ns[i]
         h = N // 2
         lo = N - 2 * h
@@ -421,7 +473,7 @@ def generalized(bufs, arith, group="cyclic", r=0):
                       "max_live_per_position": max(len(v) for v in per_pos.values())})
 
     final = {a: values[(a, cur[a][0])] for a in range(T)}
-    for i in reversed(range(L - r)):
+    for i in reversed(range(L - r if do_ag else 0)):
         N = Ns[i]
         h = N // 2
         lo = N - 2 * h
@@ -438,9 +490,13 @@ def generalized(bufs, arith, group="cyclic", r=0):
     for rank in range(P):
         b = arith.empty(n)
         for c, (clo, chi) in enumerate(ch):
-            b[clo:chi] = final[pos_of(rank, c)][clo:chi]
+            if pos_of(rank, c) in final:
+                b[clo:chi] = final[pos_of(rank, c)][clo:chi]
+            else:
+                b[clo:chi] = bufs[rank][clo:chi]
         out.append(b)
-    info = {"L": L, "T": T, "Ns": Ns, "trace": trace}
+    owner = [(rank_of(0, c), *ch[c]) for c in range(P)] if r == 0 else []
+    info = {"L": L, "T": T, "Ns": Ns, "trace": trace, "owner": owner}
     return Result(out, sent, arith.combines - start, info)
 
 
@@ -555,20 +611,22 @@ def ahc(bufs, arith, group_sizes):
     return sim.result(info)
 
 
-def run(algo, bufs, arith, group="cyclic", r=0, k1=0, group_sizes=None, blocks=1):
-    """Run one schedule by name."""
+def run(algo, bufs, arith, group="cyclic", r=0, k1=0, group_sizes=None, blocks=1, phase="allreduce"):
+    """Run one schedule by name; phase picks a half of the splitting ones."""
+    if phase != "allreduce" and algo not in ("ring", "rh", "generalized"):
+        raise ValueError(f"{algo} does not split into a reduce-scatter and an all-gather")
     if algo == "ring":
-        return ring(bufs, arith)
+        return ring(bufs, arith, phase)
     if algo == "binomial":
         return binomial(bufs, arith)
     if algo == "rd":
         return rd(bufs, arith)
     if algo == "rh":
-        return rh(bufs, arith)
+        return rh(bufs, arith, phase)
     if algo == "hybrid":
         return hybrid(bufs, arith, k1)
     if algo == "generalized":
-        return generalized(bufs, arith, group, r)
+        return generalized(bufs, arith, group, r, phase)
     if algo == "ahc":
         return ahc(bufs, arith, group_sizes)
     if algo == "pipeline":

@@ -329,3 +329,71 @@ def test_repeated_execute_and_streams():
     for t in dev:
         assert np.array_equal(to_host(t, "int32"), want)
     plan.close()
+
+
+# ---- reduce-scatter / all-gather halves -------------------------------------------------
+
+SPLIT = [("ring", {}), ("rh", {}), ("generalized", {"group": "cyclic"})]
+
+
+def _owners(algo, P, n, kw):
+    """(rank, lo, hi): who holds [lo, hi) after the oracle's reduce-scatter."""
+    zeros = [np.zeros(n, np.int32)] * P
+    return oracle.run(algo, zeros, Arith("sum", "int32"), phase="reduce_scatter", **kw).info["owner"]
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+@pytest.mark.parametrize("P", [3, 8, 12])
+def test_reduce_scatter_owned_chunks(P, dtype, form):
+    """Each owner's chunk bit-identical to the oracle's reduce-scatter; the
+    other chunks are unspecified and not compared."""
+    n = 100003
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1e-2, seed=P + 7)
+    cases = SPLIT + ([("generalized", {"group": "xor"})] if P & (P - 1) == 0 else [])
+    for algo, kw in cases:
+        for op in ("sum", "max"):
+            res = oracle.run(algo, bufs, Arith(op, dtype), phase="reduce_scatter", **kw)
+            got = engine(bufs, dtype, op, algo, form=form, phase="reduce_scatter", **kw)
+            for rank, lo, hi in res.info["owner"]:
+                assert_bit_equal(got[rank][lo:hi], res.bufs[rank][lo:hi], dtype,
+                                 f"{algo} {kw} {op} rank {rank} [{lo}, {hi})")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_reduce_scatter_fp32acc_within_tolerance(dtype):
+    P, n = 8, (1 << 22) + 9
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=41)
+    ref = direct_f64(bufs, "sum", dtype)
+    tol = 1e-6 if dtype == "float32" else 4e-3
+    from oracle.elementops import bf16_to_f32
+    for algo, kw in SPLIT:
+        owner = _owners(algo, P, n, kw)
+        got = engine(bufs, dtype, "sum", algo, order="fp32acc", phase="reduce_scatter", **kw)
+        y = np.empty(n, np.float64)
+        for rank, lo, hi in owner:
+            g = got[rank][lo:hi]
+            y[lo:hi] = bf16_to_f32(g) if dtype == "bfloat16" else g
+        assert normwise_rel_err(y, ref) <= tol, algo
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+@pytest.mark.parametrize("P", [2, 7, 12, 16])
+def test_all_gather_spreads_owned_chunks(P, dtype, form):
+    """Every rank ends with the owners' chunks, bit for bit; what the other
+    chunks held beforehand (here a sentinel) must not survive anywhere."""
+    n = 77777
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    src = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 9)
+    cases = SPLIT + ([("generalized", {"group": "xor"})] if P & (P - 1) == 0 else [])
+    for algo, kw in cases:
+        owner = _owners(algo, P, n, kw)
+        bufs = [np.full_like(b, 0x7BCD if dtype == "bfloat16" else -12345) for b in src]
+        for rank, lo, hi in owner:
+            bufs[rank][lo:hi] = src[rank][lo:hi]
+        want = oracle.run(algo, bufs, Arith("sum", dtype), phase="all_gather", **kw).bufs
+        got = engine(bufs, dtype, "sum", algo, form=form, phase="all_gather", **kw)
+        for r in range(P):
+            assert_bit_equal(got[r], want[r], dtype, f"{algo} {kw} rank {r}")

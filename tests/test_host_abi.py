@@ -150,3 +150,63 @@ def test_tree_buffer_too_small(lib):
     assert need.value == len("(3+(2+(1+0)))") + 1
     assert lib.ar_schedule_tree(s._h, 4, 0, buf, 2, ctypes.byref(need)) == 1
     assert lib.ar_schedule_tree(s._h, 0, 8, buf, 2, ctypes.byref(need)) == 1
+
+
+def _split_cases():
+    for P in (1, 2, 3, 5, 7, 8, 12, 16):
+        yield "ring", P, {}
+        yield "rh", P, {}
+        yield "generalized", P, {"group": "cyclic"}
+        if P & (P - 1) == 0:
+            yield "generalized", P, {"group": "xor"}
+
+
+@pytest.mark.parametrize("phase", ["reduce_scatter", "all_gather"])
+def test_compiler_halves_match_oracle(lib, phase):
+    """The reduce-scatter / all-gather plans: rounds, traffic and, on every
+    element the half defines, the tree, as in the oracle's simulation."""
+    for algo, P, kw in _split_cases():
+        for n in (2 * P + 3, P - 1 if P > 1 else 1):
+            s = ar.Schedule(P, n, "float32", "sum", algo, phase=phase, **kw)
+            res = oracle.run(algo, leaf_buffers(P, n), Symbolic(), phase=phase, **kw)
+            info = s.info()
+            assert info["phase"] == ar.PHASES[phase]
+            assert info["steps"] == res.steps, (algo, P, kw)
+            for i in range(res.steps):
+                assert s.step_sent(i) == res.sent[i], (algo, P, kw, i)
+            assert info["combines"] == res.combines
+            if phase == "reduce_scatter":
+                cells = [(rank, e) for rank, lo, hi in res.info["owner"] for e in range(lo, hi)]
+            else:
+                cells = [(rank, e) for rank in range(P) for e in range(n)]
+            for rank, e in cells:
+                assert s.tree(rank, e) == tree_str(res.bufs[rank][e]), (algo, P, kw, rank, e)
+            s.close()
+
+
+@pytest.mark.parametrize("algo,kw,status", [
+    ("binomial", {}, "AR_ERR_UNSUPPORTED"),
+    ("rd", {}, "AR_ERR_UNSUPPORTED"),
+    ("hybrid", {"k1": 1}, "AR_ERR_UNSUPPORTED"),
+    ("generalized", {"r": 1}, "AR_ERR_UNSUPPORTED"),
+    ("ahc", {"group_sizes": [3, 5]}, "AR_ERR_UNSUPPORTED"),
+    ("pipeline", {"blocks": 2}, "AR_ERR_UNSUPPORTED"),
+])
+def test_halves_rejected_for_other_schedules(lib, algo, kw, status):
+    for phase in ("reduce_scatter", "all_gather"):
+        with pytest.raises(ar.ArError) as e:
+            ar.Schedule(8, 64, "float32", "sum", algo, phase=phase, **kw)
+        assert e.value.name == status
+
+
+def test_halves_parameter_checks(lib):
+    with pytest.raises(ar.ArError) as e:
+        ar.Schedule(8, 64, "float32", "sum", "ring", phase="all_gather", order="fp32acc")
+    assert e.value.name == "AR_ERR_UNSUPPORTED"
+    p, _keep = ar._params()
+    p.phase = 3
+    h = ctypes.c_void_p()
+    assert lib.ar_schedule_create(8, 64, 1, 0, 0, ctypes.byref(p), ctypes.byref(h)) == 1
+    # the fp32-accumulation reduce-scatter is a one-pass plan too
+    s = ar.Schedule(8, 64, "bfloat16", "sum", "ring", phase="reduce_scatter", order="fp32acc")
+    assert s.info()["steps"] == 7

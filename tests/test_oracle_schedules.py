@@ -437,3 +437,132 @@ def test_pipeline_optimal_block_count(golden):
         m_star = (n * (p - 2) * tb / ts) ** 0.5
         assert T(m_star) <= T(m_star * 0.9) and T(m_star) <= T(m_star * 1.1)
         assert T(m_star) <= min(T(m) for m in range(1, 4 * int(m_star) + 10)) * (1 + 1e-9) or m_star < 1
+
+
+# --- reduce-scatter / all-gather halves ("All-Reduce, in depth", The APIs) ---
+
+def _split_cases(Ps=range(1, 17)):
+    for P in Ps:
+        yield "ring", P, {}
+        yield "rh", P, {}
+        yield "generalized", P, {"group": "cyclic"}
+        if _pow2(P):
+            yield "generalized", P, {"group": "xor"}
+
+
+def test_reduce_scatter_owners_are_the_pages_ranks():
+    """Ring: rank r ends the reduce-scatter with chunk r + 1 (the ring
+    algorithm's reduce-scatter); RH: rank r with chunk r (halving keeps the
+    half whose bit matches the rank's); generalized r = 0: position 0's
+    vector, whose chunk c lives on rank t_0(c) = c.  RH with P not a power of
+    two: P' chunks on ranks 0..P'-1, the excess ranks own nothing."""
+    for algo, P, p in _split_cases():
+        n = 3 * P + 2
+        res = oracle.run(algo, [np.zeros(n, np.int32)] * P, Arith("sum", "int32"), phase="reduce_scatter", **p)
+        Pp = _pow2_floor(P) if algo == "rh" else P
+        ch = split(n, Pp)
+        want = [(((c - 1) % P) if algo == "ring" else c, *ch[c]) for c in range(Pp)]
+        assert res.info["owner"] == want, (algo, P, p)
+
+
+def test_reduce_scatter_leaves_owners_complete_trees(golden):
+    for algo, P, p in _split_cases():
+        n = 2 * P + 3
+        res = oracle.run(algo, leaf_buffers(P, n), Symbolic(), phase="reduce_scatter", **p)
+        owned = set()
+        for rank, lo, hi in res.info["owner"]:
+            for e in range(lo, hi):
+                assert sorted(tree_leaves(res.bufs[rank][e])) == list(range(P)), (algo, P, p, rank, e)
+                owned.add((rank, e))
+        # every element has exactly one owner; nobody else is complete (P > 1)
+        assert sorted(e for _r, e in owned) == list(range(n))
+        if P > 1:
+            for r in range(P):
+                for e in range(n):
+                    if (r, e) not in owned:
+                        assert sorted(tree_leaves(res.bufs[r][e])) != list(range(P)), (algo, P, p, r, e)
+    # the owner's tree is the page's ring tree for its chunk
+    for case in golden("ring_trees.json")["cases"]:
+        P, K = case["P"], 3
+        res = oracle.run("ring", leaf_buffers(P, P * K), Symbolic(), phase="reduce_scatter")
+        for k, want in enumerate(case["chunk_trees"]):
+            for e in range(k * K, (k + 1) * K):
+                assert tree_str(res.bufs[(k - 1) % P][e]) == want
+
+
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+def test_reduce_scatter_then_all_gather_is_the_allreduce(dtype):
+    """The allreduce is exactly its two halves run back to back: same values
+    bit for bit, same rounds, same traffic."""
+    rng = np.random.default_rng(21)
+    for algo, P, p in _split_cases():
+        for n in (0, 1, P - 1, 2 * P + 3, 37):
+            if n < 0:
+                continue
+            if dtype == "int32":
+                bufs = [rng.integers(-1000, 1001, n).astype(np.int32) for _ in range(P)]
+            else:
+                bufs = [rng.standard_normal(n).astype(np.float32) for _ in range(P)]
+                if dtype == "bfloat16":
+                    from oracle.elementops import f32_to_bf16_rne
+                    bufs = [f32_to_bf16_rne(b) for b in bufs]
+            full = oracle.run(algo, bufs, Arith("sum", dtype), **p)
+            rs = oracle.run(algo, bufs, Arith("sum", dtype), phase="reduce_scatter", **p)
+            ag = oracle.run(algo, rs.bufs, Arith("sum", dtype), phase="all_gather", **p)
+            for r in range(P):
+                assert np.array_equal(ag.bufs[r].view(np.uint8), full.bufs[r].view(np.uint8)), (algo, P, p, n, r)
+            assert rs.steps + ag.steps == full.steps
+            assert rs.sent + ag.sent == full.sent
+            assert rs.combines == full.combines and ag.combines == 0
+
+
+def test_halves_traffic_closed_forms():
+    """Each half of the ring, of RH (P a power of two) and of the
+    bandwidth-optimal generalized schedule moves (P - 1) n / P elements per
+    rank when P divides n; the ring and generalized take P - 1 and
+    ceil(log2 P) rounds per half, RH log2 P' (+ 1 for the preparation or
+    finalization round otherwise)."""
+    for algo, P, p in _split_cases():
+        n = 8 * P
+        z = [np.zeros(n, np.int32)] * P
+        for phase in ("reduce_scatter", "all_gather"):
+            res = oracle.run(algo, z, Arith("sum", "int32"), phase=phase, **p)
+            if algo == "ring":
+                assert res.steps == P - 1
+            elif algo == "rh":
+                assert res.steps == ceil_log2(_pow2_floor(P)) + (0 if _pow2(P) else 1)
+            else:
+                assert res.steps == ceil_log2(P)
+            if algo != "rh" or _pow2(P):
+                assert res.sent_per_rank() == [(P - 1) * n // P] * P, (algo, P, phase)
+
+
+def test_all_gather_reads_only_owned_chunks():
+    """Inputs outside the owned chunks never reach the result: fill them
+    with a sentinel and every rank still ends with the owners' chunks."""
+    rng = np.random.default_rng(22)
+    for algo, P, p in _split_cases():
+        n = 3 * P + 1
+        owner = oracle.run(algo, [np.zeros(n, np.int32)] * P, Arith("sum", "int32"), phase="reduce_scatter",
+                           **p).info["owner"]
+        bufs = [np.full(n, -7777, np.int32) for _ in range(P)]
+        want = np.full(n, -7777, np.int32)
+        for rank, lo, hi in owner:
+            v = rng.integers(0, 1000, hi - lo).astype(np.int32)
+            bufs[rank][lo:hi] = v
+            want[lo:hi] = v
+        res = oracle.run(algo, bufs, Arith("sum", "int32"), phase="all_gather", **p)
+        assert (want != -7777).all() or n == 0
+        for r in range(P):
+            assert np.array_equal(res.bufs[r], want), (algo, P, p, r)
+        assert res.combines == 0
+
+
+def test_halves_only_for_splitting_schedules():
+    z = [np.zeros(8, np.int32)] * 4
+    for algo, kw in (("binomial", {}), ("rd", {}), ("pipeline", {"blocks": 2}), ("generalized", {"r": 1}),
+                     ("hybrid", {"k1": 1}), ("ahc", {"group_sizes": [2, 2]})):
+        with pytest.raises(ValueError):
+            oracle.run(algo, z, Arith("sum", "int32"), phase="reduce_scatter", **kw)
+    with pytest.raises(ValueError):
+        oracle.run("ring", z, Arith("sum", "int32"), phase="scatter")
