@@ -15,7 +15,7 @@ import ctypes
 import os
 
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2}
-OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
+OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
 ALGOS = {"ring": 0, "binomial": 1, "rh": 2, "rd": 3, "hybrid": 4, "generalized": 5, "ahc": 6, "pipeline": 7}
 FORMS = {"fused": 0, "step": 1}
 ORDERS = {"faithful": 0, "fp32acc": 1}

@@ -30,6 +30,9 @@ enum ProgKind : uint8_t { PK_CHAIN_R = 0, PK_CHAIN_L = 1, PK_DAG = 2, PK_ACC = 3
 // DevProg::flags: the outputs are every rank's own buffer in rank order, so a
 // kernel can take output o's address straight from the rank-pointer array
 constexpr uint8_t PF_OUT_ALL = 1;
+// DevProg::flags: the program's result is a complete AR_AVG sum, divided by P
+// before it is stored
+constexpr uint8_t PF_AVG = 2;
 
 // value references inside DAG instructions (10 bits)
 constexpr uint32_t REF_TMP = 0x200;  // bit 9 set: temporary index in bits 0..8
@@ -54,14 +57,16 @@ constexpr int kTreeMaxLeaves = 64;   // TREE combine counts: 2 bits per leaf in 
 // instruction word: bits 30..31 kind
 //   OP:    a = bits 0..9, b = bits 10..19, d = bits 20..29
 //   STORE: v = bits 0..9, buffer id = bits 10..25
+//   STORE_AVG: as STORE, the value divided by P first (AR_AVG results)
 constexpr uint32_t INS_OP = 0u;
 constexpr uint32_t INS_STORE = 1u;
+constexpr uint32_t INS_STORE_AVG = 2u;
 
 AR_HD inline uint32_t ins_op(uint32_t a, uint32_t b, uint32_t d) {
     return (INS_OP << 30) | a | (b << 10) | (d << 20);
 }
-AR_HD inline uint32_t ins_store(uint32_t v, uint32_t buf) {
-    return (INS_STORE << 30) | v | (buf << 10);
+AR_HD inline uint32_t ins_store(uint32_t v, uint32_t buf, bool avg = false) {
+    return ((avg ? INS_STORE_AVG : INS_STORE) << 30) | v | (buf << 10);
 }
 
 // Buffer id: (slot << 6) | rank.  Slot 0 is the rank's own buffer; slot s >= 1

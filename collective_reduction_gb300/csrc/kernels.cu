@@ -86,6 +86,20 @@ __device__ __forceinline__ uint4 vop(uint4 a, uint4 b) {
                       wop<DT, OP>(a.w, b.w));
 }
 
+// AR_AVG: a complete sum divided by the rank count d (IEEE division, round to
+// nearest even; bf16 values divided in fp32 and rounded back to bf16).
+template <int DT>
+__device__ __forceinline__ uint32_t wdiv(uint32_t w, float d) {
+    if (DT == AR_FLOAT32) return __float_as_uint(__fdiv_rn(__uint_as_float(w), d));
+    if (DT == AR_BFLOAT16) return pack_bf16x2(__fdiv_rn(bf_lo(w), d), __fdiv_rn(bf_hi(w), d));
+    return w;  // int32 has no average (refused when the plan is made)
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 vdiv(uint4 v, float d) {
+    return make_uint4(wdiv<DT>(v.x, d), wdiv<DT>(v.y, d), wdiv<DT>(v.z, d), wdiv<DT>(v.w, d));
+}
+
 // Accumulator of the FP32ACC order: int32 stays int32 (exact in any order),
 // fp32 and bf16 accumulate in fp32 and round once.
 template <int DT>
@@ -124,6 +138,15 @@ __device__ __forceinline__ void acc_combine(Acc<DT>& x, const Acc<DT>& y) {
     }
 }
 
+// AR_AVG on the fp32 accumulator, before the one rounding to the dtype
+template <int DT>
+__device__ __forceinline__ void acc_div(Acc<DT>& x, float d) {
+    if (DT != AR_INT32) {
+#pragma unroll
+        for (int q = 0; q < Acc<DT>::W; ++q) x.f[q] = __fdiv_rn(x.f[q], d);
+    }
+}
+
 template <int DT>
 __device__ __forceinline__ uint4 acc_narrow(const Acc<DT>& x) {
     if (DT == AR_INT32)
@@ -139,8 +162,9 @@ __device__ __forceinline__ uint4 acc_narrow(const Acc<DT>& x) {
 // FP32ACC order over inputs 0..n-1 (the kernels' own fixed order, identical
 // in every kernel and for every rank): blocks of 8 consecutive inputs are
 // each folded left to right, then the block results are folded left to
-// right; fp32 / bf16 accumulate in fp32 and round once at the end.  Inputs are
-// fed one at a time, so the order can be followed while inputs stream in.
+// right; fp32 / bf16 accumulate in fp32 and round once at the end (an AR_AVG
+// sum divided by div first; div = 0 for the other ops).  Inputs are fed one
+// at a time, so the order can be followed while inputs stream in.
 template <int DT, int OP>
 struct AccStream {
     Acc<DT> acc, blk;
@@ -158,22 +182,28 @@ struct AccStream {
                 acc_combine<DT, OP>(acc, blk);
         }
     }
-    __device__ __forceinline__ uint4 finish(uint32_t n) {
+    __device__ __forceinline__ uint4 finish(uint32_t n, float div) {
         if (n & 7u) {
             if (n < 8u)
                 acc = blk;
             else
                 acc_combine<DT, OP>(acc, blk);
         }
+        if (div != 0.f) acc_div<DT>(acc, div);
         return acc_narrow<DT>(acc);
     }
 };
 
 template <int DT, int OP, class Load>
-__device__ __forceinline__ uint4 acc_reduce(uint32_t n, Load load) {
+__device__ __forceinline__ uint4 acc_reduce(uint32_t n, float div, Load load) {
     AccStream<DT, OP> s;
     for (uint32_t i = 0; i < n; ++i) s.feed(i, load(i));
-    return s.finish(n);
+    return s.finish(n, div);
+}
+
+// The divisor of a program's AR_AVG results, 0 when it stores plain results.
+__device__ __forceinline__ float avg_div(const KernelArgs& a, const DevProg& pg) {
+    return (pg.flags & PF_AVG) ? static_cast<float>(a.P) : 0.f;
 }
 
 // ------------------------------------------------------------- memory access
@@ -354,6 +384,10 @@ __device__ __forceinline__ void chain_item(const KernelArgs& a, const DevProg& p
             }
         }
     }
+    if (pg.flags & PF_AVG) {
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) acc[j] = vdiv<DT>(acc[j], static_cast<float>(a.P));
+    }
     for (uint32_t o = 0; o < pg.n_out; ++o) {
         char* dst = buf_addr(a, a.refs[pg.out_off + o]) + off;
 #pragma unroll
@@ -368,7 +402,8 @@ template <int DT, int OP>
 __device__ __forceinline__ void acc_item(const KernelArgs& a, const DevProg& pg, uint32_t st, uint32_t nvec,
                                          int64_t off, int ct) {
     for (uint32_t v = ct; v < nvec; v += kConsumers) {
-        const uint4 r = acc_reduce<DT, OP>(pg.n_in, [&](uint32_t i) { return lds128(st + i * a.tile_bytes + v * 16); });
+        const uint4 r = acc_reduce<DT, OP>(pg.n_in, avg_div(a, pg),
+                                           [&](uint32_t i) { return lds128(st + i * a.tile_bytes + v * 16); });
         for (uint32_t o = 0; o < pg.n_out; ++o) stg128(buf_addr(a, a.refs[pg.out_off + o]) + off + v * 16, r);
     }
 }
@@ -399,11 +434,15 @@ __device__ __forceinline__ void dag_item(const KernelArgs& a, const DevProg& pg,
         } else {
             const uint32_t rv = w & 0x3FFu, id = (w >> 10) & 0xFFFFu;
             const uint32_t pv = ref(rv);
+            const bool avg = (w >> 30) == INS_STORE_AVG;
             char* dst = buf_addr(a, id) + off;
 #pragma unroll
             for (int j = 0; j < kVpt; ++j) {
                 const uint32_t v = ct + j * kConsumers;
-                if (v < nvec) stg128(dst + v * 16, rv == REF_ACC ? acc[j] : lds128(pv + v * 16));
+                if (v < nvec) {
+                    const uint4 x = rv == REF_ACC ? acc[j] : lds128(pv + v * 16);
+                    stg128(dst + v * 16, avg ? vdiv<DT>(x, static_cast<float>(a.P)) : x);
+                }
             }
         }
     }
@@ -454,6 +493,10 @@ __device__ __forceinline__ void tree_item(const KernelArgs& a, const DevProg& pg
     for (uint32_t i = 0; i < pg.n_in; ++i) {
         tree_push(stk, sp++, st + i * a.tile_bytes, nvec, ct);
         for (uint32_t c = (counts[i >> 4] >> (2 * (i & 15))) & 3u; c > 0; --c, --sp) tree_combine<DT, OP>(stk, sp, nvec, ct);
+    }
+    if (pg.flags & PF_AVG) {
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) stk[0][j] = vdiv<DT>(stk[0][j], static_cast<float>(a.P));
     }
     for (uint32_t o = 0; o < pg.n_out; ++o) {
         char* dst = out_addr(a, pg, o) + off;
@@ -704,7 +747,7 @@ __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
                     stream_release(a, sm, g, lane);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < NA; ++j) res[j] = acc[j].finish(pg.n_in);
+                    for (int j = 0; j < NA; ++j) res[j] = acc[j].finish(pg.n_in, avg_div(a, pg));
                     stream_finish<VPT>(a, sm, g, t, pg, off, nvec, ct, res);
                 }
             }
@@ -732,10 +775,15 @@ __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
                         if (v < nvec) res[j] = vop<DT, OP>(res[j], lds128(t + v * 16));
                     }
                 }
-                if (i + 1 < pg.n_in)
+                if (i + 1 < pg.n_in) {
                     stream_release(a, sm, g, lane);
-                else
+                } else {
+                    if (pg.flags & PF_AVG) {
+#pragma unroll
+                        for (int j = 0; j < VPT; ++j) res[j] = vdiv<DT>(res[j], static_cast<float>(a.P));
+                    }
                     stream_finish<VPT>(a, sm, g, t, pg, off, nvec, ct, res);
+                }
             }
         }
     }
@@ -796,6 +844,14 @@ __device__ __forceinline__ uint32_t eop(uint32_t a, uint32_t b) {
     return wop<DT, OP>(a, b);
 }
 
+// one element's AR_AVG division when div != 0
+template <int DT>
+__device__ __forceinline__ uint32_t ediv(uint32_t v, float div) {
+    if (div == 0.f) return v;
+    if (DT == AR_BFLOAT16) return wdiv<DT>(v & 0xFFFFu, div) & 0xFFFFu;
+    return wdiv<DT>(v, div);
+}
+
 template <int DT, int OP>
 __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ uint32_t vals[];  // [(max_in + max_tmp) rows][kElemThreads]
@@ -816,6 +872,7 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
                 const uint32_t x = vals[i * kElemThreads + t];
                 acc = pg.kind == PK_CHAIN_R ? eop<DT, OP>(x, acc) : eop<DT, OP>(acc, x);
             }
+            acc = ediv<DT>(acc, avg_div(a, pg));
             for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, acc);
         } else if (pg.kind == PK_TREE) {
             // post-order on a small stack (local memory is fine on this path)
@@ -826,11 +883,12 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
                 for (uint32_t q = (a.ins[pg.ins_off + (i >> 4)] >> (2 * (i & 15))) & 3u; q > 0; --q, --sp)
                     stk[sp - 2] = eop<DT, OP>(stk[sp - 2], stk[sp - 1]);
             }
-            for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, stk[0]);
+            const uint32_t res = ediv<DT>(stk[0], avg_div(a, pg));
+            for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, res);
         } else if (pg.kind == PK_ACC) {
             // the same order as the other kernels: the element rides in lane 0
             // of a vector (the other lanes carry zeros and are dropped)
-            const uint4 r = acc_reduce<DT, OP>(pg.n_in, [&](uint32_t i) {
+            const uint4 r = acc_reduce<DT, OP>(pg.n_in, avg_div(a, pg), [&](uint32_t i) {
                 return make_uint4(vals[i * kElemThreads + t], 0u, 0u, 0u);
             });
             const uint32_t v = DT == AR_BFLOAT16 ? (r.x & 0xFFFFu) : r.x;
@@ -850,7 +908,8 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
                         row(rd) = r;
                 } else {
                     const uint32_t rv = wd & 0x3FFu, id = (wd >> 10) & 0xFFFFu;
-                    st_elem<DT>(buf_addr(a, id) + off, rv == REF_ACC ? acc : row(rv));
+                    const float div = (wd >> 30) == INS_STORE_AVG ? static_cast<float>(a.P) : 0.f;
+                    st_elem<DT>(buf_addr(a, id) + off, ediv<DT>(rv == REF_ACC ? acc : row(rv), div));
                 }
             }
         }
@@ -874,7 +933,8 @@ KernelFn table(int which) {
 template <int DT>
 KernelFn pick(int op, int which) {
     switch (op) {
-        case AR_SUM: return table<DT, AR_SUM>(which);
+        case AR_SUM:
+        case AR_AVG: return table<DT, AR_SUM>(which);  // AVG: the sum, divided where it completes
         case AR_PROD: return table<DT, AR_PROD>(which);
         case AR_MAX: return table<DT, AR_MAX>(which);
         default: return table<DT, AR_MIN>(which);

@@ -28,7 +28,7 @@ struct Prog {
     int stores() const {
         if (kind != PK_DAG) return static_cast<int>(out.size());
         int s = 0;
-        for (uint32_t w : ins) s += (w >> 30) == INS_STORE;
+        for (uint32_t w : ins) s += (w >> 30) != INS_OP;
         return s;  // (TREE programs store to their outputs like CHAIN / ACC)
     }
 };
@@ -113,8 +113,8 @@ bool left_chain(const Dag& d, int32_t x, std::vector<int32_t>& leaves) {
 }
 
 // Straight-line code for the trees outs[k].second that ranks outs[k].first
-// must end with.
-Prog dag_program(const Dag& d, const std::vector<std::pair<int, int32_t>>& outs) {
+// must end with; avg: combined results are divided by P as they are stored.
+Prog dag_program(const Dag& d, const std::vector<std::pair<int, int32_t>>& outs, bool avg) {
     const int P = d.P();
     Prog p;
     p.kind = PK_DAG;
@@ -196,7 +196,7 @@ Prog dag_program(const Dag& d, const std::vector<std::pair<int, int32_t>>& outs)
         p.ins.push_back(ins_op(a, b, dest));
         loc[x] = dest;
         if (stores_of.count(x))
-            for (int rr : stores_of[x]) p.ins.push_back(ins_store(dest, buf_id(0, rr)));
+            for (int rr : stores_of[x]) p.ins.push_back(ins_store(dest, buf_id(0, rr), avg));
     }
     return p;
 }
@@ -250,6 +250,8 @@ Prog fused_program(Canon& cn, const Schedule& S, int seg, const std::vector<int>
     for (int r : ranks) outs.push_back({r, cn.get(S.final_at(r, seg))});
     const int32_t x = outs[0].second;
     bool same = std::all_of(outs.begin(), outs.end(), [&](const std::pair<int, int32_t>& o) { return o.second == x; });
+    // AR_AVG divides combined results (an all-gather's copies are not)
+    const bool avg = S.op == AR_AVG;
     std::vector<int32_t> leaves;
     if (same && (right_chain(cn.c, x, leaves) || left_chain(cn.c, x, leaves))) {
         Prog p;
@@ -257,6 +259,7 @@ Prog fused_program(Canon& cn, const Schedule& S, int seg, const std::vector<int>
         if (p.kind == PK_CHAIN_L) left_chain(cn.c, x, leaves);
         for (int32_t l : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, l)));
         set_outputs(p, ranks, S.P);
+        if (avg && !cn.c.leaf(x)) p.flags |= PF_AVG;
         return p;
     }
     std::vector<uint32_t> combines;
@@ -268,23 +271,30 @@ Prog fused_program(Canon& cn, const Schedule& S, int seg, const std::vector<int>
         p.ins.assign(kTreeMaxLeaves / 16, 0);
         for (size_t i = 0; i < combines.size(); ++i) p.ins[i / 16] |= combines[i] << (2 * (i % 16));
         set_outputs(p, ranks, S.P);
+        if (avg && !cn.c.leaf(x)) p.flags |= PF_AVG;
         return p;
     }
-    return dag_program(cn.c, outs);
+    return dag_program(cn.c, outs, avg);
 }
 
-Prog acc_program(int P, const std::vector<int>& ranks) {
+Prog acc_program(int P, const std::vector<int>& ranks, bool avg) {
     Prog p;
     p.kind = PK_ACC;
     for (int r = 0; r < P; ++r) p.in.push_back(static_cast<uint16_t>(buf_id(0, r)));
     set_outputs(p, ranks, P);
+    if (avg) p.flags |= PF_AVG;
     return p;
 }
 
-Prog round_program(std::vector<const Transfer*> xs) {
-    std::sort(xs.begin(), xs.end(), [](const Transfer* a, const Transfer* b) {
-        return std::make_pair(a->dst, a->dst_out) < std::make_pair(b->dst, b->dst_out);
+// One round over one segment: each transfer with whether its combine
+// completes an AR_AVG sum (that result is divided by P as it is stored).
+Prog round_program(std::vector<std::pair<const Transfer*, bool>> xa) {
+    std::sort(xa.begin(), xa.end(), [](const std::pair<const Transfer*, bool>& a,
+                                       const std::pair<const Transfer*, bool>& b) {
+        return std::make_pair(a.first->dst, a.first->dst_out) < std::make_pair(b.first->dst, b.first->dst_out);
     });
+    std::vector<const Transfer*> xs;
+    for (const auto& t : xa) xs.push_back(t.first);
     Prog p;
     if (xs.size() == 1) {  // one transfer: acc = src, then dst_in (+) acc
         const Transfer& x = *xs[0];
@@ -292,6 +302,7 @@ Prog round_program(std::vector<const Transfer*> xs) {
         p.in.push_back(static_cast<uint16_t>(buf_id(x.src_slot, x.src)));
         if (x.combine) p.in.push_back(static_cast<uint16_t>(buf_id(x.dst_in, x.dst)));
         p.out.push_back(static_cast<uint16_t>(buf_id(x.dst_out, x.dst)));
+        if (xa[0].second) p.flags |= PF_AVG;
         return p;
     }
     p.kind = PK_DAG;
@@ -309,12 +320,13 @@ Prog round_program(std::vector<const Transfer*> xs) {
         if (x->combine) input(x->dst_in, x->dst);
         input(x->src_slot, x->src);
     }
-    for (const Transfer* x : xs) {
+    for (size_t k = 0; k < xs.size(); ++k) {
+        const Transfer* x = xs[k];
         uint32_t out = buf_id(x->dst_out, x->dst);
         if (x->combine) {
             p.ins.push_back(ins_op(idx[static_cast<uint16_t>(buf_id(x->dst_in, x->dst))],
                                    idx[static_cast<uint16_t>(buf_id(x->src_slot, x->src))], REF_ACC));
-            p.ins.push_back(ins_store(REF_ACC, out));
+            p.ins.push_back(ins_store(REF_ACC, out, xa[k].second));
         } else {
             p.ins.push_back(ins_store(idx[static_cast<uint16_t>(buf_id(x->src_slot, x->src))], out));
         }
@@ -353,23 +365,24 @@ void lower(const Schedule& S, Lowered& lw) {
     if (S.P > 1 && S.n > 0) {
         if (S.params.form == AR_FORM_FUSED) {
             std::vector<Range> rs;
-            const bool commute = S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD;
+            const bool commute = S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD || S.op == AR_AVG;
             Canon cn(S.dag, commute);
             for (int s = 0; s < S.nseg(); ++s) {
                 if (S.bounds[s + 1] <= S.bounds[s]) continue;
                 const std::vector<int> ranks = defined_ranks(S, s);
                 if (ranks.empty()) continue;  // (an all-gather owner-only segment)
-                const Prog p = S.params.order == AR_ORDER_FP32ACC ? acc_program(S.P, ranks)
+                const Prog p = S.params.order == AR_ORDER_FP32ACC ? acc_program(S.P, ranks, S.op == AR_AVG)
                                                                   : fused_program(cn, S, s, ranks);
                 push_range(rs, b.add(p), S.bounds[s], S.bounds[s + 1]);
             }
             sets.push_back(rs);
         } else {
             for (const Round& rd : S.rounds) {
-                std::map<int, std::vector<const Transfer*>> by_seg;
+                std::map<int, std::vector<std::pair<const Transfer*, bool>>> by_seg;
                 for (const Transfer& x : rd.xfers) {
                     int s0 = S.seg_of(x.lo), s1 = S.seg_of(x.hi - 1) + 1;
-                    for (int s = s0; s < s1; ++s) by_seg[s].push_back(&x);
+                    for (int s = s0; s < s1; ++s)
+                        by_seg[s].push_back({&x, !x.completes.empty() && x.completes[s - s0] != 0});
                 }
                 std::vector<Range> rs;
                 for (auto& kv : by_seg)

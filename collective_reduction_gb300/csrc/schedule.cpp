@@ -442,6 +442,7 @@ void run_symbolic(Schedule& S) {
         std::vector<std::pair<size_t, int32_t>> writes;
         for (auto& x : S.rounds[ri].xfers) {
             int s0 = S.seg_of(x.lo), s1 = S.seg_of(x.hi - 1) + 1;
+            if (x.combine && S.op == AR_AVG) x.completes.assign(s1 - s0, 0);
             for (int s = s0; s < s1; ++s) {
                 int32_t v = at(x.src, x.src_slot, s);
                 if (v < 0) throw std::logic_error("schedule reads an empty slot");
@@ -449,6 +450,7 @@ void run_symbolic(Schedule& S) {
                     int32_t d = at(x.dst, x.dst_in, s);
                     if (d < 0) throw std::logic_error("schedule combines into an empty slot");
                     v = S.dag.combine(d, v);
+                    if (S.op == AR_AVG) x.completes[s - s0] = S.dag.complete(v);
                 }
                 size_t idx = (static_cast<size_t>(x.dst) * ns + x.dst_out) * nseg + s;
                 if (stamp[idx] == static_cast<int32_t>(ri)) throw std::logic_error("round writes a slot twice");
@@ -493,7 +495,8 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
                            Schedule& S) {
     if (P < 1 || n < 0) return AR_ERR_INVALID_ARG;
     if (dtype < AR_INT32 || dtype > AR_BFLOAT16) return AR_ERR_INVALID_ARG;
-    if (op < AR_SUM || op > AR_MIN) return AR_ERR_INVALID_ARG;
+    if (op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
+    if (op == AR_AVG && dtype == AR_INT32) return AR_ERR_UNSUPPORTED;
     if (algo < AR_RING || algo > AR_PIPELINE) return AR_ERR_INVALID_ARG;
     if (P > AR_MAX_RANKS) return AR_ERR_UNSUPPORTED;
     Params pr;

@@ -20,6 +20,9 @@ struct Transfer {
     int dst, dst_in, dst_out;
     int64_t lo, hi;
     bool combine;
+    // AR_AVG: per segment the transfer covers (from the first), whether its
+    // combine completes the reduction (that result is divided by P)
+    std::vector<uint8_t> completes;
 };
 
 struct Round {

@@ -59,7 +59,13 @@ typedef enum { AR_INT32 = 0, AR_FLOAT32 = 1, AR_BFLOAT16 = 2 } ar_dtype;
  * nearest-even with subnormals.  bf16 widens both operands to fp32, applies
  * the fp32 op and rounds to bf16 (nearest even) after every op.
  * max = a > b ? a : b, min = a < b ? a : b (ties and NaN keep b). */
-typedef enum { AR_SUM = 0, AR_PROD = 1, AR_MAX = 2, AR_MIN = 3 } ar_op;
+/* AR_AVG: the sum divided by P, inside the collective ("All-Reduce, in
+ * depth", The APIs: ncclAvg divides by the rank count so that no separate
+ * scaling pass is needed).  Each result is divided once, where its sum is
+ * complete (IEEE fp32 division, round to nearest even; bf16: the bf16 sum
+ * widened, divided in fp32, rounded to bf16; FP32ACC: the fp32 sum divided,
+ * then rounded).  Float types only: int32 gives AR_ERR_UNSUPPORTED. */
+typedef enum { AR_SUM = 0, AR_PROD = 1, AR_MAX = 2, AR_MIN = 3, AR_AVG = 4 } ar_op;
 
 /* Schedules.
  *  AR_RING        ring reduce-scatter + all-gather over P chunks; rank r

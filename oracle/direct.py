@@ -40,11 +40,12 @@ def as_f64(buf, dtype):
 
 
 def direct_f64(bufs, op, dtype):
-    """float64 reduction of the rank buffers, ranks taken in order 0..P-1."""
+    """float64 reduction of the rank buffers, ranks taken in order 0..P-1
+    (avg: the float64 sum divided by P)."""
     acc = as_f64(bufs[0], dtype)
     for b in bufs[1:]:
         v = as_f64(b, dtype)
-        if op == "sum":
+        if op in ("sum", "avg"):
             acc = acc + v
         elif op == "prod":
             acc = acc * v
@@ -54,6 +55,8 @@ def direct_f64(bufs, op, dtype):
             acc = np.minimum(acc, v)
         else:
             raise ValueError(op)
+    if op == "avg":
+        acc = acc / len(bufs)
     return acc
 
 

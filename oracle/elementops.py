@@ -17,13 +17,18 @@ complement readings):
          result rounded to bf16 with round-to-nearest-even after EVERY op.
   max    a > b ? a : b   (ties, +-0 and NaN keep the right operand b)
   min    a < b ? a : b
+  avg    the sum, then divided by the rank count P ("All-Reduce, in depth",
+         The APIs: ncclAvg divides by N inside the collective).  Combines are
+         sums; ``average`` divides a finished sum once: fp32 IEEE division
+         with round-to-nearest-even; bf16 widened, divided in fp32, rounded to
+         bf16.  Float types only.
 bf16 values are held as uint16 bit patterns.
 """
 
 import numpy as np
 
 DTYPES = ("int32", "float32", "bfloat16")
-OPS = ("sum", "prod", "max", "min")
+OPS = ("sum", "prod", "max", "min", "avg")
 ESIZE = {"int32": 4, "float32": 4, "bfloat16": 2}
 NP_STORAGE = {"int32": np.int32, "float32": np.float32, "bfloat16": np.uint16}
 
@@ -68,6 +73,8 @@ class Arith:
             raise ValueError(f"unknown op {op!r}")
         if dtype not in DTYPES:
             raise ValueError(f"unknown dtype {dtype!r}")
+        if op == "avg" and dtype == "int32":
+            raise ValueError("avg is defined for the float types only")
         self.op = op
         self.dtype = dtype
         self.storage = NP_STORAGE[dtype]
@@ -78,7 +85,7 @@ class Arith:
             return self._f32_op_raw(a, b)
 
     def _f32_op_raw(self, a, b):
-        if self.op == "sum":
+        if self.op in ("sum", "avg"):
             return np.add(a, b, dtype=np.float32)
         if self.op == "prod":
             return np.multiply(a, b, dtype=np.float32)
@@ -108,6 +115,16 @@ class Arith:
         if self.op == "min":
             return np.where(fa < fb, a, b)
         return f32_to_bf16_rne(self._f32_op(fa, fb))
+
+    def average(self, x, P):
+        """A finished avg sum divided by the rank count P (see the module
+        docstring); not counted as a combine."""
+        x = np.asarray(x, dtype=self.storage)
+        d = np.float32(P)
+        with np.errstate(over="ignore", invalid="ignore", under="ignore", divide="ignore"):
+            if self.dtype == "float32":
+                return np.divide(x, d, dtype=np.float32)
+            return f32_to_bf16_rne(np.divide(bf16_to_f32(x), d, dtype=np.float32))
 
     def empty(self, n):
         return np.zeros(n, dtype=self.storage)

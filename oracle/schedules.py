@@ -612,9 +612,28 @@ def ahc(bufs, arith, group_sizes):
 
 
 def run(algo, bufs, arith, group="cyclic", r=0, k1=0, group_sizes=None, blocks=1, phase="allreduce"):
-    """Run one schedule by name; phase picks a half of the splitting ones."""
+    """Run one schedule by name; phase picks a half of the splitting ones.
+
+    avg runs the schedule as a sum and divides every finished sum by P once
+    (a copy of a finished sum carries the divided value, so dividing where
+    each sum completes or every rank's result at the end is the same); an
+    all-gather combines nothing and divides nothing.
+    """
     if phase != "allreduce" and algo not in ("ring", "rh", "generalized"):
         raise ValueError(f"{algo} does not split into a reduce-scatter and an all-gather")
+    res = _run(algo, bufs, arith, group, r, k1, group_sizes, blocks, phase)
+    if getattr(arith, "op", None) == "avg" and phase != "all_gather":
+        P = len(bufs)
+        if phase == "allreduce":
+            res.bufs = [arith.average(b, P) for b in res.bufs]
+        else:
+            # the owners' chunks are the finished sums of a reduce-scatter
+            for rank, lo, hi in res.info["owner"]:
+                res.bufs[rank][lo:hi] = arith.average(res.bufs[rank][lo:hi], P)
+    return res
+
+
+def _run(algo, bufs, arith, group, r, k1, group_sizes, blocks, phase):
     if algo == "ring":
         return ring(bufs, arith, phase)
     if algo == "binomial":

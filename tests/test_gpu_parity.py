@@ -397,3 +397,59 @@ def test_all_gather_spreads_owned_chunks(P, dtype, form):
         got = engine(bufs, dtype, "sum", algo, form=form, phase="all_gather", **kw)
         for r in range(P):
             assert_bit_equal(got[r], want[r], dtype, f"{algo} {kw} rank {r}")
+
+
+# ---- avg: the sum divided by P where it completes ---------------------------------------
+
+AVG_CASES = [("ring", {}), ("binomial", {}), ("rd", {}), ("rh", {}), ("hybrid", {"k1": 1}),
+             ("generalized", {"r": 0}), ("generalized", {"r": 2}), ("ahc", {"group_sizes": [2, 3, 2]}),
+             ("pipeline", {"blocks": 3})]
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_avg_every_schedule(dtype, form):
+    P = 7
+    for n in (5, 30011):
+        bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1.0, seed=n)
+        for algo, kw in AVG_CASES:
+            check_faithful(bufs, dtype, "avg", algo, form, **kw)
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_avg_fp32acc_and_halves(dtype):
+    P, n = 8, (1 << 20) + 3
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=5)
+    ref = direct_f64(bufs, "avg", dtype)
+    tol = 1e-6 if dtype == "float32" else 4e-3
+    from oracle.elementops import bf16_to_f32
+    got = engine(bufs, dtype, "avg", "ring", order="fp32acc")
+    for g in got:
+        assert normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) <= tol
+    for form in FORMS:
+        for algo, kw in SPLIT:
+            res = oracle.run(algo, bufs, Arith("avg", dtype), phase="reduce_scatter", **kw)
+            got = engine(bufs, dtype, "avg", algo, form=form, phase="reduce_scatter", **kw)
+            for rank, lo, hi in res.info["owner"]:
+                assert_bit_equal(got[rank][lo:hi], res.bufs[rank][lo:hi], dtype, f"{algo} {form} rank {rank}")
+
+
+def test_avg_unaligned_and_int32_refused():
+    import torch
+
+    import collective_reduction_gb300 as ar
+    P, n = 3, 1001
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1.0, seed=8)
+    want = oracle.run("ring", bufs, Arith("avg", "float32")).bufs
+    base = [torch.zeros(n + 1, dtype=torch.float32, device="cuda") for _ in range(P)]
+    dev = [b[1:] for b in base]  # 4-byte offset: element-wise path
+    for d, h in zip(dev, bufs):
+        d.copy_(torch.from_numpy(h))
+    plan = ar.Plan(P, n, "float32", "avg", "ring")
+    plan.execute(dev)
+    torch.cuda.synchronize()
+    plan.check()
+    for r in range(P):
+        assert_bit_equal(dev[r].cpu().numpy(), want[r], "float32", f"rank {r}")
+    with pytest.raises(ar.ArError):
+        ar.Plan(P, n, "int32", "avg", "ring")

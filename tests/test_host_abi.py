@@ -210,3 +210,17 @@ def test_halves_parameter_checks(lib):
     # the fp32-accumulation reduce-scatter is a one-pass plan too
     s = ar.Schedule(8, 64, "bfloat16", "sum", "ring", phase="reduce_scatter", order="fp32acc")
     assert s.info()["steps"] == 7
+
+
+def test_avg_requests(lib):
+    with pytest.raises(ar.ArError) as e:
+        ar.Schedule(4, 64, "int32", "avg", "ring")
+    assert e.value.name == "AR_ERR_UNSUPPORTED"
+    h = ctypes.c_void_p()
+    assert lib.ar_schedule_create(4, 64, 1, 5, 0, None, ctypes.byref(h)) == 1
+    # avg keeps the sum's trees and counters
+    for algo, kw in (("ring", {}), ("generalized", {"r": 2}), ("binomial", {}), ("rh", {"phase": "reduce_scatter"})):
+        a = ar.Schedule(7, 40, "float32", "avg", algo, **kw).info()
+        s = ar.Schedule(7, 40, "float32", "sum", algo, **kw).info()
+        for k in ("steps", "combines", "sent_bytes_max", "sent_bytes_total", "n_segments"):
+            assert a[k] == s[k], (algo, k)

@@ -566,3 +566,50 @@ def test_halves_only_for_splitting_schedules():
             oracle.run(algo, z, Arith("sum", "int32"), phase="reduce_scatter", **kw)
     with pytest.raises(ValueError):
         oracle.run("ring", z, Arith("sum", "int32"), phase="scatter")
+
+
+# --- avg ("All-Reduce, in depth", The APIs: ncclAvg divides by N) -----------
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_avg_is_the_correctly_rounded_mean_when_sums_are_exact(dtype):
+    """Small-integer inputs make every partial sum exact (|sum| <= 128 fits
+    bf16's 8 significant bits), so every schedule's avg must be the mean
+    sum / P rounded once to the dtype.  The expected value is taken in
+    float64 and then rounded to fp32 (and on to bf16): 53 >= 2 * 24 + 2 and
+    24 >= 2 * 8 + 2, so these double roundings equal one correct rounding."""
+    from oracle.elementops import f32_to_bf16_rne
+    rng = np.random.default_rng(31)
+    for algo, P, p in _cases(range(1, 17)):
+        n = 2 * P + 5
+        ints = [rng.integers(-8, 9, n) for _ in range(P)]
+        if dtype == "float32":
+            bufs = [x.astype(np.float32) for x in ints]
+        else:
+            bufs = [f32_to_bf16_rne(x.astype(np.float32)) for x in ints]
+        mean = (np.sum(ints, axis=0).astype(np.float64) / P).astype(np.float32)
+        want = mean if dtype == "float32" else f32_to_bf16_rne(mean)
+        res = oracle.run(algo, bufs, Arith("avg", dtype), **p)
+        for r in range(P):
+            assert np.array_equal(res.bufs[r], want), (algo, P, p, r)
+
+
+def test_avg_halves():
+    """A reduce-scatter's avg divides the owners' finished sums; an
+    all-gather combines nothing and so divides nothing."""
+    rng = np.random.default_rng(32)
+    for algo, P, p in _split_cases(range(2, 13)):
+        n = 3 * P + 1
+        bufs = [rng.standard_normal(n).astype(np.float32) for _ in range(P)]
+        rs_sum = oracle.run(algo, bufs, Arith("sum", "float32"), phase="reduce_scatter", **p)
+        rs_avg = oracle.run(algo, bufs, Arith("avg", "float32"), phase="reduce_scatter", **p)
+        for rank, lo, hi in rs_avg.info["owner"]:
+            assert np.array_equal(rs_avg.bufs[rank][lo:hi], rs_sum.bufs[rank][lo:hi] / np.float32(P))
+        ag_avg = oracle.run(algo, bufs, Arith("avg", "float32"), phase="all_gather", **p)
+        ag_sum = oracle.run(algo, bufs, Arith("sum", "float32"), phase="all_gather", **p)
+        for r in range(P):
+            assert np.array_equal(ag_avg.bufs[r], ag_sum.bufs[r])
+
+
+def test_avg_has_no_integer_form():
+    with pytest.raises(ValueError):
+        Arith("avg", "int32")
