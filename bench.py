@@ -59,6 +59,10 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", default=None, help="write the size sweep as JSON lines to this file")
+    ap.add_argument("--rows", default=None,
+                    help="time every schedule at the bench size (fused and step), JSON lines to this file")
+    ap.add_argument("--costmodel", default=None,
+                    help="fit the step-form cost model and validate its step choice, JSON lines to this file")
     ap.add_argument("--configs", default=None,
                     help="time every schedule of the parity configurations, JSON lines to this file")
     return ap.parse_args()
@@ -399,7 +403,7 @@ def run_ours(a):
                      "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": alg_bytes,
                      "kernel_ms": round(kernel_ms, 6),
-                     "kernel": "stream_kernel" if (a.algo == "ring" or a.order == "fp32acc") else "staged_kernel"},
+                     "kernel": "stream_kernel" if info["kernels"] & 1 else "staged_kernel"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(whole_job_gbps(bytes_per_call, 1, world, e2e_s * 1e3), 3), "unit": "GB/s",
                 "h2d_bytes_per_step": bytes_per_call, "d2h_bytes_per_step": bytes_per_call},
@@ -650,6 +654,199 @@ def run_configs(a, path):
             plan.close()
 
 
+def time_plan(plan, dev, reps=5, calls=20):
+    """Median over reps of the mean CUDA-event time of `calls` back-to-back
+    executes (after 3 warm-up calls), in microseconds."""
+    import torch
+    for _ in range(3):
+        plan.execute(dev)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(calls):
+            plan.execute(dev)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / calls)
+    plan.check()
+    return statistics.median(ts)
+
+
+def row_cases():
+    """(row, algo, params, sample chunks) of every schedule at P = 8."""
+    out = []
+    for algo, kw, chunks, row in (("ring", {}, 8, "a3/a4 ring RS+AG"),
+                                  ("binomial", {}, 1, "a5/a6 binomial reduce+broadcast"),
+                                  ("rh", {}, 8, "a7 RH"), ("rd", {}, 1, "a8 RD"),
+                                  ("generalized", {"r": 0}, 8, "a9/a10 generalized r=0"),
+                                  ("generalized", {"r": 1}, 8, "a9/a10 generalized r=1"),
+                                  ("generalized", {"r": 3}, 8, "a9 generalized r=L"),
+                                  ("hybrid", {"k1": 1}, 8, "a11 hybrid k1=1"),
+                                  ("ahc", {"group_sizes": [4, 4]}, 8, "a12-a14 AHC {4,4}"),
+                                  ("pipeline", {"blocks": 4}, 4, "f4 pipelined chain m=4")):
+        for form in ("fused", "step"):
+            out.append((row, algo, dict(kw, form=form), chunks))
+    for algo in ("ring", "rh"):
+        for phase in ("reduce_scatter", "all_gather"):
+            out.append((f"f2 {phase}", algo, {"form": "fused", "phase": phase}, 8))
+    out.append(("a15 fp32acc", "ring", {"form": "fused", "order": "fp32acc"}, 8))
+    out.append(("a15 fp32acc", "ahc", {"form": "fused", "order": "fp32acc", "group_sizes": [4, 4]}, 8))
+    return out
+
+
+def run_rows(a, path):
+    """Every schedule of the hot path at the bench size, P = 8 x 256 MiB per
+    rank (fp32 and bf16, sum): median of 5 CUDA-event timings of 10
+    back-to-back calls, HBM GB/s from the plan's algorithmic bytes, the
+    fraction of the measured copy peak, and the oracle's verdict on a sample
+    of the result (2^14 elements from each base chunk, bit for bit;
+    fp32-accumulated results within the normwise tolerance)."""
+    import numpy as np
+    import torch
+
+    import ar_synth
+    import collective_reduction_gb300 as ar
+    import oracle
+    from oracle.direct import direct_f64, normwise_rel_err
+    from oracle.elementops import Arith, bf16_to_f32
+    torch.cuda.set_device(0)
+    peak, _ = measured_peak()
+    P, K = 8, 1 << 14
+
+    def bits(x):
+        x = np.ascontiguousarray(x)
+        return x if x.dtype == np.uint16 else x.view(np.uint32)
+
+    with open(path, "w") as out:
+        for dtype in ("float32", "bfloat16"):
+            n = (256 << 20) // esize(dtype)
+            src = ar_synth.device_inputs(P, n, dtype, sigma=1e-2, seed=3)
+            for row, algo, kw, chunks in row_cases():
+                dev = [t.clone() for t in src]
+                sample_in, idx = gather_sample(dev, P, n, K, chunks)
+                plan = ar.Plan(P, n, dtype, "sum", algo, **kw)
+                info = plan.info()
+                plan.execute(dev)
+                plan.check()
+                got = [t.index_select(0, idx) for t in dev]
+                got = [g.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bfloat16" else g.cpu().numpy()
+                       for g in got]
+                okw = {k: v for k, v in kw.items() if k in ("r", "k1", "group_sizes", "blocks", "phase")}
+                if kw.get("order") == "fp32acc":
+                    ref = direct_f64(sample_in, "sum", dtype)
+                    err = max(normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) for g in got)
+                    ok = err <= (1e-6 if dtype == "float32" else 4e-3)
+                else:
+                    want = oracle.run(algo, sample_in, Arith("sum", dtype), **okw)
+                    if kw.get("phase") == "reduce_scatter":
+                        ok = all(np.array_equal(bits(got[r][lo:hi]), bits(want.bufs[r][lo:hi]))
+                                 for r, lo, hi in want.info["owner"])
+                    else:
+                        ok = all(np.array_equal(bits(g), bits(w)) for g, w in zip(got, want.bufs))
+                us = time_plan(plan, dev, reps=5, calls=10)
+                gbps = info["hbm_bytes"] / (us / 1e6) / 1e9
+                out.write(json.dumps({
+                    "row": row, "algo": algo, "params": kw, "dtype": dtype, "P": P, "bytes_per_rank": n * esize(dtype),
+                    "verified": bool(ok), "steps": info["steps"], "launches": info["launches"],
+                    "kernels": info["kernels"], "us_per_call": round(us, 2), "hbm_bytes": info["hbm_bytes"],
+                    "hbm_GBps": round(gbps, 1), "frac_of_measured": round(gbps / peak, 4),
+                    "allreduced_GBps": round(P * n * esize(dtype) / (us / 1e6) / 1e9, 1)}) + "\n")
+                out.flush()
+                plan.close()
+                del dev
+            del src
+            torch.cuda.empty_cache()
+
+
+def run_costmodel(a, path):
+    """The step-form cost model ("A Generalization of the Allreduce
+    Operation", eqs. 36-37) on this GPU.  Fit: alpha per round, beta per byte
+    sent and gamma per byte combined (bytes over all ranks) by non-negative
+    least squares on relative error, over step-form ring, binomial, RD and
+    bandwidth-optimal generalized plans (rounds of independent transfers) at
+    P in {4, 16, 63} and 2 KiB .. 64 MiB per rank.  Validation: at P in {7, 12, 31, 63} and 1 KiB .. 16 MiB per
+    rank, every candidate the selection weighs is timed; the measured best r
+    of the generalized schedule is set against eq. (37)'s r, and the
+    selection's pick against the fastest candidate."""
+    import numpy as np
+    import torch
+    from scipy.optimize import nnls
+
+    import ar_synth
+    import collective_reduction_gb300 as ar
+    torch.cuda.set_device(0)
+    dtype = "float32"
+
+    def counters(info):
+        return [info["steps"], info["sent_bytes_total"], info["combines"] * esize(dtype)]
+
+    rows = []
+    with open(path, "w") as out:
+        for P in (4, 16, 63):
+            for lg in range(11, 27, 3):
+                S = 1 << lg
+                n = S // esize(dtype)
+                dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
+                for algo, kw in (("ring", {}), ("binomial", {}), ("rd", {}), ("generalized", {"r": 0})):
+                    plan = ar.Plan(P, n, dtype, "sum", algo, form="step", **kw)
+                    us = time_plan(plan, dev)
+                    c = counters(plan.info())
+                    rows.append((c, us))
+                    out.write(json.dumps({"phase": "fit", "P": P, "S": S, "algo": algo, "params": kw,
+                                          "steps": c[0], "sent_bytes_total": c[1], "combined_bytes": c[2],
+                                          "us": round(us, 3)}) + "\n")
+                    plan.close()
+                del dev
+                torch.cuda.empty_cache()
+        A = np.array([[x / t for x in c] for c, t in rows])
+        coef, _ = nnls(A, np.ones(len(rows)))
+        alpha, beta, gamma = (float(x) for x in coef)
+        pred = A @ coef
+        fit = {"phase": "model", "alpha_us": alpha, "beta_us_per_byte": beta, "gamma_us_per_byte": gamma,
+               "rel_rms": float(np.sqrt(np.mean((pred - 1.0) ** 2))), "rel_max": float(np.max(np.abs(pred - 1.0))),
+               "points": len(rows)}
+        out.write(json.dumps(fit) + "\n")
+        out.flush()
+        model = ar.CostModel(alpha, beta, gamma)
+        for P in (7, 12, 31, 63):
+            L = (P - 1).bit_length()
+            Lp = (1 << (P.bit_length() - 1)).bit_length() - 1
+            cands = [("ring", {}), ("binomial", {}), ("rd", {}), ("rh", {})]
+            cands += [("hybrid", {"k1": k}) for k in range(Lp + 1)]
+            cands += [("generalized", {"r": r}) for r in range(L + 1)]
+            for lg in range(10, 25, 2):
+                S = 1 << lg
+                n = S // esize(dtype)
+                dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
+                meas = {}
+                for algo, kw in cands:
+                    plan = ar.Plan(P, n, dtype, "sum", algo, form="step", **kw)
+                    meas[(algo, json.dumps(kw, sort_keys=True))] = time_plan(plan, dev)
+                    plan.close()
+                gen = {r: meas[("generalized", json.dumps({"r": r}))] for r in range(L + 1)}
+                best_r = min(gen, key=gen.get)
+                r37 = ar.optimal_r(P, S, model)
+                sel_algo, sel_params, sel_pred = ar.select(P, n, dtype, "sum", model)
+                sel_kw = {k: sel_params[k] for k in ("r", "k1") if
+                          (k == "r" and sel_algo == "generalized") or (k == "k1" and sel_algo == "hybrid")}
+                sel_us = meas[(sel_algo, json.dumps(sel_kw, sort_keys=True))]
+                best_key = min(meas, key=meas.get)
+                out.write(json.dumps({
+                    "phase": "validate", "P": P, "S": S,
+                    "generalized_us_by_r": {str(r): round(t, 3) for r, t in gen.items()},
+                    "best_r_measured": best_r, "eq37_r": r37,
+                    "eq37_loss": round(gen[r37] / gen[best_r], 4),
+                    "select": [sel_algo, sel_kw], "select_us": round(sel_us, 3),
+                    "select_predicted_us": round(sel_pred, 3),
+                    "fastest": [best_key[0], json.loads(best_key[1])], "fastest_us": round(meas[best_key], 3),
+                    "select_loss": round(sel_us / meas[best_key], 4)}) + "\n")
+                out.flush()
+                del dev
+                torch.cuda.empty_cache()
+
+
 def main():
     a = parse()
     if a.impl == "reference":
@@ -660,6 +857,12 @@ def main():
         return
     if a.configs:
         run_configs(a, a.configs)
+        return
+    if a.costmodel:
+        run_costmodel(a, a.costmodel)
+        return
+    if a.rows:
+        run_rows(a, a.rows)
         return
     run_ours(a)
 

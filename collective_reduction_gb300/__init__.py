@@ -22,6 +22,7 @@ ORDERS = {"faithful": 0, "fp32acc": 1}
 GROUPS = {"cyclic": 0, "xor": 1}
 PHASES = {"allreduce": 0, "reduce_scatter": 1, "all_gather": 2}
 ESIZE = {"int32": 4, "float32": 4, "bfloat16": 2}
+KERNEL_STREAM, KERNEL_STAGED, KERNEL_ELEMENTWISE = 1, 2, 4  # Plan.info()["kernels"] bits
 MAX_RANKS = 64
 
 STATUS = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_UNSUPPORTED", 3: "AR_ERR_CUDA",
@@ -52,10 +53,17 @@ class Info(ctypes.Structure):
                 ("max_slots", ctypes.c_int), ("n_segments", ctypes.c_int),
                 ("hbm_bytes", ctypes.c_uint64), ("scratch_bytes", ctypes.c_uint64),
                 ("launches", ctypes.c_int), ("tile_bytes", ctypes.c_int), ("n_programs", ctypes.c_int),
-                ("n_items", ctypes.c_uint64)]
+                ("n_items", ctypes.c_uint64), ("kernels", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class CostModel(ctypes.Structure):
+    """Step-form cost: alpha per round, beta per byte sent and gamma per byte
+    combined, bytes summed over all ranks."""
+    _fields_ = [("alpha_us", ctypes.c_double), ("beta_us_per_byte", ctypes.c_double),
+                ("gamma_us_per_byte", ctypes.c_double)]
 
 
 _lib = None
@@ -76,6 +84,13 @@ _EXPORTS = {
     "ar_execute_host": (ctypes.c_int, [_VP, ctypes.POINTER(_VP), ctypes.POINTER(_VP), _VP]),
     "ar_plan_check": (ctypes.c_int, [_VP]),
     "ar_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ar_cost_model_default": (ctypes.c_int, [ctypes.POINTER(CostModel)]),
+    "ar_cost_predict": (ctypes.c_int, [_VP, ctypes.POINTER(CostModel), ctypes.POINTER(ctypes.c_double)]),
+    "ar_cost_optimal_r": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64, ctypes.POINTER(CostModel),
+                                         ctypes.POINTER(ctypes.c_int)]),
+    "ar_cost_select": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(CostModel), ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(Params), ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -210,3 +225,49 @@ class Plan:
             self._h = None
 
     __del__ = close
+
+
+# ---------------------------------------------------------------- cost model
+
+def cost_model(alpha_us=None, beta_us_per_byte=None, gamma_us_per_byte=None):
+    """The fitted GB300 step-form model, with any field overridden."""
+    m = CostModel()
+    _check(lib().ar_cost_model_default(ctypes.byref(m)), "ar_cost_model_default")
+    if alpha_us is not None:
+        m.alpha_us = alpha_us
+    if beta_us_per_byte is not None:
+        m.beta_us_per_byte = beta_us_per_byte
+    if gamma_us_per_byte is not None:
+        m.gamma_us_per_byte = gamma_us_per_byte
+    return m
+
+
+def cost_predict(schedule, model=None):
+    """Predicted step-form microseconds of a Schedule."""
+    model = model or cost_model()
+    us = ctypes.c_double()
+    _check(lib().ar_cost_predict(schedule._h, ctypes.byref(model), ctypes.byref(us)), "ar_cost_predict")
+    return us.value
+
+
+def optimal_r(P, bytes_per_rank, model=None):
+    """Removed distribution steps minimising the generalized schedule's cost
+    ("A Generalization of the Allreduce Operation", eq. 37), in 0..L-1."""
+    model = model or cost_model()
+    r = ctypes.c_int()
+    _check(lib().ar_cost_optimal_r(P, bytes_per_rank, ctypes.byref(model), ctypes.byref(r)), "ar_cost_optimal_r")
+    return r.value
+
+
+def select(P, n, dtype, op, model=None):
+    """(algo, params, predicted microseconds) of the cheapest step-form
+    schedule under the model; params fit Plan(..., **params)."""
+    model = model or cost_model()
+    algo = ctypes.c_int()
+    p = Params()
+    us = ctypes.c_double()
+    _check(lib().ar_cost_select(P, n, DTYPES[dtype], OPS[op], ctypes.byref(model), ctypes.byref(algo),
+                                ctypes.byref(p), ctypes.byref(us)), "ar_cost_select")
+    name = {v: k for k, v in ALGOS.items()}[algo.value]
+    params = {"form": "step", "order": "faithful", "group": "cyclic", "r": p.r, "k1": p.k1}
+    return name, params, us.value

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libar.so")
-SOURCES = ["kernels.cu", "noalloc.cu", "schedule.cpp", "lower.cpp", "api.cpp"]
+SOURCES = ["kernels.cu", "noalloc.cu", "schedule.cpp", "lower.cpp", "api.cpp", "cost.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -153,9 +153,9 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
         if (s.stream) {
             a.tile_bytes = plan->L.stream_tile;
             a.stages = plan->L.stream_stages;
-            a.flags = plan->L.stream_tma_store ? ar::kArgTmaStore : 0;
+            a.flags = (plan->L.stream_tma_store ? ar::kArgTmaStore : 0) | (plan->L.stream_trees ? ar::kArgTrees : 0);
             a.max_in = 1;
-            a.max_tmp = 0;
+            a.max_tmp = plan->L.stream_slots;  // tree stack tiles after the stages
             e = ar::launch_stream(S.dtype, S.op, a, grid, plan->smem_stream, st);
         } else {
             a.tile_bytes = plan->L.tile_bytes;
@@ -369,6 +369,14 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info) {
     info->tile_bytes = plan->L.tile_bytes;
     info->n_programs = static_cast<int>(plan->L.progs.size());
     info->n_items = plan->L.n_items;
+    for (const ar::LaunchSet& s : plan->L.sets) {
+        if (s.small) {
+            info->kernels |= AR_KERNEL_ELEMENTWISE;
+            continue;
+        }
+        if (!s.bulk.empty()) info->kernels |= s.stream ? AR_KERNEL_STREAM : AR_KERNEL_STAGED;
+        if (!s.edge.empty()) info->kernels |= AR_KERNEL_ELEMENTWISE;
+    }
     return AR_OK;
 }
 

@@ -51,8 +51,13 @@ constexpr int kStreamVptNarrow = 4;  // rank-streaming kernel, bf16 fp32 accumul
 constexpr int kMaxStagedTile = 32 * kConsumerWarps * 16 * kStagedVpt;          // 16 KB
 constexpr int kStreamTileBytes = 32 * kConsumerWarps * 16 * kStreamVpt;        // 32 KB
 constexpr int kStreamTileNarrow = 32 * kConsumerWarps * 16 * kStreamVptNarrow; // 16 KB
-constexpr int kTreeDepth = 4;        // deepest TREE stack (a balanced 8-leaf tree needs 4)
-constexpr int kTreeMaxLeaves = 64;   // TREE combine counts: 2 bits per leaf in 4 words
+// TREE programs: leaves in post-order, and after each leaf the number of
+// combines that follow it (4 bits per leaf, 8 leaves per instruction word).
+// Evaluated with the deeper child first, a tree of at most 64 leaves needs a
+// stack of at most 7 entries; DevProg::n_tmp holds the program's depth - 1.
+constexpr int kTreeDepth = 7;
+constexpr int kTreeMaxLeaves = 64;
+constexpr int kTreeCountWords = kTreeMaxLeaves / 8;
 
 // instruction word: bits 30..31 kind
 //   OP:    a = bits 0..9, b = bits 10..19, d = bits 20..29

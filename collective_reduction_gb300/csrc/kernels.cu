@@ -1,19 +1,22 @@
 // CUDA kernels of the allreduce engine (sm_103a).
 //
-// stream_kernel: the hot path (ring fused pass and rounds, every fp32-
-// accumulate pass).  Persistent, one CTA per SM, warp-specialised: warp 0
-// resolves source addresses and its lane 0 issues one cp.async.bulk (TMA bulk
-// copy, L2 evict-first) per rank tile into a ring of shared-memory stages,
-// each completing on its own mbarrier; eight consumer warps fold every rank
-// tile into per-thread register accumulators in program order and, after the
-// item's last input, store the result to every output with 128-bit streaming
-// stores.  Rank tiles are 32 KB whatever P is, so all consumer threads stay
-// busy and the pipeline depth stays ~200 KB per SM.
+// stream_kernel: the hot path (chains, single trees and fp32 accumulation:
+// the fused pass of every schedule whose ranks share one tree per element,
+// and the step form's rounds of independent transfers).  Persistent, one CTA
+// per SM, warp-specialised: warp 0 resolves source addresses and its lane 0
+// issues one cp.async.bulk (TMA bulk copy, L2 evict-first) per rank tile into
+// a ring of shared-memory stages, each completing on its own mbarrier; eight
+// consumer warps fold every rank tile into per-thread register accumulators
+// in program order (a tree keeps its deeper stack entries in shared-memory
+// tiles after the stages) and, after the item's last input, store the result
+// to every output with 128-bit streaming stores or TMA bulk stores.  Rank
+// tiles are 32 KB (16 KB for bf16 fp32 accumulation and deep trees) whatever
+// P is, so all consumer threads stay busy and ~200 KB per SM is in flight.
 //
-// staged_kernel: for DAG programs (trees, rank-specific results).  Same
-// structure, but a stage holds all input tiles of one item, which the
-// consumers evaluate as straight-line instructions with shared-memory
-// temporaries.
+// staged_kernel: for DAG programs (rank-specific results, rounds whose
+// transfers read each other's destinations).  Same structure, but a stage
+// holds all input tiles of one item, which the consumers evaluate as
+// straight-line instructions with shared-memory temporaries.
 //
 // Every wait is bounded: after two seconds the waiter sets a bit in the
 // status word and the CTA winds down (a failing producer first waits, again
@@ -448,66 +451,6 @@ __device__ __forceinline__ void dag_item(const KernelArgs& a, const DevProg& pg,
     }
 }
 
-// Tree stack in registers: kTreeDepth entries of kVpt vectors per thread.
-// The stack pointer is uniform across the CTA but only known at run time;
-// these recursive helpers turn each access into a chain of uniform branches,
-// one per possible depth, so every stack entry keeps fixed registers.
-template <int K = 0>
-__device__ __forceinline__ void tree_push(uint4 (&stk)[kTreeDepth][kVpt], int sp, uint32_t t, uint32_t nvec,
-                                          int ct) {
-    if (sp == K) {
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) {
-            const uint32_t v = ct + j * kConsumers;
-            if (v < nvec) stk[K][j] = lds128(t + v * 16);
-        }
-    } else if constexpr (K + 1 < kTreeDepth) {
-        tree_push<K + 1>(stk, sp, t, nvec, ct);
-    }
-}
-
-// stk[sp-2] = stk[sp-2] (+) stk[sp-1]: the left subtree sits deeper
-template <int DT, int OP, int K = 2>
-__device__ __forceinline__ void tree_combine(uint4 (&stk)[kTreeDepth][kVpt], int sp, uint32_t nvec, int ct) {
-    if (sp == K) {
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) {
-            const uint32_t v = ct + j * kConsumers;
-            if (v < nvec) stk[K - 2][j] = vop<DT, OP>(stk[K - 2][j], stk[K - 1][j]);
-        }
-    } else if constexpr (K < kTreeDepth) {
-        tree_combine<DT, OP, K + 1>(stk, sp, nvec, ct);
-    }
-}
-
-// A single tree every rank receives, evaluated in post-order from the item's
-// resident leaf tiles, all of this thread's vectors at once.
-template <int DT, int OP>
-__device__ __forceinline__ void tree_item(const KernelArgs& a, const DevProg& pg, uint32_t st, uint32_t nvec,
-                                          int64_t off, int ct) {
-    uint32_t counts[kTreeMaxLeaves / 16];
-#pragma unroll
-    for (int q = 0; q < kTreeMaxLeaves / 16; ++q) counts[q] = a.ins[pg.ins_off + q];
-    uint4 stk[kTreeDepth][kVpt];
-    int sp = 0;
-    for (uint32_t i = 0; i < pg.n_in; ++i) {
-        tree_push(stk, sp++, st + i * a.tile_bytes, nvec, ct);
-        for (uint32_t c = (counts[i >> 4] >> (2 * (i & 15))) & 3u; c > 0; --c, --sp) tree_combine<DT, OP>(stk, sp, nvec, ct);
-    }
-    if (pg.flags & PF_AVG) {
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) stk[0][j] = vdiv<DT>(stk[0][j], static_cast<float>(a.P));
-    }
-    for (uint32_t o = 0; o < pg.n_out; ++o) {
-        char* dst = out_addr(a, pg, o) + off;
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) {
-            const uint32_t v = ct + j * kConsumers;
-            if (v < nvec) stg128(dst + v * 16, stk[0][j]);
-        }
-    }
-}
-
 template <int DT, int OP>
 __device__ void consume(const KernelArgs& a, const Stage& sm, int ct) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
@@ -531,7 +474,7 @@ __device__ void consume(const KernelArgs& a, const Stage& sm, int ct) {
         else if (pg.kind == PK_ACC)
             acc_item<DT, OP>(a, pg, st, nvec, off, ct);
         else if (pg.kind == PK_TREE)
-            tree_item<DT, OP>(a, pg, st, nvec, off, ct);
+            atomicOr(a.status, kStatusBadProgram);  // trees run on the rank-streaming kernel
         else
             dag_item<DT, OP>(a, pg, st, sm.tmps, nvec, off, ct);
         __syncwarp();
@@ -714,7 +657,77 @@ __device__ __forceinline__ void stream_finish(const KernelArgs& a, const Stage& 
     }
 }
 
+// A single tree streamed one leaf tile at a time.  The top of the stack
+// stays in registers (acc); the entries below it live in the shared-memory
+// stack tiles (entry k in tile k, this thread's own vectors only, so no
+// barrier is needed).  After a leaf arrives: with no combine to follow, the
+// old top moves to shared memory and the leaf becomes the top; otherwise the
+// first combine takes the leaf straight from its stage (top (+) leaf) and
+// the rest fold shared-memory entries into the top (entry (+) top: the left
+// operand is the deeper one).
 template <int DT, int OP, int VPT>
+__device__ __forceinline__ bool stream_tree(const KernelArgs& a, const Stage& sm, const DevProg& pg, uint32_t& g,
+                                            int64_t off, uint32_t nvec, int ct) {
+    const int lane = ct & 31;
+    if (pg.n_tmp > static_cast<uint32_t>(a.max_tmp)) {  // deeper than the launch's stack
+        atomicOr(a.status, kStatusBadProgram);
+        return false;
+    }
+    uint4 acc[VPT];
+    uint32_t sp = 0;  // stack entries, the top one in acc
+    for (uint32_t i = 0; i < pg.n_in; ++i, ++g) {
+        const uint32_t t = stream_acquire(a, sm, g);
+        if (!t) return false;
+        uint32_t c = (a.ins[pg.ins_off + (i >> 3)] >> (4 * (i & 7))) & 15u;
+        if (sp == 0 || c == 0) {
+            if (sp > 0) {
+                const uint32_t slot = sm.tmps + (sp - 1) * a.tile_bytes;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    const uint32_t v = ct + j * kConsumers;
+                    if (v < nvec) sts128(slot + v * 16, acc[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint32_t v = ct + j * kConsumers;
+                if (v < nvec) acc[j] = lds128(t + v * 16);
+            }
+            ++sp;
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint32_t v = ct + j * kConsumers;
+                if (v < nvec) acc[j] = vop<DT, OP>(acc[j], lds128(t + v * 16));
+            }
+            --c;
+        }
+        for (; c > 0; --c, --sp) {
+            const uint32_t slot = sm.tmps + (sp - 2) * a.tile_bytes;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const uint32_t v = ct + j * kConsumers;
+                if (v < nvec) acc[j] = vop<DT, OP>(lds128(slot + v * 16), acc[j]);
+            }
+        }
+        if (i + 1 < pg.n_in) {
+            stream_release(a, sm, g, lane);
+        } else {
+            if (pg.flags & PF_AVG) {
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) acc[j] = vdiv<DT>(acc[j], static_cast<float>(a.P));
+            }
+            stream_finish<VPT>(a, sm, g, t, pg, off, nvec, ct, acc);
+        }
+    }
+    return true;
+}
+
+// TREES: the instantiation for launches with single-tree programs (chains
+// and trees); the others run chains and fp32 accumulation.  Keeping the tree
+// stack and the accumulators in separate instantiations keeps each within
+// the register budget.
+template <int DT, int OP, int VPT, bool TREES>
 __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
     // bf16 fp32 accumulation holds 16 floats per vector: only the narrow
@@ -729,8 +742,15 @@ __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
         const uint32_t nvec = (w.count * ES) >> 4;
         const int64_t off = w.elem * ES;
         uint4 res[VPT];
-        if (pg.kind == PK_ACC) {
-            if (!kAccOk) {
+        if (pg.kind == PK_TREE) {
+            if constexpr (TREES) {
+                if (!stream_tree<DT, OP, VPT>(a, sm, pg, g, off, nvec, ct)) return;
+            } else {
+                atomicOr(a.status, kStatusBadProgram);
+                return;
+            }
+        } else if (pg.kind == PK_ACC) {
+            if (!kAccOk || TREES) {
                 atomicOr(a.status, kStatusBadProgram);
                 return;
             }
@@ -789,7 +809,7 @@ __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
     }
 }
 
-template <int DT, int OP, int VPT>
+template <int DT, int OP, int VPT, bool TREES>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
@@ -799,7 +819,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_
     sm.ready = sm.empty + 8 * a.stages;
     sm.tiles = sm.full + kBarrierBytes;
     sm.stage_bytes = a.tile_bytes;
-    sm.tmps = 0;
+    // rank-streaming kernel: the tree stack's a.max_tmp tiles follow the stages
+    sm.tmps = sm.tiles + a.stages * a.tile_bytes;
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(sm.full + 8 * s, 1);
@@ -818,7 +839,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_
         if (threadIdx.x == 32 && (a.flags & kArgTmaStore)) stream_store<ES>(a, sm);
         return;
     }
-    stream_consume<DT, OP, VPT>(a, sm, threadIdx.x - 32 * kStreamLead);
+    stream_consume<DT, OP, VPT, TREES>(a, sm, threadIdx.x - 32 * kStreamLead);
 }
 
 // --------------------------------------------------------- element kernel
@@ -864,8 +885,17 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
     };
     for (uint32_t e = t; e < w.count; e += kElemThreads) {
         const int64_t off = (w.elem + e) * ES;
-        for (uint32_t i = 0; i < pg.n_in; ++i)
-            vals[i * kElemThreads + t] = ld_elem<DT>(buf_addr(a, a.refs[pg.in_off + i]) + off);
+        // eight independent loads in flight per thread (a program can have
+        // hundreds of inputs; one load at a time would be latency-bound)
+        uint32_t i = 0;
+        for (; i + 8 <= pg.n_in; i += 8) {
+            uint32_t v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = ld_elem<DT>(buf_addr(a, a.refs[pg.in_off + i + q]) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) vals[(i + q) * kElemThreads + t] = v[q];
+        }
+        for (; i < pg.n_in; ++i) vals[i * kElemThreads + t] = ld_elem<DT>(buf_addr(a, a.refs[pg.in_off + i]) + off);
         if (pg.kind == PK_CHAIN_R || pg.kind == PK_CHAIN_L) {
             uint32_t acc = vals[t];
             for (uint32_t i = 1; i < pg.n_in; ++i) {
@@ -879,8 +909,12 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
             uint32_t stk[kTreeDepth];
             int sp = 0;
             for (uint32_t i = 0; i < pg.n_in; ++i) {
+                if (sp >= kTreeDepth) {  // the lowering never emits a deeper tree
+                    atomicOr(a.status, kStatusBadProgram);
+                    return;
+                }
                 stk[sp++] = vals[i * kElemThreads + t];
-                for (uint32_t q = (a.ins[pg.ins_off + (i >> 4)] >> (2 * (i & 15))) & 3u; q > 0; --q, --sp)
+                for (uint32_t q = (a.ins[pg.ins_off + (i >> 3)] >> (4 * (i & 7))) & 15u; q > 0 && sp >= 2; --q, --sp)
                     stk[sp - 2] = eop<DT, OP>(stk[sp - 2], stk[sp - 1]);
             }
             const uint32_t res = ediv<DT>(stk[0], avg_div(a, pg));
@@ -920,13 +954,15 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
 
 using KernelFn = void (*)(KernelArgs);
 
-enum Which { K_STAGED = 0, K_STREAM = 1, K_STREAM_NARROW = 2, K_ELEM = 3 };
+enum Which { K_STAGED = 0, K_STREAM = 1, K_STREAM_NARROW = 2, K_ELEM = 3, K_STREAM_TREE = 4, K_STREAM_TREE_WIDE = 5 };
 
 template <int DT, int OP>
 KernelFn table(int which) {
     if (which == K_STAGED) return staged_kernel<DT, OP>;
-    if (which == K_STREAM) return stream_kernel<DT, OP, kStreamVpt>;
-    if (which == K_STREAM_NARROW) return stream_kernel<DT, OP, kStreamVptNarrow>;
+    if (which == K_STREAM) return stream_kernel<DT, OP, kStreamVpt, false>;
+    if (which == K_STREAM_NARROW) return stream_kernel<DT, OP, kStreamVptNarrow, false>;
+    if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptNarrow, true>;
+    if (which == K_STREAM_TREE_WIDE) return stream_kernel<DT, OP, kStreamVpt, true>;
     return elementwise_kernel<DT, OP>;
 }
 
@@ -958,7 +994,7 @@ cudaError_t prepare_kernels(int dtype, int op) {
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    for (int which : {K_STAGED, K_STREAM, K_STREAM_NARROW, K_ELEM}) {
+    for (int which : {K_STAGED, K_STREAM, K_STREAM_NARROW, K_ELEM, K_STREAM_TREE, K_STREAM_TREE_WIDE}) {
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel_for(dtype, op, which)),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
@@ -974,7 +1010,11 @@ cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int 
 
 cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
     // the rank tile fixes the vectors per consumer thread
-    const int which = a.tile_bytes == kStreamTileBytes    ? K_STREAM
+    const int which = (a.flags & kArgTrees)
+                          ? (a.tile_bytes == kStreamTileNarrow  ? K_STREAM_TREE
+                             : a.tile_bytes == kStreamTileBytes ? K_STREAM_TREE_WIDE
+                                                                : -1)
+                      : a.tile_bytes == kStreamTileBytes  ? K_STREAM
                       : a.tile_bytes == kStreamTileNarrow ? K_STREAM_NARROW
                                                           : -1;
     if (which < 0) return cudaErrorInvalidValue;

@@ -32,6 +32,9 @@ struct KernelArgs {
 // KernelArgs::flags: the rank-streaming kernel writes results back to shared
 // memory and copies them out with TMA bulk stores (else 128-bit stores)
 constexpr int kArgTmaStore = 1;
+// KernelArgs::flags: the launch has single-tree programs (the rank-streaming
+// kernel's tree instantiations; a.max_tmp stack tiles follow the stages)
+constexpr int kArgTrees = 2;
 
 // Status word bits written by the kernels.
 constexpr int kStatusWaitFull = 1;   // a consumer gave up waiting for a stage

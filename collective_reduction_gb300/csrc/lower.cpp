@@ -13,8 +13,14 @@
 #include "lower.hpp"
 
 #include <algorithm>
+#include <functional>
 #include <map>
 #include <stdexcept>
+
+// Deepest tree stack (tiles below the top) streamed with 32 KB rank tiles.
+#ifndef AR_TREE_WIDE_SLOTS
+#define AR_TREE_WIDE_SLOTS 3
+#endif
 
 namespace ar {
 namespace {
@@ -204,32 +210,53 @@ Prog dag_program(const Dag& d, const std::vector<std::pair<int, int32_t>>& outs,
 // Post-order of a single tree: leaves left to right, and after each leaf the
 // number of combines that follow it; false if the stack gets deeper than
 // kTreeDepth.
-bool tree_program(const Dag& d, int32_t root, std::vector<int32_t>& leaves, std::vector<uint32_t>& combines) {
+bool tree_program(const Dag& d, int32_t root, bool commute, std::vector<int32_t>& leaves,
+                  std::vector<uint32_t>& combines, int& depth) {
     leaves.clear();
     combines.clear();
-    int depth = 0, max_depth = 0;
-    std::vector<std::pair<int32_t, int>> st{{root, 0}};
+    // Stack entries a subtree needs.  With a commutative op the deeper child
+    // is evaluated first (Sethi-Ullman order: a chain needs 2 entries, not
+    // one per leaf); the combine then takes the operands swapped, which
+    // gives the same bits.
+    std::map<int32_t, int> memo;
+    std::function<int(int32_t)> need = [&](int32_t x) -> int {
+        if (d.leaf(x)) return 1;
+        auto it = memo.find(x);
+        if (it != memo.end()) return it->second;
+        const int l = need(d.left(x)), r = need(d.right(x));
+        const int v = commute ? std::max(std::max(l, r), std::min(l, r) + 1) : std::max(l, r + 1);
+        return memo[x] = v;
+    };
+    depth = need(root);
+    if (depth > kTreeDepth) return false;
+    struct Frame {
+        int32_t x;
+        int state;
+        bool swap;
+    };
+    std::vector<Frame> st{{root, 0, false}};
     while (!st.empty()) {
-        auto& top = st.back();
-        const int32_t x = top.first;
+        Frame& top = st.back();
+        const int32_t x = top.x;
         if (d.leaf(x)) {
             leaves.push_back(x);
             combines.push_back(0);
-            max_depth = std::max(max_depth, ++depth);
             st.pop_back();
-        } else if (top.second == 0) {
-            top.second = 1;
-            st.push_back({d.left(x), 0});
-        } else if (top.second == 1) {
-            top.second = 2;
-            st.push_back({d.right(x), 0});
+        } else if (top.state == 0) {
+            top.state = 1;
+            top.swap = commute && need(d.right(x)) > need(d.left(x));
+            const int32_t first = top.swap ? d.right(x) : d.left(x);
+            st.push_back({first, 0, false});
+        } else if (top.state == 1) {
+            top.state = 2;
+            const int32_t second = top.swap ? d.left(x) : d.right(x);
+            st.push_back({second, 0, false});
         } else {
             ++combines.back();
-            --depth;
             st.pop_back();
         }
     }
-    return max_depth <= kTreeDepth && leaves.size() <= static_cast<size_t>(kTreeMaxLeaves);
+    return leaves.size() <= static_cast<size_t>(kTreeMaxLeaves);
 }
 
 // The ranks a fused pass writes in a segment (every rank for an allreduce).
@@ -263,13 +290,15 @@ Prog fused_program(Canon& cn, const Schedule& S, int seg, const std::vector<int>
         return p;
     }
     std::vector<uint32_t> combines;
-    if (same && tree_program(cn.c, x, leaves, combines)) {
+    int depth = 0;
+    if (same && tree_program(cn.c, x, cn.commute, leaves, combines, depth)) {
         Prog p;
         p.kind = PK_TREE;
         for (int32_t l : leaves) p.in.push_back(static_cast<uint16_t>(buf_id(0, l)));
-        // combine counts (< kTreeDepth <= 4), 2 bits per leaf, 16 per word
-        p.ins.assign(kTreeMaxLeaves / 16, 0);
-        for (size_t i = 0; i < combines.size(); ++i) p.ins[i / 16] |= combines[i] << (2 * (i % 16));
+        // combine counts (< kTreeDepth), 4 bits per leaf, 8 per word
+        p.ins.assign(kTreeCountWords, 0);
+        for (size_t i = 0; i < combines.size(); ++i) p.ins[i / 8] |= combines[i] << (4 * (i % 8));
+        p.n_tmp = static_cast<uint16_t>(depth - 1);  // stack entries below the top
         set_outputs(p, ranks, S.P);
         if (avg && !cn.c.leaf(x)) p.flags |= PF_AVG;
         return p;
@@ -286,9 +315,46 @@ Prog acc_program(int P, const std::vector<int>& ranks, bool avg) {
     return p;
 }
 
+using XferAvg = std::pair<const Transfer*, bool>;
+
+// Whether a combine's operands may be swapped without changing a bit.
+bool commute_ok(const Schedule& S) {
+    return S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD || S.op == AR_AVG;
+}
+
+// The transfers of one round over one segment, split into groups that can
+// run as separate work items: a transfer that writes a buffer joins every
+// transfer that reads it (all of a group's reads must happen before its
+// writes, which one work item guarantees); transfers sharing only sources
+// stay apart.
+std::vector<std::vector<XferAvg>> round_components(const std::vector<XferAvg>& xs) {
+    const int n = static_cast<int>(xs.size());
+    std::vector<int> parent(n);
+    for (int i = 0; i < n; ++i) parent[i] = i;
+    std::function<int(int)> find = [&](int i) { return parent[i] == i ? i : parent[i] = find(parent[i]); };
+    std::map<uint32_t, int> writer;
+    for (int i = 0; i < n; ++i) writer[buf_id(xs[i].first->dst_out, xs[i].first->dst)] = i;
+    auto join_reader = [&](int i, uint32_t buf) {
+        auto it = writer.find(buf);
+        if (it != writer.end()) parent[find(i)] = find(it->second);
+    };
+    for (int i = 0; i < n; ++i) {
+        const Transfer& x = *xs[i].first;
+        join_reader(i, buf_id(x.src_slot, x.src));
+        if (x.combine) join_reader(i, buf_id(x.dst_in, x.dst));
+    }
+    std::map<int, std::vector<XferAvg>> groups;
+    for (int i = 0; i < n; ++i) groups[find(i)].push_back(xs[i]);
+    std::vector<std::vector<XferAvg>> out;
+    for (auto& kv : groups) out.push_back(std::move(kv.second));
+    return out;
+}
+
 // One round over one segment: each transfer with whether its combine
 // completes an AR_AVG sum (that result is divided by P as it is stored).
-Prog round_program(std::vector<std::pair<const Transfer*, bool>> xa) {
+// commute: combines that swap the same two operands (the exchange of
+// recursive doubling) give one value, computed once for every output.
+Prog round_program(std::vector<XferAvg> xa, bool commute) {
     std::sort(xa.begin(), xa.end(), [](const std::pair<const Transfer*, bool>& a,
                                        const std::pair<const Transfer*, bool>& b) {
         return std::make_pair(a.first->dst, a.first->dst_out) < std::make_pair(b.first->dst, b.first->dst_out);
@@ -296,6 +362,26 @@ Prog round_program(std::vector<std::pair<const Transfer*, bool>> xa) {
     std::vector<const Transfer*> xs;
     for (const auto& t : xa) xs.push_back(t.first);
     Prog p;
+    if (commute && xs.size() > 1) {
+        // every transfer combines the same two buffers, in either order
+        const Transfer& x0 = *xs[0];
+        const uint32_t a = buf_id(x0.src_slot, x0.src), c = buf_id(x0.dst_in, x0.dst);
+        bool same = a != c;
+        for (size_t k = 0; k < xa.size() && same; ++k) {
+            const Transfer& x = *xs[k];
+            const uint32_t s0 = buf_id(x.src_slot, x.src), d0 = buf_id(x.dst_in, x.dst);
+            same = x.combine && xa[k].second == xa[0].second &&
+                   ((s0 == a && d0 == c) || (s0 == c && d0 == a));
+        }
+        if (same && x0.combine) {
+            p.kind = PK_CHAIN_R;
+            p.in.push_back(static_cast<uint16_t>(a));
+            p.in.push_back(static_cast<uint16_t>(c));
+            for (const Transfer* x : xs) p.out.push_back(static_cast<uint16_t>(buf_id(x->dst_out, x->dst)));
+            if (xa[0].second) p.flags |= PF_AVG;
+            return p;
+        }
+    }
     if (xs.size() == 1) {  // one transfer: acc = src, then dst_in (+) acc
         const Transfer& x = *xs[0];
         p.kind = PK_CHAIN_R;
@@ -354,7 +440,9 @@ int staged_smem_bytes(const Lowered& lw) {
     return kBarrierBytes + lw.tile_bytes * (lw.stages * lw.max_in + lw.max_tmp);
 }
 
-int stream_smem_bytes(const Lowered& lw) { return kBarrierBytes + lw.stream_tile * lw.stream_stages; }
+int stream_smem_bytes(const Lowered& lw) {
+    return kBarrierBytes + lw.stream_tile * (lw.stream_stages + lw.stream_slots);
+}
 
 void lower(const Schedule& S, Lowered& lw) {
     lw = Lowered();
@@ -386,18 +474,29 @@ void lower(const Schedule& S, Lowered& lw) {
                 }
                 std::vector<Range> rs;
                 for (auto& kv : by_seg)
-                    push_range(rs, b.add(round_program(kv.second)), S.bounds[kv.first], S.bounds[kv.first + 1]);
+                    for (auto& comp : round_components(kv.second))
+                        push_range(rs, b.add(round_program(comp, commute_ok(S))), S.bounds[kv.first],
+                                   S.bounds[kv.first + 1]);
                 sets.push_back(rs);
             }
         }
     }
-    // A set whose programs are all chains / fp32 accumulations streams one
-    // rank tile at a time (rank-streaming kernel); sets with a tree or DAG
-    // program stage all of an item's input tiles at once (staged kernel).
+    // A set whose programs are all chains, single trees or fp32
+    // accumulations streams one rank tile at a time (rank-streaming kernel);
+    // sets with a DAG program stage all of an item's input tiles at once
+    // (staged kernel).
     std::vector<bool> stream(sets.size(), true);
     for (size_t k = 0; k < sets.size(); ++k)
         for (auto& r : sets[k])
-            if (lw.progs[r.prog].kind == PK_DAG || lw.progs[r.prog].kind == PK_TREE) stream[k] = false;
+            if (lw.progs[r.prog].kind == PK_DAG) stream[k] = false;
+    bool stream_trees = false;
+    lw.stream_slots = 0;  // shared-memory tiles for the deepest tree stack
+    for (size_t k = 0; k < sets.size(); ++k)
+        for (auto& r : sets[k])
+            if (stream[k] && lw.progs[r.prog].kind == PK_TREE) {
+                stream_trees = true;
+                lw.stream_slots = std::max<int>(lw.stream_slots, lw.progs[r.prog].n_tmp);
+            }
     // staged-kernel geometry from the programs that own an aligned body
     lw.max_in = 1;
     lw.max_tmp = 0;
@@ -424,10 +523,16 @@ void lower(const Schedule& S, Lowered& lw) {
     t = std::min<int64_t>(t, kMaxTileBytes);
     t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
     lw.tile_bytes = static_cast<int>(t);
-    // bf16 fp32 accumulation holds 16 fp32 per vector: 16 KB rank tiles
-    const bool narrow = S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC;
+    // bf16 fp32 accumulation holds 16 fp32 per vector: 16 KB rank tiles (4
+    // vectors per thread).  A tree keeps depth - 1 stack tiles in shared
+    // memory next to the stages: 32 KB tiles while that leaves a pipeline of
+    // several stages, 16 KB tiles for deeper trees.
+    const bool narrow = (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC) ||
+                        (stream_trees && lw.stream_slots > AR_TREE_WIDE_SLOTS);
+    lw.stream_trees = stream_trees;
     lw.stream_tile = narrow ? kStreamTileNarrow : kStreamTileBytes;
-    lw.stream_stages = std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile);
+    lw.stream_stages =
+        std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile - lw.stream_slots);
     // The TMA-store epilogue holds an item's last stage until its outputs are
     // copied out: measured faster with few outputs per item (and for bf16
     // fp32 accumulation, whose direct stores are costly), slower with many.

@@ -29,6 +29,8 @@ struct Lowered {
     int stream_tile = 0;  // bytes per rank tile of the rank-streaming kernel
     int stream_stages = 0;
     bool stream_tma_store = false;  // rank-streaming kernel: TMA bulk-store epilogue
+    bool stream_trees = false;      // rank-streaming kernel: the instantiation that runs TREE programs
+    int stream_slots = 0;           // rank-streaming kernel: shared-memory tiles of the tree stack
     int max_in = 0;       // largest n_in of a program used by bulk items
     int max_tmp = 0;      // largest n_tmp of such a program
     int max_in_all = 0;   // largest n_in / n_tmp over all programs

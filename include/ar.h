@@ -153,7 +153,13 @@ typedef struct {
     int tile_bytes;              /* bytes per input tile in the staged kernel      */
     int n_programs;              /* distinct tile programs                         */
     uint64_t n_items;            /* work items over all launches                   */
+    int kernels;                 /* kernels the aligned launches use: AR_KERNEL_*  */
 } ar_plan_info;
+
+/* ar_plan_info.kernels bits: the rank-streaming kernel (chains, single trees,
+ * fp32 accumulation), the staged kernel (DAG programs), the element-wise
+ * kernel (unaligned edges and tiny passes). */
+enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4 };
 
 typedef struct ar_schedule_s* ar_schedule_t;
 typedef struct ar_plan_s* ar_plan_t;
@@ -183,6 +189,46 @@ ar_status ar_schedule_step_sent(ar_schedule_t s, int step, uint64_t* elems_per_r
  * buffer is too small (nothing useful written) or indices are out of range. */
 ar_status ar_schedule_tree(ar_schedule_t s, int rank, uint64_t elem, char* buf, size_t cap,
                            size_t* needed);
+
+/* ---- cost model and step selection (host only) ----------------------------
+ * "A Generalization of the Allreduce Operation", the complexity of the
+ * algorithm with r removed distribution steps (eq. 36) and the r that
+ * minimises it (eq. 37): every step costs a latency alpha, every byte sent
+ * beta, every byte reduced gamma.  On one GPU the messages of all P ranks in
+ * a round share the HBM, so for the engine's step form (one launch per
+ * round) a schedule costs
+ *     alpha * rounds + beta * (bytes sent, all ranks)
+ *                    + gamma * (bytes combined, all ranks)
+ * i.e. the page's per-process beta and gamma are P times these.  The fused
+ * form moves 2 P S bytes in one launch whatever the schedule, so the model
+ * selects among step-form schedules only. */
+typedef struct {
+    double alpha_us;           /* per round (one kernel launch)           */
+    double beta_us_per_byte;   /* per byte sent, summed over ranks        */
+    double gamma_us_per_byte;  /* per byte combined, summed over ranks    */
+} ar_cost_model;
+
+/* The step-form model fitted on GB300 (bench.py --costmodel). */
+ar_status ar_cost_model_default(ar_cost_model* out);
+/* Predicted step-form time of a compiled schedule under the model: from its
+ * rounds, bytes sent and combines.  AR_ERR_INVALID_ARG on null arguments. */
+ar_status ar_cost_predict(ar_schedule_t s, const ar_cost_model* model, double* us);
+/* Eq. (37) for P ranks of bytes_per_rank bytes (m): the real minimiser
+ * r* = log2(alpha / (ln 2 * m * (L beta + (2L - 2) gamma))) of eq. (36),
+ * L = ceil(log2 P), taken to whichever neighbouring integer eq. (36) rates
+ * lower and clamped to 0..L-1 (eq. 36 holds for r < L; the latency-optimal
+ * r = L is costed separately on the page, and by ar_cost_select here).
+ * P = 1 gives 0.  AR_ERR_INVALID_ARG on P < 1, P > AR_MAX_RANKS, m = 0, a
+ * non-positive alpha, negative beta or gamma, or null pointers. */
+ar_status ar_cost_optimal_r(int P, uint64_t bytes_per_rank, const ar_cost_model* model, int* r);
+/* The step-form schedule with the lowest predicted time among the ring, the
+ * binomial tree, RD, RH, the hybrid for every k1 and the cyclic generalized
+ * schedule for every r (the page's ring / tree switch and r choice made on
+ * exact counters).  Writes the algorithm, its params (step form, faithful)
+ * and the prediction; ties keep the earlier candidate in that order.  Errors
+ * as ar_schedule_create. */
+ar_status ar_cost_select(int P, uint64_t n, ar_dtype dtype, ar_op op, const ar_cost_model* model,
+                         ar_algo* algo, ar_params* params, double* us);
 
 /* ---- plans (need a CUDA device) -------------------------------------------
  * ar_plan_create compiles the schedule, lowers it to tile programs for the

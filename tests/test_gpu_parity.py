@@ -453,3 +453,39 @@ def test_avg_unaligned_and_int32_refused():
         assert_bit_equal(dev[r].cpu().numpy(), want[r], "float32", f"rank {r}")
     with pytest.raises(ar.ArError):
         ar.Plan(P, n, "int32", "avg", "ring")
+
+
+def test_kernel_choice_per_program_kind():
+    """Chains and single trees stream rank tiles (rank-streaming kernel);
+    rank-specific DAGs stage an item's tiles (staged kernel); tiny or
+    unaligned ranges go element by element."""
+    import collective_reduction_gb300 as ar
+    n = 1 << 20
+    for algo, kw in (("ring", {}), ("rh", {}), ("binomial", {}), ("rd", {}), ("ahc", {"group_sizes": [4, 4]})):
+        k = ar.Plan(8, n, "float32", "sum", algo, **kw).info()["kernels"]
+        assert k == ar.KERNEL_STREAM, (algo, k)
+    # 30 chunks of 2^20 elements: unaligned chunk edges go element-wise
+    k = ar.Plan(8, n, "float32", "sum", "ahc", group_sizes=[3, 5]).info()["kernels"]
+    assert k == ar.KERNEL_STREAM | ar.KERNEL_ELEMENTWISE, k
+    assert ar.Plan(8, n, "bfloat16", "sum", "rh").info()["kernels"] == ar.KERNEL_STREAM
+    assert ar.Plan(7, 7 * 4096, "float32", "max", "generalized", r=3).info()["kernels"] & ar.KERNEL_STAGED
+    assert ar.Plan(3, 5, "float32", "sum", "ring").info()["kernels"] == ar.KERNEL_ELEMENTWISE
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("algo,kw", [("rh", {}), ("binomial", {}), ("generalized", {"r": 0}),
+                                     ("ahc", {"group_sizes": [2, 6]}), ("rh", {"phase": "reduce_scatter"})])
+def test_streamed_trees_many_items(algo, kw, dtype):
+    """Single trees on the rank-streaming kernel over many items per CTA,
+    with a ragged tail: bit-identical to the oracle on the owned / all
+    elements."""
+    P, n = 8, (1 << 22) + 77
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=17)
+    res = oracle.run(algo, bufs, Arith("sum", dtype), **kw)
+    got = engine(bufs, dtype, "sum", algo, **kw)
+    if kw.get("phase") == "reduce_scatter":
+        for r, lo, hi in res.info["owner"]:
+            assert_bit_equal(got[r][lo:hi], res.bufs[r][lo:hi], dtype, f"{algo} rank {r}")
+    else:
+        for r in range(P):
+            assert_bit_equal(got[r], res.bufs[r], dtype, f"{algo} {kw} rank {r}")
