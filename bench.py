@@ -675,7 +675,9 @@ def time_plan(plan, dev, reps=5, calls=20):
 
 
 def row_cases():
-    """(row, algo, params, sample chunks) of every schedule at P = 8."""
+    """(row, P, op, algo, params, sample chunks): every schedule at P = 8,
+    then rank-specific DAG programs (the generalized schedule with removed
+    steps at P = 7, recursive doubling for max)."""
     out = []
     for algo, kw, chunks, row in (("ring", {}, 8, "a3/a4 ring RS+AG"),
                                   ("binomial", {}, 1, "a5/a6 binomial reduce+broadcast"),
@@ -687,12 +689,16 @@ def row_cases():
                                   ("ahc", {"group_sizes": [4, 4]}, 8, "a12-a14 AHC {4,4}"),
                                   ("pipeline", {"blocks": 4}, 4, "f4 pipelined chain m=4")):
         for form in ("fused", "step"):
-            out.append((row, algo, dict(kw, form=form), chunks))
+            out.append((row, 8, "sum", algo, dict(kw, form=form), chunks))
     for algo in ("ring", "rh"):
         for phase in ("reduce_scatter", "all_gather"):
-            out.append((f"f2 {phase}", algo, {"form": "fused", "phase": phase}, 8))
-    out.append(("a15 fp32acc", "ring", {"form": "fused", "order": "fp32acc"}, 8))
-    out.append(("a15 fp32acc", "ahc", {"form": "fused", "order": "fp32acc", "group_sizes": [4, 4]}, 8))
+            out.append((f"f2 {phase}", 8, "sum", algo, {"form": "fused", "phase": phase}, 8))
+    out.append(("a15 fp32acc", 8, "sum", "ring", {"form": "fused", "order": "fp32acc"}, 8))
+    out.append(("a15 fp32acc", 8, "sum", "ahc", {"form": "fused", "order": "fp32acc", "group_sizes": [4, 4]}, 8))
+    for r in (1, 3):
+        for form in ("fused", "step"):
+            out.append((f"a9 generalized P=7 r={r}", 7, "sum", "generalized", {"r": r, "form": form}, 7))
+    out.append(("a8 RD max (rank-specific)", 8, "max", "rd", {"form": "fused"}, 1))
     return out
 
 
@@ -713,7 +719,7 @@ def run_rows(a, path):
     from oracle.elementops import Arith, bf16_to_f32
     torch.cuda.set_device(0)
     peak, _ = measured_peak()
-    P, K = 8, 1 << 14
+    K = 1 << 14
 
     def bits(x):
         x = np.ascontiguousarray(x)
@@ -722,11 +728,11 @@ def run_rows(a, path):
     with open(path, "w") as out:
         for dtype in ("float32", "bfloat16"):
             n = (256 << 20) // esize(dtype)
-            src = ar_synth.device_inputs(P, n, dtype, sigma=1e-2, seed=3)
-            for row, algo, kw, chunks in row_cases():
-                dev = [t.clone() for t in src]
+            src = ar_synth.device_inputs(8, n, dtype, sigma=1e-2, seed=3)
+            for row, P, op, algo, kw, chunks in row_cases():
+                dev = [t.clone() for t in src[:P]]
                 sample_in, idx = gather_sample(dev, P, n, K, chunks)
-                plan = ar.Plan(P, n, dtype, "sum", algo, **kw)
+                plan = ar.Plan(P, n, dtype, op, algo, **kw)
                 info = plan.info()
                 plan.execute(dev)
                 plan.check()
@@ -735,11 +741,11 @@ def run_rows(a, path):
                        for g in got]
                 okw = {k: v for k, v in kw.items() if k in ("r", "k1", "group_sizes", "blocks", "phase")}
                 if kw.get("order") == "fp32acc":
-                    ref = direct_f64(sample_in, "sum", dtype)
+                    ref = direct_f64(sample_in, op, dtype)
                     err = max(normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) for g in got)
                     ok = err <= (1e-6 if dtype == "float32" else 4e-3)
                 else:
-                    want = oracle.run(algo, sample_in, Arith("sum", dtype), **okw)
+                    want = oracle.run(algo, sample_in, Arith(op, dtype), **okw)
                     if kw.get("phase") == "reduce_scatter":
                         ok = all(np.array_equal(bits(got[r][lo:hi]), bits(want.bufs[r][lo:hi]))
                                  for r, lo, hi in want.info["owner"])
@@ -748,7 +754,8 @@ def run_rows(a, path):
                 us = time_plan(plan, dev, reps=5, calls=10)
                 gbps = info["hbm_bytes"] / (us / 1e6) / 1e9
                 out.write(json.dumps({
-                    "row": row, "algo": algo, "params": kw, "dtype": dtype, "P": P, "bytes_per_rank": n * esize(dtype),
+                    "row": row, "algo": algo, "op": op, "params": kw, "dtype": dtype, "P": P,
+                    "bytes_per_rank": n * esize(dtype),
                     "verified": bool(ok), "steps": info["steps"], "launches": info["launches"],
                     "kernels": info["kernels"], "us_per_call": round(us, 2), "hbm_bytes": info["hbm_bytes"],
                     "hbm_GBps": round(gbps, 1), "frac_of_measured": round(gbps / peak, 4),
@@ -765,8 +772,10 @@ def run_costmodel(a, path):
     Operation", eqs. 36-37) on this GPU.  Fit: alpha per round, beta per byte
     sent and gamma per byte combined (bytes over all ranks) by non-negative
     least squares on relative error, over step-form ring, binomial, RD and
-    bandwidth-optimal generalized plans (rounds of independent transfers) at
-    P in {4, 16, 63} and 2 KiB .. 64 MiB per rank.  Validation: at P in {7, 12, 31, 63} and 1 KiB .. 16 MiB per
+    bandwidth-optimal generalized plans (rounds of independent transfers) and
+    the ring's reduce-scatter (combines) and all-gather (copies) halves, which
+    tell beta and gamma apart, at P in {4, 16, 63} and 2 KiB .. 64 MiB per
+    rank.  Validation: at P in {7, 12, 31, 63} and 1 KiB .. 16 MiB per
     rank, every candidate the selection weighs is timed; the measured best r
     of the generalized schedule is set against eq. (37)'s r, and the
     selection's pick against the fastest candidate."""
@@ -789,7 +798,8 @@ def run_costmodel(a, path):
                 S = 1 << lg
                 n = S // esize(dtype)
                 dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
-                for algo, kw in (("ring", {}), ("binomial", {}), ("rd", {}), ("generalized", {"r": 0})):
+                for algo, kw in (("ring", {}), ("binomial", {}), ("rd", {}), ("generalized", {"r": 0}),
+                                 ("ring", {"phase": "reduce_scatter"}), ("ring", {"phase": "all_gather"})):
                     plan = ar.Plan(P, n, dtype, "sum", algo, form="step", **kw)
                     us = time_plan(plan, dev)
                     c = counters(plan.info())
