@@ -21,8 +21,9 @@ FORMS = {"fused": 0, "step": 1}
 ORDERS = {"faithful": 0, "fp32acc": 1}
 GROUPS = {"cyclic": 0, "xor": 1}
 PHASES = {"allreduce": 0, "reduce_scatter": 1, "all_gather": 2}
+JIT = {"auto": 0, "on": 1, "off": -1}
 ESIZE = {"int32": 4, "float32": 4, "bfloat16": 2}
-KERNEL_STREAM, KERNEL_STAGED, KERNEL_ELEMENTWISE = 1, 2, 4  # Plan.info()["kernels"] bits
+KERNEL_STREAM, KERNEL_STAGED, KERNEL_ELEMENTWISE, KERNEL_DAG_JIT = 1, 2, 4, 8  # Plan.info()["kernels"] bits
 MAX_RANKS = 64
 
 STATUS = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_UNSUPPORTED", 3: "AR_ERR_CUDA",
@@ -42,7 +43,7 @@ class Params(ctypes.Structure):
     _fields_ = [("form", ctypes.c_int), ("order", ctypes.c_int), ("group", ctypes.c_int),
                 ("r", ctypes.c_int), ("k1", ctypes.c_int), ("n_groups", ctypes.c_int),
                 ("group_sizes", ctypes.POINTER(ctypes.c_int)), ("blocks", ctypes.c_int),
-                ("phase", ctypes.c_int)]
+                ("phase", ctypes.c_int), ("jit", ctypes.c_int)]
 
 
 class Info(ctypes.Structure):
@@ -84,6 +85,7 @@ _EXPORTS = {
     "ar_execute_host": (ctypes.c_int, [_VP, ctypes.POINTER(_VP), ctypes.POINTER(_VP), _VP]),
     "ar_plan_check": (ctypes.c_int, [_VP]),
     "ar_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ar_schedule_dag_kernel": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     "ar_cost_model_default": (ctypes.c_int, [ctypes.POINTER(CostModel)]),
     "ar_cost_predict": (ctypes.c_int, [_VP, ctypes.POINTER(CostModel), ctypes.POINTER(ctypes.c_double)]),
     "ar_cost_optimal_r": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64, ctypes.POINTER(CostModel),
@@ -123,8 +125,9 @@ def _check(status, where):
 
 
 def _params(form="fused", order="faithful", group="cyclic", r=0, k1=0, group_sizes=None, blocks=1,
-            phase="allreduce"):
-    p = Params(FORMS[form], ORDERS[order], GROUPS[group], int(r), int(k1), 0, None, int(blocks), PHASES[phase])
+            phase="allreduce", jit="auto"):
+    p = Params(FORMS[form], ORDERS[order], GROUPS[group], int(r), int(k1), 0, None, int(blocks), PHASES[phase],
+               JIT[jit])
     keep = None
     if group_sizes is not None:
         keep = (ctypes.c_int * len(group_sizes))(*[int(g) for g in group_sizes])
@@ -177,6 +180,13 @@ class Schedule:
         _check(lib().ar_schedule_tree(self._h, rank, elem, buf, need.value, ctypes.byref(need)),
                "ar_schedule_tree")
         return buf.value.decode()
+
+    def dag_kernel_bytes(self):
+        """Code size of the run-time DAG kernel a plan of this schedule would
+        compile (0: no DAG program on the staged kernel); compiles on the host."""
+        n = ctypes.c_size_t(0)
+        _check(lib().ar_schedule_dag_kernel(self._h, ctypes.byref(n)), "ar_schedule_dag_kernel")
+        return n.value
 
     def close(self):
         if getattr(self, "_h", None):

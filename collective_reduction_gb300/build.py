@@ -19,7 +19,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libar.so")
-SOURCES = ["kernels.cu", "noalloc.cu", "schedule.cpp", "lower.cpp", "api.cpp", "cost.cpp"]
+SOURCES = ["kernels.cu", "noalloc.cu", "schedule.cpp", "lower.cpp", "api.cpp", "cost.cpp", "jit.cpp"]
+# headers the run-time compiled DAG kernels include, embedded into jit.cpp
+JIT_HEADERS = [os.path.join(INCLUDE, "ar.h")] + [os.path.join(CSRC, h) for h in ("devprog.hpp", "kargs.hpp",
+                                                                                  "device.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,12 +37,33 @@ def nvcc():
     return p
 
 
+def write_jit_headers(path):
+    """The JIT headers as C++ raw string literals, by include name."""
+    names, bodies = [], []
+    for h in JIT_HEADERS:
+        with open(h) as f:
+            text = f.read()
+        if ")ARJIT\"" in text:
+            raise RuntimeError(f"{h} contains the raw-string delimiter")
+        names.append(os.path.basename(h))
+        bodies.append(text)
+    with open(path, "w") as f:
+        f.write(f"constexpr int kJitHeaderCount = {len(names)};\n")
+        f.write("const char* const kJitHeaderNames[] = {" + ", ".join(f'"{n}"' for n in names) + "};\n")
+        f.write("const char* const kJitHeaders[] = {\n")
+        for b in bodies:
+            f.write('R"ARJIT(' + b + ')ARJIT",\n')
+        f.write("};\n")
+
+
 def build(verbose=False, defines=(), out=None):
     """Compile and link; `defines` are extra -D macros, `out` another path."""
     nv = nvcc()
     common = ["-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
     common += [f"-D{d}" for d in defines]
     with tempfile.TemporaryDirectory(prefix="ar_build_") as tmp:
+        write_jit_headers(os.path.join(tmp, "jit_headers.inc"))
+        common += ["-I", tmp]
         procs, objs = [], []
         for src in SOURCES:
             obj = os.path.join(tmp, src + ".o")
@@ -60,7 +84,7 @@ def build(verbose=False, defines=(), out=None):
         if failed:
             raise RuntimeError("libar build failed:\n" + "\n".join(failed))
         tmp_lib = os.path.join(tmp, "libar.so")
-        link = [nv, "-shared", "-o", tmp_lib] + objs + ARCH + ["-cudart", "static"]
+        link = [nv, "-shared", "-o", tmp_lib] + objs + ARCH + ["-cudart", "static", "-ldl"]
         r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("libar link failed:\n" + r.stdout.decode(errors="replace"))

@@ -10,9 +10,20 @@
 #include <vector>
 
 #include "ar.h"
+#include "jit.hpp"
 #include "kernels.hpp"
 #include "lower.hpp"
 #include "schedule.hpp"
+
+namespace {
+// AR_JIT_AUTO compiles a plan's DAG kernel when its staged launches move at
+// least this much: smaller ones are launch-bound, where interpreting costs
+// little and the compile time (a fraction of a second) would dominate.
+constexpr uint64_t kJitMinBytes = 16ull << 20;
+// Programs beyond this many instruction words stay interpreted: the
+// compile time grows past a few seconds.
+constexpr size_t kJitMaxWords = 4096;
+}  // namespace
 
 struct ar_schedule_s {
     ar::Schedule S;
@@ -31,6 +42,7 @@ struct ar_plan_s {
     uint64_t slot_stride = 0;
     uint64_t scratch_bytes = 0;
     int* d_status = nullptr;
+    const void* dag_fn = nullptr;  // run-time compiled staged kernel, or null: interpret
     struct Set {
         const ar::WorkItem* bulk;
         const ar::WorkItem* edge;
@@ -162,7 +174,13 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
             a.stages = plan->L.stages;
             a.max_in = plan->L.max_in;
             a.max_tmp = plan->L.max_tmp;
-            e = ar::launch_staged(S.dtype, S.op, a, grid, plan->smem_staged, st);
+            if (plan->dag_fn) {
+                void* args[] = {&a};
+                e = cudaLaunchKernel(plan->dag_fn, dim3(grid), dim3(ar::kStagedThreads), args,
+                                     static_cast<size_t>(plan->smem_staged), st);
+            } else {
+                e = ar::launch_staged(S.dtype, S.op, a, grid, plan->smem_staged, st);
+            }
         }
     }
     if (e == cudaSuccess && e1 > e0) {
@@ -269,6 +287,27 @@ ar_status ar_schedule_tree(ar_schedule_t s, int rank, uint64_t elem, char* buf, 
     }
 }
 
+ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes) {
+    if (!s || !cubin_bytes) return AR_ERR_INVALID_ARG;
+    *cubin_bytes = 0;
+    try {
+        ar::Lowered L;
+        ar::lower(s->S, L);
+        const std::string src = ar::dag_kernel_source(s->S, L);
+        if (src.empty()) return AR_OK;
+        std::string cubin;
+        const int rc = ar::compile_dag_kernel(src, cubin, nullptr);
+        if (rc == 1) return AR_ERR_UNSUPPORTED;
+        if (rc != 0) return AR_ERR_CUDA;
+        *cubin_bytes = cubin.size();
+        return AR_OK;
+    } catch (const std::length_error&) {
+        return AR_ERR_UNSUPPORTED;
+    } catch (const std::bad_alloc&) {
+        return AR_ERR_NOMEM;
+    }
+}
+
 ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo, const ar_params* params,
                          ar_plan_t* out) {
     if (!out) return AR_ERR_INVALID_ARG;
@@ -304,6 +343,15 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
         if (p->smem_staged > optin || p->smem_stream > optin || p->smem_elem > optin) {
             delete p;
             return AR_ERR_UNSUPPORTED;
+        }
+        // the staged launches' DAG programs as run-time compiled code
+        const size_t words = ar::dag_kernel_words(L);
+        if (words > 0 && words <= kJitMaxWords && p->S.params.jit != AR_JIT_OFF) {
+            uint64_t dag_bytes = 0;
+            for (const ar::LaunchSet& s : L.sets)
+                if (!s.stream && !s.small && !s.bulk.empty()) dag_bytes += s.bytes;
+            if (p->S.params.jit == AR_JIT_ON || dag_bytes >= kJitMinBytes)
+                p->dag_fn = ar::load_dag_kernel(ar::dag_kernel_source(p->S, L));
         }
         // one device blob: programs, refs, instructions, then every item list
         std::vector<char> blob;
@@ -375,6 +423,7 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info) {
             continue;
         }
         if (!s.bulk.empty()) info->kernels |= s.stream ? AR_KERNEL_STREAM : AR_KERNEL_STAGED;
+        if (!s.bulk.empty() && !s.stream && plan->dag_fn) info->kernels |= AR_KERNEL_DAG_JIT;
         if (!s.edge.empty()) info->kernels |= AR_KERNEL_ELEMENTWISE;
     }
     return AR_OK;

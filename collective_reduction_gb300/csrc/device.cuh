@@ -1,0 +1,487 @@
+// Device code shared by the engine's compiled kernels (kernels.cu) and the
+// DAG kernels it compiles at run time for a plan: element arithmetic, memory
+// and mbarrier helpers, and the staged kernel's producer / consumer loop.
+// Compiles under nvcc and NVRTC (no host headers under NVRTC).
+#pragma once
+
+#include "kargs.hpp"
+
+namespace ar {
+namespace {
+
+
+constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits give up after 2 s
+constexpr int kVpt = kStagedVpt;             // 16-byte vectors per consumer thread per item
+constexpr int kConsumers = 32 * kConsumerWarps;
+
+// ---------------------------------------------------------------- arithmetic
+
+template <int OP>
+__device__ __forceinline__ float fop(float a, float b) {
+    if (OP == AR_SUM) return __fadd_rn(a, b);
+    if (OP == AR_PROD) return __fmul_rn(a, b);
+    if (OP == AR_MAX) return a > b ? a : b;
+    return a < b ? a : b;
+}
+
+template <int OP>
+__device__ __forceinline__ int32_t iop(int32_t a, int32_t b) {
+    if (OP == AR_SUM) return static_cast<int32_t>(static_cast<uint32_t>(a) + static_cast<uint32_t>(b));
+    if (OP == AR_PROD) return static_cast<int32_t>(static_cast<uint32_t>(a) * static_cast<uint32_t>(b));
+    if (OP == AR_MAX) return a > b ? a : b;
+    return a < b ? a : b;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// two fp32 values rounded to bf16 (nearest even) and packed, lo in bits 0..15
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// a (+) b on one 32-bit word: one int32 / fp32 element or two bf16 elements
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t wop(uint32_t a, uint32_t b) {
+    if (DT == AR_INT32) return static_cast<uint32_t>(iop<OP>(static_cast<int32_t>(a), static_cast<int32_t>(b)));
+    if (DT == AR_FLOAT32) return __float_as_uint(fop<OP>(__uint_as_float(a), __uint_as_float(b)));
+    const float al = bf_lo(a), ah = bf_hi(a), bl = bf_lo(b), bh = bf_hi(b);
+    if (OP == AR_MAX || OP == AR_MIN) {
+        const bool pl = OP == AR_MAX ? al > bl : al < bl;
+        const bool ph = OP == AR_MAX ? ah > bh : ah < bh;
+        return ((pl ? a : b) & 0xFFFFu) | ((ph ? a : b) & 0xFFFF0000u);
+    }
+    return pack_bf16x2(fop<OP>(al, bl), fop<OP>(ah, bh));
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint4 vop(uint4 a, uint4 b) {
+    return make_uint4(wop<DT, OP>(a.x, b.x), wop<DT, OP>(a.y, b.y), wop<DT, OP>(a.z, b.z),
+                      wop<DT, OP>(a.w, b.w));
+}
+
+// AR_AVG: a complete sum divided by the rank count d (IEEE division, round to
+// nearest even; bf16 values divided in fp32 and rounded back to bf16).
+template <int DT>
+__device__ __forceinline__ uint32_t wdiv(uint32_t w, float d) {
+    if (DT == AR_FLOAT32) return __float_as_uint(__fdiv_rn(__uint_as_float(w), d));
+    if (DT == AR_BFLOAT16) return pack_bf16x2(__fdiv_rn(bf_lo(w), d), __fdiv_rn(bf_hi(w), d));
+    return w;  // int32 has no average (refused when the plan is made)
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 vdiv(uint4 v, float d) {
+    return make_uint4(wdiv<DT>(v.x, d), wdiv<DT>(v.y, d), wdiv<DT>(v.z, d), wdiv<DT>(v.w, d));
+}
+
+// Accumulator of the FP32ACC order: int32 stays int32 (exact in any order),
+// fp32 and bf16 accumulate in fp32 and round once.
+template <int DT>
+struct Acc {
+    static constexpr int W = DT == AR_BFLOAT16 ? 8 : 4;
+    float f[W];
+    int32_t i[4];
+};
+
+template <int DT>
+__device__ __forceinline__ void acc_widen(Acc<DT>& x, uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (DT == AR_INT32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x.i[q] = static_cast<int32_t>(w[q]);
+    } else if (DT == AR_FLOAT32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x.f[q] = __uint_as_float(w[q]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            x.f[2 * q] = bf_lo(w[q]);
+            x.f[2 * q + 1] = bf_hi(w[q]);
+        }
+    }
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ void acc_combine(Acc<DT>& x, const Acc<DT>& y) {
+    if (DT == AR_INT32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x.i[q] = iop<OP>(x.i[q], y.i[q]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < Acc<DT>::W; ++q) x.f[q] = fop<OP>(x.f[q], y.f[q]);
+    }
+}
+
+// AR_AVG on the fp32 accumulator, before the one rounding to the dtype
+template <int DT>
+__device__ __forceinline__ void acc_div(Acc<DT>& x, float d) {
+    if (DT != AR_INT32) {
+#pragma unroll
+        for (int q = 0; q < Acc<DT>::W; ++q) x.f[q] = __fdiv_rn(x.f[q], d);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 acc_narrow(const Acc<DT>& x) {
+    if (DT == AR_INT32)
+        return make_uint4(static_cast<uint32_t>(x.i[0]), static_cast<uint32_t>(x.i[1]),
+                          static_cast<uint32_t>(x.i[2]), static_cast<uint32_t>(x.i[3]));
+    if (DT == AR_FLOAT32)
+        return make_uint4(__float_as_uint(x.f[0]), __float_as_uint(x.f[1]), __float_as_uint(x.f[2]),
+                          __float_as_uint(x.f[3]));
+    return make_uint4(pack_bf16x2(x.f[0], x.f[1]), pack_bf16x2(x.f[2], x.f[3]), pack_bf16x2(x.f[4], x.f[5]),
+                      pack_bf16x2(x.f[6], x.f[7]));
+}
+
+// FP32ACC order over inputs 0..n-1 (the kernels' own fixed order, identical
+// in every kernel and for every rank): blocks of 8 consecutive inputs are
+// each folded left to right, then the block results are folded left to
+// right; fp32 / bf16 accumulate in fp32 and round once at the end (an AR_AVG
+// sum divided by div first; div = 0 for the other ops).  Inputs are fed one
+// at a time, so the order can be followed while inputs stream in.
+template <int DT, int OP>
+struct AccStream {
+    Acc<DT> acc, blk;
+    __device__ __forceinline__ void feed(uint32_t i, uint4 x) {
+        Acc<DT> w;
+        acc_widen<DT>(w, x);
+        if ((i & 7u) == 0)
+            blk = w;
+        else
+            acc_combine<DT, OP>(blk, w);
+        if ((i & 7u) == 7u) {
+            if (i == 7u)
+                acc = blk;
+            else
+                acc_combine<DT, OP>(acc, blk);
+        }
+    }
+    __device__ __forceinline__ uint4 finish(uint32_t n, float div) {
+        if (n & 7u) {
+            if (n < 8u)
+                acc = blk;
+            else
+                acc_combine<DT, OP>(acc, blk);
+        }
+        if (div != 0.f) acc_div<DT>(acc, div);
+        return acc_narrow<DT>(acc);
+    }
+};
+
+template <int DT, int OP, class Load>
+__device__ __forceinline__ uint4 acc_reduce(uint32_t n, float div, Load load) {
+    AccStream<DT, OP> s;
+    for (uint32_t i = 0; i < n; ++i) s.feed(i, load(i));
+    return s.finish(n, div);
+}
+
+// The divisor of a program's AR_AVG results, 0 when it stores plain results.
+__device__ __forceinline__ float avg_div(const KernelArgs& a, const DevProg& pg) {
+    return (pg.flags & PF_AVG) ? static_cast<float>(a.P) : 0.f;
+}
+
+// ------------------------------------------------------------- memory access
+
+__device__ __forceinline__ char* buf_addr(const KernelArgs& a, uint32_t id) {
+    const uint32_t slot = id >> 6, rank = id & 63u;
+    if (slot == 0) return static_cast<char*>(a.bufs[rank]);
+    return a.scratch + (static_cast<uint64_t>(slot - 1) * a.P + rank) * a.slot_stride;
+}
+
+__device__ __forceinline__ char* out_addr(const KernelArgs& a, const DevProg& pg, uint32_t o) {
+    if (pg.flags & PF_OUT_ALL) return static_cast<char*>(a.bufs[o]);
+    return buf_addr(a, a.refs[pg.out_off + o]);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+#ifndef AR_STORE_CS
+#define AR_STORE_CS 1
+#endif
+
+// results are never re-read by the kernel: streaming (evict-first) stores
+__device__ __forceinline__ void stg128(char* p, uint4 v) {
+    if (AR_STORE_CS)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                     "r"(v.w)
+                     : "memory");
+    else
+        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                     "r"(v.w)
+                     : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of the given parity; false after kWaitNs.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitNs) return false;
+    }
+}
+
+// loads are read once: ask L2 to evict them first
+#ifndef AR_L2_EVICT_FIRST
+#define AR_L2_EVICT_FIRST 1
+#endif
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    if (AR_L2_EVICT_FIRST) {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+            "%4;" ::"r"(dst),
+            "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+            "l"(src), "r"(bytes), "r"(bar)
+            : "memory");
+    }
+}
+
+// ------------------------------------------------------------ staged kernel
+
+struct Stage {
+    uint32_t full, empty;  // mbarrier arrays (shared addresses)
+    uint32_t ready;        // rank-streaming kernel: per stage, an item's result is in it
+    uint32_t tiles;        // stage 0 tiles
+    uint32_t tmps;         // temporaries
+    uint32_t stage_bytes;
+};
+
+template <int ES>
+__device__ void produce(const KernelArgs& a, const Stage& sm) {
+    const uint64_t policy = AR_L2_EVICT_FIRST ? evict_first_policy() : 0;
+    uint32_t k = 0;
+    bool ok = true;
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x, ++k) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        const uint32_t s = k % a.stages, ph = (k / a.stages) & 1u;
+        if (!mbar_wait(sm.empty + 8 * s, ph ^ 1u)) {
+            atomicOr(a.status, kStatusWaitEmpty);
+            ok = false;
+            break;
+        }
+        const uint32_t nb = w.count * ES;
+        const uint32_t bar = sm.full + 8 * s;
+        mbar_expect_tx(bar, nb * pg.n_in);
+        const uint32_t dst = sm.tiles + s * sm.stage_bytes;
+        for (uint32_t i = 0; i < pg.n_in; ++i) {
+            const char* src = buf_addr(a, a.refs[pg.in_off + i]) + w.elem * ES;
+            bulk_load(dst + i * a.tile_bytes, src, nb, bar, policy);
+        }
+    }
+    if (!ok) {
+        // let the copies already issued land before the CTA can exit
+        const uint32_t first = k > static_cast<uint32_t>(a.stages) ? k - a.stages : 0;
+        for (uint32_t j = first; j < k; ++j)
+            if (!mbar_wait(sm.full + 8 * (j % a.stages), (j / a.stages) & 1u)) atomicOr(a.status, kStatusDrain);
+    }
+}
+
+template <int DT, int OP, bool RIGHT>
+__device__ __forceinline__ void chain_item(const KernelArgs& a, const DevProg& pg, uint32_t st, uint32_t nvec,
+                                           int64_t off, int ct) {
+    uint4 acc[kVpt];
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) {
+        const uint32_t v = ct + j * kConsumers;
+        if (v < nvec) acc[j] = lds128(st + v * 16);
+    }
+    for (uint32_t i = 1; i < pg.n_in; ++i) {
+        const uint32_t t = st + i * a.tile_bytes;
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            const uint32_t v = ct + j * kConsumers;
+            if (v < nvec) {
+                const uint4 x = lds128(t + v * 16);
+                acc[j] = RIGHT ? vop<DT, OP>(x, acc[j]) : vop<DT, OP>(acc[j], x);
+            }
+        }
+    }
+    if (pg.flags & PF_AVG) {
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) acc[j] = vdiv<DT>(acc[j], static_cast<float>(a.P));
+    }
+    for (uint32_t o = 0; o < pg.n_out; ++o) {
+        char* dst = buf_addr(a, a.refs[pg.out_off + o]) + off;
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            const uint32_t v = ct + j * kConsumers;
+            if (v < nvec) stg128(dst + v * 16, acc[j]);
+        }
+    }
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ void acc_item(const KernelArgs& a, const DevProg& pg, uint32_t st, uint32_t nvec,
+                                         int64_t off, int ct) {
+    for (uint32_t v = ct; v < nvec; v += kConsumers) {
+        const uint4 r = acc_reduce<DT, OP>(pg.n_in, avg_div(a, pg),
+                                           [&](uint32_t i) { return lds128(st + i * a.tile_bytes + v * 16); });
+        for (uint32_t o = 0; o < pg.n_out; ++o) stg128(buf_addr(a, a.refs[pg.out_off + o]) + off + v * 16, r);
+    }
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ void dag_item(const KernelArgs& a, const DevProg& pg, uint32_t st, uint32_t tmps,
+                                         uint32_t nvec, int64_t off, int ct) {
+    uint4 acc[kVpt];
+    auto ref = [&](uint32_t r) { return (r & REF_TMP) ? tmps + (r & 0x1FFu) * a.tile_bytes : st + r * a.tile_bytes; };
+    for (uint32_t q = 0; q < pg.n_ins; ++q) {
+        const uint32_t w = a.ins[pg.ins_off + q];
+        if ((w >> 30) == INS_OP) {
+            const uint32_t ra = w & 0x3FFu, rb = (w >> 10) & 0x3FFu, rd = (w >> 20) & 0x3FFu;
+            const uint32_t pa = ref(ra), pb = ref(rb), pd = ref(rd);
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                const uint32_t v = ct + j * kConsumers;
+                if (v < nvec) {
+                    const uint4 x = ra == REF_ACC ? acc[j] : lds128(pa + v * 16);
+                    const uint4 y = rb == REF_ACC ? acc[j] : lds128(pb + v * 16);
+                    const uint4 r = vop<DT, OP>(x, y);
+                    if (rd == REF_ACC)
+                        acc[j] = r;
+                    else
+                        sts128(pd + v * 16, r);
+                }
+            }
+        } else {
+            const uint32_t rv = w & 0x3FFu, id = (w >> 10) & 0xFFFFu;
+            const uint32_t pv = ref(rv);
+            const bool avg = (w >> 30) == INS_STORE_AVG;
+            char* dst = buf_addr(a, id) + off;
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                const uint32_t v = ct + j * kConsumers;
+                if (v < nvec) {
+                    const uint4 x = rv == REF_ACC ? acc[j] : lds128(pv + v * 16);
+                    stg128(dst + v * 16, avg ? vdiv<DT>(x, static_cast<float>(a.P)) : x);
+                }
+            }
+        }
+    }
+}
+
+// Dag: how the launch evaluates DAG programs, called as
+// dag(pg, prog_index, stage_tiles, nvec, byte_offset, consumer_thread).
+template <int DT, int OP, class Dag>
+__device__ void consume(const KernelArgs& a, const Stage& sm, int ct, Dag dag) {
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    const int lane = ct & 31;
+    uint32_t k = 0;
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x, ++k) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        const uint32_t s = k % a.stages, ph = (k / a.stages) & 1u;
+        if (!mbar_wait(sm.full + 8 * s, ph)) {
+            atomicOr(a.status, kStatusWaitFull);
+            return;
+        }
+        const uint32_t st = sm.tiles + s * sm.stage_bytes;
+        const uint32_t nvec = (w.count * ES) >> 4;
+        const int64_t off = w.elem * ES;
+        if (pg.kind == PK_CHAIN_R)
+            chain_item<DT, OP, true>(a, pg, st, nvec, off, ct);
+        else if (pg.kind == PK_CHAIN_L)
+            chain_item<DT, OP, false>(a, pg, st, nvec, off, ct);
+        else if (pg.kind == PK_ACC)
+            acc_item<DT, OP>(a, pg, st, nvec, off, ct);
+        else if (pg.kind == PK_TREE)
+            atomicOr(a.status, kStatusBadProgram);  // trees run on the rank-streaming kernel
+        else
+            dag(pg, w.prog, st, nvec, off, ct);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty + 8 * s);
+    }
+}
+
+// The staged kernel: barrier setup, one producer thread, eight consumer
+// warps.  smem is the dynamic shared memory; dag evaluates DAG programs.
+template <int DT, int OP, class Dag>
+__device__ __forceinline__ void staged_body(const KernelArgs& a, uint8_t* smem, Dag dag) {
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    Stage sm;
+    sm.full = smem_addr(smem);
+    sm.empty = sm.full + 8 * a.stages;
+    sm.tiles = sm.full + kBarrierBytes;
+    sm.stage_bytes = static_cast<uint32_t>(a.tile_bytes) * a.max_in;
+    sm.tmps = sm.tiles + a.stages * sm.stage_bytes;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(sm.full + 8 * s, 1);
+            mbar_init(sm.empty + 8 * s, kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) produce<ES>(a, sm);
+        return;
+    }
+    consume<DT, OP>(a, sm, threadIdx.x - 32, [&](const DevProg& pg, uint32_t prog, uint32_t st, uint32_t nvec,
+                                                  int64_t off, int ct) { dag(sm, pg, prog, st, nvec, off, ct); });
+}
+
+}  // namespace
+}  // namespace ar

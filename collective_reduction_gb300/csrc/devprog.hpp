@@ -7,7 +7,7 @@
 //   ACC      fp32 accumulation of all inputs in the kernel's fixed order
 //   TREE     one tree evaluated in post-order on a stack: push in[i], then
 //            c_i times replace the two top entries a, b by a (+) b, where c_i
-//            is bits 2(i mod 16)..+1 of ins[i / 16]
+//            is bits 4(i mod 8)..+3 of ins[i / 8]
 // followed by storing acc (the tree: the last stack entry) to every output
 // buffer, or
 //   DAG      a straight-line list of instructions over inputs, temporaries
@@ -16,7 +16,9 @@
 // program may overwrite buffers it reads (the step form relies on this).
 #pragma once
 
+#if !defined(__CUDACC_RTC__)
 #include <cstdint>
+#endif
 
 #if defined(__CUDACC__)
 #define AR_HD __host__ __device__

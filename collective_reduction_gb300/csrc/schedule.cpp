@@ -508,6 +508,7 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
         pr.k1 = p->k1;
         pr.blocks = p->blocks == 0 ? 1 : p->blocks;
         pr.phase = p->phase;
+        pr.jit = p->jit;
         if (algo == AR_AHC) {
             if (p->n_groups < 1 || !p->group_sizes) return AR_ERR_INVALID_ARG;
             pr.group_sizes.assign(p->group_sizes, p->group_sizes + p->n_groups);
@@ -520,6 +521,7 @@ ar_status compile_schedule(int P, int64_t n, int dtype, int op, int algo, const 
     if (pr.group != AR_GROUP_CYCLIC && pr.group != AR_GROUP_XOR) return AR_ERR_INVALID_ARG;
     if (pr.form == AR_FORM_STEP && pr.order == AR_ORDER_FP32ACC) return AR_ERR_UNSUPPORTED;
     if (pr.phase < AR_PHASE_ALLREDUCE || pr.phase > AR_PHASE_ALL_GATHER) return AR_ERR_INVALID_ARG;
+    if (pr.jit < AR_JIT_OFF || pr.jit > AR_JIT_ON) return AR_ERR_INVALID_ARG;
     // the halves exist for the schedules that split into a reduce-scatter and
     // an all-gather: the ring, RH and the bandwidth-optimal generalized one
     if (pr.phase != AR_PHASE_ALLREDUCE) {

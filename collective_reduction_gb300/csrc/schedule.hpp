@@ -60,6 +60,7 @@ struct Params {
     std::vector<int> group_sizes;
     int blocks = 1;
     int phase = AR_PHASE_ALLREDUCE;
+    int jit = AR_JIT_AUTO;
 };
 
 struct Schedule {

@@ -33,8 +33,10 @@
 #ifndef AR_H
 #define AR_H
 
+#if !defined(__CUDACC_RTC__) /* the engine's run-time compiled kernels bring their own */
 #include <stddef.h>
 #include <stdint.h>
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -134,7 +136,17 @@ typedef struct {
     const int* group_sizes; /* AR_AHC: G sizes adding up to P (copied at create)  */
     int blocks;             /* AR_PIPELINE: blocks m, 1..4096 (0 means 1)         */
     int phase;              /* AR_PHASE_*; 0 = the whole allreduce               */
+    int jit;                /* DAG programs as run-time compiled code: AR_JIT_*  */
 } ar_params;
+
+/* ar_params.jit.  A plan whose staged launches evaluate DAG programs
+ * (rank-specific results, rounds with cyclic transfers) can run them as
+ * straight-line code compiled for the plan with NVRTC when the plan is
+ * created (bit-identical results; see ar_plan_info.kernels).  AUTO: when
+ * those launches move at least 16 MiB and the programs hold at most 4096
+ * instruction words; ON: whenever they fit that size; OFF: always
+ * interpret.  Without NVRTC on the system the plan interprets. */
+enum { AR_JIT_AUTO = 0, AR_JIT_ON = 1, AR_JIT_OFF = -1 };
 
 typedef struct {
     int P;
@@ -159,7 +171,7 @@ typedef struct {
 /* ar_plan_info.kernels bits: the rank-streaming kernel (chains, single trees,
  * fp32 accumulation), the staged kernel (DAG programs), the element-wise
  * kernel (unaligned edges and tiny passes). */
-enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4 };
+enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4, AR_KERNEL_DAG_JIT = 8 };
 
 typedef struct ar_schedule_s* ar_schedule_t;
 typedef struct ar_plan_s* ar_plan_t;
@@ -229,6 +241,13 @@ ar_status ar_cost_optimal_r(int P, uint64_t bytes_per_rank, const ar_cost_model*
  * as ar_schedule_create. */
 ar_status ar_cost_select(int P, uint64_t n, ar_dtype dtype, ar_op op, const ar_cost_model* model,
                          ar_algo* algo, ar_params* params, double* us);
+
+/* Host only: compiles, without a GPU, the run-time DAG kernel a plan with
+ * these parameters would use (params.jit ignored); *cubin_bytes receives the
+ * code size, 0 when the plan has no DAG program on the staged kernel.
+ * AR_ERR_UNSUPPORTED when NVRTC cannot be loaded, AR_ERR_CUDA when the
+ * compilation fails. */
+ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes);
 
 /* ---- plans (need a CUDA device) -------------------------------------------
  * ar_plan_create compiles the schedule, lowers it to tile programs for the

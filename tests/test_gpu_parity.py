@@ -489,3 +489,49 @@ def test_streamed_trees_many_items(algo, kw, dtype):
     else:
         for r in range(P):
             assert_bit_equal(got[r], res.bufs[r], dtype, f"{algo} {kw} rank {r}")
+
+
+# ---- run-time compiled DAG kernels --------------------------------------------------------
+
+JIT_CASES = [("generalized", 7, "sum", {"r": 1}), ("generalized", 7, "sum", {"r": 3}), ("rd", 8, "max", {}),
+             ("generalized", 12, "min", {"r": 2}), ("generalized", 7, "avg", {"r": 2}),
+             ("hybrid", 8, "max", {"k1": 1}), ("generalized", 7, "max", {"r": 3, "form": "step"}),
+             ("generalized", 12, "sum", {"r": 4, "form": "step"})]
+
+
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+@pytest.mark.parametrize("algo,P,op,kw", JIT_CASES)
+def test_dag_kernel_jit_bit_exact(algo, P, op, kw, dtype):
+    """DAG programs as run-time compiled straight-line code give the
+    interpreter's bits, which are the oracle's; the plan reports which path
+    it took."""
+    import torch
+
+    import collective_reduction_gb300 as ar
+    if op == "avg" and dtype == "int32":
+        pytest.skip("avg has no integer form")
+    n = 50021
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + len(kw))
+    okw = {k: v for k, v in kw.items() if k != "form"}
+    want = oracle.run(algo, bufs, Arith(op, dtype), **okw).bufs
+    for jit in ("on", "off"):
+        plan = ar.Plan(P, n, dtype, op, algo, jit=jit, **kw)
+        info = plan.info()
+        staged = bool(info["kernels"] & ar.KERNEL_STAGED)
+        assert bool(info["kernels"] & ar.KERNEL_DAG_JIT) == (staged and jit == "on"), (jit, info["kernels"])
+        dev = [to_dev(b, dtype) for b in bufs]
+        plan.execute(dev)
+        torch.cuda.synchronize()
+        plan.check()
+        for r in range(P):
+            assert_bit_equal(to_host(dev[r], dtype), want[r], dtype, f"{algo} {kw} jit={jit} rank {r}")
+        plan.close()
+
+
+def test_dag_kernel_jit_auto_threshold():
+    import collective_reduction_gb300 as ar
+    small = ar.Plan(7, 7 * 1024, "float32", "sum", "generalized", r=3).info()["kernels"]
+    large = ar.Plan(7, 1 << 22, "float32", "sum", "generalized", r=3).info()["kernels"]
+    assert small & ar.KERNEL_STAGED and not small & ar.KERNEL_DAG_JIT
+    assert large & ar.KERNEL_DAG_JIT

@@ -224,3 +224,40 @@ def test_avg_requests(lib):
         s = ar.Schedule(7, 40, "float32", "sum", algo, **kw).info()
         for k in ("steps", "combines", "sent_bytes_max", "sent_bytes_total", "n_segments"):
             assert a[k] == s[k], (algo, k)
+
+
+@pytest.mark.parametrize("algo,P,op,kw", [
+    ("generalized", 7, "sum", {"r": 1}), ("generalized", 7, "sum", {"r": 3}), ("rd", 8, "max", {}),
+    ("generalized", 12, "min", {"r": 2}), ("generalized", 7, "avg", {"r": 2}),
+    ("generalized", 7, "sum", {"r": 3, "form": "step"}),
+])
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+def test_dag_kernel_compiles_on_the_host(lib, algo, P, op, kw, dtype):
+    """The run-time DAG kernel of a plan with rank-specific programs compiles
+    for sm_103a (NVRTC, no GPU needed)."""
+    if op == "avg" and dtype == "int32":
+        pytest.skip("avg has no integer form")
+    s = ar.Schedule(P, P * 4096, dtype, op, algo, **kw)
+    try:
+        nbytes = s.dag_kernel_bytes()
+    except ar.ArError as e:
+        if e.name == "AR_ERR_UNSUPPORTED":
+            pytest.skip("NVRTC is not available on this host")
+        raise
+    if dtype == "int32" and algo == "rd":
+        assert nbytes == 0  # every int32 op commutes: one shared tree, no DAG program
+    else:
+        assert nbytes > 0
+
+
+def test_no_dag_kernel_for_streaming_plans(lib):
+    for algo, kw in (("ring", {}), ("rh", {}), ("binomial", {}), ("generalized", {"r": 2})):
+        # sum trees are shared by every rank: no DAG program, nothing to compile
+        assert ar.Schedule(8, 8 * 4096, "float32", "sum", algo, **kw).dag_kernel_bytes() == 0
+
+
+def test_jit_parameter_checked(lib):
+    p, _keep = ar._params()
+    p.jit = 2
+    h = ctypes.c_void_p()
+    assert lib.ar_schedule_create(8, 64, 1, 0, 0, ctypes.byref(p), ctypes.byref(h)) == 1
