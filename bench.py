@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--order", default="faithful")
     ap.add_argument("--r", type=int, default=0)
     ap.add_argument("--k1", type=int, default=0)
+    ap.add_argument("--jit", default="auto", choices=["auto", "on", "off"],
+                    help="DAG programs as run-time compiled code (auto / on) or interpreted (off)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", default=None, help="write the size sweep as JSON lines to this file")
@@ -302,7 +304,7 @@ def run_ours(a):
     es = esize(a.dtype)
     n = int(a.mib * (1 << 20)) // es
     S = n * es
-    params = dict(form=a.form, order=a.order)
+    params = dict(form=a.form, order=a.order, jit=a.jit)
     if a.algo == "generalized":
         params["r"] = a.r
     if a.algo == "hybrid":
@@ -403,7 +405,8 @@ def run_ours(a):
                      "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": alg_bytes,
                      "kernel_ms": round(kernel_ms, 6),
-                     "kernel": "stream_kernel" if info["kernels"] & 1 else "staged_kernel"},
+                     "kernel": ("stream_kernel" if info["kernels"] & 1
+                                else "ar_dag_kernel" if info["kernels"] & 8 else "staged_kernel")},
         "cpu_baseline": cpu,
         "e2e": {"value": round(whole_job_gbps(bytes_per_call, 1, world, e2e_s * 1e3), 3), "unit": "GB/s",
                 "h2d_bytes_per_step": bytes_per_call, "d2h_bytes_per_step": bytes_per_call},
