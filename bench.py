@@ -38,7 +38,7 @@ NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "allreduced bytes/s (P x S per call)"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
-KERNEL_SRC = os.path.join(ROOT, "collective_reduction_gb300", "csrc", "kernels.cu")
+KERNEL_SRC = [os.path.join(ROOT, "collective_reduction_gb300", "csrc", f) for f in ("kernels.cu", "device.cuh")]
 
 
 def parse():
@@ -100,8 +100,10 @@ def kernel_hash():
     recorded ncu traffic figure stays valid across comment-only edits and is
     dropped as soon as the code changes."""
     import re
-    with open(KERNEL_SRC) as f:
-        src = f.read()
+    src = ""
+    for path in KERNEL_SRC:
+        with open(path) as f:
+            src += f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     lines = [ln.split("//", 1)[0].rstrip() for ln in src.splitlines()]
     code = "\n".join(ln for ln in lines if ln.strip())

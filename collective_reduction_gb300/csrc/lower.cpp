@@ -17,9 +17,15 @@
 #include <map>
 #include <stdexcept>
 
+// Most outputs per item for which the rank-streaming kernel stores results
+// with TMA bulk copies from shared memory (more: 128-bit stores).
+#ifndef AR_TMA_STORE_MAX_OUT
+#define AR_TMA_STORE_MAX_OUT 4
+#endif
+
 // Deepest tree stack (tiles below the top) streamed with 32 KB rank tiles.
 #ifndef AR_TREE_WIDE_SLOTS
-#define AR_TREE_WIDE_SLOTS 3
+#define AR_TREE_WIDE_SLOTS 4
 #endif
 
 namespace ar {
@@ -526,7 +532,8 @@ void lower(const Schedule& S, Lowered& lw) {
     // bf16 fp32 accumulation holds 16 fp32 per vector: 16 KB rank tiles (4
     // vectors per thread).  A tree keeps depth - 1 stack tiles in shared
     // memory next to the stages: 32 KB tiles while that leaves a pipeline of
-    // several stages, 16 KB tiles for deeper trees.
+    // at least 3 stages (trees of up to 16 leaves; measured +6% at P = 16 over
+    // 16 KB tiles), 16 KB tiles for deeper trees.
     const bool narrow = (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC) ||
                         (stream_trees && lw.stream_slots > AR_TREE_WIDE_SLOTS);
     lw.stream_trees = stream_trees;
@@ -534,14 +541,22 @@ void lower(const Schedule& S, Lowered& lw) {
     lw.stream_stages =
         std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile - lw.stream_slots);
     // The TMA-store epilogue holds an item's last stage until its outputs are
-    // copied out: measured faster with few outputs per item (and for bf16
-    // fp32 accumulation, whose direct stores are costly), slower with many.
-    int max_out = 0;
+    // copied out.  Measured at the bench size: it wins for copies (one input,
+    // many outputs: the all-gather, +4-5%), for bf16 with few outputs and for
+    // few inputs and outputs (P = 2, +5%), and for bf16 fp32 accumulation,
+    // whose direct stores are costly; 128-bit stores from registers win with
+    // many outputs (allreduce at P >= 8, up to +5%) and for fp32 passes with
+    // many inputs per output (the reduce-scatter, +2-3%).
+    int max_out = 0, max_in_stream = 0;
     for (size_t k = 0; k < sets.size(); ++k)
         if (stream[k])
-            for (auto& r : sets[k]) max_out = std::max<int>(max_out, lw.progs[r.prog].n_out);
-    lw.stream_tma_store =
-        max_out <= 4 || (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC);
+            for (auto& r : sets[k]) {
+                max_out = std::max<int>(max_out, lw.progs[r.prog].n_out);
+                max_in_stream = std::max<int>(max_in_stream, lw.progs[r.prog].n_in);
+            }
+    const bool few_out = max_out <= AR_TMA_STORE_MAX_OUT;
+    lw.stream_tma_store = max_in_stream <= 1 || (few_out && (S.dtype == AR_BFLOAT16 || max_in_stream <= 4)) ||
+                          (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC);
     for (size_t k = 0; k < sets.size(); ++k) {
         LaunchSet ls;
         ls.stream = stream[k];
