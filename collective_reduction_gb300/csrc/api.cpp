@@ -175,9 +175,7 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
             a.max_in = plan->L.max_in;
             a.max_tmp = plan->L.max_tmp;
             if (plan->dag_fn) {
-                void* args[] = {&a};
-                e = cudaLaunchKernel(plan->dag_fn, dim3(grid), dim3(ar::kStagedThreads), args,
-                                     static_cast<size_t>(plan->smem_staged), st);
+                e = ar::launch_dependent(plan->dag_fn, grid, ar::kStagedThreads, plan->smem_staged, st, a);
             } else {
                 e = ar::launch_staged(S.dtype, S.op, a, grid, plan->smem_staged, st);
             }

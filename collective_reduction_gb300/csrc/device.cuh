@@ -6,6 +6,12 @@
 
 #include "kargs.hpp"
 
+// Launch kernels as programmatic dependents of their predecessor (1) or
+// plainly stream-ordered (0); the host side reads the same macro.
+#ifndef AR_PDL
+#define AR_PDL 1
+#endif
+
 namespace ar {
 namespace {
 
@@ -232,6 +238,28 @@ __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// ------------------------------------------------------ dependent launches
+//
+// The engine launches its kernels with programmatic stream serialization: a
+// launch that follows another kernel in the stream may start (CTA launch,
+// barrier setup) while that kernel finishes.  A kernel touches global memory
+// only after griddep_wait, which returns once the preceding grid has
+// completed and its writes are visible (at once when there is none), and
+// lets its successor start early with griddep_launch_dependents, which takes
+// effect only when every CTA of the grid has issued it (so all of them are
+// resident) or exited.
+__device__ __forceinline__ void griddep_wait() {
+#if AR_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+#if AR_PDL
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -475,6 +503,8 @@ __device__ __forceinline__ void staged_body(const KernelArgs& a, uint8_t* smem, 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) produce<ES>(a, sm);
         return;

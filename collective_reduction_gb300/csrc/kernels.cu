@@ -369,6 +369,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5;
     if (warp == 0) {
         stream_produce<ES>(a, sm);
@@ -416,6 +418,8 @@ template <int DT, int OP>
 __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ uint32_t vals[];  // [(max_in + max_tmp) rows][kElemThreads]
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    griddep_wait();
+    griddep_launch_dependents();
     const WorkItem w = a.items[blockIdx.x];
     const DevProg pg = a.progs[w.prog];
     const int t = threadIdx.x;
@@ -526,6 +530,21 @@ KernelFn kernel_for(int dtype, int op, int which) {
 
 }  // namespace
 
+cudaError_t launch_dependent(const void* f, int grid, int block, int smem, cudaStream_t st, const KernelArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = AR_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {const_cast<KernelArgs*>(&a)};
+    return cudaLaunchKernelExC(&cfg, f, args);
+}
+
 cudaError_t prepare_kernels(int dtype, int op) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -543,8 +562,7 @@ cudaError_t prepare_kernels(int dtype, int op) {
 
 cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
     KernelFn f = kernel_for(dtype, op, K_STAGED);
-    f<<<grid, kStagedThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(reinterpret_cast<const void*>(f), grid, kStagedThreads, smem, st, a);
 }
 
 cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
@@ -559,14 +577,12 @@ cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int 
     if (which < 0) return cudaErrorInvalidValue;
     if (a.stages < 1 || a.stages > 32 || 24 * a.stages > kBarrierBytes) return cudaErrorInvalidValue;
     KernelFn f = kernel_for(dtype, op, which);
-    f<<<grid, kStreamThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(reinterpret_cast<const void*>(f), grid, kStreamThreads, smem, st, a);
 }
 
 cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem, cudaStream_t st) {
     KernelFn f = kernel_for(dtype, op, K_ELEM);
-    f<<<a.n_items, kElemThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(reinterpret_cast<const void*>(f), static_cast<int>(a.n_items), kElemThreads, smem, st, a);
 }
 
 }  // namespace ar

@@ -138,5 +138,5 @@ def test_eq36_extra_terms_against_the_compiled_schedules(lib, P):
 def test_default_model_is_positive(lib):
     m = ar.cost_model()
     assert m.alpha_us > 0 and m.beta_us_per_byte > 0 and m.gamma_us_per_byte >= 0
-    # the fitted GB300 values: about 5 us per round, about 3 TB/s per byte sent over all ranks
+    # the fitted GB300 values: a few us per round, about 3 TB/s per byte sent over all ranks
     assert 1.0 < m.alpha_us < 20.0 and 1e-7 < m.beta_us_per_byte < 1e-6
