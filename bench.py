@@ -468,15 +468,51 @@ def run_reference(a):
 
 # ------------------------------------------------------------------- sweep
 
+def sweep_check(ar, oracle_mods, plan, dev, P, n, dtype, order):
+    """Runs the plan once on dev and checks the result against the oracle:
+    every element when P x n <= 2^24, else 2^12 elements sampled from each of
+    the P chunks (bit for bit; fp32-accumulated within tolerance)."""
+    import numpy as np
+    import torch
+    oracle, Arith, direct_f64, normwise_rel_err, bf16_to_f32 = oracle_mods
+    full = P * n <= (1 << 24)
+    K = n // P if full else min(1 << 12, n // P)
+    if full:
+        idx = None
+        sample_in = [t.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bfloat16" else t.cpu().numpy()
+                     for t in dev]
+    else:
+        sample_in, idx = gather_sample(dev, P, n, K, P)
+    plan.execute(dev)
+    plan.check()
+    got = [t if idx is None else t.index_select(0, idx) for t in dev]
+    got = [g.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bfloat16" else g.cpu().numpy() for g in got]
+    if order == "fp32acc":
+        ref = direct_f64(sample_in, "sum", dtype)
+        err = max(normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) for g in got)
+        return bool(err <= (1e-6 if dtype == "float32" else 4e-3)), full
+    want = oracle.run("ring", sample_in, Arith("sum", dtype)).bufs
+
+    def bits(x):
+        x = np.ascontiguousarray(x)
+        return x if x.dtype == np.uint16 else x.view(np.uint32)
+    return all(np.array_equal(bits(g), bits(w)) for g, w in zip(got, want)), full
+
+
 def run_sweep(a, path):
     """Configuration 5: ring fused (faithful, fp32acc) and ring step form over
     P in {2, 8, 16, 64} and 1 KiB .. 256 MiB per rank, fp32 and bf16; one
-    JSON line per point.  Points up to 64 KiB are timed as a CUDA graph of
-    100 calls."""
+    JSON line per point.  Every point is first checked against the oracle
+    (sweep_check).  Points up to 64 KiB are timed as a CUDA graph of 100
+    calls."""
     import torch
 
     import ar_synth
     import collective_reduction_gb300 as ar
+    import oracle
+    from oracle.direct import direct_f64, normwise_rel_err
+    from oracle.elementops import Arith, bf16_to_f32
+    oracle_mods = (oracle, Arith, direct_f64, normwise_rel_err, bf16_to_f32)
     torch.cuda.set_device(0)
     free = torch.cuda.mem_get_info()[0]
     peak, _ = measured_peak()
@@ -494,6 +530,9 @@ def run_sweep(a, path):
                             continue
                         plan = ar.Plan(P, n, dtype, "sum", "ring", form=form, order=order)
                         info = plan.info()
+                        fresh = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P + 1)
+                        ok, full = sweep_check(ar, oracle_mods, plan, fresh, P, n, dtype, order)
+                        del fresh
                         for _ in range(3):
                             plan.execute(dev)
                         torch.cuda.synchronize()
@@ -533,7 +572,8 @@ def run_sweep(a, path):
                                "busbw_GBps": S / (ms / 1e3) * 2 * (P - 1) / P / 1e9,
                                "hbm_GBps": info["hbm_bytes"] / (ms / 1e3) / 1e9,
                                "frac_of_measured": info["hbm_bytes"] / (ms / 1e3) / 1e9 / peak,
-                               "launches": info["launches"]}
+                               "launches": info["launches"], "verified": ok,
+                               "checked": "every element" if full else "2^12 sampled elements per chunk"}
                         out.write(json.dumps(row) + "\n")
                         out.flush()
                         plan.close()
