@@ -47,6 +47,7 @@ constexpr int kBarrierBytes = 512;   // mbarrier area at the start of a kernel's
 // staged / rank-streaming kernels, 16-byte vectors each consumer thread takes
 // per item tile (staged: up to kStagedVpt) or per rank tile (streaming).
 constexpr int kConsumerWarps = 8;
+constexpr int kElemBlock = 64;       // element-wise kernel: threads = elements per block
 constexpr int kStagedVpt = 4;
 constexpr int kStreamVpt = 8;        // rank-streaming kernel, chains and fp32 / int32 accumulation
 constexpr int kStreamVptNarrow = 4;  // rank-streaming kernel, bf16 fp32 accumulation (16 fp32 per vector)

@@ -44,6 +44,6 @@ constexpr int kStatusDrain = 4;      // a failing producer gave up draining its 
 constexpr int kStatusBadProgram = 8; // a program kind the launched kernel does not run
 
 constexpr int kStagedThreads = 32 * (1 + kConsumerWarps);
-constexpr int kElemThreads = 64;
+constexpr int kElemThreads = kElemBlock;
 
 }  // namespace ar

@@ -426,70 +426,93 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
     auto row = [&](uint32_t r) -> uint32_t& {
         return (r & REF_TMP) ? vals[(a.max_in + (r & 0x1FFu)) * kElemThreads + t] : vals[r * kElemThreads + t];
     };
-    for (uint32_t e = t; e < w.count; e += kElemThreads) {
-        const int64_t off = (w.elem + e) * ES;
-        // eight independent loads in flight per thread (a program can have
-        // hundreds of inputs; one load at a time would be latency-bound)
-        uint32_t i = 0;
-        for (; i + 8 <= pg.n_in; i += 8) {
-            uint32_t v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = ld_elem<DT>(buf_addr(a, a.refs[pg.in_off + i + q]) + off);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) vals[(i + q) * kElemThreads + t] = v[q];
+    if (pg.kind == PK_TREE) {
+        // a tree deeper than the stack (never emitted by the lowering) is
+        // refused by every thread alike, before any barrier
+        int sp = 0;
+        for (uint32_t i = 0; i < pg.n_in; ++i) {
+            if (++sp > kTreeDepth) {
+                if (t == 0) atomicOr(a.status, kStatusBadProgram);
+                return;
+            }
+            sp -= min(static_cast<int>((a.ins[pg.ins_off + (i >> 3)] >> (4 * (i & 7))) & 15u), sp - 1);
         }
-        for (; i < pg.n_in; ++i) vals[i * kElemThreads + t] = ld_elem<DT>(buf_addr(a, a.refs[pg.in_off + i]) + off);
-        if (pg.kind == PK_CHAIN_R || pg.kind == PK_CHAIN_L) {
-            uint32_t acc = vals[t];
-            for (uint32_t i = 1; i < pg.n_in; ++i) {
-                const uint32_t x = vals[i * kElemThreads + t];
-                acc = pg.kind == PK_CHAIN_R ? eop<DT, OP>(x, acc) : eop<DT, OP>(acc, x);
+    }
+    // Blocks of up to 64 elements.  All threads load a block's inputs
+    // together (value q is input q / cnt of element q % cnt, so a tiny item
+    // with many inputs still has every thread loading), then each thread
+    // evaluates the program for its element.
+    for (uint32_t base = 0; base < w.count; base += kElemThreads) {
+        const uint32_t cnt = min(static_cast<uint32_t>(kElemThreads), w.count - base);
+        const uint32_t total = cnt * pg.n_in;
+        uint32_t q = t;
+        for (; q + 3 * kElemThreads < total; q += 4 * kElemThreads) {
+            uint32_t v[4], slot[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t qq = q + k * kElemThreads, i = qq / cnt, e = qq - i * cnt;
+                v[k] = ld_elem<DT>(buf_addr(a, a.refs[pg.in_off + i]) + (w.elem + base + e) * ES);
+                slot[k] = i * kElemThreads + e;
             }
-            acc = ediv<DT>(acc, avg_div(a, pg));
-            for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, acc);
-        } else if (pg.kind == PK_TREE) {
-            // post-order on a small stack (local memory is fine on this path)
-            uint32_t stk[kTreeDepth];
-            int sp = 0;
-            for (uint32_t i = 0; i < pg.n_in; ++i) {
-                if (sp >= kTreeDepth) {  // the lowering never emits a deeper tree
-                    atomicOr(a.status, kStatusBadProgram);
-                    return;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) vals[slot[k]] = v[k];
+        }
+        for (; q < total; q += kElemThreads) {
+            const uint32_t i = q / cnt, e = q - i * cnt;
+            vals[i * kElemThreads + e] = ld_elem<DT>(buf_addr(a, a.refs[pg.in_off + i]) + (w.elem + base + e) * ES);
+        }
+        __syncthreads();
+        if (static_cast<uint32_t>(t) < cnt) {
+            const int64_t off = (w.elem + base + t) * ES;
+            if (pg.kind == PK_CHAIN_R || pg.kind == PK_CHAIN_L) {
+                uint32_t acc = vals[t];
+                for (uint32_t i = 1; i < pg.n_in; ++i) {
+                    const uint32_t x = vals[i * kElemThreads + t];
+                    acc = pg.kind == PK_CHAIN_R ? eop<DT, OP>(x, acc) : eop<DT, OP>(acc, x);
                 }
-                stk[sp++] = vals[i * kElemThreads + t];
-                for (uint32_t q = (a.ins[pg.ins_off + (i >> 3)] >> (4 * (i & 7))) & 15u; q > 0 && sp >= 2; --q, --sp)
-                    stk[sp - 2] = eop<DT, OP>(stk[sp - 2], stk[sp - 1]);
-            }
-            const uint32_t res = ediv<DT>(stk[0], avg_div(a, pg));
-            for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, res);
-        } else if (pg.kind == PK_ACC) {
-            // the same order as the other kernels: the element rides in lane 0
-            // of a vector (the other lanes carry zeros and are dropped)
-            const uint4 r = acc_reduce<DT, OP>(pg.n_in, avg_div(a, pg), [&](uint32_t i) {
-                return make_uint4(vals[i * kElemThreads + t], 0u, 0u, 0u);
-            });
-            const uint32_t v = DT == AR_BFLOAT16 ? (r.x & 0xFFFFu) : r.x;
-            for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, v);
-        } else {
-            uint32_t acc = 0;
-            for (uint32_t q = 0; q < pg.n_ins; ++q) {
-                const uint32_t wd = a.ins[pg.ins_off + q];
-                if ((wd >> 30) == INS_OP) {
-                    const uint32_t ra = wd & 0x3FFu, rb = (wd >> 10) & 0x3FFu, rd = (wd >> 20) & 0x3FFu;
-                    const uint32_t x = ra == REF_ACC ? acc : row(ra);
-                    const uint32_t y = rb == REF_ACC ? acc : row(rb);
-                    const uint32_t r = eop<DT, OP>(x, y);
-                    if (rd == REF_ACC)
-                        acc = r;
-                    else
-                        row(rd) = r;
-                } else {
-                    const uint32_t rv = wd & 0x3FFu, id = (wd >> 10) & 0xFFFFu;
-                    const float div = (wd >> 30) == INS_STORE_AVG ? static_cast<float>(a.P) : 0.f;
-                    st_elem<DT>(buf_addr(a, id) + off, ediv<DT>(rv == REF_ACC ? acc : row(rv), div));
+                acc = ediv<DT>(acc, avg_div(a, pg));
+                for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, acc);
+            } else if (pg.kind == PK_TREE) {
+                // post-order on a small stack (local memory is fine on this path)
+                uint32_t stk[kTreeDepth];
+                int sp = 0;
+                for (uint32_t i = 0; i < pg.n_in; ++i) {
+                    stk[sp++] = vals[i * kElemThreads + t];  // depth checked above
+                    for (uint32_t q = (a.ins[pg.ins_off + (i >> 3)] >> (4 * (i & 7))) & 15u; q > 0 && sp >= 2; --q, --sp)
+                        stk[sp - 2] = eop<DT, OP>(stk[sp - 2], stk[sp - 1]);
+                }
+                const uint32_t res = ediv<DT>(stk[0], avg_div(a, pg));
+                for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, res);
+            } else if (pg.kind == PK_ACC) {
+                // the same order as the other kernels: the element rides in lane 0
+                // of a vector (the other lanes carry zeros and are dropped)
+                const uint4 r = acc_reduce<DT, OP>(pg.n_in, avg_div(a, pg), [&](uint32_t i) {
+                    return make_uint4(vals[i * kElemThreads + t], 0u, 0u, 0u);
+                });
+                const uint32_t v = DT == AR_BFLOAT16 ? (r.x & 0xFFFFu) : r.x;
+                for (uint32_t o = 0; o < pg.n_out; ++o) st_elem<DT>(buf_addr(a, a.refs[pg.out_off + o]) + off, v);
+            } else {
+                uint32_t acc = 0;
+                for (uint32_t q = 0; q < pg.n_ins; ++q) {
+                    const uint32_t wd = a.ins[pg.ins_off + q];
+                    if ((wd >> 30) == INS_OP) {
+                        const uint32_t ra = wd & 0x3FFu, rb = (wd >> 10) & 0x3FFu, rd = (wd >> 20) & 0x3FFu;
+                        const uint32_t x = ra == REF_ACC ? acc : row(ra);
+                        const uint32_t y = rb == REF_ACC ? acc : row(rb);
+                        const uint32_t r = eop<DT, OP>(x, y);
+                        if (rd == REF_ACC)
+                            acc = r;
+                        else
+                            row(rd) = r;
+                    } else {
+                        const uint32_t rv = wd & 0x3FFu, id = (wd >> 10) & 0xFFFFu;
+                        const float div = (wd >> 30) == INS_STORE_AVG ? static_cast<float>(a.P) : 0.f;
+                        st_elem<DT>(buf_addr(a, id) + off, ediv<DT>(rv == REF_ACC ? acc : row(rv), div));
+                    }
                 }
             }
         }
+        __syncthreads();  // the block's values are read before the next block's loads
     }
 }
 

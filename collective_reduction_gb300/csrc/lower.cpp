@@ -431,6 +431,37 @@ struct Range {
     int64_t lo, hi;
 };
 
+// Elements per work item of a set: a whole tile, unless the set is one range
+// (one program over every element: the fp32-accumulate pass) whose whole
+// tiles leave fewer items than half the GPU's 152 SMs — then about one item
+// per SM, at least 1 KB per rank tile (a multiple of V elements, so items
+// stay 16-byte aligned).  Measured: P = 64 x 256 KiB fp32 accumulation went
+// from 95 us (8 items) to 24 us; splitting the ring's per-chunk ranges the
+// same way made it slower (smaller rank tiles of many more items).
+constexpr int64_t kFewItems = 152 / 2;
+constexpr int64_t kSpreadItems = 152;
+
+int64_t item_elems(const std::vector<Range>& rs, int64_t tile_elems, int64_t V) {
+    int64_t body = 0, items = 0;
+    for (const Range& r : rs) {
+        const int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
+        if (a < e) {
+            body += e - a;
+            items += (e - a + tile_elems - 1) / tile_elems;
+        }
+    }
+    if (body <= 0 || items >= kFewItems || rs.size() != 1) return tile_elems;
+    const int64_t want = (body + kSpreadItems - 1) / kSpreadItems;
+    return std::min(tile_elems, std::max(1024 / (16 / V), (want + V - 1) / V * V));
+}
+
+// Mean elements per range (segment) of a set.
+int64_t mean_range(const std::vector<Range>& rs) {
+    int64_t n = 0;
+    for (const Range& r : rs) n += r.hi - r.lo;
+    return rs.empty() ? 0 : n / static_cast<int64_t>(rs.size());
+}
+
 void push_range(std::vector<Range>& v, uint32_t prog, int64_t lo, int64_t hi) {
     if (hi <= lo) return;
     if (!v.empty() && v.back().prog == prog && v.back().hi == lo)
@@ -495,11 +526,28 @@ void lower(const Schedule& S, Lowered& lw) {
     for (size_t k = 0; k < sets.size(); ++k)
         for (auto& r : sets[k])
             if (lw.progs[r.prog].kind == PK_DAG) stream[k] = false;
+    // Small sets (<= 256 KB of traffic) run as one element-wise launch: every
+    // item's inputs load at once, where streaming P rank tiles one after the
+    // other would pay P memory latencies.  Sets of chains whose segments are
+    // under 4 KB per rank (tiny rank tiles) stage all of an item's tiles for
+    // the same reason.
+    std::vector<bool> small(sets.size(), false);
+    for (size_t k = 0; k < sets.size(); ++k) {
+        uint64_t bytes = 0;
+        bool trees = false;
+        for (auto& r : sets[k]) {
+            const DevProg& d = lw.progs[r.prog];
+            bytes += static_cast<uint64_t>(d.n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
+            trees |= d.kind == PK_TREE;
+        }
+        small[k] = !sets[k].empty() && bytes <= (256u << 10);
+        if (stream[k] && !small[k] && !trees && mean_range(sets[k]) * es < 4096) stream[k] = false;
+    }
     bool stream_trees = false;
     lw.stream_slots = 0;  // shared-memory tiles for the deepest tree stack
     for (size_t k = 0; k < sets.size(); ++k)
         for (auto& r : sets[k])
-            if (stream[k] && lw.progs[r.prog].kind == PK_TREE) {
+            if (stream[k] && !small[k] && lw.progs[r.prog].kind == PK_TREE) {
                 stream_trees = true;
                 lw.stream_slots = std::max<int>(lw.stream_slots, lw.progs[r.prog].n_tmp);
             }
@@ -512,7 +560,7 @@ void lower(const Schedule& S, Lowered& lw) {
             lw.max_in_all = std::max<int>(lw.max_in_all, d.n_in);
             lw.max_tmp_all = std::max<int>(lw.max_tmp_all, d.n_tmp);
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
-            if (a < e && !stream[k]) {
+            if (a < e && !stream[k] && !small[k]) {
                 lw.max_in = std::max<int>(lw.max_in, d.n_in);
                 lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
             }
@@ -560,7 +608,7 @@ void lower(const Schedule& S, Lowered& lw) {
     for (size_t k = 0; k < sets.size(); ++k) {
         LaunchSet ls;
         ls.stream = stream[k];
-        const int64_t tile_elems = (stream[k] ? lw.stream_tile : lw.tile_bytes) / es;
+        const int64_t tile_elems = item_elems(sets[k], (stream[k] ? lw.stream_tile : lw.tile_bytes) / es, V);
         for (auto& r : sets[k]) {
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
             if (a < e) {
@@ -571,14 +619,15 @@ void lower(const Schedule& S, Lowered& lw) {
             } else {
                 ls.edge.push_back({r.lo, static_cast<uint32_t>(r.hi - r.lo), r.prog});
             }
-            for (int64_t x = r.lo; x < r.hi; x += 4096)
-                ls.fallback.push_back({x, static_cast<uint32_t>(std::min<int64_t>(4096, r.hi - x)), r.prog});
+            // element-wise items: one block of the element kernel each for a
+            // small set (parallelism), 4096 elements otherwise
+            const int64_t fb = small[k] ? kElemBlock : 4096;
+            for (int64_t x = r.lo; x < r.hi; x += fb)
+                ls.fallback.push_back({x, static_cast<uint32_t>(std::min<int64_t>(fb, r.hi - x)), r.prog});
             const DevProg& d = lw.progs[r.prog];
             ls.bytes += static_cast<uint64_t>(d.n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
         }
-        // a tiny set that would need a staged launch and an edge launch runs
-        // as one element-wise launch instead (launch latency dominates there)
-        ls.small = !ls.bulk.empty() && !ls.edge.empty() && ls.bytes <= (256u << 10);
+        ls.small = small[k];
         lw.hbm_bytes += ls.bytes;
         lw.n_items += ls.small ? ls.fallback.size() : ls.bulk.size() + ls.edge.size();
         lw.launches += ls.small ? 1 : (!ls.bulk.empty()) + (!ls.edge.empty());

@@ -16,7 +16,7 @@ struct LaunchSet {
     std::vector<WorkItem> fallback;  // whole ranges for unaligned buffers
     uint64_t bytes = 0;              // algorithmic HBM bytes of the set
     bool stream = false;             // bulk items run on the rank-streaming kernel
-    bool small = false;              // tiny set with edges: one element-wise launch over fallback
+    bool small = false;              // small set (<= 256 KB): one element-wise launch over fallback
 };
 
 struct Lowered {
