@@ -535,3 +535,34 @@ def test_dag_kernel_jit_auto_threshold():
     large = ar.Plan(7, 1 << 22, "float32", "sum", "generalized", r=3).info()["kernels"]
     assert small & ar.KERNEL_STAGED and not small & ar.KERNEL_DAG_JIT
     assert large & ar.KERNEL_DAG_JIT
+
+
+@pytest.mark.parametrize("algo,kw", [("ring", {}), ("rh", {"form": "step"}), ("generalized", {"r": 3, "jit": "on"}),
+                                     ("ring", {"order": "fp32acc"})])
+def test_execute_captures_in_a_cuda_graph(algo, kw):
+    """ar_execute only enqueues kernels: it can be captured in a CUDA graph
+    whose replays give the same results as direct calls."""
+    import torch
+
+    import collective_reduction_gb300 as ar
+    P, n = 7, (1 << 18) + 13
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2, seed=23)
+    plan = ar.Plan(P, n, "float32", "sum", algo, **kw)
+    direct = [to_dev(b, "float32") for b in bufs]
+    plan.execute(direct)
+    torch.cuda.synchronize()
+    graphed = [to_dev(b, "float32") for b in bufs]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            plan.execute(graphed, stream=s)
+    torch.cuda.synchronize()
+    for d, b in zip(graphed, bufs):  # capture does not run the kernels: restore, replay once
+        d.copy_(to_dev(b, "float32"))
+    g.replay()
+    torch.cuda.synchronize()
+    plan.check()
+    for r in range(P):
+        assert_bit_equal(to_host(graphed[r], "float32"), to_host(direct[r], "float32"), "float32", f"rank {r}")
