@@ -366,9 +366,10 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
         if (e == cudaSuccess) e = cudaMalloc(&p->d_status, 256);
         if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, 256);
         const int es = ar::esize_of(dtype);
-        if (e == cudaSuccess && p->S.params.form == AR_FORM_STEP && p->S.max_slots > 1) {
+        if (e == cudaSuccess && p->S.params.form == AR_FORM_STEP && L.phys_slots > 1) {
+            // second partials and the twins of versioned rounds, per rank
             p->slot_stride = (static_cast<uint64_t>(n) * es + 255) / 256 * 256;
-            p->scratch_bytes = static_cast<uint64_t>(p->S.max_slots - 1) * P * p->slot_stride;
+            p->scratch_bytes = static_cast<uint64_t>(L.phys_slots - 1) * P * p->slot_stride;
             e = cudaMalloc(&p->d_scratch, p->scratch_bytes);
         }
         if (e != cudaSuccess) {

@@ -470,6 +470,108 @@ void push_range(std::vector<Range>& v, uint32_t prog, int64_t lo, int64_t hi) {
         v.push_back({prog, lo, hi});
 }
 
+// Step form.  Each round, per segment, is split into groups of transfers
+// that read each other's destinations (round_components).  A group of one
+// transfer, or recursive doubling's commutative exchange, runs in place.
+// Any other group (the cyclic rounds of the generalized schedule with removed
+// steps) is versioned instead of co-located: each of its transfers reads the
+// current copy of its sources and writes its destination to another copy of
+// that buffer, so every transfer is an independent chain that streams.  Every
+// logical (rank, slot, segment) has three physical copies: its own buffer
+// (slot) and two twins in the plan's scratch (slot + S, slot + 2S, S =
+// max_slots); a redirected write goes to the twin that is not the current
+// copy, and the last write of a rank's result (slot 0) goes back to the
+// rank's own buffer whenever its current copy is a twin (nobody reads the
+// stale home copy then).  Results that still end in a twin are copied home
+// by one final round.
+void step_sets(const Schedule& S, Builder& b, std::vector<std::vector<Range>>& sets, Lowered& lw) {
+    const int P = S.P, ns = S.max_slots, nseg = S.nseg();
+    auto key = [&](int rank, int slot, int seg) { return (static_cast<size_t>(rank) * ns + slot) * nseg + seg; };
+    std::vector<int> loc(static_cast<size_t>(P) * ns * nseg);
+    for (int r = 0; r < P; ++r)
+        for (int sl = 0; sl < ns; ++sl)
+            for (int sg = 0; sg < nseg; ++sg) loc[key(r, sl, sg)] = sl;
+    // the round of the last write of every rank's own buffer, per segment
+    std::vector<int> last(static_cast<size_t>(P) * nseg, -1);
+    for (size_t ri = 0; ri < S.rounds.size(); ++ri)
+        for (const Transfer& x : S.rounds[ri].xfers)
+            if (x.dst_out == 0)
+                for (int sg = S.seg_of(x.lo), s1 = S.seg_of(x.hi - 1) + 1; sg < s1; ++sg)
+                    last[static_cast<size_t>(x.dst) * nseg + sg] = static_cast<int>(ri);
+    int phys_max = ns - 1;
+    const bool commute = commute_ok(S);
+    for (size_t ri = 0; ri < S.rounds.size(); ++ri) {
+        const Round& rd = S.rounds[ri];
+        std::map<int, std::vector<XferAvg>> by_seg;
+        for (const Transfer& x : rd.xfers) {
+            int s0 = S.seg_of(x.lo), s1 = S.seg_of(x.hi - 1) + 1;
+            for (int sg = s0; sg < s1; ++sg)
+                by_seg[sg].push_back({&x, !x.completes.empty() && x.completes[sg - s0] != 0});
+        }
+        std::vector<Range> rs;
+        std::vector<std::pair<size_t, int>> moves;  // copies written this round: (key, physical slot)
+        for (auto& kv : by_seg) {
+            const int sg = kv.first;
+            for (auto& comp : round_components(kv.second)) {
+                const bool versioned = comp.size() > 1 && round_program(comp, commute).kind == PK_DAG;
+                std::vector<Transfer> phys;
+                phys.reserve(comp.size());
+                for (const XferAvg& xa : comp) {
+                    const Transfer& x = *xa.first;
+                    Transfer y = x;
+                    y.src_slot = loc[key(x.src, x.src_slot, sg)];
+                    y.dst_in = loc[key(x.dst, x.dst_in, sg)];
+                    const int cur = loc[key(x.dst, x.dst_out, sg)];
+                    int out = cur;
+                    if (x.dst_out == 0 && last[static_cast<size_t>(x.dst) * nseg + sg] == static_cast<int>(ri) &&
+                        cur != 0)
+                        out = 0;
+                    else if (versioned)
+                        out = cur == x.dst_out + ns ? x.dst_out + 2 * ns : x.dst_out + ns;
+                    y.dst_out = out;
+                    phys_max = std::max(phys_max, out);
+                    moves.push_back({key(x.dst, x.dst_out, sg), out});
+                    phys.push_back(y);
+                }
+                if (versioned) {
+                    for (size_t k = 0; k < phys.size(); ++k)
+                        push_range(rs, b.add(round_program({{&phys[k], comp[k].second}}, commute)), S.bounds[sg],
+                                   S.bounds[sg + 1]);
+                } else {
+                    std::vector<XferAvg> pc;
+                    for (size_t k = 0; k < phys.size(); ++k) pc.push_back({&phys[k], comp[k].second});
+                    push_range(rs, b.add(round_program(pc, commute)), S.bounds[sg], S.bounds[sg + 1]);
+                }
+            }
+        }
+        for (const auto& m : moves) loc[m.first] = m.second;
+        sets.push_back(rs);
+    }
+    // results left in a twin: one more round of copies home
+    std::vector<Transfer> copies;
+    for (int r = 0; r < P; ++r)
+        for (int sg = 0; sg < nseg; ++sg)
+            if (loc[key(r, 0, sg)] != 0 && S.bounds[sg + 1] > S.bounds[sg]) {
+                Transfer c{};
+                c.src = r;
+                c.src_slot = loc[key(r, 0, sg)];
+                c.dst = r;
+                c.dst_in = 0;
+                c.dst_out = 0;
+                c.lo = S.bounds[sg];
+                c.hi = S.bounds[sg + 1];
+                c.combine = false;
+                copies.push_back(c);
+            }
+    std::vector<Range> home;
+    for (const Transfer& c : copies) {
+        const int sg = S.seg_of(c.lo);
+        push_range(home, b.add(round_program({{&c, false}}, commute)), S.bounds[sg], S.bounds[sg + 1]);
+    }
+    if (!home.empty()) sets.push_back(home);
+    lw.phys_slots = phys_max + 1;
+}
+
 }  // namespace
 
 int staged_smem_bytes(const Lowered& lw) {
@@ -502,20 +604,7 @@ void lower(const Schedule& S, Lowered& lw) {
             }
             sets.push_back(rs);
         } else {
-            for (const Round& rd : S.rounds) {
-                std::map<int, std::vector<std::pair<const Transfer*, bool>>> by_seg;
-                for (const Transfer& x : rd.xfers) {
-                    int s0 = S.seg_of(x.lo), s1 = S.seg_of(x.hi - 1) + 1;
-                    for (int s = s0; s < s1; ++s)
-                        by_seg[s].push_back({&x, !x.completes.empty() && x.completes[s - s0] != 0});
-                }
-                std::vector<Range> rs;
-                for (auto& kv : by_seg)
-                    for (auto& comp : round_components(kv.second))
-                        push_range(rs, b.add(round_program(comp, commute_ok(S))), S.bounds[kv.first],
-                                   S.bounds[kv.first + 1]);
-                sets.push_back(rs);
-            }
+            step_sets(S, b, sets, lw);
         }
     }
     // A set whose programs are all chains, single trees or fp32

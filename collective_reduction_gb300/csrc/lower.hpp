@@ -38,6 +38,7 @@ struct Lowered {
     uint64_t hbm_bytes = 0;
     uint64_t n_items = 0;
     int launches = 0;     // launches per execute on aligned buffers
+    int phys_slots = 1;   // step form: physical copies per rank buffer (slots and their twins)
 };
 
 // Staged-kernel geometry shared by lowering and launch: shared-memory budget

@@ -123,9 +123,9 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
         }
         if (blob.size() > kTableArea) return AR_ERR_UNSUPPORTED;
         uint64_t slot_stride = 0;
-        if (S.params.form == AR_FORM_STEP && S.max_slots > 1) {
+        if (S.params.form == AR_FORM_STEP && L.phys_slots > 1) {
             slot_stride = (bytes + 255) / 256 * 256;
-            if (static_cast<uint64_t>(S.max_slots - 1) * P * slot_stride > kSlotArea) return AR_ERR_UNSUPPORTED;
+            if (static_cast<uint64_t>(L.phys_slots - 1) * P * slot_stride > kSlotArea) return AR_ERR_UNSUPPORTED;
         }
 
         int dev = 0;

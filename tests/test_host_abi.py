@@ -229,7 +229,6 @@ def test_avg_requests(lib):
 @pytest.mark.parametrize("algo,P,op,kw", [
     ("generalized", 7, "sum", {"r": 1}), ("generalized", 7, "sum", {"r": 3}), ("rd", 8, "max", {}),
     ("generalized", 12, "min", {"r": 2}), ("generalized", 7, "avg", {"r": 2}),
-    ("generalized", 7, "sum", {"r": 3, "form": "step"}),
 ])
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
 def test_dag_kernel_compiles_on_the_host(lib, algo, P, op, kw, dtype):
@@ -254,6 +253,10 @@ def test_no_dag_kernel_for_streaming_plans(lib):
     for algo, kw in (("ring", {}), ("rh", {}), ("binomial", {}), ("generalized", {"r": 2})):
         # sum trees are shared by every rank: no DAG program, nothing to compile
         assert ar.Schedule(8, 8 * 4096, "float32", "sum", algo, **kw).dag_kernel_bytes() == 0
+    # the step form's cyclic rounds are versioned into independent chains
+    for P, r in ((7, 3), (12, 4), (31, 5)):
+        s = ar.Schedule(P, P * 4096, "float32", "max", "generalized", r=r, form="step")
+        assert s.dag_kernel_bytes() == 0, (P, r)
 
 
 def test_jit_parameter_checked(lib):
