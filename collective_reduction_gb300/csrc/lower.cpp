@@ -476,14 +476,14 @@ void push_range(std::vector<Range>& v, uint32_t prog, int64_t lo, int64_t hi) {
 // Any other group (the cyclic rounds of the generalized schedule with removed
 // steps) is versioned instead of co-located: each of its transfers reads the
 // current copy of its sources and writes its destination to another copy of
-// that buffer, so every transfer is an independent chain that streams.  Every
-// logical (rank, slot, segment) has three physical copies: its own buffer
-// (slot) and two twins in the plan's scratch (slot + S, slot + 2S, S =
-// max_slots); a redirected write goes to the twin that is not the current
-// copy, and the last write of a rank's result (slot 0) goes back to the
-// rank's own buffer whenever its current copy is a twin (nobody reads the
-// stale home copy then).  Results that still end in a twin are copied home
-// by one final round.
+// that buffer, so every transfer is an independent chain that streams.  A
+// rank's result (slot 0) has three physical copies: its own buffer and two
+// twins in the plan's scratch (slots S and 2S, S = max_slots); redirected
+// writes alternate between the twins, and its last write goes back to the
+// rank's own buffer whenever the current copy is a twin (nobody reads the
+// stale home copy then).  A second partial (slot k >= 1) toggles between its
+// slot and one twin (k + S).  Results that still end in a twin are copied
+// home by one final round.
 void step_sets(const Schedule& S, Builder& b, std::vector<std::vector<Range>>& sets, Lowered& lw) {
     const int P = S.P, ns = S.max_slots, nseg = S.nseg();
     auto key = [&](int rank, int slot, int seg) { return (static_cast<size_t>(rank) * ns + slot) * nseg + seg; };
@@ -526,8 +526,10 @@ void step_sets(const Schedule& S, Builder& b, std::vector<std::vector<Range>>& s
                     if (x.dst_out == 0 && last[static_cast<size_t>(x.dst) * nseg + sg] == static_cast<int>(ri) &&
                         cur != 0)
                         out = 0;
+                    else if (versioned && x.dst_out == 0)
+                        out = cur == ns ? 2 * ns : ns;  // alternate between the two twins, away from home
                     else if (versioned)
-                        out = cur == x.dst_out + ns ? x.dst_out + 2 * ns : x.dst_out + ns;
+                        out = cur == x.dst_out ? x.dst_out + ns : x.dst_out;  // a partial: its slot or its twin
                     y.dst_out = out;
                     phys_max = std::max(phys_max, out);
                     moves.push_back({key(x.dst, x.dst_out, sg), out});
