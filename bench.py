@@ -261,38 +261,89 @@ def base_chunks(a):
     return a.P
 
 
-def cpu_baseline_and_check(a, sample_in, sample_out_engine):
-    """The oracle, as it stands, timed on host cores on a bounded sample of
-    the workload; also checks the engine's output on that sample."""
-    import numpy as np
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
 
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_repeat(job):
+    """Pool worker: the oracle on one sample, repeated for `seconds` (at least
+    once); returns (runs, seconds)."""
+    algo, kw, op, dtype, sample, seconds = job
     import oracle
     from oracle.elementops import Arith
-    kw = {}
-    if a.algo == "generalized":
-        kw = {"r": a.r}
-    if a.algo == "hybrid":
-        kw = {"k1": a.k1}
     t0 = time.perf_counter()
-    reps = 0
-    res = None
+    runs = 0
     while True:
-        res = oracle.run(a.algo, sample_in, Arith(a.op, a.dtype), **kw)
-        reps += 1
-        if time.perf_counter() - t0 >= a.cpu_seconds:
+        oracle.run(algo, sample, Arith(op, dtype), **kw)
+        runs += 1
+        if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
-    nbytes = a.P * sample_in[0].size * esize(a.dtype)
+    return runs, time.perf_counter() - t0
+
+
+def split_sample(sample, P, parts):
+    """The per-chunk blocks of a gathered sample cut into `parts` samples,
+    each keeping the chunk structure (a ceil split gives the same P chunks)."""
+    import numpy as np
+    K = sample[0].size // P // parts
+    out = []
+    for j in range(parts):
+        out.append([np.ascontiguousarray(np.concatenate(
+            [b[c * K * parts + j * K: c * K * parts + (j + 1) * K] for c in range(P)])) for b in sample])
+    return out
+
+
+def oracle_kw(a):
+    return {"r": a.r} if a.algo == "generalized" else ({"k1": a.k1} if a.algo == "hybrid" else {})
+
+
+def cpu_baseline_and_check(a, sample_in, sample_out_engine, parts):
+    """The oracle, as it stands, timed on the host cores on a bounded sample
+    of the workload: one sample per core, each in its own process (spawned),
+    for half the time budget, after a single-process run on the first sample
+    for the other half that also checks the engine's output there."""
+    import multiprocessing as mp
+
+    import numpy as np
+    subs = split_sample(sample_in, a.P, parts)
+    outs = split_sample(sample_out_engine, a.P, parts) if sample_out_engine is not None else None
+    kw = oracle_kw(a)
+    import oracle
+    from oracle.elementops import Arith
+    res = oracle.run(a.algo, subs[0], Arith(a.op, a.dtype), **kw)
     ok = None
-    if sample_out_engine is not None and a.order == "faithful":
+    if outs is not None and a.order == "faithful":
         def bits(x):
             x = np.ascontiguousarray(x)
             return x if x.dtype == np.uint16 else x.view(np.uint32)
-        ok = all(np.array_equal(bits(res.bufs[r]), bits(sample_out_engine[r])) for r in range(a.P))
-    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{sample_in[0].size} elements per rank ({sample_in[0].size // a.P} from each of the "
-                      f"{a.P} chunks of the benchmark buffers), {reps} oracle runs in {dt:.1f} s, "
-                      f"NumPy single-threaded"}, ok
+        ok = all(np.array_equal(bits(res.bufs[r]), bits(outs[0][r])) for r in range(a.P))
+    half = a.cpu_seconds / 2
+    nbytes = a.P * subs[0][0].size * esize(a.dtype)
+    runs1, dt1 = oracle_repeat((a.algo, kw, a.op, a.dtype, subs[0], half))
+    with mp.get_context("spawn").Pool(parts) as pool:
+        done = pool.map(oracle_repeat, [(a.algo, kw, a.op, a.dtype, sub, half) for sub in subs])
+    runs = sum(r for r, _ in done)
+    wall = max(t for _, t in done)
+    return {"value": nbytes * runs / wall / 1e9, "unit": "GB/s", "cores": parts, "kind": "oracle",
+            "single_thread_value": nbytes * runs1 / dt1 / 1e9, "cpu_model": cpu_model(),
+            "sample": f"{parts} samples of {subs[0][0].size} elements per rank ({subs[0][0].size // a.P} from "
+                      f"each of the {a.P} chunks of the benchmark buffers), one per core in its own process: "
+                      f"{runs} oracle runs in {wall:.1f} s (single process: {runs1} runs in {dt1:.1f} s)"}, ok
 
 
 def run_ours(a):
@@ -321,11 +372,12 @@ def run_ours(a):
     stream = torch.cuda.current_stream()
 
     # sampled check + CPU baseline (rank 0 only): sample before the first call
+    parts = host_cores() if rank == 0 else 1
     sample_k = 1 << 17 if a.dtype != "bfloat16" else 1 << 18
-    sample_k = max(1, min(sample_k // a.P, n // a.P))
+    sample_k = max(1, min(sample_k // a.P, n // a.P // parts))
     sample_in, idx = (None, None)
     if rank == 0:
-        sample_in, idx = gather_sample(dev, a.P, n, sample_k, base_chunks(a))
+        sample_in, idx = gather_sample(dev, a.P, n, sample_k * parts, base_chunks(a))
     plan.execute(dev, stream)
     plan.check()
     sample_out = None
@@ -382,7 +434,7 @@ def run_ours(a):
 
     cpu, verified = (None, None)
     if rank == 0:
-        cpu, verified = cpu_baseline_and_check(a, sample_in, sample_out)
+        cpu, verified = cpu_baseline_and_check(a, sample_in, sample_out, parts)
 
     line = {
         "metric": METRIC,
@@ -427,29 +479,48 @@ def run_ours(a):
 
 # ------------------------------------------------------------ reference arm
 
+_REF_BUFS = None
+
+
+def _reference_init(P, n, dtype, dist):
+    """Pool worker start-up: this worker's own seeded sample of the workload."""
+    global _REF_BUFS
+    import ar_synth
+    _REF_BUFS = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1e-3, seed=os.getpid())
+
+
+def _reference_step(job):
+    algo, kw, op, dtype = job
+    import oracle
+    from oracle.elementops import Arith
+    oracle.run(algo, _REF_BUFS, Arith(op, dtype), **kw)
+    return True
+
+
 def run_reference(a):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import ar_synth
-    import oracle
-    from oracle.elementops import Arith
-    # bounded sample of the workload: up to 2^20 elements per rank (chunk structure
-    # kept: a ceil split of the sample gives the same P chunks)
+    import multiprocessing as mp
+    # bounded sample of the workload: up to 2^20 elements per rank per core
+    # (chunk structure kept: a ceil split of the sample gives the same P
+    # chunks), one sample per core, each in its own (spawned) process; a step
+    # is one oracle run on every core's sample
+    cores = host_cores()
     n = max(a.P, min(int(a.mib * (1 << 20)) // esize(a.dtype), 1 << 20) // a.P * a.P)
     dist = "uniform_int" if a.dtype == "int32" else "normal"
-    bufs = ar_synth.rank_inputs(a.P, n, a.dtype, dist, sigma=1e-3)
-    kw = {"r": a.r} if a.algo == "generalized" else ({"k1": a.k1} if a.algo == "hybrid" else {})
-    for _ in range(a.warmup):
-        oracle.run(a.algo, bufs, Arith(a.op, a.dtype), **kw)
-    times = []
-    for _ in range(a.steps):
-        t0 = time.perf_counter()
-        oracle.run(a.algo, bufs, Arith(a.op, a.dtype), **kw)
-        times.append(time.perf_counter() - t0)
+    job = (a.algo, oracle_kw(a), a.op, a.dtype)
+    with mp.get_context("spawn").Pool(cores, initializer=_reference_init, initargs=(a.P, n, a.dtype, dist)) as pool:
+        for _ in range(a.warmup):
+            pool.map(_reference_step, [job] * cores, chunksize=1)
+        times = []
+        for _ in range(a.steps):
+            t0 = time.perf_counter()
+            pool.map(_reference_step, [job] * cores, chunksize=1)
+            times.append(time.perf_counter() - t0)
     total = sum(times)
-    nbytes = a.P * n * esize(a.dtype)
+    nbytes = a.P * n * esize(a.dtype) * cores
     value = nbytes * a.steps / total / 1e9
     line = {
         "impl": "reference",
@@ -459,9 +530,11 @@ def run_reference(a):
         "config": {"workload": workload_name(a), "P": a.P, "bytes_per_rank": int(a.mib * (1 << 20)),
                    "algo": a.algo, "form": a.form, "order": a.order, "op": a.op,
                    "sample_elements_per_rank": n},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} elements per rank (of {int(a.mib * (1 << 20)) // esize(a.dtype)}), "
-                                   f"one oracle run per step, NumPy single-threaded"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
+                         "sample": f"{cores} samples (one per core, each in its own process) of {n} elements "
+                                   f"per rank (of {int(a.mib * (1 << 20)) // esize(a.dtype)}); a step is one "
+                                   f"oracle run on every sample"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
