@@ -86,6 +86,7 @@ _EXPORTS = {
     "ar_plan_check": (ctypes.c_int, [_VP]),
     "ar_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ar_schedule_dag_kernel": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
+    "ar_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _VP]),
     "ar_cost_model_default": (ctypes.c_int, [ctypes.POINTER(CostModel)]),
     "ar_cost_predict": (ctypes.c_int, [_VP, ctypes.POINTER(CostModel), ctypes.POINTER(ctypes.c_double)]),
     "ar_cost_optimal_r": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64, ctypes.POINTER(CostModel),
@@ -281,3 +282,10 @@ def select(P, n, dtype, op, model=None):
     name = {v: k for k, v in ALGOS.items()}[algo.value]
     params = {"form": "step", "order": "faithful", "group": "cyclic", "r": p.r, "k1": p.k1}
     return name, params, us.value
+
+
+def selftest_bounded_wait(timeout_ms=100, stream=None):
+    """Runs the bounded-wait self-test; returns the status name ("AR_ERR_TIMEOUT"
+    when the wait gave up as designed)."""
+    st = lib().ar_selftest_bounded_wait(int(timeout_ms), _VP(_stream_handle(stream)))
+    return STATUS.get(st, str(st))

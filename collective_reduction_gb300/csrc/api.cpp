@@ -285,6 +285,22 @@ ar_status ar_schedule_tree(ar_schedule_t s, int rank, uint64_t elem, char* buf, 
     }
 }
 
+ar_status ar_selftest_bounded_wait(uint32_t timeout_ms, void* stream) {
+    if (timeout_ms < 1 || timeout_ms > 10000) return AR_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* d_status = nullptr;
+    cudaError_t e = cudaMalloc(&d_status, sizeof(int));
+    if (e == cudaErrorMemoryAllocation) return AR_ERR_NOMEM;
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_status, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = ar::launch_wait_selftest(d_status, static_cast<uint64_t>(timeout_ms) * 1000000ull, st);
+    int status = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&status, d_status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(d_status);
+    if (e != cudaSuccess) return cuda_status(e);
+    return (status & ar::kStatusWaitFull) ? AR_ERR_TIMEOUT : AR_OK;
+}
+
 ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes) {
     if (!s || !cubin_bytes) return AR_ERR_INVALID_ARG;
     *cubin_bytes = 0;

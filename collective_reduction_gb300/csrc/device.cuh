@@ -288,16 +288,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase of the given parity; false after kWaitNs.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Waits for the phase of the given parity; false after ns nanoseconds.
+__device__ __noinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitNs) return false;
+        if (globaltimer() - t0 > ns) return false;
     }
 }
+
+// The kernels' wait: false after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_for(bar, parity, kWaitNs); }
 
 // loads are read once: ask L2 to evict them first
 #ifndef AR_L2_EVICT_FIRST

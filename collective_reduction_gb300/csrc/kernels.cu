@@ -516,6 +516,22 @@ __global__ void __launch_bounds__(kElemThreads) elementwise_kernel(const __grid_
     }
 }
 
+// --------------------------------------------------------- wait self-test
+
+// One CTA waits on an mbarrier that nothing completes, gives up after ns
+// nanoseconds the way every kernel's bounded wait does, records the same
+// status bit and returns.
+__global__ void wait_selftest_kernel(int* status, uint64_t ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait_for(b, 0, ns)) atomicOr(status, kStatusWaitFull);
+}
+
 // ----------------------------------------------------------------- dispatch
 
 using KernelFn = void (*)(KernelArgs);
@@ -566,6 +582,11 @@ cudaError_t launch_dependent(const void* f, int grid, int block, int smem, cudaS
     cfg.numAttrs = 1;
     void* args[] = {const_cast<KernelArgs*>(&a)};
     return cudaLaunchKernelExC(&cfg, f, args);
+}
+
+cudaError_t launch_wait_selftest(int* status, uint64_t ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(status, ns);
+    return cudaGetLastError();
 }
 
 cudaError_t prepare_kernels(int dtype, int op) {

@@ -12,6 +12,8 @@ namespace ar {
 // Launches kernel f (one KernelArgs parameter) as a programmatic dependent
 // of the previous kernel in the stream (see device.cuh).
 cudaError_t launch_dependent(const void* f, int grid, int block, int smem, cudaStream_t st, const KernelArgs& a);
+// One CTA that waits on an mbarrier nothing completes, bounded by ns.
+cudaError_t launch_wait_selftest(int* status, uint64_t ns, cudaStream_t st);
 // Sets the dynamic shared-memory limits of the (dtype, op) kernels.
 cudaError_t prepare_kernels(int dtype, int op);
 // Persistent staged kernel over a.items (all 16-byte aligned), grid CTAs.

@@ -285,6 +285,14 @@ ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream);
  * must not overlap (they share the internal streams). */
 ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* dev_bufs,
                           void* stream);
+/* Self-test of the bounded waits every kernel uses (no plan needed): launches
+ * one CTA that waits on an mbarrier nothing ever completes; the wait gives up
+ * after timeout_ms (1..10000) exactly as a kernel's wait does after two
+ * seconds, records the status bit and returns, so the device stays usable.
+ * Synchronises `stream`.  Returns AR_ERR_TIMEOUT when the wait gave up (the
+ * expected result), AR_OK if it completed, AR_ERR_INVALID_ARG for a timeout
+ * out of range, AR_ERR_CUDA / AR_ERR_NOMEM on failures. */
+ar_status ar_selftest_bounded_wait(uint32_t timeout_ms, void* stream);
 /* Synchronises the device and reads the plan's device status word: AR_OK, or
  * AR_ERR_TIMEOUT if a bounded wait in a kernel gave up since the last check
  * (the word is then cleared).  AR_ERR_CUDA if synchronisation fails. */

@@ -566,3 +566,16 @@ def test_execute_captures_in_a_cuda_graph(algo, kw):
     plan.check()
     for r in range(P):
         assert_bit_equal(to_host(graphed[r], "float32"), to_host(direct[r], "float32"), "float32", f"rank {r}")
+
+
+def test_bounded_wait_gives_up_and_the_device_stays_usable():
+    """A wait that nothing completes gives up after its limit, reports
+    AR_ERR_TIMEOUT, and the next allreduce still runs correctly."""
+    import time
+
+    import collective_reduction_gb300 as ar
+    t0 = time.perf_counter()
+    assert ar.selftest_bounded_wait(200) == "AR_ERR_TIMEOUT"
+    assert 0.19 <= time.perf_counter() - t0 < 5.0
+    bufs = ar_synth.rank_inputs(4, 4099, "float32", "normal", seed=31)
+    check_faithful(bufs, "float32", "sum", "ring", "fused")

@@ -264,3 +264,8 @@ def test_jit_parameter_checked(lib):
     p.jit = 2
     h = ctypes.c_void_p()
     assert lib.ar_schedule_create(8, 64, 1, 0, 0, ctypes.byref(p), ctypes.byref(h)) == 1
+
+
+def test_selftest_timeout_range_checked_on_host(lib):
+    assert lib.ar_selftest_bounded_wait(0, None) == 1
+    assert lib.ar_selftest_bounded_wait(10001, None) == 1
