@@ -596,12 +596,17 @@ void lower(const Schedule& S, Lowered& lw) {
             std::vector<Range> rs;
             const bool commute = S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD || S.op == AR_AVG;
             Canon cn(S.dag, commute);
+            // With two ranks the fp32 accumulation is the schedule's single
+            // combine (fp32 op, one rounding) for sum, prod and every int32
+            // op, bit for bit: run the faithful program, which streams the
+            // wider tiles.
+            const bool acc = S.params.order == AR_ORDER_FP32ACC &&
+                             !(S.P == 2 && (S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD));
             for (int s = 0; s < S.nseg(); ++s) {
                 if (S.bounds[s + 1] <= S.bounds[s]) continue;
                 const std::vector<int> ranks = defined_ranks(S, s);
                 if (ranks.empty()) continue;  // (an all-gather owner-only segment)
-                const Prog p = S.params.order == AR_ORDER_FP32ACC ? acc_program(S.P, ranks, S.op == AR_AVG)
-                                                                  : fused_program(cn, S, s, ranks);
+                const Prog p = acc ? acc_program(S.P, ranks, S.op == AR_AVG) : fused_program(cn, S, s, ranks);
                 push_range(rs, b.add(p), S.bounds[s], S.bounds[s + 1]);
             }
             sets.push_back(rs);

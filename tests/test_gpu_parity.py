@@ -579,3 +579,16 @@ def test_bounded_wait_gives_up_and_the_device_stays_usable():
     assert 0.19 <= time.perf_counter() - t0 < 5.0
     bufs = ar_synth.rank_inputs(4, 4099, "float32", "normal", seed=31)
     check_faithful(bufs, "float32", "sum", "ring", "fused")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("op", ["sum", "prod"])
+def test_two_rank_fp32acc_is_the_single_combine(dtype, op):
+    """With two ranks the fp32 accumulation is one fp32 op and one rounding:
+    the same bits as the order-faithful pass (which the plan then runs)."""
+    dist = "small_int" if (dtype == "int32" and op == "prod") else ("uniform_int" if dtype == "int32" else "normal")
+    bufs = ar_synth.rank_inputs(2, (1 << 20) + 7, dtype, dist, sigma=1.0, seed=5)
+    want = engine(bufs, dtype, op, "ring")
+    got = engine(bufs, dtype, op, "ring", order="fp32acc")
+    for r in range(2):
+        assert_bit_equal(got[r], want[r], dtype, f"rank {r}")
