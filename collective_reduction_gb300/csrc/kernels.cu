@@ -13,17 +13,20 @@
 // tiles are 32 KB (16 KB for bf16 fp32 accumulation and deep trees) whatever
 // P is, so all consumer threads stay busy and ~200 KB per SM is in flight.
 //
-// staged_kernel: for DAG programs (rank-specific results, rounds whose
-// transfers read each other's destinations).  Same structure, but a stage
-// holds all input tiles of one item, which the consumers evaluate as
-// straight-line instructions with shared-memory temporaries.
+// staged_kernel: for DAG programs (rank-specific results) and for chains
+// whose rank tiles would be tiny.  Same structure, but a stage holds all
+// input tiles of one item, which the consumers evaluate as straight-line
+// instructions with shared-memory temporaries (the plan's DAG programs can
+// instead run as compiled code: the same loop, compiled per plan at run time
+// from device.cuh).
 //
 // Every wait is bounded: after two seconds the waiter sets a bit in the
 // status word and the CTA winds down (a failing producer first waits, again
 // bounded, for its copies in flight).
 //
-// elementwise_kernel: one CTA per work item, one element per thread; used for
-// the unaligned heads / tails of ranges and for buffers that are not 16-byte
+// elementwise_kernel: one CTA per work item, one element per thread (the
+// CTA's threads load the item's inputs together); used for small passes, the
+// unaligned heads / tails of ranges and buffers that are not 16-byte
 // aligned.  Same programs, same arithmetic, same accumulation order.
 //
 // Element arithmetic (sum / prod / max / min over int32, fp32, bf16): int32

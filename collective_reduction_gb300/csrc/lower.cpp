@@ -8,8 +8,9 @@
 // in operand order share one evaluation.  max / min keep the operand order
 // (they differ on +-0 and NaN).
 //
-// Step form: every round's program reads each source and destination once and
-// applies the round's transfers (receiver on the left).
+// Step form: every round's transfers (receiver on the left), grouped so that
+// independent transfers run as separate chains and transfers that read each
+// other's destinations are versioned into twin copies (step_sets).
 #include "lower.hpp"
 
 #include <algorithm>

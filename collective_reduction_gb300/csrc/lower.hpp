@@ -11,7 +11,7 @@ namespace ar {
 
 // One kernel-launch set: the items of one fused pass or of one round.
 struct LaunchSet {
-    std::vector<WorkItem> bulk;      // 16-byte aligned ranges, staged kernel
+    std::vector<WorkItem> bulk;      // 16-byte aligned ranges: rank-streaming or staged kernel
     std::vector<WorkItem> edge;      // unaligned heads / tails, element kernel
     std::vector<WorkItem> fallback;  // whole ranges for unaligned buffers
     uint64_t bytes = 0;              // algorithmic HBM bytes of the set
