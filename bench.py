@@ -564,13 +564,15 @@ def sweep_check(ar, oracle_mods, plan, dev, P, n, dtype, order):
     if order == "fp32acc":
         ref = direct_f64(sample_in, "sum", dtype)
         err = max(normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) for g in got)
-        return bool(err <= (1e-6 if dtype == "float32" else 4e-3)), full
+        return bool(err <= (1e-6 if dtype == "float32" else 4e-3)), full, None
+    t0 = time.perf_counter()
     want = oracle.run("ring", sample_in, Arith("sum", dtype)).bufs
+    oracle_s = time.perf_counter() - t0
 
     def bits(x):
         x = np.ascontiguousarray(x)
         return x if x.dtype == np.uint16 else x.view(np.uint32)
-    return all(np.array_equal(bits(g), bits(w)) for g, w in zip(got, want)), full
+    return all(np.array_equal(bits(g), bits(w)) for g, w in zip(got, want)), full, oracle_s
 
 
 def run_sweep(a, path):
@@ -605,9 +607,9 @@ def run_sweep(a, path):
                         plan = ar.Plan(P, n, dtype, "sum", "ring", form=form, order=order)
                         info = plan.info()
                         fresh = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P + 1)
-                        ok, full = sweep_check(ar, oracle_mods, plan, fresh, P, n, dtype, order)
+                        ok, full, oracle_s = sweep_check(ar, oracle_mods, plan, fresh, P, n, dtype, order)
                         del fresh
-                        for _ in range(3):
+                        for _ in range(5):  # 5 warm-up calls
                             plan.execute(dev)
                         torch.cuda.synchronize()
                         if S <= 65536:
@@ -648,6 +650,8 @@ def run_sweep(a, path):
                                "frac_of_measured": info["hbm_bytes"] / (ms / 1e3) / 1e9 / peak,
                                "launches": info["launches"], "verified": ok,
                                "checked": "every element" if full else "2^12 sampled elements per chunk"}
+                        if full and oracle_s:  # the oracle timed on the whole point (NumPy, one process)
+                            row["oracle_GBps"] = P * S / oracle_s / 1e9
                         out.write(json.dumps(row) + "\n")
                         out.flush()
                         plan.close()
@@ -775,9 +779,9 @@ def run_configs(a, path):
 
 def time_plan(plan, dev, reps=5, calls=20):
     """Median over reps of the mean CUDA-event time of `calls` back-to-back
-    executes (after 3 warm-up calls), in microseconds."""
+    executes (after 5 warm-up calls), in microseconds."""
     import torch
-    for _ in range(3):
+    for _ in range(5):
         plan.execute(dev)
     torch.cuda.synchronize()
     ts = []
