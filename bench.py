@@ -38,7 +38,9 @@ NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "allreduced bytes/s (P x S per call)"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
-KERNEL_SRC = [os.path.join(ROOT, "collective_reduction_gb300", "csrc", f) for f in ("kernels.cu", "device.cuh")]
+# the kernel code and the lowering that fixes its launch shape (tiles, stages, stores)
+KERNEL_SRC = [os.path.join(ROOT, "collective_reduction_gb300", "csrc", f)
+              for f in ("kernels.cu", "device.cuh", "devprog.hpp", "lower.cpp", "lower.hpp")]
 
 
 def parse():

@@ -60,6 +60,15 @@ class Info(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class LoweringInfo(ctypes.Structure):
+    _fields_ = [("items", ctypes.c_uint64), ("launch_sets", ctypes.c_int), ("windows", ctypes.c_int),
+                ("tiling_ok", ctypes.c_int), ("windows_ok", ctypes.c_int), ("wave_balance", ctypes.c_double),
+                ("stream_tile_bytes", ctypes.c_int), ("stream_stages", ctypes.c_int)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
 class CostModel(ctypes.Structure):
     """Step-form cost: alpha per round, beta per byte sent and gamma per byte
     combined, bytes summed over all ranks."""
@@ -86,6 +95,7 @@ _EXPORTS = {
     "ar_plan_check": (ctypes.c_int, [_VP]),
     "ar_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ar_schedule_dag_kernel": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
+    "ar_schedule_lowering": (ctypes.c_int, [_VP, ctypes.POINTER(LoweringInfo)]),
     "ar_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _VP]),
     "ar_cost_model_default": (ctypes.c_int, [ctypes.POINTER(CostModel)]),
     "ar_cost_predict": (ctypes.c_int, [_VP, ctypes.POINTER(CostModel), ctypes.POINTER(ctypes.c_double)]),
@@ -188,6 +198,13 @@ class Schedule:
         n = ctypes.c_size_t(0)
         _check(lib().ar_schedule_dag_kernel(self._h, ctypes.byref(n)), "ar_schedule_dag_kernel")
         return n.value
+
+    def lowering(self):
+        """The work items a plan of this schedule would launch, with the host
+        checks of their tiling and host-path windows (ar_schedule_lowering)."""
+        info = LoweringInfo()
+        _check(lib().ar_schedule_lowering(self._h, ctypes.byref(info)), "ar_schedule_lowering")
+        return info.as_dict()
 
     def close(self):
         if getattr(self, "_h", None):

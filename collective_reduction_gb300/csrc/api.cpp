@@ -52,12 +52,8 @@ struct ar_plan_s {
         bool small;
     };
     std::vector<Set> sets;
-    // element windows of a fused plan for the pipelined host path: window w
-    // covers elements [lo, hi), bulk items [b0, b1) and edge items [e0, e1)
-    struct Window {
-        int64_t lo, hi;
-        uint32_t b0, b1, e0, e1;
-    };
+    // element windows of a fused plan for the pipelined host path
+    using Window = ar::Window;
     std::vector<Window> windows;
     // copy streams of the pipelined host path, created on first use: the
     // copies of rank r go to stream r mod kCopyStreams in each direction
@@ -191,31 +187,12 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
     return e;
 }
 
-// Element windows for the pipelined host path (fused plans): about 128 MB of
-// rank data per window, at most 32 windows, cut at bulk-item boundaries.
+// Element windows for the pipelined host path (fused plans; ar::host_windows).
 void make_windows(ar_plan_s* p) {
     p->windows.clear();
     if (p->L.sets.size() != 1) return;
-    const ar::LaunchSet& ls = p->L.sets[0];
-    const uint64_t nb = ls.bulk.size();
     const uint64_t total = static_cast<uint64_t>(p->S.P) * p->S.n * ar::esize_of(p->S.dtype);
-    uint64_t W = std::min<uint64_t>({total / (128ull << 20), 32, nb});
-    if (W < 2) return;
-    auto first_edge_at = [&](int64_t x) {
-        uint32_t k = 0;
-        while (k < ls.edge.size() && ls.edge[k].elem < x) ++k;
-        return k;
-    };
-    for (uint64_t w = 0; w < W; ++w) {
-        ar_plan_s::Window win;
-        win.b0 = static_cast<uint32_t>(nb * w / W);
-        win.b1 = static_cast<uint32_t>(nb * (w + 1) / W);
-        win.lo = w == 0 ? 0 : ls.bulk[win.b0].elem;
-        win.hi = w + 1 == W ? p->S.n : ls.bulk[win.b1].elem;
-        win.e0 = first_edge_at(win.lo);
-        win.e1 = w + 1 == W ? static_cast<uint32_t>(ls.edge.size()) : first_edge_at(win.hi);
-        p->windows.push_back(win);
-    }
+    p->windows = ar::host_windows(p->L.sets[0], p->S.n, total);
 }
 
 }  // namespace
@@ -317,6 +294,31 @@ ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes) {
         return AR_OK;
     } catch (const std::length_error&) {
         return AR_ERR_UNSUPPORTED;
+    } catch (const std::bad_alloc&) {
+        return AR_ERR_NOMEM;
+    }
+}
+
+ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
+    if (!s || !out) return AR_ERR_INVALID_ARG;
+    *out = ar_lowering_info{};
+    try {
+        ar::Lowered L;
+        ar::lower(s->S, L);
+        const int es = ar::esize_of(s->S.dtype);
+        std::vector<ar::Window> W;
+        if (L.sets.size() == 1)
+            W = ar::host_windows(L.sets[0], s->S.n, static_cast<uint64_t>(s->S.P) * s->S.n * es);
+        const ar::LoweringCheck c = ar::check_lowering(L, s->S.n, es, W);
+        out->items = c.items;
+        out->launch_sets = static_cast<int>(L.sets.size());
+        out->windows = static_cast<int>(W.size());
+        out->tiling_ok = c.tiling_ok;
+        out->windows_ok = c.windows_ok;
+        out->wave_balance = c.wave_balance;
+        out->stream_tile_bytes = L.stream_tile;
+        out->stream_stages = L.stream_stages;
+        return AR_OK;
     } catch (const std::bad_alloc&) {
         return AR_ERR_NOMEM;
     }
@@ -541,6 +543,10 @@ ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* d
         cudaEvent_t* in_done = ev + per_win * w;      // K events
         cudaEvent_t reduced = ev[per_win * w + K];
         cudaEvent_t* out_done = ev + per_win * w + K + 1;  // K events
+        if (win.lo < 0 || win.hi <= win.lo || win.hi > S.n) {  // never a copy outside the buffers
+            e = cudaErrorInvalidValue;
+            break;
+        }
         const size_t off = static_cast<size_t>(win.lo) * es, len = static_cast<size_t>(win.hi - win.lo) * es;
         for (int r = 0; r < P; ++r)
             chk(cudaMemcpyAsync(static_cast<char*>(dev_bufs[r]) + off, static_cast<const char*>(host_bufs[r]) + off,

@@ -546,7 +546,7 @@ KernelFn table(int which) {
     if (which == K_STAGED) return staged_kernel<DT, OP>;
     if (which == K_STREAM) return stream_kernel<DT, OP, kStreamVpt, false>;
     if (which == K_STREAM_NARROW) return stream_kernel<DT, OP, kStreamVptNarrow, false>;
-    if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptNarrow, true>;
+    if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptTree, true>;
     if (which == K_STREAM_TREE_WIDE) return stream_kernel<DT, OP, kStreamVpt, true>;
     return elementwise_kernel<DT, OP>;
 }
@@ -615,7 +615,7 @@ cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int 
 cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st) {
     // the rank tile fixes the vectors per consumer thread
     const int which = (a.flags & kArgTrees)
-                          ? (a.tile_bytes == kStreamTileNarrow  ? K_STREAM_TREE
+                          ? (a.tile_bytes == kStreamTileTree    ? K_STREAM_TREE
                              : a.tile_bytes == kStreamTileBytes ? K_STREAM_TREE_WIDE
                                                                 : -1)
                       : a.tile_bytes == kStreamTileBytes  ? K_STREAM

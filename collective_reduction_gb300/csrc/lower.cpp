@@ -29,6 +29,12 @@
 #define AR_TREE_WIDE_SLOTS 4
 #endif
 
+// Pipeline depth of the rank-streaming kernel for chains over 4-byte
+// elements (the others use as many stages as shared memory holds).
+#ifndef AR_CHAIN_STAGES_4B
+#define AR_CHAIN_STAGES_4B 3
+#endif
+
 namespace ar {
 namespace {
 
@@ -678,13 +684,26 @@ void lower(const Schedule& S, Lowered& lw) {
     // vectors per thread).  A tree keeps depth - 1 stack tiles in shared
     // memory next to the stages: 32 KB tiles while that leaves a pipeline of
     // at least 3 stages (trees of up to 16 leaves; measured +6% at P = 16 over
-    // 16 KB tiles), 16 KB tiles for deeper trees.
-    const bool narrow = (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC) ||
-                        (stream_trees && lw.stream_slots > AR_TREE_WIDE_SLOTS);
+    // 16 KB tiles), 24 KB tiles for deeper trees (3 stages at 64 leaves, 4 at
+    // 32; measured +7% / +12% fp32 and +10% / +11% bf16 at P = 64 / 32 over
+    // 16 KB tiles with 8 / 9 stages).
+    const bool narrow = S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC;
+    const bool deep = stream_trees && lw.stream_slots > AR_TREE_WIDE_SLOTS;
     lw.stream_trees = stream_trees;
-    lw.stream_tile = narrow ? kStreamTileNarrow : kStreamTileBytes;
+    lw.stream_tile = narrow ? kStreamTileNarrow : deep ? kStreamTileTree : kStreamTileBytes;
     lw.stream_stages =
         std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile - lw.stream_slots);
+    // Chains over 4-byte elements stream best with a short pipeline: with 7
+    // stages in flight per SM the reads crowd out the writes.  Measured at
+    // 256 MiB per rank, 3 stages against 7: fused ring +4% at P = 4 and 8,
+    // +7% at P = 6, within 2% either way at P = 2, 12 ... 64; the step rounds
+    // of every schedule at P = 8 up to +2%.  bf16 chains (more work per byte) and
+    // fp32 accumulation measured better with the full pipeline.
+    bool acc_streamed = false;
+    for (size_t k = 0; k < sets.size(); ++k)
+        if (stream[k] && !small[k])
+            for (auto& r : sets[k]) acc_streamed |= lw.progs[r.prog].kind == PK_ACC;
+    if (!stream_trees && !acc_streamed && es == 4) lw.stream_stages = std::min(lw.stream_stages, AR_CHAIN_STAGES_4B);
     // The TMA-store epilogue holds an item's last stage until its outputs are
     // copied out.  Measured at the bench size: it wins for copies (one input,
     // many outputs: the all-gather, +4-5%), for bf16 with few outputs and for
@@ -730,6 +749,127 @@ void lower(const Schedule& S, Lowered& lw) {
         lw.launches += ls.small ? 1 : (!ls.bulk.empty()) + (!ls.edge.empty());
         lw.sets.push_back(std::move(ls));
     }
+}
+
+std::vector<Window> host_windows(const LaunchSet& ls, int64_t n, uint64_t total_bytes) {
+    std::vector<Window> out;
+    const size_t nb = ls.bulk.size(), ne = ls.edge.size();
+    const uint64_t W = std::min<uint64_t>({total_bytes / (128ull << 20), 32, static_cast<uint64_t>(nb)});
+    if (W < 2) return out;
+    // suffix_lo[b]: the lowest start of items b.., prefix_hi: the highest end of items ..b-1
+    std::vector<int64_t> suffix_lo(nb + 1, n);
+    for (size_t b = nb; b-- > 0;) suffix_lo[b] = std::min(suffix_lo[b + 1], ls.bulk[b].elem);
+    std::vector<size_t> cuts(1, 0);
+    int64_t prefix_hi = 0;
+    size_t best = 0;  // the last valid cut seen
+    uint64_t w = 1;
+    for (size_t b = 0; b < nb && w < W; ++b) {
+        if (b > 0 && prefix_hi <= suffix_lo[b]) best = b;
+        while (w < W && b >= nb * w / W) {  // cut w is due at item nb w / W: take the last valid one
+            if (best > cuts.back()) cuts.push_back(best);
+            ++w;
+        }
+        prefix_hi = std::max(prefix_hi, ls.bulk[b].elem + static_cast<int64_t>(ls.bulk[b].count));
+    }
+    if (cuts.size() < 2) return out;
+    cuts.push_back(nb);
+    auto first_edge_at = [&](int64_t x) {
+        uint32_t k = 0;
+        while (k < ne && ls.edge[k].elem < x) ++k;
+        return k;
+    };
+    for (size_t k = 0; k + 1 < cuts.size(); ++k) {
+        Window win;
+        win.b0 = static_cast<uint32_t>(cuts[k]);
+        win.b1 = static_cast<uint32_t>(cuts[k + 1]);
+        win.lo = k == 0 ? 0 : suffix_lo[cuts[k]];
+        win.hi = k + 2 == cuts.size() ? n : suffix_lo[cuts[k + 1]];
+        win.e0 = k == 0 ? 0 : first_edge_at(win.lo);
+        win.e1 = k + 2 == cuts.size() ? static_cast<uint32_t>(ne) : first_edge_at(win.hi);
+        out.push_back(win);
+    }
+    // check: consecutive windows over [0, n), every item inside its window
+    bool ok = out.front().lo == 0 && out.back().hi == n && out.back().b1 == nb && out.back().e1 == ne;
+    for (size_t k = 0; k < out.size() && ok; ++k) {
+        const Window& x = out[k];
+        ok = x.lo < x.hi && x.b0 < x.b1 && x.e0 <= x.e1 && x.hi <= n &&
+             (k == 0 || (x.lo == out[k - 1].hi && x.b0 == out[k - 1].b1 && x.e0 == out[k - 1].e1));
+        for (uint32_t b = x.b0; b < x.b1 && ok; ++b)
+            ok = ls.bulk[b].elem >= x.lo && ls.bulk[b].elem + static_cast<int64_t>(ls.bulk[b].count) <= x.hi;
+        for (uint32_t b = x.e0; b < x.e1 && ok; ++b)
+            ok = ls.edge[b].elem >= x.lo && ls.edge[b].elem + static_cast<int64_t>(ls.edge[b].count) <= x.hi;
+    }
+    if (!ok) out.clear();
+    return out;
+}
+
+LoweringCheck check_lowering(const Lowered& L, int64_t n, int es, const std::vector<Window>& windows) {
+    LoweringCheck c;
+    using Span = std::pair<int64_t, int64_t>;
+    // sorted, merged spans; {-1, -1} marks an overlap
+    auto merged = [](std::vector<Span> v) {
+        std::sort(v.begin(), v.end());
+        std::vector<Span> m;
+        for (const Span& x : v) {
+            if (!m.empty() && m.back().second > x.first) return std::vector<Span>{{-1, -1}};
+            if (!m.empty() && m.back().second == x.first)
+                m.back().second = x.second;
+            else
+                m.push_back(x);
+        }
+        return m;
+    };
+    for (const LaunchSet& ls : L.sets) {
+        std::map<uint32_t, std::vector<Span>> want, got;
+        for (const WorkItem& w : ls.fallback) want[w.prog].push_back({w.elem, w.elem + w.count});
+        for (const WorkItem& w : ls.bulk) {
+            got[w.prog].push_back({w.elem, w.elem + w.count});
+            if (w.count == 0 || (w.elem * es) % 16 || (static_cast<int64_t>(w.count) * es) % 16) c.tiling_ok = false;
+        }
+        for (const WorkItem& w : ls.edge) got[w.prog].push_back({w.elem, w.elem + w.count});
+        c.items += ls.bulk.size() + ls.edge.size();
+        if (want.size() != got.size()) c.tiling_ok = false;
+        for (auto& kv : want) {
+            auto g = got.find(kv.first);
+            if (g == got.end() || merged(kv.second) != merged(g->second)) c.tiling_ok = false;
+        }
+        if (ls.stream && !ls.small && !ls.bulk.empty()) {
+            const size_t G = std::min<size_t>(152, ls.bulk.size());
+            std::vector<double> share(G, 0.0);
+            double total = 0;
+            for (size_t i = 0; i < ls.bulk.size(); ++i) {
+                const DevProg& d = L.progs[ls.bulk[i].prog];
+                const double b = static_cast<double>(d.n_in + d.n_out) * ls.bulk[i].count;
+                share[i % G] += b;
+                total += b;
+            }
+            c.wave_balance = std::max(c.wave_balance, *std::max_element(share.begin(), share.end()) / (total / G));
+        }
+    }
+    if (!windows.empty()) {
+        const LaunchSet& ls = L.sets.at(0);
+        std::vector<int> bulk_seen(ls.bulk.size(), 0), edge_seen(ls.edge.size(), 0);
+        int64_t at = 0;
+        for (const Window& w : windows) {
+            if (w.lo != at || w.hi <= w.lo || w.hi > n || w.b1 > ls.bulk.size() || w.e1 > ls.edge.size()) {
+                c.windows_ok = false;
+                break;
+            }
+            at = w.hi;
+            for (uint32_t b = w.b0; b < w.b1; ++b) {
+                ++bulk_seen[b];
+                if (ls.bulk[b].elem < w.lo || ls.bulk[b].elem + ls.bulk[b].count > w.hi) c.windows_ok = false;
+            }
+            for (uint32_t b = w.e0; b < w.e1; ++b) {
+                ++edge_seen[b];
+                if (ls.edge[b].elem < w.lo || ls.edge[b].elem + ls.edge[b].count > w.hi) c.windows_ok = false;
+            }
+        }
+        if (at != n) c.windows_ok = false;
+        for (int x : bulk_seen) c.windows_ok &= x == 1;
+        for (int x : edge_seen) c.windows_ok &= x == 1;
+    }
+    return c;
 }
 
 }  // namespace ar

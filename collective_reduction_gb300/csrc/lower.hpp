@@ -65,6 +65,36 @@ constexpr int kMaxStages = kBarrierBytes / 24;
 // Builds the fused pass (one set) or the rounds (one set per round).
 void lower(const Schedule& S, Lowered& out);
 
+// Element window of a fused pass for the pipelined host path: elements
+// [lo, hi) of every rank, bulk items [b0, b1) and edge items [e0, e1).
+struct Window {
+    int64_t lo, hi;
+    uint32_t b0, b1, e0, e1;
+};
+
+// About 128 MB of rank data per window, at most 32 windows, consecutive and
+// covering [0, n).  A window ends only between bulk items b - 1 and b where
+// every item before b ends at or before the start of every item from b on,
+// so each window's items lie inside its elements whatever the order of the
+// item list.  Every window is checked against the items before it is
+// returned; on any mismatch the result is empty and the host path runs as
+// one pass (a window's copies must never leave the rank buffers).
+std::vector<Window> host_windows(const LaunchSet& ls, int64_t n, uint64_t total_bytes);
+
+// Checks of a lowering that share no code with it: whether the bulk and edge
+// items of every set tile its ranges (taken from the set's whole-range
+// fallback items) program by program, bulk items 16-byte aligned; whether
+// the windows are consecutive over [0, n) with every item inside its
+// window; and the round-robin byte balance of the streamed sets over 152
+// CTAs (largest share / mean share).
+struct LoweringCheck {
+    bool tiling_ok = true;
+    bool windows_ok = true;
+    double wave_balance = 1.0;
+    uint64_t items = 0;
+};
+LoweringCheck check_lowering(const Lowered& L, int64_t n, int es, const std::vector<Window>& windows);
+
 // Dynamic shared memory the staged / rank-streaming kernels need.
 int staged_smem_bytes(const Lowered& lw);
 int stream_smem_bytes(const Lowered& lw);

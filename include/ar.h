@@ -249,6 +249,31 @@ ar_status ar_cost_select(int P, uint64_t n, ar_dtype dtype, ar_op op, const ar_c
  * compilation fails. */
 ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes);
 
+/* Host only: the work a plan with these parameters would launch, lowered as
+ * ar_plan_create lowers it (no device needed) and checked two ways, each by
+ * code apart from the lowering's own:
+ *   tiling_ok   every launch set's bulk and edge items tile its element
+ *               ranges exactly, program by program (no gap, no overlap), and
+ *               every bulk item is 16-byte aligned in offset and length;
+ *   windows_ok  the windows of the pipelined host path (ar_execute_host) are
+ *               consecutive over [0, n) and every item lies inside its
+ *               window's elements (1 when there are no windows).
+ * wave_balance: over the rank-streaming launch sets, the largest byte share
+ * one of 152 CTAs takes when the items are dealt round robin, over the mean
+ * share (1 = even).
+ * AR_ERR_INVALID_ARG on null arguments, AR_ERR_NOMEM. */
+typedef struct {
+    uint64_t items;          /* bulk + edge items over all launch sets          */
+    int launch_sets;         /* launch sets (one per round; one when fused)     */
+    int windows;             /* windows of the host path; 0: one pass           */
+    int tiling_ok;           /* 1 or 0, as above                                */
+    int windows_ok;          /* 1 or 0, as above                                */
+    double wave_balance;     /* >= 1, as above (1 with no streamed items)       */
+    int stream_tile_bytes;   /* rank tile of the rank-streaming kernel          */
+    int stream_stages;       /* its pipeline depth                              */
+} ar_lowering_info;
+ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out);
+
 /* ---- plans (need a CUDA device) -------------------------------------------
  * ar_plan_create compiles the schedule, lowers it to tile programs for the
  * chosen form and uploads them to the current device; it allocates the

@@ -158,6 +158,21 @@ def test_many_items_per_cta(P, dtype):
         assert normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) <= tol
 
 
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("P,n,algo,form,kw", [
+    (64, (1 << 20) + 7, "rh", "fused", {}),            # deep trees, 24 KB tiles, 1.1 waves of items
+    (16, (3 << 20) + 3, "rh", "step", {}),             # 2.5 waves per round
+    (5, (1 << 22) + 1, "ahc", "fused", {"group_sizes": [2, 3]}),
+    (12, 2_000_003, "generalized", "step", {"r": 2}),  # versioned cyclic rounds
+])
+def test_partial_last_wave(P, n, algo, form, kw, dtype):
+    """Sizes whose rank-streaming items end in a partial wave over the 152
+    SMs (some CTAs take one item more than others), deep trees on 24 KB tiles
+    and versioned rounds among them: full oracle comparison."""
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=P + 7)
+    check_faithful(bufs, dtype, "sum", algo, form, **kw)
+
+
 # ---- every (dtype, op) through a chain and a DAG program -------------------------------
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
@@ -301,6 +316,29 @@ def test_execute_host_pipelined_windows(order):
             for r in range(P):
                 assert normwise_rel_err(host[r].numpy(), ref) <= 1e-6
                 assert np.array_equal(host[r].numpy(), dev[r].cpu().numpy())
+    plan.close()
+
+
+@pytest.mark.parametrize("P,n,dtype,algo", [(64, 1 << 20, "float32", "rh"), (8, (1 << 24) + 3, "bfloat16", "ring")])
+def test_execute_host_windows_trees_and_bf16(P, n, dtype, algo):
+    """Windowed host path for a deep-tree plan (24 KB tiles) and a ragged
+    bf16 ring: every window's copies hold its items, so the results match
+    the oracle bit for bit."""
+    import torch
+    import collective_reduction_gb300 as ar
+    assert ar.Schedule(P, n, dtype, "sum", algo).lowering()["windows"] >= 2
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=P + 31)
+    tdt = torch.bfloat16 if dtype == "bfloat16" else torch.float32
+    host = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16).copy()).view(tdt).pin_memory()
+            if dtype == "bfloat16" else torch.from_numpy(b.copy()).pin_memory() for b in bufs]
+    dev = [torch.empty(n, dtype=tdt, device="cuda") for _ in range(P)]
+    plan = ar.Plan(P, n, dtype, "sum", algo)
+    plan.execute_host(host, dev)
+    plan.check()
+    want = oracle.run(algo, bufs, Arith("sum", dtype)).bufs
+    for r in range(P):
+        got = host[r].view(torch.int16).numpy().view(np.uint16) if dtype == "bfloat16" else host[r].numpy()
+        assert_bit_equal(got, want[r], dtype, f"host rank {r}")
     plan.close()
 
 

@@ -269,3 +269,83 @@ def test_jit_parameter_checked(lib):
 def test_selftest_timeout_range_checked_on_host(lib):
     assert lib.ar_selftest_bounded_wait(0, None) == 1
     assert lib.ar_selftest_bounded_wait(10001, None) == 1
+
+
+# ---- the lowering: work items and host-path windows -----------------------------------
+
+def _random_plans(count, seed):
+    rng = np.random.default_rng(seed)
+    algos = ["ring", "binomial", "rh", "rd", "hybrid", "generalized", "ahc", "pipeline"]
+    out = []
+    while len(out) < count:
+        P = int(rng.choice([2, 3, 4, 5, 7, 8, 12, 13, 16, 31, 32, 63, 64]))
+        n = int(rng.choice([rng.integers(1, 5000), rng.integers(1 << 18, 1 << 22), rng.integers(1 << 22, 1 << 25)]))
+        algo = str(rng.choice(algos))
+        dtype = str(rng.choice(["int32", "float32", "bfloat16"]))
+        kw = {"form": str(rng.choice(["fused", "step"]))}
+        if algo == "generalized":
+            kw["r"] = int(rng.integers(0, ceil_log2(P) + 1))
+        if algo == "hybrid":
+            kw["k1"] = int(rng.integers(0, ceil_log2(P) + 1))
+        if algo == "ahc":
+            kw["group_sizes"] = [P // 2, P - P // 2] if P >= 4 else [P]
+        if algo == "pipeline":
+            kw["blocks"] = int(rng.integers(1, 9))
+        if kw["form"] == "fused" and rng.random() < 0.3:
+            kw["order"] = "fp32acc"
+        try:
+            s = ar.Schedule(P, n, dtype, "sum", algo, **kw)
+        except RuntimeError:
+            continue  # a combination the compiler rejects (e.g. RH at P != 2^k)
+        out.append(((P, n, dtype, algo, kw), s))
+    return out
+
+
+def test_lowering_tiles_every_range_and_windows_hold_their_items(lib):
+    """For random plans (sizes from a few elements to 2^25, every schedule,
+    both forms), the work items the kernels would run cover every element
+    range exactly once per program, and the host path's windows are
+    consecutive and contain their items — checked by code apart from the
+    lowering."""
+    for args, s in _random_plans(160, seed=11):
+        low = s.lowering()
+        assert low["tiling_ok"] == 1, args
+        assert low["windows_ok"] == 1, args
+        assert low["wave_balance"] >= 1.0
+        s.close()
+
+
+def test_wave_balance_closed_form(lib):
+    """Round robin over 152 CTAs: P = 64 x 2^23 fp32 ring has 64 chunks of
+    2^17 elements, 16 whole 32 KB tiles each, 1024 equal items: 112 CTAs take
+    7 and 40 take 6, so the largest share over the mean is 7 / (1024 / 152).
+    P = 8 x 2^26 has 8192 items: 54 / (8192 / 152).  Windows: 2 GiB of rank
+    data makes 16 windows of 128 MB."""
+    low = ar.Schedule(64, 1 << 23, "float32", "sum", "ring").lowering()
+    assert low["items"] == 1024 and low["windows"] == 16
+    assert abs(low["wave_balance"] - 7 / (1024 / 152)) < 1e-9
+    low = ar.Schedule(8, 1 << 26, "float32", "sum", "ring").lowering()
+    assert low["items"] == 8192 and low["windows"] == 16
+    assert abs(low["wave_balance"] - 54 / (8192 / 152)) < 1e-9
+
+
+def test_stream_geometry_follows_the_programs(lib):
+    """Pipeline depth and rank tile as the lowering picks them: 3 stages of
+    32 KB for chains over 4-byte elements, the full 7 for bf16 chains, 24 KB
+    tiles for trees deeper than 16 leaves, 16 KB tiles for bf16 fp32
+    accumulation."""
+    def geo(P, dtype, algo, **kw):
+        low = ar.Schedule(P, P * (1 << 16), dtype, "sum", algo, **kw).lowering()
+        return low["stream_tile_bytes"], low["stream_stages"]
+    assert geo(8, "float32", "ring") == (32768, 3)
+    assert geo(8, "int32", "ring") == (32768, 3)
+    assert geo(8, "bfloat16", "ring") == (32768, 7)
+    assert geo(8, "float32", "rh") == (32768, 4)        # 3 stack tiles + 4 stages
+    assert geo(64, "float32", "rh") == (24576, 3)       # 6 stack tiles + 3 stages
+    assert geo(32, "bfloat16", "binomial") == (24576, 4)
+    assert geo(8, "bfloat16", "ring", order="fp32acc") == (16384, 14)
+    assert geo(8, "float32", "ring", order="fp32acc")[1] == 7
+
+
+def test_lowering_null_checks(lib):
+    assert lib.ar_schedule_lowering(None, None) == 1
