@@ -29,10 +29,14 @@
 #define AR_TREE_WIDE_SLOTS 4
 #endif
 
-// Pipeline depth of the rank-streaming kernel for chains over 4-byte
-// elements (the others use as many stages as shared memory holds).
+// Pipeline depth of the rank-streaming kernel for chains and for fp32
+// accumulation over 4-byte elements (the others use as many stages as
+// shared memory holds).
 #ifndef AR_CHAIN_STAGES_4B
 #define AR_CHAIN_STAGES_4B 3
+#endif
+#ifndef AR_ACC_STAGES_4B
+#define AR_ACC_STAGES_4B 5
 #endif
 
 namespace ar {
@@ -697,13 +701,15 @@ void lower(const Schedule& S, Lowered& lw) {
     // stages in flight per SM the reads crowd out the writes.  Measured at
     // 256 MiB per rank, 3 stages against 7: fused ring +4% at P = 4 and 8,
     // +7% at P = 6, within 2% either way at P = 2, 12 ... 64; the step rounds
-    // of every schedule at P = 8 up to +2%.  bf16 chains (more work per byte) and
-    // fp32 accumulation measured better with the full pipeline.
+    // of every schedule at P = 8 up to +2%.  bf16 chains (more work per byte)
+    // measured better with the full pipeline.  fp32 accumulation (fp32 and
+    // int32 elements) peaks at 5 stages: +4% over 7 at P = 8, equal at 64.
     bool acc_streamed = false;
     for (size_t k = 0; k < sets.size(); ++k)
         if (stream[k] && !small[k])
             for (auto& r : sets[k]) acc_streamed |= lw.progs[r.prog].kind == PK_ACC;
-    if (!stream_trees && !acc_streamed && es == 4) lw.stream_stages = std::min(lw.stream_stages, AR_CHAIN_STAGES_4B);
+    if (!stream_trees && es == 4)
+        lw.stream_stages = std::min(lw.stream_stages, acc_streamed ? AR_ACC_STAGES_4B : AR_CHAIN_STAGES_4B);
     // The TMA-store epilogue holds an item's last stage until its outputs are
     // copied out.  Measured at the bench size: it wins for copies (one input,
     // many outputs: the all-gather, +4-5%), for bf16 with few outputs and for

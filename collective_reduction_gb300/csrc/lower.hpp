@@ -42,15 +42,18 @@ struct Lowered {
 };
 
 // Staged-kernel geometry shared by lowering and launch: shared-memory budget
-// per CTA, largest input tile, pipeline depth.
+// per CTA (the GB300 opt-in maximum), largest input tile, pipeline depth.
+// Measured on the run-time compiled DAG kernels at 256 MiB per rank, 4
+// stages in 227 KB against 3 in 200 KB: P = 7 generalized r = 1 / r = 3
+// +3% / +4% fp32, r = 1 bf16 and RD max bf16 at P = 8 +2%.
 #ifndef AR_SMEM_BUDGET
-#define AR_SMEM_BUDGET (200 * 1024)
+#define AR_SMEM_BUDGET (227 * 1024)
 #endif
 #ifndef AR_MAX_TILE
 #define AR_MAX_TILE kMaxStagedTile
 #endif
 #ifndef AR_STAGES
-#define AR_STAGES 3
+#define AR_STAGES 4
 #endif
 constexpr int kSmemBudget = AR_SMEM_BUDGET;
 constexpr int kMaxTileBytes = AR_MAX_TILE;
