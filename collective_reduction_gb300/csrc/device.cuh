@@ -47,18 +47,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return d;
 }
 
+// Two bf16 sums (products) in one instruction, each the exact result rounded
+// once to bf16, nearest even, subnormals kept.  That is bit for bit the
+// element op's definition (computed in fp32, then rounded to bf16): a
+// result rounded to nearest in a format of p' >= 2p + 2 significand bits and
+// then to nearest in p bits equals the direct rounding for +, -, x, / and
+// square root (Figueroa, "When is double rounding innocuous?", 1995), and
+// fp32 carries 24 >= 2 * 8 + 2 bits over the same exponent range as bf16.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // a (+) b on one 32-bit word: one int32 / fp32 element or two bf16 elements
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t wop(uint32_t a, uint32_t b) {
     if (DT == AR_INT32) return static_cast<uint32_t>(iop<OP>(static_cast<int32_t>(a), static_cast<int32_t>(b)));
     if (DT == AR_FLOAT32) return __float_as_uint(fop<OP>(__uint_as_float(a), __uint_as_float(b)));
+    if (OP == AR_SUM) return add_bf16x2(a, b);
+    if (OP == AR_PROD) return mul_bf16x2(a, b);
     const float al = bf_lo(a), ah = bf_hi(a), bl = bf_lo(b), bh = bf_hi(b);
-    if (OP == AR_MAX || OP == AR_MIN) {
-        const bool pl = OP == AR_MAX ? al > bl : al < bl;
-        const bool ph = OP == AR_MAX ? ah > bh : ah < bh;
-        return ((pl ? a : b) & 0xFFFFu) | ((ph ? a : b) & 0xFFFF0000u);
-    }
-    return pack_bf16x2(fop<OP>(al, bl), fop<OP>(ah, bh));
+    const bool pl = OP == AR_MAX ? al > bl : al < bl;
+    const bool ph = OP == AR_MAX ? ah > bh : ah < bh;
+    return ((pl ? a : b) & 0xFFFFu) | ((ph ? a : b) & 0xFFFF0000u);
 }
 
 template <int DT, int OP>

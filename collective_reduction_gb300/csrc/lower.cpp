@@ -38,6 +38,10 @@
 #ifndef AR_ACC_STAGES_4B
 #define AR_ACC_STAGES_4B 5
 #endif
+// ... and for bf16 sum / product chains (single bf16x2 instructions)
+#ifndef AR_CHAIN_STAGES_BF16
+#define AR_CHAIN_STAGES_BF16 4
+#endif
 
 namespace ar {
 namespace {
@@ -701,15 +705,21 @@ void lower(const Schedule& S, Lowered& lw) {
     // stages in flight per SM the reads crowd out the writes.  Measured at
     // 256 MiB per rank, 3 stages against 7: fused ring +4% at P = 4 and 8,
     // +7% at P = 6, within 2% either way at P = 2, 12 ... 64; the step rounds
-    // of every schedule at P = 8 up to +2%.  bf16 chains (more work per byte)
-    // measured better with the full pipeline.  fp32 accumulation (fp32 and
+    // of every schedule at P = 8 up to +2%.  fp32 accumulation (fp32 and
     // int32 elements) peaks at 5 stages: +4% over 7 at P = 8, equal at 64.
+    // bf16 sum and product chains, one bf16x2 instruction per element pair,
+    // peak at 4: against 7, fused ring +1% at P = 8, +3% at P = 16 and 64,
+    // step rounds +1%, the reduce-scatter +5%; bf16 max / min chains (more
+    // work per byte) and bf16 fp32 accumulation keep the full pipeline.
     bool acc_streamed = false;
     for (size_t k = 0; k < sets.size(); ++k)
         if (stream[k] && !small[k])
             for (auto& r : sets[k]) acc_streamed |= lw.progs[r.prog].kind == PK_ACC;
     if (!stream_trees && es == 4)
         lw.stream_stages = std::min(lw.stream_stages, acc_streamed ? AR_ACC_STAGES_4B : AR_CHAIN_STAGES_4B);
+    const bool bf16_arith = S.op == AR_SUM || S.op == AR_PROD || S.op == AR_AVG;
+    if (!stream_trees && es == 2 && !acc_streamed && bf16_arith)
+        lw.stream_stages = std::min(lw.stream_stages, AR_CHAIN_STAGES_BF16);
     // The TMA-store epilogue holds an item's last stage until its outputs are
     // copied out.  Measured at the bench size: it wins for copies (one input,
     // many outputs: the all-gather, +4-5%), for bf16 with few outputs and for
