@@ -65,6 +65,23 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// bf16 max (min) on two pairs: per element a > b ? a : b (a < b ? a : b),
+// the comparison one ordered bf16x2 compare, like the fp32 one: false when
+// either value is NaN, +0 and -0 equal, subnormals compared exactly.
+template <int OP>
+__device__ __forceinline__ uint32_t select_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t lo, hi;
+    if (OP == AR_MAX)
+        asm("{\n\t.reg .pred p, q;\n\tsetp.gt.bf16x2 p|q, %2, %3;\n\t"
+            "selp.b32 %0, %2, %3, p;\n\tselp.b32 %1, %2, %3, q;\n\t}"
+            : "=r"(lo), "=r"(hi) : "r"(a), "r"(b));
+    else
+        asm("{\n\t.reg .pred p, q;\n\tsetp.lt.bf16x2 p|q, %2, %3;\n\t"
+            "selp.b32 %0, %2, %3, p;\n\tselp.b32 %1, %2, %3, q;\n\t}"
+            : "=r"(lo), "=r"(hi) : "r"(a), "r"(b));
+    return (lo & 0xFFFFu) | (hi & 0xFFFF0000u);
+}
+
 // a (+) b on one 32-bit word: one int32 / fp32 element or two bf16 elements
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t wop(uint32_t a, uint32_t b) {
@@ -72,10 +89,7 @@ __device__ __forceinline__ uint32_t wop(uint32_t a, uint32_t b) {
     if (DT == AR_FLOAT32) return __float_as_uint(fop<OP>(__uint_as_float(a), __uint_as_float(b)));
     if (OP == AR_SUM) return add_bf16x2(a, b);
     if (OP == AR_PROD) return mul_bf16x2(a, b);
-    const float al = bf_lo(a), ah = bf_hi(a), bl = bf_lo(b), bh = bf_hi(b);
-    const bool pl = OP == AR_MAX ? al > bl : al < bl;
-    const bool ph = OP == AR_MAX ? ah > bh : ah < bh;
-    return ((pl ? a : b) & 0xFFFFu) | ((ph ? a : b) & 0xFFFF0000u);
+    return select_bf16x2<OP>(a, b);
 }
 
 template <int DT, int OP>

@@ -688,14 +688,18 @@ void lower(const Schedule& S, Lowered& lw) {
     t = std::min<int64_t>(t, kMaxTileBytes);
     t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
     lw.tile_bytes = static_cast<int>(t);
-    // bf16 fp32 accumulation holds 16 fp32 per vector: 16 KB rank tiles (4
-    // vectors per thread).  A tree keeps depth - 1 stack tiles in shared
+    // bf16 fp32 accumulation programs hold 16 fp32 per vector: 16 KB rank
+    // tiles (4 vectors per thread).  A tree keeps depth - 1 stack tiles in shared
     // memory next to the stages: 32 KB tiles while that leaves a pipeline of
     // at least 3 stages (trees of up to 16 leaves; measured +6% at P = 16 over
     // 16 KB tiles), 24 KB tiles for deeper trees (3 stages at 64 leaves, 4 at
     // 32; measured +7% / +12% fp32 and +10% / +11% bf16 at P = 64 / 32 over
     // 16 KB tiles with 8 / 9 stages).
-    const bool narrow = S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC;
+    bool acc_streamed = false;
+    for (size_t k = 0; k < sets.size(); ++k)
+        if (stream[k] && !small[k])
+            for (auto& r : sets[k]) acc_streamed |= lw.progs[r.prog].kind == PK_ACC;
+    const bool narrow = S.dtype == AR_BFLOAT16 && acc_streamed;
     const bool deep = stream_trees && lw.stream_slots > AR_TREE_WIDE_SLOTS;
     lw.stream_trees = stream_trees;
     lw.stream_tile = narrow ? kStreamTileNarrow : deep ? kStreamTileTree : kStreamTileBytes;
@@ -711,10 +715,6 @@ void lower(const Schedule& S, Lowered& lw) {
     // peak at 4: against 7, fused ring +1% at P = 8, +3% at P = 16 and 64,
     // step rounds +1%, the reduce-scatter +5%; bf16 max / min chains (more
     // work per byte) and bf16 fp32 accumulation keep the full pipeline.
-    bool acc_streamed = false;
-    for (size_t k = 0; k < sets.size(); ++k)
-        if (stream[k] && !small[k])
-            for (auto& r : sets[k]) acc_streamed |= lw.progs[r.prog].kind == PK_ACC;
     if (!stream_trees && es == 4)
         lw.stream_stages = std::min(lw.stream_stages, acc_streamed ? AR_ACC_STAGES_4B : AR_CHAIN_STAGES_4B);
     const bool bf16_arith = S.op == AR_SUM || S.op == AR_PROD || S.op == AR_AVG;
@@ -736,7 +736,7 @@ void lower(const Schedule& S, Lowered& lw) {
             }
     const bool few_out = max_out <= AR_TMA_STORE_MAX_OUT;
     lw.stream_tma_store = max_in_stream <= 1 || (few_out && (S.dtype == AR_BFLOAT16 || max_in_stream <= 4)) ||
-                          (S.dtype == AR_BFLOAT16 && S.params.order == AR_ORDER_FP32ACC);
+                          (S.dtype == AR_BFLOAT16 && acc_streamed);
     for (size_t k = 0; k < sets.size(); ++k) {
         LaunchSet ls;
         ls.stream = stream[k];

@@ -217,7 +217,7 @@ def test_bf16_rounding_edge_grid():
         check_faithful([x, y], "bfloat16", op, "ring", "step")
 
 
-@pytest.mark.parametrize("op", ["sum", "prod"])
+@pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
 @pytest.mark.parametrize("P,algo,kw", [(3, "ring", {}), (4, "rd", {}), (5, "generalized", {"r": 2}),
                                        (8, "rh", {}), (2, "ring", {})])
 def test_bf16_every_bit_pattern_class(P, algo, kw, op):
@@ -225,7 +225,8 @@ def test_bf16_every_bit_pattern_class(P, algo, kw, op):
     NaN bf16 values of both signs) through the rank-streaming kernel's chains
     and trees and a DAG program, fused and step: bf16 sums and products are
     single bf16x2 instructions there, and must give the element op's bits
-    (fp32 result rounded to bf16) everywhere."""
+    (fp32 result rounded to bf16) everywhere; max / min take one bf16x2
+    compare and must select as a > b ? a : b (a < b ? a : b) does."""
     n = 300_007
     rng = np.random.default_rng(1000 + P)
     bufs = [rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16) for _ in range(P)]

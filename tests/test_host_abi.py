@@ -346,6 +346,8 @@ def test_stream_geometry_follows_the_programs(lib):
     assert geo(64, "float32", "rh") == (24576, 3)       # 6 stack tiles + 3 stages
     assert geo(32, "bfloat16", "binomial") == (24576, 4)
     assert geo(8, "bfloat16", "ring", order="fp32acc") == (16384, 14)
+    # P = 2: the fp32 accumulation of a sum is the one faithful combine
+    assert geo(2, "bfloat16", "ring", order="fp32acc") == (32768, 4)
     assert geo(8, "float32", "ring", order="fp32acc") == (32768, 5)
 
 
