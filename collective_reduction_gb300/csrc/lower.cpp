@@ -38,7 +38,7 @@
 #ifndef AR_ACC_STAGES_4B
 #define AR_ACC_STAGES_4B 5
 #endif
-// ... and for bf16 sum / product chains (single bf16x2 instructions)
+// ... and for bf16 chains (one bf16x2 instruction per element pair)
 #ifndef AR_CHAIN_STAGES_BF16
 #define AR_CHAIN_STAGES_BF16 4
 #endif
@@ -711,15 +711,13 @@ void lower(const Schedule& S, Lowered& lw) {
     // +7% at P = 6, within 2% either way at P = 2, 12 ... 64; the step rounds
     // of every schedule at P = 8 up to +2%.  fp32 accumulation (fp32 and
     // int32 elements) peaks at 5 stages: +4% over 7 at P = 8, equal at 64.
-    // bf16 sum and product chains, one bf16x2 instruction per element pair,
-    // peak at 4: against 7, fused ring +1% at P = 8, +3% at P = 16 and 64,
-    // step rounds +1%, the reduce-scatter +5%; bf16 max / min chains (more
-    // work per byte) and bf16 fp32 accumulation keep the full pipeline.
+    // bf16 chains, one bf16x2 instruction (or compare) per element pair,
+    // peak at 4: against 7, sum fused ring +1% at P = 8, +3% at P = 16 and
+    // 64, step rounds +1%, the reduce-scatter +5%; max / min +3-4%.  bf16
+    // fp32 accumulation keeps the full pipeline.
     if (!stream_trees && es == 4)
         lw.stream_stages = std::min(lw.stream_stages, acc_streamed ? AR_ACC_STAGES_4B : AR_CHAIN_STAGES_4B);
-    const bool bf16_arith = S.op == AR_SUM || S.op == AR_PROD || S.op == AR_AVG;
-    if (!stream_trees && es == 2 && !acc_streamed && bf16_arith)
-        lw.stream_stages = std::min(lw.stream_stages, AR_CHAIN_STAGES_BF16);
+    if (!stream_trees && es == 2 && !acc_streamed) lw.stream_stages = std::min(lw.stream_stages, AR_CHAIN_STAGES_BF16);
     // The TMA-store epilogue holds an item's last stage until its outputs are
     // copied out.  Measured at the bench size: it wins for copies (one input,
     // many outputs: the all-gather, +4-5%), for bf16 with few outputs and for

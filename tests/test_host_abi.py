@@ -332,16 +332,15 @@ def test_wave_balance_closed_form(lib):
 def test_stream_geometry_follows_the_programs(lib):
     """Pipeline depth and rank tile as the lowering picks them: 3 stages of
     32 KB for chains over 4-byte elements, 5 for their fp32 accumulation, 4
-    for bf16 sum / product chains, the full 7 for bf16 max / min chains, 24 KB
-    tiles for trees deeper than 16 leaves, 16 KB tiles for bf16 fp32
-    accumulation."""
+    for bf16 chains, 24 KB tiles for trees deeper than 16 leaves, 16 KB tiles
+    (14 stages) for bf16 fp32 accumulation."""
     def geo(P, dtype, algo, op="sum", **kw):
         low = ar.Schedule(P, P * (1 << 16), dtype, op, algo, **kw).lowering()
         return low["stream_tile_bytes"], low["stream_stages"]
     assert geo(8, "float32", "ring") == (32768, 3)
     assert geo(8, "int32", "ring") == (32768, 3)
     assert geo(8, "bfloat16", "ring") == (32768, 4)
-    assert geo(8, "bfloat16", "ring", op="max") == (32768, 7)
+    assert geo(8, "bfloat16", "ring", op="max") == (32768, 4)
     assert geo(8, "float32", "rh") == (32768, 4)        # 3 stack tiles + 4 stages
     assert geo(64, "float32", "rh") == (24576, 3)       # 6 stack tiles + 3 stages
     assert geo(32, "bfloat16", "binomial") == (24576, 4)
