@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--order", default="faithful")
     ap.add_argument("--r", type=int, default=0)
     ap.add_argument("--k1", type=int, default=0)
+    ap.add_argument("--phase", default="allreduce", choices=["allreduce", "reduce_scatter", "all_gather"],
+                    help="the whole allreduce, or one half (ring, rh, generalized r = 0)")
     ap.add_argument("--jit", default="auto", choices=["auto", "on", "off"],
                     help="DAG programs as run-time compiled code (auto / on) or interpreted (off)")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -81,7 +83,8 @@ def esize(dtype):
 def workload_name(a):
     return (f"{a.algo} allreduce, {a.form} {a.order}, P={a.P} x {a.mib:g} MiB {a.dtype} per rank, "
             f"op={a.op}" + (f", r={a.r}" if a.algo == "generalized" else "")
-            + (f", k1={a.k1}" if a.algo == "hybrid" else ""))
+            + (f", k1={a.k1}" if a.algo == "hybrid" else "")
+            + (f", phase={a.phase}" if a.phase != "allreduce" else ""))
 
 
 def dtype_tag(dtype):
@@ -311,7 +314,10 @@ def split_sample(sample, P, parts):
 
 
 def oracle_kw(a):
-    return {"r": a.r} if a.algo == "generalized" else ({"k1": a.k1} if a.algo == "hybrid" else {})
+    kw = {"r": a.r} if a.algo == "generalized" else ({"k1": a.k1} if a.algo == "hybrid" else {})
+    if a.phase != "allreduce":
+        kw["phase"] = a.phase
+    return kw
 
 
 def cpu_baseline_and_check(a, sample_in, sample_out_engine, parts):
@@ -333,7 +339,12 @@ def cpu_baseline_and_check(a, sample_in, sample_out_engine, parts):
         def bits(x):
             x = np.ascontiguousarray(x)
             return x if x.dtype == np.uint16 else x.view(np.uint32)
-        ok = all(np.array_equal(bits(res.bufs[r]), bits(outs[0][r])) for r in range(a.P))
+        if a.phase == "reduce_scatter":
+            # only the owners' chunks are defined after a reduce-scatter
+            ok = all(np.array_equal(bits(res.bufs[r][lo:hi]), bits(outs[0][r][lo:hi]))
+                     for r, lo, hi in res.info["owner"])
+        else:
+            ok = all(np.array_equal(bits(res.bufs[r]), bits(outs[0][r])) for r in range(a.P))
     half = a.cpu_seconds / 2
     nbytes = a.P * subs[0][0].size * esize(a.dtype)
     runs1, dt1 = oracle_repeat((a.algo, kw, a.op, a.dtype, subs[0], half))
@@ -360,6 +371,8 @@ def run_ours(a):
     n = int(a.mib * (1 << 20)) // es
     S = n * es
     params = dict(form=a.form, order=a.order, jit=a.jit)
+    if a.phase != "allreduce":
+        params["phase"] = a.phase
     if a.algo == "generalized":
         params["r"] = a.r
     if a.algo == "hybrid":
@@ -452,7 +465,7 @@ def run_ours(a):
         "dtype": dtype_tag(a.dtype),
         "data": "synthetic",
         "config": {"workload": workload_name(a), "P": a.P, "bytes_per_rank": S, "elements_per_rank": n,
-                   "algo": a.algo, "form": a.form, "order": a.order, "op": a.op,
+                   "algo": a.algo, "form": a.form, "order": a.order, "op": a.op, "phase": a.phase,
                    "l2": "inputs larger than L2 (P x S = %.1f GiB vs 129 MB)" % (a.P * S / 2 ** 30),
                    "busbw_GBps": round(busbw_gbps(S, total_ms / a.steps / 1e3, a.P), 2),
                    "algbw_GBps": round(S / (total_ms / a.steps / 1e3) / 1e9, 2),
@@ -530,7 +543,7 @@ def run_reference(a):
         "warmup": a.warmup, "ms_per_step": round(total / a.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype_tag(a.dtype), "data": "synthetic",
         "config": {"workload": workload_name(a), "P": a.P, "bytes_per_rank": int(a.mib * (1 << 20)),
-                   "algo": a.algo, "form": a.form, "order": a.order, "op": a.op,
+                   "algo": a.algo, "form": a.form, "order": a.order, "op": a.op, "phase": a.phase,
                    "sample_elements_per_rank": n},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "cpu_model": cpu_model(),
