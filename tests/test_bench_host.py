@@ -58,3 +58,24 @@ def test_busbw_matches_worked_examples(golden):
         t = 2 * (c["N"] - 1) / c["N"] * c["S_bytes"] / c["busbw_Bps"]
         assert t == pytest.approx(c["time_s_about"], rel=c["rel_tol"])
         assert bench.busbw_gbps(c["S_bytes"], t, c["N"]) == pytest.approx(c["busbw_Bps"] / 1e9)
+
+
+def test_phase_option_reaches_the_oracle_and_the_workload_name():
+    """`--phase` runs one half: the oracle gets the same phase (and the
+    schedule's own parameters), the workload name says which half."""
+    import sys
+    argv = sys.argv
+    try:
+        sys.argv = ["bench.py", "--phase", "reduce_scatter", "--algo", "generalized", "--r", "0"]
+        a = bench.parse()
+    finally:
+        sys.argv = argv
+    assert bench.oracle_kw(a) == {"r": 0, "phase": "reduce_scatter"}
+    assert bench.workload_name(a).endswith("r=0, phase=reduce_scatter")
+    sys.argv = ["bench.py"]
+    try:
+        a = bench.parse()
+    finally:
+        sys.argv = argv
+    assert a.phase == "allreduce" and bench.oracle_kw(a) == {}
+    assert "phase" not in bench.workload_name(a)
