@@ -51,13 +51,14 @@ __global__ void __launch_bounds__(kStagedThreads, 1) staged_kernel(const __grid_
 
 // ---------------------------------------------------- rank-streaming kernel
 //
-// For programs that are a chain or an fp32 accumulation (the ring's fused
-// pass and rounds, every FP32ACC pass) the inputs are consumed strictly in
-// order, so an item's tiles need not be resident together: the producer
-// streams one rank tile (kStreamVpt vectors per consumer thread) per stage
-// through a deep ring of stages, and each consumer thread keeps its vectors'
-// accumulators in registers across the item's inputs.  Tile size and thread
-// utilisation no longer shrink with P.
+// For programs that are a chain, a single tree or an fp32 accumulation (the
+// ring's fused pass and rounds, the fused trees of the other schedules,
+// every FP32ACC pass) the inputs are consumed strictly in order, so an
+// item's tiles need not be resident together: the producer streams one rank
+// tile (VPT vectors per consumer thread) per stage through a ring of stages
+// (as many as the lowering asks for), and each consumer thread keeps its
+// vectors' accumulators in registers across the item's inputs.  Tile size
+// and thread utilisation do not shrink with P.
 
 template <int ES>
 __device__ void stream_produce(const KernelArgs& a, const Stage& sm) {
