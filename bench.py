@@ -623,8 +623,6 @@ def run_sweep(a, path):
                     n = S // esize(dtype)
                     dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
                     for form, order in (("fused", "faithful"), ("fused", "fp32acc"), ("step", "faithful")):
-                        if form == "step" and S > (1 << 26) and P == 64:
-                            continue
                         plan = ar.Plan(P, n, dtype, "sum", "ring", form=form, order=order)
                         info = plan.info()
                         fresh = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P + 1)
