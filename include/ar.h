@@ -170,7 +170,8 @@ typedef struct {
 
 /* ar_plan_info.kernels bits: the rank-streaming kernel (chains, single trees,
  * fp32 accumulation), the staged kernel (DAG programs), the element-wise
- * kernel (unaligned edges and tiny passes). */
+ * kernel (unaligned edges and tiny passes), and DAG_JIT when the staged
+ * launches run the plan's run-time compiled DAG kernel. */
 enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4, AR_KERNEL_DAG_JIT = 8 };
 
 typedef struct ar_schedule_s* ar_schedule_t;
@@ -292,8 +293,8 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info);
  * to the element size (AR_ERR_INVALID_ARG otherwise).  With n = 0 the call
  * is a no-op and the pointers are not inspected.  Every buffer is both input
  * and output.
- * 16-byte aligned buffers use the staged kernels; any other alignment is
- * valid and takes a slower element-wise path.  Executes of one plan must be
+ * 16-byte aligned buffers use the tiled kernels (rank-streaming, staged); any
+ * other alignment is valid and takes a slower element-wise path.  Executes of one plan must be
  * ordered on one stream (they share the plan's scratch).  The launch itself
  * is checked (AR_ERR_CUDA); kernel-side failures are reported by
  * ar_plan_check. */
