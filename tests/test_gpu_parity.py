@@ -266,6 +266,32 @@ def test_unaligned_buffers_take_elementwise_path():
         plan.close()
 
 
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+@pytest.mark.parametrize("P,algo,kw", [(5, "ring", {}), (8, "ring", {}), (64, "ring", {}),
+                                       (5, "ahc", {"group_sizes": [2, 3]})])
+def test_fp32acc_same_bits_in_every_kernel(P, algo, kw, dtype):
+    """The fp32-accumulate order is the engine's own and the same in every
+    kernel: the rank-streaming kernel (bf16 on 16 KB tiles, fp32 on 32 KB)
+    must give exactly the bits of the element-wise kernel, which unaligned
+    buffers take."""
+    import torch
+    import collective_reduction_gb300 as ar
+    n = 300_007
+    bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=P + 3)
+    fast = engine(bufs, dtype, "sum", algo, order="fp32acc", **kw)
+    tdt = torch.bfloat16 if dtype == "bfloat16" else torch.float32
+    big = [torch.zeros(n + 1, dtype=tdt, device="cuda") for _ in range(P)]
+    views = [big[r][1:] for r in range(P)]  # one element off: not 16-byte aligned
+    for r in range(P):
+        views[r].copy_(to_dev(bufs[r], dtype))
+    plan = ar.Plan(P, n, dtype, "sum", algo, order="fp32acc", **kw)
+    plan.execute(views)
+    plan.check()
+    for r in range(P):
+        assert_bit_equal(to_host(views[r], dtype), fast[r], dtype, f"{algo} P={P} rank {r}")
+    plan.close()
+
+
 @pytest.mark.parametrize("form", FORMS)
 def test_p64_latency_optimal_max(form):
     """P = 64, r = ceil(log2 P): a rank-specific tree per rank (max keeps the
