@@ -385,6 +385,32 @@ def test_execute_host_windows_trees_and_bf16(P, n, dtype, algo):
     plan.close()
 
 
+@pytest.mark.parametrize("algo,phase", [("ring", "reduce_scatter"), ("ring", "all_gather"),
+                                         ("rh", "reduce_scatter")])
+def test_execute_host_windows_for_the_halves(algo, phase):
+    """The windowed host path for one half of the allreduce: a fused
+    reduce-scatter writes only the owners' chunks (the rest come back as they
+    went in), an all-gather every non-owner's."""
+    import torch
+    import collective_reduction_gb300 as ar
+    P, n = 8, (1 << 23) + 5
+    assert ar.Schedule(P, n, "float32", "sum", algo, phase=phase).lowering()["windows"] >= 2
+    bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2, seed=17)
+    host = [torch.from_numpy(b.copy()).pin_memory() for b in bufs]
+    dev = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(P)]
+    plan = ar.Plan(P, n, "float32", "sum", algo, phase=phase)
+    plan.execute_host(host, dev)
+    plan.check()
+    want = oracle.run(algo, bufs, Arith("sum", "float32"), phase=phase)
+    if phase == "reduce_scatter":
+        for r, lo, hi in want.info["owner"]:
+            assert_bit_equal(host[r].numpy()[lo:hi], want.bufs[r][lo:hi], "float32", f"owner {r}")
+    else:
+        for r in range(P):
+            assert_bit_equal(host[r].numpy(), want.bufs[r], "float32", f"host rank {r}")
+    plan.close()
+
+
 def test_repeated_execute_and_streams():
     """Back-to-back executes on a side stream, then on the default stream."""
     import torch
