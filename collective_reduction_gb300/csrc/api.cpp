@@ -50,6 +50,7 @@ struct ar_plan_s {
         uint32_t n_bulk, n_edge, n_fallback;
         bool stream;
         bool small;
+        bool tma_store;
     };
     std::vector<Set> sets;
     // element windows of a fused plan for the pipelined host path
@@ -161,7 +162,7 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
         if (s.stream) {
             a.tile_bytes = plan->L.stream_tile;
             a.stages = plan->L.stream_stages;
-            a.flags = (plan->L.stream_tma_store ? ar::kArgTmaStore : 0) | (plan->L.stream_trees ? ar::kArgTrees : 0);
+            a.flags = (s.tma_store ? ar::kArgTmaStore : 0) | (plan->L.stream_trees ? ar::kArgTrees : 0);
             a.max_in = 1;
             a.max_tmp = plan->L.stream_slots;  // tree stack tiles after the stages
             e = ar::launch_stream(S.dtype, S.op, a, grid, plan->smem_stream, st);
@@ -407,6 +408,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             s.n_fallback = static_cast<uint32_t>(L.sets[i].fallback.size());
             s.stream = L.sets[i].stream;
             s.small = L.sets[i].small;
+            s.tma_store = L.sets[i].tma_store;
             p->sets.push_back(s);
         }
         make_windows(p);

@@ -719,25 +719,33 @@ void lower(const Schedule& S, Lowered& lw) {
         lw.stream_stages = std::min(lw.stream_stages, acc_streamed ? AR_ACC_STAGES_4B : AR_CHAIN_STAGES_4B);
     if (!stream_trees && es == 2 && !acc_streamed) lw.stream_stages = std::min(lw.stream_stages, AR_CHAIN_STAGES_BF16);
     // The TMA-store epilogue holds an item's last stage until its outputs are
-    // copied out.  Measured at the bench size: it wins for copies (one input,
-    // many outputs: the all-gather, +4-5%), for bf16 with few outputs and for
-    // few inputs and outputs (P = 2, +5%), and for bf16 fp32 accumulation,
-    // whose direct stores are costly; 128-bit stores from registers win with
-    // many outputs (allreduce at P >= 8, up to +5%) and for fp32 passes with
-    // many inputs per output (the reduce-scatter, +2-3%).
-    int max_out = 0, max_in_stream = 0;
-    for (size_t k = 0; k < sets.size(); ++k)
-        if (stream[k])
-            for (auto& r : sets[k]) {
-                max_out = std::max<int>(max_out, lw.progs[r.prog].n_out);
-                max_in_stream = std::max<int>(max_in_stream, lw.progs[r.prog].n_in);
-            }
-    const bool few_out = max_out <= AR_TMA_STORE_MAX_OUT;
-    lw.stream_tma_store = max_in_stream <= 1 || (few_out && (S.dtype == AR_BFLOAT16 || max_in_stream <= 4)) ||
-                          (S.dtype == AR_BFLOAT16 && acc_streamed);
+    // copied out.  Measured at the bench size with the pipelines above: in a
+    // fused pass it wins for copies (one input, many outputs: the all-gather,
+    // +2%), for few inputs and outputs (P = 2, bf16 +3%) and for bf16 fp32
+    // accumulation, whose direct stores are costly (+30%); 128-bit stores
+    // from registers win with many outputs (allreduce at P >= 8, up to +5%)
+    // and with many inputs per output (the reduce-scatter: bf16 ring +4%, RH
+    // +1%).  The step form's rounds run faster with 128-bit stores in every
+    // round, copies included: ring, pipeline, binomial, generalized at P = 8
+    // and 12 +1-3.5% over TMA stores (and over TMA stores in either kind of
+    // round alone) — except bf16 rounds whose transfers have two outputs
+    // (recursive doubling's exchanges: TMA stores +3.5%, as for P = 2).
+    const bool rounds = sets.size() > 1 || S.params.form == AR_FORM_STEP;
+    auto tma_store = [&](const std::vector<Range>& set) {
+        if (S.dtype == AR_BFLOAT16 && acc_streamed) return true;
+        int max_out = 0, max_in = 0;
+        for (auto& r : set) {
+            max_out = std::max<int>(max_out, lw.progs[r.prog].n_out);
+            max_in = std::max<int>(max_in, lw.progs[r.prog].n_in);
+        }
+        const bool few = max_out <= AR_TMA_STORE_MAX_OUT && max_in <= 4;
+        if (rounds) return S.dtype == AR_BFLOAT16 && few && max_out >= 2;
+        return max_in <= 1 || few;
+    };
     for (size_t k = 0; k < sets.size(); ++k) {
         LaunchSet ls;
         ls.stream = stream[k];
+        ls.tma_store = stream[k] && tma_store(sets[k]);
         const int64_t tile_elems = item_elems(sets[k], (stream[k] ? lw.stream_tile : lw.tile_bytes) / es, V);
         for (auto& r : sets[k]) {
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;

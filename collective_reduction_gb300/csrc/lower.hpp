@@ -16,6 +16,7 @@ struct LaunchSet {
     std::vector<WorkItem> fallback;  // whole ranges for unaligned buffers
     uint64_t bytes = 0;              // algorithmic HBM bytes of the set
     bool stream = false;             // bulk items run on the rank-streaming kernel
+    bool tma_store = false;          // ... with the TMA bulk-store epilogue (else 128-bit stores)
     bool small = false;              // small set (<= 256 KB): one element-wise launch over fallback
 };
 
@@ -28,7 +29,6 @@ struct Lowered {
     int stages = 0;       // pipeline depth of the staged kernel
     int stream_tile = 0;  // bytes per rank tile of the rank-streaming kernel
     int stream_stages = 0;
-    bool stream_tma_store = false;  // rank-streaming kernel: TMA bulk-store epilogue
     bool stream_trees = false;      // rank-streaming kernel: the instantiation that runs TREE programs
     int stream_slots = 0;           // rank-streaming kernel: shared-memory tiles of the tree stack
     int max_in = 0;       // largest n_in of a program used by bulk items

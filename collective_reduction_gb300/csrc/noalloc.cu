@@ -172,7 +172,7 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
                     if (s.stream) {
                         a.tile_bytes = L.stream_tile;
                         a.stages = L.stream_stages;
-                        a.flags = (L.stream_tma_store ? ar::kArgTmaStore : 0) | (L.stream_trees ? ar::kArgTrees : 0);
+                        a.flags = (s.tma_store ? ar::kArgTmaStore : 0) | (L.stream_trees ? ar::kArgTrees : 0);
                         a.max_in = 1;
                         a.max_tmp = L.stream_slots;  // tree stack tiles after the stages
                         e = ar::launch_stream(dtype, op, a, grid, smem_stream, cs);
