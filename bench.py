@@ -912,10 +912,11 @@ def run_rows(a, path):
 def run_costmodel(a, path):
     """The step-form cost model ("A Generalization of the Allreduce
     Operation", eqs. 36-37) on this GPU.  Fit: alpha per round, beta per byte
-    sent and gamma per byte combined (bytes over all ranks) by non-negative
-    least squares on relative error, over step-form ring, binomial, RD and
-    bandwidth-optimal generalized plans (rounds of independent transfers) and
-    the ring's reduce-scatter (combines) and all-gather (copies) halves, which
+    sent, gamma per byte combined (bytes over all ranks) and delta per
+    message by non-negative least squares on relative error, over step-form
+    ring, binomial, RD, the bandwidth-optimal and the latency-optimal
+    generalized plans (the latter's rounds are many small messages) and the
+    ring's reduce-scatter (combines) and all-gather (copies) halves, which
     tell beta and gamma apart, at P in {4, 16, 63} and 2 KiB .. 64 MiB per
     rank.  Validation: at P in {7, 12, 31, 63} and 1 KiB .. 16 MiB per
     rank, every candidate the selection weighs is timed; the measured best r
@@ -931,7 +932,7 @@ def run_costmodel(a, path):
     dtype = "float32"
 
     def counters(info):
-        return [info["steps"], info["sent_bytes_total"], info["combines"] * esize(dtype)]
+        return [info["steps"], info["sent_bytes_total"], info["combines"] * esize(dtype), info["messages"]]
 
     rows = []
     with open(path, "w") as out:
@@ -940,7 +941,9 @@ def run_costmodel(a, path):
                 S = 1 << lg
                 n = S // esize(dtype)
                 dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
+                L = (P - 1).bit_length()
                 for algo, kw in (("ring", {}), ("binomial", {}), ("rd", {}), ("generalized", {"r": 0}),
+                                 ("generalized", {"r": L}),
                                  ("ring", {"phase": "reduce_scatter"}), ("ring", {"phase": "all_gather"})):
                     plan = ar.Plan(P, n, dtype, "sum", algo, form="step", **kw)
                     us = time_plan(plan, dev)
@@ -948,20 +951,21 @@ def run_costmodel(a, path):
                     rows.append((c, us))
                     out.write(json.dumps({"phase": "fit", "P": P, "S": S, "algo": algo, "params": kw,
                                           "steps": c[0], "sent_bytes_total": c[1], "combined_bytes": c[2],
-                                          "us": round(us, 3)}) + "\n")
+                                          "messages": c[3], "us": round(us, 3)}) + "\n")
                     plan.close()
                 del dev
                 torch.cuda.empty_cache()
         A = np.array([[x / t for x in c] for c, t in rows])
         coef, _ = nnls(A, np.ones(len(rows)))
-        alpha, beta, gamma = (float(x) for x in coef)
+        alpha, beta, gamma, delta = (float(x) for x in coef)
         pred = A @ coef
         fit = {"phase": "model", "alpha_us": alpha, "beta_us_per_byte": beta, "gamma_us_per_byte": gamma,
+               "delta_us_per_message": delta,
                "rel_rms": float(np.sqrt(np.mean((pred - 1.0) ** 2))), "rel_max": float(np.max(np.abs(pred - 1.0))),
                "points": len(rows)}
         out.write(json.dumps(fit) + "\n")
         out.flush()
-        model = ar.CostModel(alpha, beta, gamma)
+        model = ar.CostModel(alpha, beta, gamma, delta)
         for P in (7, 12, 31, 63):
             L = (P - 1).bit_length()
             Lp = (1 << (P.bit_length() - 1)).bit_length() - 1

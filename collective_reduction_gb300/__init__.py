@@ -54,7 +54,7 @@ class Info(ctypes.Structure):
                 ("max_slots", ctypes.c_int), ("n_segments", ctypes.c_int),
                 ("hbm_bytes", ctypes.c_uint64), ("scratch_bytes", ctypes.c_uint64),
                 ("launches", ctypes.c_int), ("tile_bytes", ctypes.c_int), ("n_programs", ctypes.c_int),
-                ("n_items", ctypes.c_uint64), ("kernels", ctypes.c_int)]
+                ("n_items", ctypes.c_uint64), ("kernels", ctypes.c_int), ("messages", ctypes.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -70,10 +70,10 @@ class LoweringInfo(ctypes.Structure):
 
 
 class CostModel(ctypes.Structure):
-    """Step-form cost: alpha per round, beta per byte sent and gamma per byte
-    combined, bytes summed over all ranks."""
+    """Step-form cost: alpha per round, beta per byte sent, gamma per byte
+    combined and delta per message, summed over all ranks."""
     _fields_ = [("alpha_us", ctypes.c_double), ("beta_us_per_byte", ctypes.c_double),
-                ("gamma_us_per_byte", ctypes.c_double)]
+                ("gamma_us_per_byte", ctypes.c_double), ("delta_us_per_message", ctypes.c_double)]
 
 
 _lib = None

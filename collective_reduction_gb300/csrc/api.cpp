@@ -93,6 +93,7 @@ void fill_info(const ar::Schedule& S, ar_plan_info* info) {
         info->sent_bytes_max = std::max(info->sent_bytes_max, b);
     }
     info->combines = static_cast<uint64_t>(S.combines);
+    for (auto& rd : S.rounds) info->messages += rd.xfers.size();
     info->max_slots = S.max_slots;
     info->n_segments = S.nseg();
 }

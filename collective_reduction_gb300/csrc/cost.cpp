@@ -11,18 +11,18 @@
 namespace {
 
 // Fitted on GB300 by `bench.py --costmodel`: non-negative least squares on
-// relative error over 108 step-form plans (ring, binomial, RD, generalized
-// r = 0 and the ring's two halves; P = 4, 16, 63; 2 KiB .. 64 MiB per rank),
-// rms relative error 0.22, with the kernels launched as programmatic
-// dependents.  The fit puts little separate price on a combined byte (4% of
-// a sent byte's): the extra read of the receiver's value mostly hides under
-// the per-byte cost of the message.
-constexpr ar_cost_model kGB300 = {3.11, 3.33e-7, 1.22e-8};
+// relative error over 126 step-form plans (ring, binomial, RD, generalized
+// r = 0 and r = L, the ring's two halves; P = 4, 16, 63; 2 KiB .. 64 MiB per
+// rank), rms relative error 0.23, with the kernels launched as programmatic
+// dependents.  A combined byte costs a fifth of a sent one (the receiver's
+// extra read mostly hides under the message), a message about 5 ns on top
+// of its bytes: what makes thousands of tiny transfers expensive.
+constexpr ar_cost_model kGB300 = {3.03, 3.02e-7, 6.95e-8, 4.78e-3};
 
 bool model_ok(const ar_cost_model* m) {
     return m && m->alpha_us > 0 && m->beta_us_per_byte >= 0 && m->gamma_us_per_byte >= 0 &&
-           std::isfinite(m->alpha_us) && std::isfinite(m->beta_us_per_byte) &&
-           std::isfinite(m->gamma_us_per_byte);
+           m->delta_us_per_message >= 0 && std::isfinite(m->alpha_us) && std::isfinite(m->beta_us_per_byte) &&
+           std::isfinite(m->gamma_us_per_byte) && std::isfinite(m->delta_us_per_message);
 }
 
 // Eq. (36) in the engine's terms: with u = m / P bytes per chunk and the
@@ -53,7 +53,7 @@ ar_status ar_cost_predict(ar_schedule_t s, const ar_cost_model* model, double* u
     if (st != AR_OK) return st;
     const double combined = static_cast<double>(i.combines) * ar::esize_of(i.dtype);
     *us = model->alpha_us * i.steps + model->beta_us_per_byte * static_cast<double>(i.sent_bytes_total) +
-          model->gamma_us_per_byte * combined;
+          model->gamma_us_per_byte * combined + model->delta_us_per_message * static_cast<double>(i.messages);
     return AR_OK;
 }
 

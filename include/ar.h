@@ -166,6 +166,7 @@ typedef struct {
     int n_programs;              /* distinct tile programs                         */
     uint64_t n_items;            /* work items over all launches                   */
     int kernels;                 /* kernels the aligned launches use: AR_KERNEL_*  */
+    uint64_t messages;           /* transfers over all rounds (one per message)    */
 } ar_plan_info;
 
 /* ar_plan_info.kernels bits: the rank-streaming kernel (chains, single trees,
@@ -212,13 +213,18 @@ ar_status ar_schedule_tree(ar_schedule_t s, int rank, uint64_t elem, char* buf, 
  * round) a schedule costs
  *     alpha * rounds + beta * (bytes sent, all ranks)
  *                    + gamma * (bytes combined, all ranks)
- * i.e. the page's per-process beta and gamma are P times these.  The fused
- * form moves 2 P S bytes in one launch whatever the schedule, so the model
- * selects among step-form schedules only. */
+ *                    + delta * (messages, all ranks and rounds)
+ * i.e. the page's per-process beta and gamma are P times these.  delta is
+ * the engine's own term, not on the page: each message is at least one work
+ * item, which costs time however few its bytes (0 gives the page's model;
+ * eqs. 36-37 and ar_cost_optimal_r leave it out).  The fused form moves
+ * 2 P S bytes in one launch whatever the schedule, so the model selects
+ * among step-form schedules only. */
 typedef struct {
-    double alpha_us;           /* per round (one kernel launch)           */
-    double beta_us_per_byte;   /* per byte sent, summed over ranks        */
-    double gamma_us_per_byte;  /* per byte combined, summed over ranks    */
+    double alpha_us;              /* per round (one kernel launch)           */
+    double beta_us_per_byte;      /* per byte sent, summed over ranks        */
+    double gamma_us_per_byte;     /* per byte combined, summed over ranks    */
+    double delta_us_per_message;  /* per message (transfer), summed          */
 } ar_cost_model;
 
 /* The step-form model fitted on GB300 (bench.py --costmodel). */

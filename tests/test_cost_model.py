@@ -69,13 +69,13 @@ def test_invalid_cost_requests(lib):
 
 
 def test_predict_is_the_counters_under_the_model(lib):
-    model = ar.CostModel(3.0, 2e-7, 5e-8)
+    model = ar.CostModel(3.0, 2e-7, 5e-8, 0.01)
     for algo, kw in (("ring", {}), ("binomial", {}), ("generalized", {"r": 2}), ("hybrid", {"k1": 1}),
                      ("ahc", {"group_sizes": [3, 4]}), ("pipeline", {"blocks": 4})):
         for dtype, es in (("float32", 4), ("bfloat16", 2)):
             s = ar.Schedule(7, 7000, dtype, "sum", algo, form="step", **kw)
             i = s.info()
-            want = 3.0 * i["steps"] + 2e-7 * i["sent_bytes_total"] + 5e-8 * i["combines"] * es
+            want = 3.0 * i["steps"] + 2e-7 * i["sent_bytes_total"] + 5e-8 * i["combines"] * es + 0.01 * i["messages"]
             assert math.isclose(ar.cost_predict(s, model), want, rel_tol=1e-12)
 
 
@@ -137,6 +137,6 @@ def test_eq36_extra_terms_against_the_compiled_schedules(lib, P):
 
 def test_default_model_is_positive(lib):
     m = ar.cost_model()
-    assert m.alpha_us > 0 and m.beta_us_per_byte > 0 and m.gamma_us_per_byte >= 0
+    assert m.alpha_us > 0 and m.beta_us_per_byte > 0 and m.gamma_us_per_byte >= 0 and m.delta_us_per_message >= 0
     # the fitted GB300 values: a few us per round, about 3 TB/s per byte sent over all ranks
     assert 1.0 < m.alpha_us < 20.0 and 1e-7 < m.beta_us_per_byte < 1e-6
