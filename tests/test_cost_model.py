@@ -140,3 +140,14 @@ def test_default_model_is_positive(lib):
     assert m.alpha_us > 0 and m.beta_us_per_byte > 0 and m.gamma_us_per_byte >= 0 and m.delta_us_per_message >= 0
     # the fitted GB300 values: a few us per round, about 3 TB/s per byte sent over all ranks
     assert 1.0 < m.alpha_us < 20.0 and 1e-7 < m.beta_us_per_byte < 1e-6
+
+
+@pytest.mark.parametrize("P", [2, 3, 8, 13])
+def test_message_count_closed_forms(lib, P):
+    """The delta term's counter: the ring sends P messages in each of its
+    2 (P - 1) rounds; RD at P = 2^k sends P in each of its log2 P rounds;
+    the binomial reduce + broadcast sends P - 1 messages each way."""
+    assert ar.Schedule(P, P * 100, "float32", "sum", "ring").info()["messages"] == 2 * P * (P - 1)
+    assert ar.Schedule(P, P * 100, "float32", "sum", "binomial").info()["messages"] == 2 * (P - 1)
+    if P & (P - 1) == 0:
+        assert ar.Schedule(P, P * 100, "float32", "sum", "rd").info()["messages"] == P * (P.bit_length() - 1)
