@@ -173,6 +173,33 @@ def test_partial_last_wave(P, n, algo, form, kw, dtype):
     check_faithful(bufs, dtype, "sum", algo, form, **kw)
 
 
+@pytest.mark.parametrize("dtype,form", [("float32", "fused"), ("bfloat16", "fused"), ("float32", "step")])
+def test_bench_workload_at_full_size_sampled(dtype, form):
+    """The bench's own workload and launch configuration — the ring over
+    P = 8 x 256 MiB per rank, inputs drawn on the device as the bench draws
+    them — checked on 4096 sampled elements of each of the 8 chunks of every
+    rank: the sample keeps the chunk structure (a ceil split puts each
+    chunk's elements in the same chunk), so the oracle's literal run on it
+    owes exactly the sampled outputs, bit for bit."""
+    import torch
+    import bench
+    import collective_reduction_gb300 as ar
+    P = 8
+    n = (256 << 20) // (2 if dtype == "bfloat16" else 4)
+    dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=0)
+    sample_in, idx = bench.gather_sample(dev, P, n, 4096, P)
+    plan = ar.Plan(P, n, dtype, "sum", "ring", form=form)
+    plan.execute(dev)
+    plan.check()
+    want = oracle.run("ring", sample_in, Arith("sum", dtype)).bufs
+    for r in range(P):
+        got = to_host(dev[r].index_select(0, idx), dtype)
+        assert_bit_equal(got, want[r], dtype, f"rank {r}")
+    plan.close()
+    del dev
+    torch.cuda.empty_cache()
+
+
 # ---- every (dtype, op) through a chain and a DAG program -------------------------------
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
