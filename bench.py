@@ -997,7 +997,8 @@ def run_costmodel(a, path):
                     "select": [sel_algo, sel_kw], "select_us": round(sel_us, 3),
                     "select_predicted_us": round(sel_pred, 3),
                     "fastest": [best_key[0], json.loads(best_key[1])], "fastest_us": round(meas[best_key], 3),
-                    "select_loss": round(sel_us / meas[best_key], 4)}) + "\n")
+                    "select_loss": round(sel_us / meas[best_key], 4),
+                    "candidates_us": {f"{k[0]} {k[1]}": round(t, 3) for k, t in meas.items()}}) + "\n")
                 out.flush()
                 del dev
                 torch.cuda.empty_cache()
