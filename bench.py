@@ -1002,6 +1002,30 @@ def run_costmodel(a, path):
                 out.flush()
                 del dev
                 torch.cuda.empty_cache()
+        # the pipelined chain's block count: the page's optimal m (BSP runtime
+        # (T_start + n/m T_byte)(p + m - 2)), with a round's T_start = alpha +
+        # (P - 1) delta and a block byte's T_byte = (P - 1)(beta + gamma),
+        # against the measured best over a geometric range of m
+        for P in (8, 16):
+            for lg in (18, 22, 26):
+                S = 1 << lg
+                n = S // esize(dtype)
+                dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
+                t_start = alpha + (P - 1) * delta
+                t_byte = (P - 1) * (beta + gamma)
+                m_pred = int(min(4096, max(1, round((S * (P - 2) * t_byte / t_start) ** 0.5))))
+                times = {}
+                for m in sorted({1, 2, 4, 8, 16, 32, 64, 128, 256, m_pred}):
+                    plan = ar.Plan(P, n, dtype, "sum", "pipeline", form="step", blocks=m)
+                    times[m] = time_plan(plan, dev)
+                    plan.close()
+                best = min(times, key=times.get)
+                out.write(json.dumps({"phase": "pipeline", "P": P, "S": S, "m_pred": m_pred, "m_best": best,
+                                      "pred_loss": round(times[m_pred] / times[best], 4),
+                                      "times_us": {str(k): round(v, 3) for k, v in times.items()}}) + "\n")
+                out.flush()
+                del dev
+                torch.cuda.empty_cache()
 
 
 def main():
