@@ -612,7 +612,9 @@ def test_kernel_choice_per_program_kind():
 def test_streamed_trees_many_items(algo, kw, dtype):
     """Single trees on the rank-streaming kernel over many items per CTA,
     with a ragged tail: bit-identical to the oracle on the owned / all
-    elements."""
+    elements.  For bf16 the whole tiles and each range's partial last tile
+    run different compilations of the tree consumer (without and with the
+    per-vector bounds test); this size gives every rank both."""
     P, n = 8, (1 << 22) + 77
     bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=17)
     res = oracle.run(algo, bufs, Arith("sum", dtype), **kw)
