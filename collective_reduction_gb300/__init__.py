@@ -27,7 +27,7 @@ KERNEL_STREAM, KERNEL_STAGED, KERNEL_ELEMENTWISE, KERNEL_DAG_JIT = 1, 2, 4, 8  #
 MAX_RANKS = 64
 
 STATUS = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_UNSUPPORTED", 3: "AR_ERR_CUDA",
-          4: "AR_ERR_NOMEM", 5: "AR_ERR_TIMEOUT"}
+          4: "AR_ERR_NOMEM", 5: "AR_ERR_TIMEOUT", 6: "AR_ERR_INTERNAL"}
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libar.so")
 
@@ -63,7 +63,8 @@ class Info(ctypes.Structure):
 class LoweringInfo(ctypes.Structure):
     _fields_ = [("items", ctypes.c_uint64), ("launch_sets", ctypes.c_int), ("windows", ctypes.c_int),
                 ("tiling_ok", ctypes.c_int), ("windows_ok", ctypes.c_int), ("wave_balance", ctypes.c_double),
-                ("stream_tile_bytes", ctypes.c_int), ("stream_stages", ctypes.c_int)]
+                ("stream_tile_bytes", ctypes.c_int), ("stream_stages", ctypes.c_int),
+                ("staged_tile_bytes", ctypes.c_int), ("staged_stages", ctypes.c_int), ("dag_words", ctypes.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -93,6 +94,7 @@ _EXPORTS = {
     "ar_execute": (ctypes.c_int, [_VP, ctypes.POINTER(_VP), _VP]),
     "ar_execute_host": (ctypes.c_int, [_VP, ctypes.POINTER(_VP), ctypes.POINTER(_VP), _VP]),
     "ar_plan_check": (ctypes.c_int, [_VP]),
+    "ar_plan_check_buffers": (ctypes.c_int, [_VP, ctypes.POINTER(_VP)]),
     "ar_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ar_schedule_dag_kernel": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     "ar_schedule_lowering": (ctypes.c_int, [_VP, ctypes.POINTER(LoweringInfo)]),
@@ -244,8 +246,17 @@ class Plan:
                "ar_execute_host")
 
     def check(self):
-        """Synchronise and raise ArError(AR_ERR_TIMEOUT) if a kernel gave up a wait."""
+        """Synchronise; raise ArError(AR_ERR_TIMEOUT) if a kernel gave up a wait,
+        ArError(AR_ERR_INTERNAL) if a kernel met a program it does not run or
+        wrote past the plan's scratch."""
         _check(lib().ar_plan_check(self._h), "ar_plan_check")
+
+    def check_buffers(self, bufs):
+        """The status ar_execute's buffer checks give these P buffers (residency
+        on the plan's device, extent, alignment, overlap); launches nothing."""
+        if len(bufs) != self.P:
+            raise ValueError(f"expected {self.P} buffers, got {len(bufs)}")
+        return STATUS.get(lib().ar_plan_check_buffers(self._h, _ptrs(bufs)), "unknown")
 
     def close(self):
         if getattr(self, "_h", None):

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libar.so")
-SOURCES = ["kernels.cu", "noalloc.cu", "schedule.cpp", "lower.cpp", "api.cpp", "cost.cpp", "jit.cpp"]
+SOURCES = ["kernels.cu", "noalloc.cu", "schedule.cpp", "lower.cpp", "api.cpp", "bufcheck.cpp", "cost.cpp", "jit.cpp"]
 # headers the run-time compiled DAG kernels include, embedded into jit.cpp
 JIT_HEADERS = [os.path.join(INCLUDE, "ar.h")] + [os.path.join(CSRC, h) for h in ("devprog.hpp", "kargs.hpp",
                                                                                   "device.cuh")]

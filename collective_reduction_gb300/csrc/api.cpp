@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "ar.h"
+#include "bufcheck.hpp"
 #include "jit.hpp"
 #include "kernels.hpp"
 #include "lower.hpp"
@@ -23,6 +24,12 @@ constexpr uint64_t kJitMinBytes = 16ull << 20;
 // Programs beyond this many instruction words stay interpreted: the
 // compile time grows past a few seconds.
 constexpr size_t kJitMaxWords = 4096;
+// Guard bands around the step form's scratch: written with kGuardByte when
+// the plan is created and compared by ar_plan_check, so a kernel that writes
+// past either end of the scratch is reported rather than silently
+// corrupting device memory.
+constexpr size_t kGuardBytes = 256;
+constexpr unsigned char kGuardByte = 0xA5;
 }  // namespace
 
 struct ar_schedule_s {
@@ -38,6 +45,7 @@ struct ar_plan_s {
     int smem_stream = 0;
     int smem_elem = 0;
     char* d_tables = nullptr;
+    char* d_scratch_alloc = nullptr;  // [guard | scratch | guard]
     char* d_scratch = nullptr;
     uint64_t slot_stride = 0;
     uint64_t scratch_bytes = 0;
@@ -64,6 +72,8 @@ struct ar_plan_s {
     const ar::DevProg* d_progs = nullptr;
     const uint16_t* d_refs = nullptr;
     const uint32_t* d_ins = nullptr;
+    // the last pointer set whose residency ar_execute checked and accepted
+    std::vector<uintptr_t> checked;
 };
 
 namespace {
@@ -114,29 +124,26 @@ void destroy_plan(ar_plan_s* p) {
         if (p->s_out[k]) cudaStreamDestroy(p->s_out[k]);
     }
     if (p->d_tables) cudaFree(p->d_tables);
-    if (p->d_scratch) cudaFree(p->d_scratch);
+    if (p->d_scratch_alloc) cudaFree(p->d_scratch_alloc);
     if (p->d_status) cudaFree(p->d_status);
     delete p;
 }
 
-// Checks P device pointers: non-null, element-aligned, pairwise disjoint.
-ar_status validate_bufs(const ar_plan_s* plan, void* const* bufs, bool* aligned16) {
+// The rank buffers of an execute: alignment and overlap every time; device
+// residency and extent (ar::check_rank_buffers) whenever the pointer set
+// differs from the last one accepted on this plan.
+ar_status validate_bufs(ar_plan_s* plan, void* const* bufs, bool* aligned16) {
     const ar::Schedule& S = plan->S;
-    const uint64_t es = ar::esize_of(S.dtype);
-    const uint64_t bytes = static_cast<uint64_t>(S.n) * es;
-    std::vector<std::pair<uintptr_t, int>> addr;
-    bool aligned = true;
-    for (int r = 0; r < S.P; ++r) {
-        uintptr_t a = reinterpret_cast<uintptr_t>(bufs[r]);
-        if (!a || a % es) return AR_ERR_INVALID_ARG;
-        aligned = aligned && a % 16 == 0;
-        addr.emplace_back(a, r);
+    const bool known = plan->checked.size() == static_cast<size_t>(S.P) &&
+                       std::equal(plan->checked.begin(), plan->checked.end(), bufs,
+                                  [](uintptr_t a, void* b) { return a == reinterpret_cast<uintptr_t>(b); });
+    ar_status v = ar::check_rank_buffers(S.P, static_cast<uint64_t>(S.n), ar::esize_of(S.dtype), plan->device, bufs,
+                                         !known, aligned16);
+    if (v == AR_OK && !known) {
+        plan->checked.clear();
+        for (int r = 0; r < S.P; ++r) plan->checked.push_back(reinterpret_cast<uintptr_t>(bufs[r]));
     }
-    std::sort(addr.begin(), addr.end());
-    for (int r = 0; r + 1 < S.P; ++r)
-        if (addr[r].first == addr[r + 1].first || addr[r].first + bytes > addr[r + 1].first) return AR_ERR_INVALID_ARG;
-    *aligned16 = aligned;
-    return AR_OK;
+    return v;
 }
 
 void base_args(const ar_plan_s* plan, void* const* bufs, ar::KernelArgs& a) {
@@ -209,6 +216,7 @@ const char* ar_status_string(ar_status s) {
         case AR_ERR_CUDA: return "AR_ERR_CUDA: CUDA runtime error";
         case AR_ERR_NOMEM: return "AR_ERR_NOMEM: out of memory";
         case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT: a bounded wait in a kernel gave up";
+        case AR_ERR_INTERNAL: return "AR_ERR_INTERNAL: a kernel met a program it does not run, or wrote past the plan's scratch";
     }
     return "unknown ar_status";
 }
@@ -320,6 +328,9 @@ ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
         out->wave_balance = c.wave_balance;
         out->stream_tile_bytes = L.stream_tile;
         out->stream_stages = L.stream_stages;
+        out->staged_tile_bytes = L.tile_bytes;
+        out->staged_stages = L.stages;
+        out->dag_words = ar::dag_kernel_words(L);
         return AR_OK;
     } catch (const std::bad_alloc&) {
         return AR_ERR_NOMEM;
@@ -390,7 +401,12 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             // second partials and the twins of versioned rounds, per rank
             p->slot_stride = (static_cast<uint64_t>(n) * es + 255) / 256 * 256;
             p->scratch_bytes = static_cast<uint64_t>(L.phys_slots - 1) * P * p->slot_stride;
-            e = cudaMalloc(&p->d_scratch, p->scratch_bytes);
+            e = cudaMalloc(&p->d_scratch_alloc, p->scratch_bytes + 2 * kGuardBytes);
+            if (e == cudaSuccess) {
+                p->d_scratch = p->d_scratch_alloc + kGuardBytes;
+                e = cudaMemset(p->d_scratch_alloc, kGuardByte, kGuardBytes);
+            }
+            if (e == cudaSuccess) e = cudaMemset(p->d_scratch + p->scratch_bytes, kGuardByte, kGuardBytes);
         }
         if (e != cudaSuccess) {
             destroy_plan(p);
@@ -447,6 +463,15 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info) {
         if (!s.edge.empty()) info->kernels |= AR_KERNEL_ELEMENTWISE;
     }
     return AR_OK;
+}
+
+ar_status ar_plan_check_buffers(ar_plan_t plan, void* const* rank_bufs) {
+    if (!plan || !rank_bufs) return AR_ERR_INVALID_ARG;
+    const ar::Schedule& S = plan->S;
+    if (S.n == 0) return AR_OK;
+    bool aligned = false;
+    return ar::check_rank_buffers(S.P, static_cast<uint64_t>(S.n), ar::esize_of(S.dtype), plan->device, rank_bufs,
+                                  true, &aligned);
 }
 
 ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
@@ -577,11 +602,18 @@ ar_status ar_plan_check(ar_plan_t plan) {
     cudaError_t e = cudaDeviceSynchronize();
     int word = 0;
     if (e == cudaSuccess) e = cudaMemcpy(&word, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_status(e);
-    if (word != 0) {
-        cudaMemset(plan->d_status, 0, sizeof(int));
-        return AR_ERR_TIMEOUT;
+    bool guards_ok = true;
+    if (e == cudaSuccess && plan->d_scratch_alloc) {
+        unsigned char g[2 * kGuardBytes];
+        e = cudaMemcpy(g, plan->d_scratch_alloc, kGuardBytes, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g + kGuardBytes, plan->d_scratch + plan->scratch_bytes, kGuardBytes, cudaMemcpyDeviceToHost);
+        for (size_t i = 0; e == cudaSuccess && i < sizeof(g); ++i) guards_ok = guards_ok && g[i] == kGuardByte;
     }
+    if (e != cudaSuccess) return cuda_status(e);
+    if (word != 0) cudaMemset(plan->d_status, 0, sizeof(int));
+    if (!guards_ok || (word & ar::kStatusBadProgram)) return AR_ERR_INTERNAL;
+    if (word != 0) return AR_ERR_TIMEOUT;
     return AR_OK;
 }
 

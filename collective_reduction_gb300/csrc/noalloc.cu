@@ -16,7 +16,12 @@
 // holds AR_STATIC_SCRATCH_BYTES of it).  Host code only ever sees the array's
 // name as a host-side stand-in; its device address is obtained once per
 // device with cudaGetSymbolAddress, on the first call made with that device
-// current.
+// current, and kept for the life of the process (a cudaDeviceReset after that
+// call is not supported: the array may then sit elsewhere).
+//
+// The kernels report a bounded wait that gave up, or a program they do not
+// run, in the array's status word.  ar_allreduce_static clears it at the
+// start of every call; ar_allreduce_static_check reads it back.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -27,6 +32,8 @@
 #include <vector>
 
 #include "ar.h"
+#include "bufcheck.hpp"
+#include "kargs.hpp"
 #include "kernels.hpp"
 #include "lower.hpp"
 #include "schedule.hpp"
@@ -93,17 +100,11 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
         const uint64_t es = ar::esize_of(dtype);
         const uint64_t bytes = n * es;
         if (n == 0) return AR_OK;
-        std::vector<std::pair<uintptr_t, int>> addr;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
         bool aligned = true;
-        for (int r = 0; r < P; ++r) {
-            uintptr_t a = reinterpret_cast<uintptr_t>(rank_bufs[r]);
-            if (!a || a % es) return AR_ERR_INVALID_ARG;
-            aligned = aligned && a % 16 == 0;
-            addr.emplace_back(a, r);
-        }
-        std::sort(addr.begin(), addr.end());
-        for (int r = 0; r + 1 < P; ++r)
-            if (addr[r].first + bytes > addr[r + 1].first) return AR_ERR_INVALID_ARG;
+        st = ar::check_rank_buffers(P, n, static_cast<int>(es), dev, rank_bufs, true, &aligned);
+        if (st != AR_OK) return st;
         if (P == 1) return AR_OK;
 
         ar::Lowered L;
@@ -128,8 +129,6 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
             if (static_cast<uint64_t>(L.phys_slots - 1) * P * slot_stride > kSlotArea) return AR_ERR_UNSUPPORTED;
         }
 
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
         DeviceState* d = nullptr;
         st = setup(dev, d);
         if (st != AR_OK) return st;
@@ -204,4 +203,27 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
     } catch (const std::bad_alloc&) {
         return AR_ERR_NOMEM;
     }
+}
+
+extern "C" ar_status ar_allreduce_static_check(void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return AR_ERR_UNSUPPORTED;
+    char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        if (g_dev[dev].ready) base = g_dev[dev].base;
+    }
+    if (!base) return AR_OK;  // no call has run on this device
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, base, sizeof(int), cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e == cudaSuccess && word != 0) {
+        e = cudaMemsetAsync(base, 0, sizeof(int), cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    }
+    if (e != cudaSuccess) return AR_ERR_CUDA;
+    if (word & ar::kStatusBadProgram) return AR_ERR_INTERNAL;
+    return word ? AR_ERR_TIMEOUT : AR_OK;
 }

@@ -50,7 +50,10 @@ typedef enum {
     AR_ERR_UNSUPPORTED = 2, /* valid request this engine does not implement   */
     AR_ERR_CUDA = 3,        /* a CUDA runtime call failed                      */
     AR_ERR_NOMEM = 4,       /* host or device allocation failed                */
-    AR_ERR_TIMEOUT = 5      /* a bounded wait inside a kernel gave up          */
+    AR_ERR_TIMEOUT = 5,     /* a bounded wait inside a kernel gave up          */
+    AR_ERR_INTERNAL = 6     /* a kernel met a program kind it does not run, or
+                               a guard band around plan scratch was overwritten:
+                               an engine fault, never the caller's              */
 } ar_status;
 
 typedef enum { AR_INT32 = 0, AR_FLOAT32 = 1, AR_BFLOAT16 = 2 } ar_dtype;
@@ -278,6 +281,11 @@ typedef struct {
     double wave_balance;     /* >= 1, as above (1 with no streamed items)       */
     int stream_tile_bytes;   /* rank tile of the rank-streaming kernel          */
     int stream_stages;       /* its pipeline depth                              */
+    int staged_tile_bytes;   /* input tile of the staged kernel (DAG programs)  */
+    int staged_stages;       /* its pipeline depth                              */
+    uint64_t dag_words;      /* instruction words of the staged launches' DAG
+                                programs (what a run-time compiled DAG kernel
+                                holds)                                          */
 } ar_lowering_info;
 ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out);
 
@@ -293,19 +301,32 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
 ar_status ar_plan_destroy(ar_plan_t plan);
 /* Counters of the schedule and of its lowering. */
 ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info);
+/* Checks P rank buffers as ar_execute does, launching nothing: non-null,
+ * aligned to the element size, pairwise disjoint, and each one device memory
+ * of the plan's device (cudaMalloc'd, from a pool, or managed) whose n
+ * elements lie inside the allocation holding it ("All-Reduce, in depth", The
+ * APIs: the collective works on device buffers the caller owns).  Pageable or
+ * pinned host memory, another device's memory, and a pointer whose n
+ * elements run past its allocation give AR_ERR_INVALID_ARG.  (The extent is
+ * checked where the driver reports allocation ranges.)  With n = 0: AR_OK. */
+ar_status ar_plan_check_buffers(ar_plan_t plan, void* const* rank_bufs);
 /* Enqueues the allreduce on `stream` (0 = legacy default stream) and returns.
  * rank_bufs: host array of P device pointers, each to n elements of the
  * plan's dtype on the plan's device, distinct, non-overlapping and aligned
- * to the element size (AR_ERR_INVALID_ARG otherwise).  With n = 0 the call
- * is a no-op and the pointers are not inspected.  Every buffer is both input
- * and output.
+ * to the element size (AR_ERR_INVALID_ARG otherwise, before any launch).
+ * Residency and extent are checked as by ar_plan_check_buffers whenever the
+ * pointer set differs from the last one this plan accepted (a repeated set
+ * is not re-queried: freeing a buffer and passing its pointer again is the
+ * caller's error).  With n = 0 the call is a no-op and the pointers are not
+ * inspected.  Every buffer is both input and output.
  * 16-byte aligned buffers use the tiled kernels (rank-streaming, staged); any
  * other alignment is valid and takes a slower element-wise path.  Executes of one plan must be
  * ordered on one stream (they share the plan's scratch).  The launch itself
  * is checked (AR_ERR_CUDA); kernel-side failures are reported by
  * ar_plan_check. */
 ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream);
-/* End-to-end variant: copies P host buffers to the P device buffers, runs the
+/* End-to-end variant: copies P host buffers to the P device buffers (checked
+ * as ar_execute checks them), runs the
  * allreduce and copies every device buffer back to its host buffer, then
  * synchronises `stream`.  Large fused plans on 16-byte-aligned device buffers
  * are processed in element windows of about 128 MB: the copies in of window
@@ -325,9 +346,12 @@ ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* d
  * expected result), AR_OK if it completed, AR_ERR_INVALID_ARG for a timeout
  * out of range, AR_ERR_CUDA / AR_ERR_NOMEM on failures. */
 ar_status ar_selftest_bounded_wait(uint32_t timeout_ms, void* stream);
-/* Synchronises the device and reads the plan's device status word: AR_OK, or
- * AR_ERR_TIMEOUT if a bounded wait in a kernel gave up since the last check
- * (the word is then cleared).  AR_ERR_CUDA if synchronisation fails. */
+/* Synchronises the device and reads the plan's device status word and the
+ * guard bands around its scratch: AR_OK; AR_ERR_INTERNAL if a kernel met a
+ * program kind it does not run or a guard band was overwritten (this takes
+ * precedence); AR_ERR_TIMEOUT if a bounded wait in a kernel gave up.  The
+ * status word is cleared after a failure is read.  AR_ERR_CUDA if
+ * synchronisation fails. */
 ar_status ar_plan_check(ar_plan_t plan);
 
 /* Static text for a status code (never NULL). */
@@ -352,7 +376,8 @@ const char* ar_status_string(ar_status s);
  * host memory is used only while the schedule is compiled.
  *   - Set-up: the first call made with a given device current resolves the
  *     array's device address (cudaGetSymbolAddress) for that device; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The address is kept for the life
+ *     of the process: a cudaDeviceReset after the first call is not supported.
  *   - Limits: AR_ERR_UNSUPPORTED when the schedule's tables need more than
  *     AR_STATIC_TABLE_BYTES or its partial slots more than what is left of the
  *     array (AR_STATIC_SCRATCH_BYTES - AR_STATIC_TABLE_BYTES - 256 bytes).
@@ -360,12 +385,21 @@ const char* ar_status_string(ar_status s);
  *     call's contents (the status word is cleared, the tables rewritten, on
  *     `stream`).  Calls that can overlap on the GPU race with each other:
  *     issue them on one stream, or order them with events.
- *   - Errors as ar_plan_create + ar_execute; the bounded waits of the kernels
- *     are not reported by this call. */
+ *   - Errors as ar_plan_create + ar_execute, the rank buffers checked as by
+ *     ar_plan_check_buffers on every call.  Kernel-side failures (a bounded
+ *     wait that gave up, a program a kernel does not run) land in the array's
+ *     status word, which each call clears when it starts: read it with
+ *     ar_allreduce_static_check after a call and before the next one. */
 #define AR_STATIC_SCRATCH_BYTES (32u << 20)
 #define AR_STATIC_TABLE_BYTES (1u << 20)
 ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo,
                               const ar_params* params, void* const* rank_bufs, void* stream);
+/* Synchronises `stream`, then reads and clears the status word the kernels of
+ * ar_allreduce_static calls on the current device write: AR_OK (also when no
+ * call has run on this device), AR_ERR_INTERNAL if a kernel met a program it
+ * does not run, AR_ERR_TIMEOUT if a bounded wait gave up, AR_ERR_CUDA if the
+ * copy or the synchronisation fails.  Allocates nothing. */
+ar_status ar_allreduce_static_check(void* stream);
 
 #ifdef __cplusplus
 }

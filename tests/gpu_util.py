@@ -30,16 +30,75 @@ def to_host(t, dtype):
     return t.cpu().numpy()
 
 
-def engine(bufs, dtype, op, algo, **params):
-    """Run the allreduce on copies of host buffers; returns host results."""
+# Guard bands: every rank buffer sits inside a larger allocation, between two
+# bands of GUARD_BYTES filled with a sentinel bit pattern; a test checks after
+# each call that no byte of either band changed (an out-of-range store from an
+# edge tile, a TMA copy one tile too long, a slot written past its stride).
+# This stands in for a memory checker, which this GPU pool does not offer.
+GUARD_BYTES = 4096
+_SENTINEL = {4: 0x5AA5C33C, 2: -0x3CA6}   # int32 / int16 bit patterns
+
+
+class RankBufs:
+    """P device rank buffers of n elements with guard bands before and after
+    each; ``offset`` elements more before the buffer shift its alignment (the
+    skipped elements belong to the leading band).  ``views`` are the buffers
+    to pass to the engine; their contents start undefined (``from_host``
+    fills them)."""
+
+    def __init__(self, P, n, dtype, offset=0):
+        import torch
+        self.dtype, self.P, self.n = dtype, P, n
+        es = 2 if dtype == "bfloat16" else 4
+        self.lead = GUARD_BYTES // es + offset
+        self.tail = GUARD_BYTES // es
+        tdt = {"bfloat16": torch.bfloat16, "float32": torch.float32, "int32": torch.int32}[dtype]
+        self._ity = torch.int16 if es == 2 else torch.int32
+        self.big = []
+        for _ in range(P):
+            t = torch.empty(self.lead + n + self.tail, dtype=tdt, device="cuda")
+            t.view(self._ity).fill_(_SENTINEL[es])
+            self.big.append(t)
+        self.views = [t[self.lead:self.lead + n] for t in self.big]
+
+    @classmethod
+    def from_host(cls, host_bufs, dtype, offset=0):
+        rb = cls(len(host_bufs), len(host_bufs[0]), dtype, offset)
+        rb.fill(host_bufs)
+        return rb
+
+    def fill(self, host_bufs):
+        for v, h in zip(self.views, host_bufs):
+            v.copy_(to_dev(h, self.dtype))
+
+    def check_guards(self, what=""):
+        import torch
+        torch.cuda.synchronize()
+        es = 2 if self.dtype == "bfloat16" else 4
+        for r, t in enumerate(self.big):
+            w = t.view(self._ity)
+            for name, band in (("leading", w[:self.lead]), ("trailing", w[self.lead + self.n:])):
+                bad = torch.nonzero(band != _SENTINEL[es]).flatten()
+                if bad.numel():
+                    raise AssertionError(f"{what}: rank {r} {name} guard band overwritten at "
+                                         f"{bad[:5].tolist()} ({bad.numel()} elements)")
+
+    def results(self):
+        return [to_host(v, self.dtype) for v in self.views]
+
+
+def engine(bufs, dtype, op, algo, offset=0, **params):
+    """Run the allreduce on guarded copies of host buffers; checks the plan's
+    status and every guard band, returns host results."""
     import torch
     P, n = len(bufs), len(bufs[0])
-    dev = [to_dev(b, dtype) for b in bufs]
+    rb = RankBufs.from_host(bufs, dtype, offset)
     plan = ar.Plan(P, n, dtype, op, algo, **params)
-    plan.execute(dev)
+    plan.execute(rb.views)
     torch.cuda.synchronize()
     plan.check()
-    out = [to_host(t, dtype) for t in dev]
+    rb.check_guards(f"{algo} {dtype} {op} {params}")
+    out = rb.results()
     plan.close()
     return out
 

@@ -13,7 +13,7 @@ from oracle.chunking import ceil_log2
 from oracle.direct import direct_f64, direct_int, normwise_rel_err
 from oracle.elementops import Arith
 
-from gpu_util import assert_bit_equal, engine, ensure_built, to_dev, to_host
+from gpu_util import RankBufs, assert_bit_equal, engine, ensure_built, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -186,17 +186,22 @@ def test_bench_workload_at_full_size_sampled(dtype, form):
     import collective_reduction_gb300 as ar
     P = 8
     n = (256 << 20) // (2 if dtype == "bfloat16" else 4)
-    dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=0)
-    sample_in, idx = bench.gather_sample(dev, P, n, 4096, P)
+    src = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=0)
+    sample_in, idx = bench.gather_sample(src, P, n, 4096, P)
+    rb = RankBufs(P, n, dtype)
+    for v, t in zip(rb.views, src):
+        v.copy_(t)
+    del src
     plan = ar.Plan(P, n, dtype, "sum", "ring", form=form)
-    plan.execute(dev)
+    plan.execute(rb.views)
     plan.check()
+    rb.check_guards("bench workload")
     want = oracle.run("ring", sample_in, Arith("sum", dtype)).bufs
     for r in range(P):
-        got = to_host(dev[r].index_select(0, idx), dtype)
+        got = to_host(rb.views[r].index_select(0, idx), dtype)
         assert_bit_equal(got, want[r], dtype, f"rank {r}")
     plan.close()
-    del dev
+    del rb
     torch.cuda.empty_cache()
 
 
@@ -273,24 +278,15 @@ def test_ragged_and_tiny_lengths(P, n):
 
 
 def test_unaligned_buffers_take_elementwise_path():
-    import torch
-    import collective_reduction_gb300 as ar
+    """Buffers one element past a 16-byte boundary: the element-wise path,
+    the skipped leading element checked with the guard band before it."""
     P, n = 6, 3001
     bufs = ar_synth.rank_inputs(P, n, "float32", "normal", seed=4)
     want = oracle.run("generalized", bufs, Arith("sum", "float32"), r=1).bufs
-    big = [torch.zeros(n + 1, dtype=torch.float32, device="cuda") for _ in range(P)]
-    views = [big[r][1:] for r in range(P)]  # 4-byte offset: not 16-byte aligned
-    for r in range(P):
-        views[r].copy_(torch.from_numpy(bufs[r]))
     for form in FORMS:
+        got = engine(bufs, "float32", "sum", "generalized", offset=1, r=1, form=form)
         for r in range(P):
-            views[r].copy_(torch.from_numpy(bufs[r]))
-        plan = ar.Plan(P, n, "float32", "sum", "generalized", r=1, form=form)
-        plan.execute(views)
-        plan.check()
-        for r in range(P):
-            assert_bit_equal(views[r].cpu().numpy(), want[r], "float32", f"unaligned {form} rank {r}")
-        plan.close()
+            assert_bit_equal(got[r], want[r], "float32", f"unaligned {form} rank {r}")
 
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
@@ -301,22 +297,12 @@ def test_fp32acc_same_bits_in_every_kernel(P, algo, kw, dtype):
     kernel: the rank-streaming kernel (bf16 on 16 KB tiles, fp32 on 32 KB)
     must give exactly the bits of the element-wise kernel, which unaligned
     buffers take."""
-    import torch
-    import collective_reduction_gb300 as ar
     n = 300_007
     bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=P + 3)
     fast = engine(bufs, dtype, "sum", algo, order="fp32acc", **kw)
-    tdt = torch.bfloat16 if dtype == "bfloat16" else torch.float32
-    big = [torch.zeros(n + 1, dtype=tdt, device="cuda") for _ in range(P)]
-    views = [big[r][1:] for r in range(P)]  # one element off: not 16-byte aligned
+    slow = engine(bufs, dtype, "sum", algo, offset=1, order="fp32acc", **kw)  # not 16-byte aligned
     for r in range(P):
-        views[r].copy_(to_dev(bufs[r], dtype))
-    plan = ar.Plan(P, n, dtype, "sum", algo, order="fp32acc", **kw)
-    plan.execute(views)
-    plan.check()
-    for r in range(P):
-        assert_bit_equal(to_host(views[r], dtype), fast[r], dtype, f"{algo} P={P} rank {r}")
-    plan.close()
+        assert_bit_equal(slow[r], fast[r], dtype, f"{algo} P={P} rank {r}")
 
 
 @pytest.mark.parametrize("form", FORMS)
@@ -343,6 +329,48 @@ def test_invalid_buffers_rejected():
     plan.close()
 
 
+def _segment_of(t):
+    """(address, size) of the caching allocator's segment holding tensor t."""
+    import torch
+    p = t.data_ptr()
+    for seg in torch.cuda.memory_snapshot():
+        if seg["address"] <= p < seg["address"] + seg["total_size"]:
+            return seg["address"], seg["total_size"]
+    return None
+
+
+def test_buffer_residency_checked_before_any_launch():
+    """ar_plan_check_buffers applies ar_execute's buffer checks and launches
+    nothing: device memory of the plan's device passes; pageable host memory,
+    pinned host memory and a buffer whose n elements run past the allocation
+    holding it are refused.  (Tested through the check alone, so that no bad
+    pointer could reach a kernel even if the check regressed.)"""
+    import os
+
+    import torch
+    import collective_reduction_gb300 as ar
+    P, n = 3, 1 << 20
+    plan = ar.Plan(P, n, "float32", "sum", "ring")
+    good = [torch.zeros(n, device="cuda") for _ in range(P)]
+    assert plan.check_buffers(good) == "AR_OK"
+    pageable = np.zeros(n, np.float32)
+    assert plan.check_buffers([good[0], good[1], pageable.ctypes.data]) == "AR_ERR_INVALID_ARG"
+    pinned = torch.zeros(n).pin_memory()
+    assert plan.check_buffers([good[0], pinned.data_ptr(), good[2]]) == "AR_ERR_INVALID_ARG"
+    assert plan.check_buffers([good[0], good[1], 0]) == "AR_ERR_INVALID_ARG"
+    assert plan.check_buffers([good[0], good[1], good[1].data_ptr() + 4096]) == "AR_ERR_INVALID_ARG"  # overlap
+    if "expandable_segments:True" not in os.environ.get("PYTORCH_CUDA_ALLOC_CONF", ""):
+        big = torch.empty(24 << 20, dtype=torch.uint8, device="cuda")
+        seg = _segment_of(big)
+        assert seg is not None
+        base, size = seg
+        inside = base + size - 4 * n            # the last n elements of the segment: fine
+        past = inside + 4096                    # starts inside, ends 4 KiB past the segment
+        assert plan.check_buffers([good[0], good[1], inside]) == "AR_OK"
+        assert plan.check_buffers([good[0], good[1], past]) == "AR_ERR_INVALID_ARG"
+    plan.close()
+
+
 def test_execute_host_end_to_end():
     import torch
     import collective_reduction_gb300 as ar
@@ -350,10 +378,12 @@ def test_execute_host_end_to_end():
     bufs = ar_synth.rank_inputs(P, n, "float32", "normal", seed=8)
     want = oracle.run("ring", bufs, Arith("sum", "float32")).bufs
     host = [torch.from_numpy(b.copy()).pin_memory() for b in bufs]
-    dev = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(P)]
+    rb = RankBufs(P, n, "float32")
+    dev = rb.views
     plan = ar.Plan(P, n, "float32", "sum", "ring")
     plan.execute_host(host, dev)
     plan.check()
+    rb.check_guards("e2e")
     for r in range(P):
         assert_bit_equal(host[r].numpy(), want[r], "float32", f"e2e rank {r}")
         assert_bit_equal(dev[r].cpu().numpy(), want[r], "float32", f"e2e dev rank {r}")
@@ -369,13 +399,15 @@ def test_execute_host_pipelined_windows(order):
     P, n = 7, 10_000_003
     bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2, seed=77)
     host = [torch.from_numpy(b.copy()).pin_memory() for b in bufs]
-    dev = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(P)]
+    rb = RankBufs(P, n, "float32")
+    dev = rb.views
     plan = ar.Plan(P, n, "float32", "sum", "ring", order=order)
     for _ in range(2):  # second call reuses the plan's streams and events
         for r in range(P):
             host[r].copy_(torch.from_numpy(bufs[r]))
         plan.execute_host(host, dev)
         plan.check()
+        rb.check_guards("windows")
         if order == "faithful":
             want = oracle.run("ring", bufs, Arith("sum", "float32")).bufs
             for r in range(P):
@@ -401,10 +433,12 @@ def test_execute_host_windows_trees_and_bf16(P, n, dtype, algo):
     tdt = torch.bfloat16 if dtype == "bfloat16" else torch.float32
     host = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16).copy()).view(tdt).pin_memory()
             if dtype == "bfloat16" else torch.from_numpy(b.copy()).pin_memory() for b in bufs]
-    dev = [torch.empty(n, dtype=tdt, device="cuda") for _ in range(P)]
+    rb = RankBufs(P, n, dtype)
+    dev = rb.views
     plan = ar.Plan(P, n, dtype, "sum", algo)
     plan.execute_host(host, dev)
     plan.check()
+    rb.check_guards("windows")
     want = oracle.run(algo, bufs, Arith("sum", dtype)).bufs
     for r in range(P):
         got = host[r].view(torch.int16).numpy().view(np.uint16) if dtype == "bfloat16" else host[r].numpy()
@@ -424,10 +458,12 @@ def test_execute_host_windows_for_the_halves(algo, phase):
     assert ar.Schedule(P, n, "float32", "sum", algo, phase=phase).lowering()["windows"] >= 2
     bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2, seed=17)
     host = [torch.from_numpy(b.copy()).pin_memory() for b in bufs]
-    dev = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(P)]
+    rb = RankBufs(P, n, "float32")
+    dev = rb.views
     plan = ar.Plan(P, n, "float32", "sum", algo, phase=phase)
     plan.execute_host(host, dev)
     plan.check()
+    rb.check_guards("windows")
     want = oracle.run(algo, bufs, Arith("sum", "float32"), phase=phase)
     if phase == "reduce_scatter":
         for r, lo, hi in want.info["owner"]:
@@ -445,7 +481,8 @@ def test_repeated_execute_and_streams():
     P, n = 8, 1 << 18
     bufs = ar_synth.rank_inputs(P, n, "int32", "small_int", seed=2)
     plan = ar.Plan(P, n, "int32", "sum", "ring")
-    dev = [to_dev(b, "int32") for b in bufs]
+    rb = RankBufs.from_host(bufs, "int32")
+    dev = rb.views
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -460,6 +497,7 @@ def test_repeated_execute_and_streams():
     for _ in range(3):
         x = (x * P)
     want = (x.astype(np.int64) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
+    rb.check_guards("repeated")
     for t in dev:
         assert np.array_equal(to_host(t, "int32"), want)
     plan.close()
@@ -569,22 +607,13 @@ def test_avg_fp32acc_and_halves(dtype):
 
 
 def test_avg_unaligned_and_int32_refused():
-    import torch
-
     import collective_reduction_gb300 as ar
     P, n = 3, 1001
     bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1.0, seed=8)
     want = oracle.run("ring", bufs, Arith("avg", "float32")).bufs
-    base = [torch.zeros(n + 1, dtype=torch.float32, device="cuda") for _ in range(P)]
-    dev = [b[1:] for b in base]  # 4-byte offset: element-wise path
-    for d, h in zip(dev, bufs):
-        d.copy_(torch.from_numpy(h))
-    plan = ar.Plan(P, n, "float32", "avg", "ring")
-    plan.execute(dev)
-    torch.cuda.synchronize()
-    plan.check()
+    got = engine(bufs, "float32", "avg", "ring", offset=1)  # 4-byte offset: element-wise path
     for r in range(P):
-        assert_bit_equal(dev[r].cpu().numpy(), want[r], "float32", f"rank {r}")
+        assert_bit_equal(got[r], want[r], "float32", f"rank {r}")
     with pytest.raises(ar.ArError):
         ar.Plan(P, n, "int32", "avg", "ring")
 
@@ -656,12 +685,13 @@ def test_dag_kernel_jit_bit_exact(algo, P, op, kw, dtype):
         info = plan.info()
         staged = bool(info["kernels"] & ar.KERNEL_STAGED)
         assert bool(info["kernels"] & ar.KERNEL_DAG_JIT) == (staged and jit == "on"), (jit, info["kernels"])
-        dev = [to_dev(b, dtype) for b in bufs]
-        plan.execute(dev)
+        rb = RankBufs.from_host(bufs, dtype)
+        plan.execute(rb.views)
         torch.cuda.synchronize()
         plan.check()
+        rb.check_guards(f"{algo} {kw} jit={jit}")
         for r in range(P):
-            assert_bit_equal(to_host(dev[r], dtype), want[r], dtype, f"{algo} {kw} jit={jit} rank {r}")
+            assert_bit_equal(to_host(rb.views[r], dtype), want[r], dtype, f"{algo} {kw} jit={jit} rank {r}")
         plan.close()
 
 
@@ -684,10 +714,12 @@ def test_execute_captures_in_a_cuda_graph(algo, kw):
     P, n = 7, (1 << 18) + 13
     bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2, seed=23)
     plan = ar.Plan(P, n, "float32", "sum", algo, **kw)
-    direct = [to_dev(b, "float32") for b in bufs]
+    rd = RankBufs.from_host(bufs, "float32")
+    direct = rd.views
     plan.execute(direct)
     torch.cuda.synchronize()
-    graphed = [to_dev(b, "float32") for b in bufs]
+    rg = RankBufs.from_host(bufs, "float32")
+    graphed = rg.views
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
@@ -695,11 +727,12 @@ def test_execute_captures_in_a_cuda_graph(algo, kw):
         with torch.cuda.graph(g, stream=s):
             plan.execute(graphed, stream=s)
     torch.cuda.synchronize()
-    for d, b in zip(graphed, bufs):  # capture does not run the kernels: restore, replay once
-        d.copy_(to_dev(b, "float32"))
+    rg.fill(bufs)  # capture does not run the kernels: restore, replay once
     g.replay()
     torch.cuda.synchronize()
     plan.check()
+    rd.check_guards("direct")
+    rg.check_guards("graphed")
     for r in range(P):
         assert_bit_equal(to_host(graphed[r], "float32"), to_host(direct[r], "float32"), "float32", f"rank {r}")
 
