@@ -64,6 +64,11 @@ def parse():
                     help="DAG programs as run-time compiled code (auto / on) or interpreted (off)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--offset", type=int, default=0,
+                    help="place every rank buffer this many elements past a 256-byte boundary "
+                         "(not a multiple of 16 bytes: the element-wise path)")
+    ap.add_argument("--no-floor", action="store_true",
+                    help="skip the config5_floor points timed after the headline")
     ap.add_argument("--sweep", default=None, help="write the size sweep as JSON lines to this file")
     ap.add_argument("--rows", default=None,
                     help="time every schedule at the bench size (fused and step), JSON lines to this file")
@@ -83,6 +88,7 @@ def esize(dtype):
 def workload_name(a):
     return (f"{a.algo} allreduce, {a.form} {a.order}, P={a.P} x {a.mib:g} MiB {a.dtype} per rank, "
             f"op={a.op}" + (f", r={a.r}" if a.algo == "generalized" else "")
+            + (f", buffers offset by {a.offset} elements" if getattr(a, "offset", 0) else "")
             + (f", k1={a.k1}" if a.algo == "hybrid" else "")
             + (f", phase={a.phase}" if a.phase != "allreduce" else ""))
 
@@ -363,6 +369,72 @@ def cpu_baseline_and_check(a, sample_in, sample_out_engine, parts, timed=True):
                       f"{runs} oracle runs in {wall:.1f} s (single process: {runs1} runs in {dt1:.1f} s)"}, ok
 
 
+# The weakest points of the large-size target (the fused kernel at >= 64 MB per
+# rank): the ring over the sweep's largest P and size, both dtypes, both orders.
+FLOOR_POINTS = [(64, 256, "float32", "faithful"), (64, 256, "float32", "fp32acc"),
+                (64, 256, "bfloat16", "faithful"), (64, 256, "bfloat16", "fp32acc")]
+
+
+def config5_floor(stream, peak, steps=20, warmup=3):
+    """Times each FLOOR_POINTS plan (fused ring) back to back with CUDA events
+    on the launching stream, after checking it against the oracle on 512
+    sampled elements of every chunk (bit for bit; fp32-accumulated within
+    tolerance).  One dict per point."""
+    import numpy as np
+    import torch
+
+    import ar_synth
+    import collective_reduction_gb300 as ar
+    import oracle
+    from oracle.direct import direct_f64, normwise_rel_err
+    from oracle.elementops import Arith, bf16_to_f32
+    mods = (oracle, Arith, direct_f64, normwise_rel_err, bf16_to_f32)
+    out = []
+    for P, mib, dtype, order in FLOOR_POINTS:
+        n = (mib << 20) // esize(dtype)
+        if P * n * esize(dtype) * 1.1 > torch.cuda.mem_get_info()[0]:
+            out.append({"P": P, "bytes_per_rank": mib << 20, "dtype": dtype, "order": order, "skipped": "memory"})
+            continue
+        dev = ar_synth.device_inputs(P, n, dtype, sigma=1e-3, seed=P)
+        plan = ar.Plan(P, n, dtype, "sum", "ring", order=order)
+        info = plan.info()
+        sample_in, idx = gather_sample(dev, P, n, 512, P)
+        plan.execute(dev, stream)
+        plan.check()
+        got = [t.index_select(0, idx) for t in dev]
+        got = [g.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bfloat16" else g.cpu().numpy()
+               for g in got]
+        if order == "fp32acc":
+            ref = direct_f64(sample_in, "sum", dtype)
+            err = max(normwise_rel_err(bf16_to_f32(g) if dtype == "bfloat16" else g, ref) for g in got)
+            ok = bool(err <= (1e-6 if dtype == "float32" else 4e-3))
+        else:
+            want = oracle.run("ring", sample_in, Arith("sum", dtype)).bufs
+            ok = all(np.array_equal(np.ascontiguousarray(g).view(np.uint8), np.ascontiguousarray(w).view(np.uint8))
+                     for g, w in zip(got, want))
+        for _ in range(warmup):
+            plan.execute(dev, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            plan.execute(dev, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        plan.check()
+        ms = e0.elapsed_time(e1) / steps
+        gbps = info["hbm_bytes"] / (ms / 1e3) / 1e9
+        out.append({"P": P, "bytes_per_rank": mib << 20, "dtype": dtype, "form": "fused", "order": order,
+                    "steps": steps, "ms_per_step": round(ms, 4), "allreduced_GBps": round(P * n * esize(dtype) / ms / 1e6, 1),
+                    "achieved_hbm_GBps": round(gbps, 1), "frac": round(gbps / peak, 4),
+                    "frac_of_nominal_7900": round(gbps / NOMINAL_HBM_GBS, 4),
+                    "verified_sample_vs_oracle": ok})
+        plan.close()
+        del dev
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(a):
     import numpy as np
     import torch
@@ -386,6 +458,13 @@ def run_ours(a):
                              generator=torch.Generator("cuda").manual_seed(r)) for r in range(a.P)]
     else:
         dev = ar_synth.device_inputs(a.P, n, a.dtype, sigma=1e-3, seed=rank)
+    if a.offset:
+        shifted = []
+        for t in dev:
+            big = torch.empty(n + a.offset, dtype=t.dtype, device="cuda")
+            big[a.offset:].copy_(t)
+            shifted.append(big[a.offset:])
+        dev = shifted
     plan = ar.Plan(a.P, n, a.dtype, a.op, a.algo, **params)
     info = plan.info()
     stream = torch.cuda.current_stream()
@@ -451,6 +530,16 @@ def run_ours(a):
     e2e_s = max_over_ranks(e2e_s, world)
     plan.check()
 
+    # the weakest large-size points, timed after the headline's region with
+    # its buffers released
+    floor = None
+    if not a.no_floor:
+        del host
+        plan.close()
+        del dev
+        torch.cuda.empty_cache()
+        floor = config5_floor(stream, peak)
+
     # the CPU baseline is timed at N = 1 only (with N ranks on one host the
     # host cores are shared); rank 0 still checks its sample against the oracle
     cpu, verified = (None, None)
@@ -490,6 +579,8 @@ def run_ours(a):
         "gpu_launches": info["launches"] * a.steps,
         "verified_sample_vs_oracle": verified,
     }
+    if floor is not None:
+        line["config5_floor"] = floor
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()

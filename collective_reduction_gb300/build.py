@@ -37,12 +37,17 @@ def nvcc():
     return p
 
 
-def write_jit_headers(path):
-    """The JIT headers as C++ raw string literals, by include name."""
+def write_jit_headers(path, defines=()):
+    """The JIT headers as C++ raw string literals, by include name; the
+    build's -D macros lead the first one, so the run-time compiled kernels
+    see the configuration the compiled ones do."""
     names, bodies = [], []
+    prefix = "".join(f"#define {d.split('=', 1)[0]} {d.split('=', 1)[1] if '=' in d else 1}\n" for d in defines)
     for h in JIT_HEADERS:
         with open(h) as f:
             text = f.read()
+        if h == JIT_HEADERS[0]:
+            text = prefix + text
         if ")ARJIT\"" in text:
             raise RuntimeError(f"{h} contains the raw-string delimiter")
         names.append(os.path.basename(h))
@@ -62,7 +67,7 @@ def build(verbose=False, defines=(), out=None):
     common = ["-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
     common += [f"-D{d}" for d in defines]
     with tempfile.TemporaryDirectory(prefix="ar_build_") as tmp:
-        write_jit_headers(os.path.join(tmp, "jit_headers.inc"))
+        write_jit_headers(os.path.join(tmp, "jit_headers.inc"), defines)
         common += ["-I", tmp]
         procs, objs = [], []
         for src in SOURCES:

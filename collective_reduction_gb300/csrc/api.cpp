@@ -24,6 +24,15 @@ constexpr uint64_t kJitMinBytes = 16ull << 20;
 // Programs beyond this many instruction words stay interpreted: the
 // compile time grows past a few seconds.
 constexpr size_t kJitMaxWords = 4096;
+// DAG programs with at least this many inputs run on the run-time compiled
+// word kernel (registers) rather than the staged kernel (shared-memory
+// tiles that shrink as the input count grows).
+#ifndef AR_WORD_MIN_IN
+#define AR_WORD_MIN_IN 33
+#endif
+constexpr int kWordMinIn = AR_WORD_MIN_IN;
+// Persistent grid of the chain word kernel: CTAs per SM (16 warps).
+constexpr int kChainWordCtasPerSm = 4;
 // Guard bands around the step form's scratch: written with kGuardByte when
 // the plan is created and compared by ar_plan_check, so a kernel that writes
 // past either end of the scratch is reported rather than silently
@@ -50,7 +59,9 @@ struct ar_plan_s {
     uint64_t slot_stride = 0;
     uint64_t scratch_bytes = 0;
     int* d_status = nullptr;
-    const void* dag_fn = nullptr;  // run-time compiled staged kernel, or null: interpret
+    const void* dag_fn = nullptr;   // run-time compiled staged kernel, or null: interpret
+    const void* word_fn = nullptr;  // run-time compiled word kernel (word sets need it)
+    int word_grid = 0;              // its persistent grid: SMs x resident CTAs
     struct Set {
         const ar::WorkItem* bulk;
         const ar::WorkItem* edge;
@@ -59,6 +70,10 @@ struct ar_plan_s {
         bool stream;
         bool small;
         bool tma_store;
+        bool words;
+        bool chain_words;
+        bool chains;
+        int max_in;
     };
     std::vector<Set> sets;
     // element windows of a fused plan for the pipelined host path
@@ -167,10 +182,17 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
         a.items = s.bulk + b0;
         a.n_items = b1 - b0;
         const int grid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms));
-        if (s.stream) {
+        if (s.words) {
+            const int wgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->word_grid));
+            e = ar::launch_dependent(plan->word_fn, wgrid, ar::kWordThreads, 0, st, a);
+        } else if (s.chain_words) {
+            const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * kChainWordCtasPerSm));
+            e = ar::launch_chain_words(S.dtype, S.op, a, s.max_in, cgrid, st);
+        } else if (s.stream) {
             a.tile_bytes = plan->L.stream_tile;
             a.stages = plan->L.stream_stages;
-            a.flags = (s.tma_store ? ar::kArgTmaStore : 0) | (plan->L.stream_trees ? ar::kArgTrees : 0);
+            a.flags = (s.tma_store ? ar::kArgTmaStore : 0) | (plan->L.stream_trees ? ar::kArgTrees : 0) |
+                      (plan->L.stream_tmem ? ar::kArgTmemStack : 0);
             a.max_in = 1;
             a.max_tmp = plan->L.stream_slots;  // tree stack tiles after the stages
             e = ar::launch_stream(S.dtype, S.op, a, grid, plan->smem_stream, st);
@@ -194,6 +216,17 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
         e = ar::launch_elementwise(S.dtype, S.op, a, plan->smem_elem, st);
     }
     return e;
+}
+
+// How a plan with this jit setting lowers: the word kernel for DAG sets when
+// the run-time compiler is there (AUTO: for sets of at least kJitMinBytes).
+ar::LowerOptions lower_options(int jit) {
+    ar::LowerOptions lo;
+    lo.jit_dag = jit != AR_JIT_OFF && ar::jit_available();
+    lo.word_dag = lo.jit_dag;
+    lo.word_min_in = kWordMinIn;
+    lo.word_min_bytes = jit == AR_JIT_ON ? 0 : kJitMinBytes;
+    return lo;
 }
 
 // Element windows for the pipelined host path (fused plans; ar::host_windows).
@@ -293,14 +326,17 @@ ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes) {
     *cubin_bytes = 0;
     try {
         ar::Lowered L;
-        ar::lower(s->S, L);
-        const std::string src = ar::dag_kernel_source(s->S, L);
-        if (src.empty()) return AR_OK;
-        std::string cubin;
-        const int rc = ar::compile_dag_kernel(src, cubin, nullptr);
-        if (rc == 1) return AR_ERR_UNSUPPORTED;
-        if (rc != 0) return AR_ERR_CUDA;
-        *cubin_bytes = cubin.size();
+        ar::LowerOptions lo = lower_options(AR_JIT_ON);
+        lo.word_dag = true;  // compile the word kernel too (a missing NVRTC is reported below)
+        ar::lower(s->S, L, lo);
+        for (const std::string& src : {ar::dag_kernel_source(s->S, L), ar::word_kernel_source(s->S, L)}) {
+            if (src.empty()) continue;
+            std::string cubin;
+            const int rc = ar::compile_dag_kernel(src, cubin, nullptr);
+            if (rc == 1) return AR_ERR_UNSUPPORTED;
+            if (rc != 0) return AR_ERR_CUDA;
+            *cubin_bytes += cubin.size();
+        }
         return AR_OK;
     } catch (const std::length_error&) {
         return AR_ERR_UNSUPPORTED;
@@ -314,7 +350,7 @@ ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
     *out = ar_lowering_info{};
     try {
         ar::Lowered L;
-        ar::lower(s->S, L);
+        ar::lower(s->S, L, lower_options(s->S.params.jit));
         const int es = ar::esize_of(s->S.dtype);
         std::vector<ar::Window> W;
         if (L.sets.size() == 1)
@@ -331,6 +367,8 @@ ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
         out->staged_tile_bytes = L.tile_bytes;
         out->staged_stages = L.stages;
         out->dag_words = ar::dag_kernel_words(L);
+        out->word_kernel_words = ar::word_kernel_words(L);
+        for (const ar::LaunchSet& ls : L.sets) out->word_sets += ls.words;
         return AR_OK;
     } catch (const std::bad_alloc&) {
         return AR_ERR_NOMEM;
@@ -350,8 +388,9 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             delete p;
             return st;
         }
+        ar::LowerOptions lo = lower_options(p->S.params.jit);
         try {
-            ar::lower(p->S, p->L);
+            ar::lower(p->S, p->L, lo);
         } catch (const std::length_error&) {
             delete p;
             return AR_ERR_UNSUPPORTED;
@@ -365,6 +404,25 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             delete p;
             return cuda_status(e);
         }
+        // the word-kernel sets' programs as run-time compiled code; without
+        // it (no NVRTC, too many instruction words, a failed compile) the
+        // plan is lowered again with those sets on the staged kernel
+        const size_t wwords = ar::word_kernel_words(p->L);
+        if (wwords > 0) {
+            if (wwords <= kJitMaxWords)
+                p->word_fn = ar::load_dag_kernel(ar::word_kernel_source(p->S, p->L), "ar_word_kernel");
+            int nb = 0;
+            if (p->word_fn &&
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, p->word_fn, ar::kWordThreads, 0) == cudaSuccess &&
+                nb > 0) {
+                p->word_grid = p->num_sms * nb;
+            } else {
+                cudaGetLastError();
+                p->word_fn = nullptr;
+                lo.word_dag = false;
+                ar::lower(p->S, p->L, lo);
+            }
+        }
         const ar::Lowered& L = p->L;
         p->smem_staged = ar::staged_smem_bytes(L);
         p->smem_stream = ar::stream_smem_bytes(L);
@@ -373,14 +431,26 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             delete p;
             return AR_ERR_UNSUPPORTED;
         }
-        // the staged launches' DAG programs as run-time compiled code
+        // the staged launches' DAG programs as run-time compiled code; a plan
+        // lowered for compiled programs (no shared-memory temporaries) that
+        // is not compiled after all is lowered again for the interpreter
         const size_t words = ar::dag_kernel_words(L);
         if (words > 0 && words <= kJitMaxWords && p->S.params.jit != AR_JIT_OFF) {
             uint64_t dag_bytes = 0;
             for (const ar::LaunchSet& s : L.sets)
-                if (!s.stream && !s.small && !s.bulk.empty()) dag_bytes += s.bytes;
+                if (!s.stream && !s.small && !s.words && !s.chain_words && !s.bulk.empty()) dag_bytes += s.bytes;
             if (p->S.params.jit == AR_JIT_ON || dag_bytes >= kJitMinBytes)
                 p->dag_fn = ar::load_dag_kernel(ar::dag_kernel_source(p->S, L));
+        }
+        if (!p->dag_fn && lo.jit_dag && words > 0) {
+            lo.jit_dag = false;
+            ar::lower(p->S, p->L, lo);
+            p->smem_staged = ar::staged_smem_bytes(L);
+            p->smem_elem = (L.max_in_all + L.max_tmp_all) * ar::kElemThreads * 4;
+            if (p->smem_staged > optin || p->smem_elem > optin) {
+                delete p;
+                return AR_ERR_UNSUPPORTED;
+            }
         }
         // one device blob: programs, refs, instructions, then every item list
         std::vector<char> blob;
@@ -426,6 +496,10 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             s.stream = L.sets[i].stream;
             s.small = L.sets[i].small;
             s.tma_store = L.sets[i].tma_store;
+            s.words = L.sets[i].words;
+            s.chain_words = L.sets[i].chain_words;
+            s.max_in = L.sets[i].max_in;
+            s.chains = L.sets[i].chains;
             p->sets.push_back(s);
         }
         make_windows(p);
@@ -458,8 +532,12 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info) {
             info->kernels |= AR_KERNEL_ELEMENTWISE;
             continue;
         }
-        if (!s.bulk.empty()) info->kernels |= s.stream ? AR_KERNEL_STREAM : AR_KERNEL_STAGED;
-        if (!s.bulk.empty() && !s.stream && plan->dag_fn) info->kernels |= AR_KERNEL_DAG_JIT;
+        if (!s.bulk.empty())
+            info->kernels |= s.words         ? AR_KERNEL_WORD_JIT
+                             : s.chain_words ? AR_KERNEL_CHAIN_WORD
+                             : s.stream      ? AR_KERNEL_STREAM
+                                             : AR_KERNEL_STAGED;
+        if (!s.bulk.empty() && !s.stream && !s.words && plan->dag_fn) info->kernels |= AR_KERNEL_DAG_JIT;
         if (!s.edge.empty()) info->kernels |= AR_KERNEL_ELEMENTWISE;
     }
     return AR_OK;
@@ -485,10 +563,19 @@ ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ar::KernelArgs a;
     base_args(plan, rank_bufs, a);
+    // buffers off 16-byte alignment: chains of 4-byte elements (every
+    // element on a 32-bit word) on the chain word kernel, the rest element
+    // by element
+    const bool words_ok = ar::esize_of(S.dtype) == 4;
     for (const auto& s : plan->sets) {
         cudaError_t e = cudaSuccess;
         if (aligned && !s.small) {
             e = launch_range(plan, a, s, 0, s.n_bulk, 0, s.n_edge, st);
+        } else if (s.n_fallback && !aligned && !s.small && words_ok && s.chains) {
+            a.items = s.fallback;
+            a.n_items = s.n_fallback;
+            const int cgrid = static_cast<int>(std::min<uint32_t>(s.n_fallback, plan->num_sms * kChainWordCtasPerSm));
+            e = ar::launch_chain_words(S.dtype, S.op, a, s.max_in, cgrid, st);
         } else if (s.n_fallback) {
             a.items = s.fallback;
             a.n_items = s.n_fallback;

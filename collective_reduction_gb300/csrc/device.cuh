@@ -118,16 +118,20 @@ template <int DT>
 struct Acc {
     static constexpr int W = DT == AR_BFLOAT16 ? 8 : 4;
     float f[W];
+};
+template <>
+struct Acc<AR_INT32> {
+    static constexpr int W = 4;
     int32_t i[4];
 };
 
 template <int DT>
 __device__ __forceinline__ void acc_widen(Acc<DT>& x, uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    if (DT == AR_INT32) {
+    if constexpr (DT == AR_INT32) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) x.i[q] = static_cast<int32_t>(w[q]);
-    } else if (DT == AR_FLOAT32) {
+    } else if constexpr (DT == AR_FLOAT32) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) x.f[q] = __uint_as_float(w[q]);
     } else {
@@ -141,7 +145,7 @@ __device__ __forceinline__ void acc_widen(Acc<DT>& x, uint4 v) {
 
 template <int DT, int OP>
 __device__ __forceinline__ void acc_combine(Acc<DT>& x, const Acc<DT>& y) {
-    if (DT == AR_INT32) {
+    if constexpr (DT == AR_INT32) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) x.i[q] = iop<OP>(x.i[q], y.i[q]);
     } else {
@@ -153,7 +157,7 @@ __device__ __forceinline__ void acc_combine(Acc<DT>& x, const Acc<DT>& y) {
 // AR_AVG on the fp32 accumulator, before the one rounding to the dtype
 template <int DT>
 __device__ __forceinline__ void acc_div(Acc<DT>& x, float d) {
-    if (DT != AR_INT32) {
+    if constexpr (DT != AR_INT32) {
 #pragma unroll
         for (int q = 0; q < Acc<DT>::W; ++q) x.f[q] = __fdiv_rn(x.f[q], d);
     }
@@ -161,28 +165,41 @@ __device__ __forceinline__ void acc_div(Acc<DT>& x, float d) {
 
 template <int DT>
 __device__ __forceinline__ uint4 acc_narrow(const Acc<DT>& x) {
-    if (DT == AR_INT32)
+    if constexpr (DT == AR_INT32)
         return make_uint4(static_cast<uint32_t>(x.i[0]), static_cast<uint32_t>(x.i[1]),
                           static_cast<uint32_t>(x.i[2]), static_cast<uint32_t>(x.i[3]));
-    if (DT == AR_FLOAT32)
+    else if constexpr (DT == AR_FLOAT32)
         return make_uint4(__float_as_uint(x.f[0]), __float_as_uint(x.f[1]), __float_as_uint(x.f[2]),
                           __float_as_uint(x.f[3]));
-    return make_uint4(pack_bf16x2(x.f[0], x.f[1]), pack_bf16x2(x.f[2], x.f[3]), pack_bf16x2(x.f[4], x.f[5]),
-                      pack_bf16x2(x.f[6], x.f[7]));
+    else
+        return make_uint4(pack_bf16x2(x.f[0], x.f[1]), pack_bf16x2(x.f[2], x.f[3]), pack_bf16x2(x.f[4], x.f[5]),
+                          pack_bf16x2(x.f[6], x.f[7]));
 }
 
 // FP32ACC order over inputs 0..n-1 (the kernels' own fixed order, identical
-// in every kernel and for every rank): blocks of 8 consecutive inputs are
-// each folded left to right, then the block results are folded left to
-// right; fp32 / bf16 accumulate in fp32 and round once at the end (an AR_AVG
-// sum divided by div first; div = 0 for the other ops).  Inputs are fed one
-// at a time, so the order can be followed while inputs stream in.
+// in every kernel and for every rank).  fp32 and int32: blocks of 8
+// consecutive inputs are each folded left to right, then the block results
+// are folded left to right.  bf16: one fp32 running sum folded left to right
+// over all inputs (its rounding error, at most (n - 1) fp32 half-units of
+// the running magnitudes, stays far below the one final rounding to bf16,
+// and one accumulator per value keeps a 32 KB rank tile in registers).
+// fp32 / bf16 round once at the end (an AR_AVG sum divided by div first;
+// div = 0 for the other ops).  Inputs are fed one at a time, so the order
+// can be followed while inputs stream in.
 template <int DT, int OP>
 struct AccStream {
+    static constexpr bool kBlocks = DT != AR_BFLOAT16;
     Acc<DT> acc, blk;
     __device__ __forceinline__ void feed(uint32_t i, uint4 x) {
         Acc<DT> w;
         acc_widen<DT>(w, x);
+        if constexpr (!kBlocks) {
+            if (i == 0)
+                acc = w;
+            else
+                acc_combine<DT, OP>(acc, w);
+            return;
+        }
         if ((i & 7u) == 0)
             blk = w;
         else
@@ -195,7 +212,7 @@ struct AccStream {
         }
     }
     __device__ __forceinline__ uint4 finish(uint32_t n, float div) {
-        if (n & 7u) {
+        if (kBlocks && (n & 7u)) {
             if (n < 8u)
                 acc = blk;
             else
@@ -231,6 +248,18 @@ __device__ __forceinline__ char* out_addr(const KernelArgs& a, const DevProg& pg
     return buf_addr(a, a.refs[pg.out_off + o]);
 }
 
+// 32-bit global accesses of the run-time compiled word kernel: each value is
+// read once and its slot written once by the same thread (streaming hints)
+__device__ __forceinline__ uint32_t ldg32(const char* p) {
+    uint32_t v;
+    asm volatile("ld.global.cs.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg32(char* p, uint32_t v) {
+    asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -240,6 +269,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
 
@@ -270,6 +305,46 @@ __device__ __forceinline__ uint64_t globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+
+// ------------------------------------------------------ tensor memory (TMEM)
+//
+// The rank-streaming kernel's deep-tree instantiation keeps its stack in the
+// SM's tensor memory (256 KB: 128 lanes x 512 columns of 32 bits) instead of
+// shared memory, which then holds only pipeline stages.  One warp allocates
+// the columns (the address goes to shared memory for the others) and frees
+// them once every user is done; a warp reaches the 32 lanes of its quarter
+// (warp id mod 4), each thread its own lane.
+__device__ __forceinline__ void tmem_alloc(uint32_t smem_dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_dst), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// this thread's 8 x 16 bytes to 32 consecutive columns of its lane (the
+// whole warp executes it)
+__device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint4 (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w), "r"(v[4].x), "r"(v[4].y), "r"(v[4].z), "r"(v[4].w), "r"(v[5].x), "r"(v[5].y), "r"(v[5].z), "r"(v[5].w), "r"(v[6].x), "r"(v[6].y), "r"(v[6].z), "r"(v[6].w), "r"(v[7].x), "r"(v[7].y), "r"(v[7].z), "r"(v[7].w) : "memory");
+}
+
+// ... and back; waits for the warp's earlier stores and for this load
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, uint4 (&v)[8]) {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0].x), "=r"(v[0].y), "=r"(v[0].z), "=r"(v[0].w), "=r"(v[1].x), "=r"(v[1].y), "=r"(v[1].z), "=r"(v[1].w), "=r"(v[2].x), "=r"(v[2].y), "=r"(v[2].z), "=r"(v[2].w), "=r"(v[3].x), "=r"(v[3].y), "=r"(v[3].z), "=r"(v[3].w), "=r"(v[4].x), "=r"(v[4].y), "=r"(v[4].z), "=r"(v[4].w), "=r"(v[5].x), "=r"(v[5].y), "=r"(v[5].z), "=r"(v[5].w), "=r"(v[6].x), "=r"(v[6].y), "=r"(v[6].z), "=r"(v[6].w), "=r"(v[7].x), "=r"(v[7].y), "=r"(v[7].z), "=r"(v[7].w)
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------ dependent launches
 //
@@ -370,8 +445,56 @@ struct Stage {
     uint32_t stage_bytes;
 };
 
+// Items with more inputs than this take the warp-wide staged producer.
+constexpr uint32_t kWarpProducerMinIn = 16;
+
 template <int ES>
 __device__ void produce(const KernelArgs& a, const Stage& sm) {
+    // The whole warp: lane 0 waits for a free stage and issues the copies;
+    // the lanes resolve 32 source addresses at a time (one global load of a
+    // buffer id each, all in flight together) and hand them to lane 0.
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t policy = AR_L2_EVICT_FIRST ? evict_first_policy() : 0;
+    uint32_t k = 0;
+    bool ok = true;
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x, ++k) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        const uint32_t s = k % a.stages, ph = (k / a.stages) & 1u;
+        int free = 0;
+        if (lane == 0) free = mbar_wait(sm.empty + 8 * s, ph ^ 1u);
+        if (!__shfl_sync(0xFFFFFFFFu, free, 0)) {
+            if (lane == 0) atomicOr(a.status, kStatusWaitEmpty);
+            ok = false;
+            break;
+        }
+        const uint32_t nb = w.count * ES;
+        const uint32_t bar = sm.full + 8 * s;
+        if (lane == 0) mbar_expect_tx(bar, nb * pg.n_in);
+        const uint32_t dst = sm.tiles + s * sm.stage_bytes;
+        for (uint32_t i0 = 0; i0 < pg.n_in; i0 += 32) {
+            const char* mine = nullptr;
+            if (i0 + lane < pg.n_in) mine = buf_addr(a, a.refs[pg.in_off + i0 + lane]) + w.elem * ES;
+            const uint32_t cnt = min(32u, pg.n_in - i0);
+            for (uint32_t j = 0; j < cnt; ++j) {
+                const char* src = reinterpret_cast<const char*>(
+                    __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(mine), j));
+                if (lane == 0) bulk_load(dst + (i0 + j) * a.tile_bytes, src, nb, bar, policy);
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        // let the copies already issued land before the CTA can exit
+        const uint32_t first = k > static_cast<uint32_t>(a.stages) ? k - a.stages : 0;
+        for (uint32_t j = first; j < k; ++j)
+            if (!mbar_wait(sm.full + 8 * (j % a.stages), (j / a.stages) & 1u)) atomicOr(a.status, kStatusDrain);
+    }
+}
+
+// The staged producer for items of few inputs: one thread resolves each
+// address and issues its copy.
+template <int ES>
+__device__ void produce1(const KernelArgs& a, const Stage& sm) {
     const uint64_t policy = AR_L2_EVICT_FIRST ? evict_first_policy() : 0;
     uint32_t k = 0;
     bool ok = true;
@@ -540,7 +663,13 @@ __device__ __forceinline__ void staged_body(const KernelArgs& a, uint8_t* smem, 
     griddep_wait();
     griddep_launch_dependents();
     if (threadIdx.x < 32) {
-        if (threadIdx.x == 0) produce<ES>(a, sm);
+        // many inputs per item: the whole warp resolves the addresses
+        // (measured +15-20 points of the copy peak at P = 31 ... 64); few:
+        // one thread (the warp's shuffles cost 30-40 points at P = 7 ... 16)
+        if (a.max_in > kWarpProducerMinIn)
+            produce<ES>(a, sm);
+        else if (threadIdx.x == 0)
+            produce1<ES>(a, sm);
         return;
     }
     consume<DT, OP>(a, sm, threadIdx.x - 32, [&](const DevProg& pg, uint32_t prog, uint32_t st, uint32_t nvec,

@@ -50,11 +50,13 @@ constexpr int kConsumerWarps = 8;
 constexpr int kElemBlock = 64;       // element-wise kernel: threads = elements per block
 constexpr int kStagedVpt = 4;
 constexpr int kStreamVpt = 8;        // rank-streaming kernel, chains and fp32 / int32 accumulation
-constexpr int kStreamVptNarrow = 4;  // rank-streaming kernel, bf16 fp32 accumulation (16 fp32 per vector)
-constexpr int kStreamVptTree = 6;    // rank-streaming kernel, trees deeper than the wide tiles allow
+constexpr int kStreamVptTree = 6;    // rank-streaming kernel: trees deeper than the wide tiles allow, bf16 fp32 accumulation
 constexpr int kMaxStagedTile = 32 * kConsumerWarps * 16 * kStagedVpt;          // 16 KB
+// chain word kernel: threads per CTA (one 32-bit word each per item pass),
+// most inputs / outputs of a program it runs
+constexpr int kChainWordThreads = 128;
+constexpr int kChainWordMaxIn = 64;
 constexpr int kStreamTileBytes = 32 * kConsumerWarps * 16 * kStreamVpt;        // 32 KB
-constexpr int kStreamTileNarrow = 32 * kConsumerWarps * 16 * kStreamVptNarrow; // 16 KB
 constexpr int kStreamTileTree = 32 * kConsumerWarps * 16 * kStreamVptTree;     // 24 KB
 // TREE programs: leaves in post-order, and after each leaf the number of
 // combines that follow it (4 bits per leaf, 8 leaves per instruction word).

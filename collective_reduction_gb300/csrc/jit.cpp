@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <dlfcn.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <map>
 #include <mutex>
@@ -16,6 +17,16 @@
 
 #include "kargs.hpp"
 
+// Word kernel code generation: prefetch the next position's input words
+// (1) or load each position's words when it is reached (0); CTAs per SM the
+// launch bounds ask registers for.
+#ifndef AR_WORD_PIPE
+#define AR_WORD_PIPE 0
+#endif
+#ifndef AR_WORD_MIN_BLOCKS
+#define AR_WORD_MIN_BLOCKS 1
+#endif
+
 namespace ar {
 namespace {
 
@@ -26,7 +37,7 @@ namespace {
 std::set<uint32_t> staged_dag_programs(const Lowered& L) {
     std::set<uint32_t> ids;
     for (const LaunchSet& s : L.sets) {
-        if (s.stream || s.small) continue;
+        if (s.stream || s.small || s.words) continue;
         for (const WorkItem& w : s.bulk)
             if (L.progs[w.prog].kind == PK_DAG) ids.insert(w.prog);
     }
@@ -88,7 +99,286 @@ void emit_program(std::ostringstream& o, const Lowered& L, uint32_t id, int P) {
     o << "    }\n}\n\n";
 }
 
+// Programs used by bulk items of word-kernel launches.
+std::set<uint32_t> word_programs(const Lowered& L) {
+    std::set<uint32_t> ids;
+    for (const LaunchSet& s : L.sets) {
+        if (!s.words) continue;
+        for (const WorkItem& w : s.bulk) ids.insert(w.prog);
+    }
+    return ids;
+}
+
+// Address expression of buffer id at byte position `pos` (P ranks).
+std::string word_addr(uint32_t id, int P, bool out, const char* pos) {
+    const uint32_t slot = id >> 6, rank = id & 63u;
+    std::ostringstream o;
+    if (slot == 0)
+        o << "static_cast<" << (out ? "char*" : "const char*") << ">(a.bufs[" << rank << "])";
+    else
+        o << "(a.scratch + " << static_cast<uint64_t>(slot - 1) * P + rank << "ull * a.slot_stride)";
+    o << " + " << pos;
+    return o.str();
+}
+
+// One program over 32-bit words.  Each thread takes word t, t + kWordThreads,
+// ... of the item; it holds every input word of the current position in
+// registers (x*) and, with `pipe`, has the next position's words in flight
+// (y*) while it combines and stores the current one, so a warp's loads stay
+// outstanding through its arithmetic.  The combines follow the program's
+// order (chains: the fold; DAG: the instruction list).  Loads of the next
+// position never touch an address the current stores write (positions
+// differ), and every word of a position is loaded before any is stored.
+void emit_word_program(std::ostringstream& o, const Lowered& L, uint32_t id, int P, int threads, bool pipe) {
+    const DevProg& d = L.progs[id];
+    auto loads = [&](const char* var, const char* pos, const char* indent) {
+        for (uint32_t i = 0; i < d.n_in; ++i)
+            o << indent << var << i << " = ldg32(" << word_addr(L.refs[d.in_off + i], P, false, pos) << ");\n";
+    };
+    o << "__device__ __forceinline__ void wp_" << id << "(const KernelArgs& a, int64_t off, uint32_t nw) {\n";
+    o << "    uint32_t t = threadIdx.x;\n    if (t >= nw) return;\n";
+    o << "    uint32_t";
+    for (uint32_t i = 0; i < d.n_in; ++i) o << (i ? ", x" : " x") << i;
+    o << ";\n";
+    if (pipe) {
+        o << "    {\n        const int64_t pos = off + 4 * static_cast<int64_t>(t);\n";
+        loads("x", "pos", "        ");
+        o << "    }\n";
+    }
+    o << "#pragma unroll 1\n"
+         "    for (; t < nw; t += "
+      << threads
+      << "u) {\n"
+         "        const int64_t pos = off + 4 * static_cast<int64_t>(t);\n";
+    if (pipe) {
+        o << "        const uint32_t tn = t + " << threads << "u;\n";
+        o << "        const int64_t npos = off + 4 * static_cast<int64_t>(tn < nw ? tn : t);\n";
+        o << "        uint32_t";
+        for (uint32_t i = 0; i < d.n_in; ++i) o << (i ? ", y" : " y") << i;
+        o << ";\n";
+        loads("y", "npos", "        ");
+    } else {
+        loads("x", "pos", "        ");
+    }
+    auto store = [&](uint32_t buf, const std::string& v, bool avg) {
+        o << "        stg32(" << word_addr(buf, P, true, "pos") << ", "
+          << (avg ? "wdiv<DT>(" + v + ", " + std::to_string(P) + ".0f)" : v) << ");\n";
+    };
+    if (d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L) {
+        std::string acc = "x0";
+        for (uint32_t i = 1; i < d.n_in; ++i) {
+            const std::string t = "c" + std::to_string(i);
+            const std::string x = "x" + std::to_string(i);
+            o << "        const uint32_t " << t << " = wop<DT, OP>(" << (d.kind == PK_CHAIN_R ? x + ", " + acc : acc + ", " + x)
+              << ");\n";
+            acc = t;
+        }
+        const bool avg = (d.flags & PF_AVG) != 0;
+        for (uint32_t q = 0; q < d.n_out; ++q)
+            store((d.flags & PF_OUT_ALL) ? buf_id(0, static_cast<int>(q)) : L.refs[d.out_off + q], acc, avg);
+    } else if (d.kind == PK_DAG) {
+        // The instruction list in SSA form (ops name fresh values; the
+        // temporaries and the accumulator of the list are reused slots),
+        // then emitted level by level: an op after the ops it reads, in
+        // order of its depth above the inputs.  Every combine reads the same
+        // two values in any such order, so the results are the list's bits,
+        // and a level's values die once the next level has read them (a
+        // butterfly keeps about 2 P values live, not the post-order's many).
+        struct Op {
+            int a, b, level;
+        };
+        std::vector<Op> ops;                          // value n_in + k is ops[k]
+        std::vector<std::pair<uint32_t, std::pair<int, bool>>> stores;  // (buffer, (value, avg))
+        std::map<uint32_t, int> tmp;
+        int acc = -1;
+        auto value = [&](uint32_t r) -> int {
+            if (r == REF_ACC) return acc;
+            if (r & REF_TMP) return tmp.at(r & 0x1FFu);
+            if (r >= d.n_in) throw std::logic_error("dag program reads a missing input");
+            return static_cast<int>(r);
+        };
+        auto level = [&](int v) { return v < static_cast<int>(d.n_in) ? 0 : ops[v - d.n_in].level; };
+        for (uint32_t q = 0; q < d.n_ins; ++q) {
+            const uint32_t w = L.ins[d.ins_off + q];
+            if ((w >> 30) == INS_OP) {
+                const int x = value(w & 0x3FFu), y = value((w >> 10) & 0x3FFu);
+                if (x < 0 || y < 0) throw std::logic_error("dag program reads an unset accumulator");
+                ops.push_back({x, y, std::max(level(x), level(y)) + 1});
+                const int v = static_cast<int>(d.n_in + ops.size() - 1);
+                const uint32_t rd = (w >> 20) & 0x3FFu;
+                if (rd == REF_ACC)
+                    acc = v;
+                else
+                    tmp[rd & 0x1FFu] = v;
+            } else {
+                const int v = value(w & 0x3FFu);
+                if (v < 0) throw std::logic_error("dag program stores an unset accumulator");
+                stores.push_back({(w >> 10) & 0xFFFFu, {v, (w >> 30) == INS_STORE_AVG}});
+            }
+        }
+        std::vector<int> order(ops.size());
+        for (size_t k = 0; k < ops.size(); ++k) order[k] = static_cast<int>(k);
+        std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return ops[x].level < ops[y].level; });
+        auto name = [&](int v) {
+            return v < static_cast<int>(d.n_in) ? "x" + std::to_string(v) : "t" + std::to_string(v - d.n_in);
+        };
+        std::map<int, std::vector<size_t>> stores_of;
+        for (size_t k = 0; k < stores.size(); ++k) stores_of[stores[k].second.first].push_back(k);
+        auto emit_stores = [&](int v) {
+            auto it = stores_of.find(v);
+            if (it == stores_of.end()) return;
+            for (size_t k : it->second) store(stores[k].first, name(v), stores[k].second.second);
+        };
+        for (uint32_t i = 0; i < d.n_in; ++i) emit_stores(static_cast<int>(i));
+        for (int k : order) {
+            o << "        const uint32_t t" << k << " = wop<DT, OP>(" << name(ops[k].a) << ", " << name(ops[k].b)
+              << ");\n";
+            emit_stores(static_cast<int>(d.n_in) + k);
+        }
+    } else {
+        throw std::logic_error("word kernel: a program kind it does not run");
+    }
+    if (pipe)
+        for (uint32_t i = 0; i < d.n_in; ++i) o << "        x" << i << " = y" << i << ";\n";
+    o << "    }\n}\n\n";
+}
+
+// A DAG program of the staged kernel over 32-bit words (programs of many
+// inputs, whose 16-byte vectors would not all fit in registers): each
+// consumer thread takes words ct, ct + kConsumers, ... of the item's tiles,
+// loads an input word from its stage tile at first use, and evaluates the
+// instruction list in SSA form level by level (an op after the ops it
+// reads, in order of its depth above the inputs: the same combines of the
+// same values as the list's order, with fewer values live at once), storing
+// each result word straight to its output.
+void emit_program_words(std::ostringstream& o, const Lowered& L, uint32_t id, int P) {
+    const DevProg& d = L.progs[id];
+    struct Op {
+        int a, b, level;
+    };
+    std::vector<Op> ops;  // value n_in + k is ops[k]
+    std::vector<std::pair<uint32_t, std::pair<int, bool>>> stores;  // (buffer, (value, avg))
+    std::map<uint32_t, int> tmp;
+    int acc = -1;
+    auto value = [&](uint32_t r) -> int {
+        if (r == REF_ACC) return acc;
+        if (r & REF_TMP) return tmp.at(r & 0x1FFu);
+        if (r >= d.n_in) throw std::logic_error("dag program reads a missing input");
+        return static_cast<int>(r);
+    };
+    auto level = [&](int v) { return v < static_cast<int>(d.n_in) ? 0 : ops[v - d.n_in].level; };
+    for (uint32_t q = 0; q < d.n_ins; ++q) {
+        const uint32_t w = L.ins[d.ins_off + q];
+        if ((w >> 30) == INS_OP) {
+            const int x = value(w & 0x3FFu), y = value((w >> 10) & 0x3FFu);
+            if (x < 0 || y < 0) throw std::logic_error("dag program reads an unset accumulator");
+            ops.push_back({x, y, std::max(level(x), level(y)) + 1});
+            const int v = static_cast<int>(d.n_in + ops.size() - 1);
+            const uint32_t rd = (w >> 20) & 0x3FFu;
+            if (rd == REF_ACC)
+                acc = v;
+            else
+                tmp[rd & 0x1FFu] = v;
+        } else {
+            const int v = value(w & 0x3FFu);
+            if (v < 0) throw std::logic_error("dag program stores an unset accumulator");
+            stores.push_back({(w >> 10) & 0xFFFFu, {v, (w >> 30) == INS_STORE_AVG}});
+        }
+    }
+    std::vector<int> order(ops.size());
+    for (size_t k = 0; k < ops.size(); ++k) order[k] = static_cast<int>(k);
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return ops[x].level < ops[y].level; });
+    std::map<int, std::vector<size_t>> stores_of;
+    for (size_t k = 0; k < stores.size(); ++k) stores_of[stores[k].second.first].push_back(k);
+
+    o << "__device__ __forceinline__ void dag_" << id
+      << "(const KernelArgs& a, uint32_t st, uint32_t nvec, int64_t off, int ct) {\n"
+         "#pragma unroll 1\n"
+         "    for (uint32_t w = ct; w < 4u * nvec; w += kConsumers) {\n"
+         "        const uint32_t s = st + 4u * w;\n"
+         "        const int64_t pos = off + 4 * static_cast<int64_t>(w);\n";
+    std::vector<char> loaded(d.n_in, 0);
+    auto name = [&](int v) -> std::string {
+        if (v >= static_cast<int>(d.n_in)) return "t" + std::to_string(v - d.n_in);
+        if (!loaded[v]) {
+            o << "        const uint32_t x" << v << " = lds32(s + " << static_cast<uint64_t>(v) * L.tile_bytes
+              << "u);\n";
+            loaded[v] = 1;
+        }
+        return "x" + std::to_string(v);
+    };
+    auto emit_stores = [&](int v) {
+        auto it = stores_of.find(v);
+        if (it == stores_of.end()) return;
+        const std::string x = name(v);
+        for (size_t k : it->second) {
+            const uint32_t buf = stores[k].first, slot = buf >> 6, rank = buf & 63u;
+            o << "        stg32(";
+            if (slot == 0)
+                o << "static_cast<char*>(a.bufs[" << rank << "])";
+            else
+                o << "(a.scratch + " << static_cast<uint64_t>(slot - 1) * P + rank << "ull * a.slot_stride)";
+            o << " + pos, " << (stores[k].second.second ? "wdiv<DT>(" + x + ", " + std::to_string(P) + ".0f)" : x)
+              << ");\n";
+        }
+    };
+    for (uint32_t i = 0; i < d.n_in; ++i) emit_stores(static_cast<int>(i));
+    for (int k : order) {
+        const std::string x = name(ops[k].a), y = name(ops[k].b);
+        o << "        const uint32_t t" << k << " = wop<DT, OP>(" << x << ", " << y << ");\n";
+        emit_stores(static_cast<int>(d.n_in) + k);
+    }
+    o << "    }\n}\n\n";
+}
+
 }  // namespace
+
+size_t word_kernel_words(const Lowered& L) {
+    size_t n = 0;
+    for (uint32_t id : word_programs(L)) n += L.progs[id].kind == PK_DAG ? L.progs[id].n_ins : L.progs[id].n_in;
+    return n;
+}
+
+std::string word_kernel_source(const Schedule& S, const Lowered& L) {
+    const std::set<uint32_t> ids = word_programs(L);
+    if (ids.empty()) return std::string();
+    const int op = S.op == AR_AVG ? AR_SUM : S.op;  // avg: sums, divided where stored
+    const int es = esize_of(S.dtype);
+    std::ostringstream o;
+    o << "// word kernel of one plan: P = " << S.P << ", dtype " << S.dtype << ", op " << S.op << ", " << ids.size()
+      << " programs\n"
+         "typedef signed char int8_t;\ntypedef unsigned char uint8_t;\ntypedef short int16_t;\n"
+         "typedef unsigned short uint16_t;\ntypedef int int32_t;\ntypedef unsigned int uint32_t;\n"
+         "typedef long long int64_t;\ntypedef unsigned long long uint64_t;\n"
+         "#include \"device.cuh\"\n"
+         "namespace ar {\nnamespace {\n"
+      << "constexpr int DT = " << S.dtype << ";\nconstexpr int OP = " << op << ";\n\n";
+    for (uint32_t id : ids) emit_word_program(o, L, id, S.P, kWordThreads, AR_WORD_PIPE != 0);
+    o << "}  // namespace\n}  // namespace ar\n\n"
+         "extern \"C\" __global__ void __launch_bounds__("
+      << kWordThreads << ", " << AR_WORD_MIN_BLOCKS
+      << ")\n"
+         "ar_word_kernel(const __grid_constant__ ar::KernelArgs a) {\n"
+         "    ar::griddep_wait();\n"
+         "    ar::griddep_launch_dependents();\n"
+         "    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {\n"
+         "        const ar::WorkItem w = a.items[it];\n"
+         "        const int64_t off = w.elem * "
+      << es
+      << ";\n"
+         "        const uint32_t nw = static_cast<uint32_t>((static_cast<uint64_t>(w.count) * "
+      << es
+      << ") >> 2);\n"
+         "        switch (w.prog) {\n";
+    for (uint32_t id : ids) o << "            case " << id << "u: ar::wp_" << id << "(a, off, nw); break;\n";
+    o << "            default:\n"
+         "                if (threadIdx.x == 0) atomicOr(a.status, ar::kStatusBadProgram);\n"
+         "                return;\n"
+         "        }\n"
+         "    }\n"
+         "}\n";
+    return o.str();
+}
 
 size_t dag_kernel_words(const Lowered& L) {
     size_t n = 0;
@@ -109,7 +399,12 @@ std::string dag_kernel_source(const Schedule& S, const Lowered& L) {
          "#include \"device.cuh\"\n"
          "namespace ar {\nnamespace {\n"
       << "constexpr int DT = " << S.dtype << ";\nconstexpr int OP = " << op << ";\n\n";
-    for (uint32_t id : ids) emit_program(o, L, id, S.P);
+    for (uint32_t id : ids) {
+        if (L.progs[id].n_in > kWordConsumerMinIn)
+            emit_program_words(o, L, id, S.P);
+        else
+            emit_program(o, L, id, S.P);
+    }
     o << "}  // namespace\n}  // namespace ar\n\n"
          "extern \"C\" __global__ void __launch_bounds__(ar::kStagedThreads, 1)\n"
          "ar_dag_kernel(const __grid_constant__ ar::KernelArgs a) {\n"
@@ -166,6 +461,8 @@ const Nvrtc& nvrtc() {
 
 }  // namespace
 
+bool jit_available() { return nvrtc().ok; }
+
 int compile_dag_kernel(const std::string& src, std::string& cubin, std::string* log) {
     const Nvrtc& n = nvrtc();
     if (!n.ok) return 1;
@@ -195,7 +492,7 @@ int compile_dag_kernel(const std::string& src, std::string& cubin, std::string* 
     return status;
 }
 
-const void* load_dag_kernel(const std::string& src) {
+const void* load_dag_kernel(const std::string& src, const char* name) {
     static std::mutex mu;
     static std::map<std::pair<int, std::string>, const void*> cache;  // (device, source) -> kernel
     int dev = 0;
@@ -213,7 +510,7 @@ const void* load_dag_kernel(const std::string& src) {
         // the library stays loaded for the life of the process (shared by
         // every plan with the same programs)
         if (cudaLibraryLoadData(&lib, cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0) == cudaSuccess &&
-            cudaLibraryGetKernel(&k, lib, "ar_dag_kernel") == cudaSuccess &&
+            cudaLibraryGetKernel(&k, lib, name) == cudaSuccess &&
             cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
             cudaFuncSetAttribute(reinterpret_cast<const void*>(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin) == cudaSuccess)

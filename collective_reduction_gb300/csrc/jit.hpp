@@ -9,6 +9,12 @@
 // NVRTC (loaded at run time, so the library does not depend on it) and loads
 // it with the CUDA runtime.  The arithmetic is the interpreter's, in the
 // interpreter's order: the results are bit for bit the same.
+//
+// Sets whose DAG programs read many inputs run instead on the word kernel,
+// written here too: each thread takes one 32-bit word of every input
+// buffer straight from global memory into registers, evaluates the item's
+// program on them (chains and DAG programs alike) and stores one word to
+// every output, so its footprint does not depend on the input count.
 #pragma once
 
 #include <cstddef>
@@ -33,9 +39,20 @@ std::string dag_kernel_source(const Schedule& S, const Lowered& L);
 // compiler's log in *log when log is not null).
 int compile_dag_kernel(const std::string& src, std::string& cubin, std::string* log);
 
-// The loaded kernel for src on the current device (compiled and loaded once
-// per source and device, then cached), ready for cudaLaunchKernel with the
-// dynamic shared memory limit raised; nullptr on any failure.
-const void* load_dag_kernel(const std::string& src);
+// Instruction words of the programs the plan's word-kernel launches run
+// (0: no word-kernel launch).
+size_t word_kernel_words(const Lowered& L);
+
+// CUDA C source of the plan's word kernel (its entry point is
+// ar_word_kernel); empty when word_kernel_words(L) is 0.
+std::string word_kernel_source(const Schedule& S, const Lowered& L);
+
+// True when NVRTC can be loaded (the run-time compiled kernels are possible).
+bool jit_available();
+
+// The loaded kernel `name` of src on the current device (compiled and loaded
+// once per source and device, then cached), ready for cudaLaunchKernel with
+// the dynamic shared memory limit raised; nullptr on any failure.
+const void* load_dag_kernel(const std::string& src, const char* name = "ar_dag_kernel");
 
 }  // namespace ar

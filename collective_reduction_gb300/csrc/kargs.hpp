@@ -36,6 +36,9 @@ constexpr int kArgTmaStore = 1;
 // KernelArgs::flags: the launch has single-tree programs (the rank-streaming
 // kernel's tree instantiations; a.max_tmp stack tiles follow the stages)
 constexpr int kArgTrees = 2;
+// KernelArgs::flags: the tree stack lives in tensor memory (the 32 KB-tile
+// tree instantiation that allocates it; a.max_tmp entries, at most 8)
+constexpr int kArgTmemStack = 4;
 
 // Status word bits written by the kernels.
 constexpr int kStatusWaitFull = 1;   // a consumer gave up waiting for a stage

@@ -109,6 +109,13 @@ __device__ void stream_produce(const KernelArgs& a, const Stage& sm) {
 // warp 0 produces, warp 1 stores (TMA-store epilogue only), the rest consume
 constexpr int kStreamLead = 2;
 constexpr int kStreamThreads = 32 * (kStreamLead + kConsumerWarps);
+// tensor-memory tree stack: all 512 columns (two consumer warps per lane
+// quarter, 256 columns = 8 entries of 32 each), the allocated address kept in
+// the last word of the barrier area (full / ready / empty barriers take 24
+// bytes per stage, at most kMaxStreamStages stages)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemAddrOffset = kBarrierBytes - 8;
+static_assert(kTmemAddrOffset >= 24 * (kBarrierBytes / 24), "the barrier area's last word is free");
 
 __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -209,9 +216,14 @@ __device__ __forceinline__ void stream_finish(const KernelArgs& a, const Stage& 
 // the rest fold shared-memory entries into the top (entry (+) top: the left
 // operand is the deeper one).  FULL: the item covers a whole tile, so every
 // thread's VPT vectors are in range and the bounds test is left out.
-template <int DT, int OP, int VPT, bool FULL>
+//
+// TM: the stack entries below the top live in tensor memory instead (tstack:
+// this warp's lanes and columns; 32 columns per entry, one tcgen05.st / ld per
+// push / pop, by the whole warp, every vector alike).
+template <int DT, int OP, int VPT, bool FULL, bool TM>
 __device__ __forceinline__ bool stream_tree(const KernelArgs& a, const Stage& sm, const DevProg& pg, uint32_t& g,
-                                            int64_t off, uint32_t nvec, int ct) {
+                                            int64_t off, uint32_t nvec, int ct, uint32_t tstack) {
+    static_assert(!TM || VPT == 8, "the TMEM stack moves 8 vectors per entry");
     const int lane = ct & 31;
     if (pg.n_tmp > static_cast<uint32_t>(a.max_tmp)) {  // deeper than the launch's stack
         atomicOr(a.status, kStatusBadProgram);
@@ -225,11 +237,15 @@ __device__ __forceinline__ bool stream_tree(const KernelArgs& a, const Stage& sm
         uint32_t c = (a.ins[pg.ins_off + (i >> 3)] >> (4 * (i & 7))) & 15u;
         if (sp == 0 || c == 0) {
             if (sp > 0) {
-                const uint32_t slot = sm.tmps + (sp - 1) * a.tile_bytes;
+                if constexpr (TM) {
+                    tmem_store32(tstack + (sp - 1) * 32u, acc);
+                } else {
+                    const uint32_t slot = sm.tmps + (sp - 1) * a.tile_bytes;
 #pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    const uint32_t v = ct + j * kConsumers;
-                    if (FULL || v < nvec) sts128(slot + v * 16, acc[j]);
+                    for (int j = 0; j < VPT; ++j) {
+                        const uint32_t v = ct + j * kConsumers;
+                        if (FULL || v < nvec) sts128(slot + v * 16, acc[j]);
+                    }
                 }
             }
 #pragma unroll
@@ -247,11 +263,18 @@ __device__ __forceinline__ bool stream_tree(const KernelArgs& a, const Stage& sm
             --c;
         }
         for (; c > 0; --c, --sp) {
-            const uint32_t slot = sm.tmps + (sp - 2) * a.tile_bytes;
+            if constexpr (TM) {
+                uint4 e[VPT];
+                tmem_load32(tstack + (sp - 2) * 32u, e);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const uint32_t v = ct + j * kConsumers;
-                if (FULL || v < nvec) acc[j] = vop<DT, OP>(lds128(slot + v * 16), acc[j]);
+                for (int j = 0; j < VPT; ++j) acc[j] = vop<DT, OP>(e[j], acc[j]);
+            } else {
+                const uint32_t slot = sm.tmps + (sp - 2) * a.tile_bytes;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    const uint32_t v = ct + j * kConsumers;
+                    if (FULL || v < nvec) acc[j] = vop<DT, OP>(lds128(slot + v * 16), acc[j]);
+                }
             }
         }
         if (i + 1 < pg.n_in) {
@@ -271,12 +294,13 @@ __device__ __forceinline__ bool stream_tree(const KernelArgs& a, const Stage& sm
 // and trees); the others run chains and fp32 accumulation.  Keeping the tree
 // stack and the accumulators in separate instantiations keeps each within
 // the register budget.
-template <int DT, int OP, int VPT, bool TREES>
-__device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
+template <int DT, int OP, int VPT, bool TREES, bool TM>
+__device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct, uint32_t tstack) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
-    // bf16 fp32 accumulation holds 16 floats per vector: only the narrow
-    // instantiation runs it (the lowering picks the narrow tile for it)
-    constexpr bool kAccOk = !(DT == AR_BFLOAT16 && VPT > kStreamVptNarrow);
+    // fp32 accumulation holds 8 floats per 16-byte vector (bf16: one running
+    // sum of 8 values; fp32: a block and a running sum of 4): at most
+    // kStreamVpt vectors per thread stay in registers
+    constexpr bool kAccOk = VPT <= kStreamVpt;
     constexpr int NA = kAccOk ? VPT : 1;
     const int lane = ct & 31;
     uint32_t g = 0;
@@ -293,8 +317,8 @@ __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
                 // trees gained nothing and keep one instantiation)
                 constexpr bool kWholeTilePath = DT == AR_BFLOAT16;
                 const bool ok = (kWholeTilePath && nvec == static_cast<uint32_t>(VPT * kConsumers))
-                                    ? stream_tree<DT, OP, VPT, kWholeTilePath>(a, sm, pg, g, off, nvec, ct)
-                                    : stream_tree<DT, OP, VPT, false>(a, sm, pg, g, off, nvec, ct);
+                                    ? stream_tree<DT, OP, VPT, kWholeTilePath, TM>(a, sm, pg, g, off, nvec, ct, tstack)
+                                    : stream_tree<DT, OP, VPT, false, TM>(a, sm, pg, g, off, nvec, ct, tstack);
                 if (!ok) return;
             } else {
                 atomicOr(a.status, kStatusBadProgram);
@@ -360,7 +384,11 @@ __device__ void stream_consume(const KernelArgs& a, const Stage& sm, int ct) {
     }
 }
 
-template <int DT, int OP, int VPT, bool TREES>
+// TM (tree instantiations): the tree stack in tensor memory; the first
+// consumer warp allocates kTmemCols columns before the roles split and frees
+// them after every consumer warp is done (a named barrier among them), on
+// every path out of the consumer loop.
+template <int DT, int OP, int VPT, bool TREES, bool TM = false>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_constant__ KernelArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
@@ -380,10 +408,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    const int warp = threadIdx.x >> 5;
+    const uint32_t tslot = sm.full + kTmemAddrOffset;  // the allocated address, in the barrier area
+    if constexpr (TM) {
+        if (warp == kStreamLead) tmem_alloc(tslot, kTmemCols);
+        tmem_fence_before();
+    }
     __syncthreads();
+    if constexpr (TM) tmem_fence_after();
     griddep_wait();
     griddep_launch_dependents();
-    const int warp = threadIdx.x >> 5;
     if (warp == 0) {
         stream_produce<ES>(a, sm);
         return;
@@ -392,7 +426,23 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const __grid_
         if (threadIdx.x == 32 && (a.flags & kArgTmaStore)) stream_store<ES>(a, sm);
         return;
     }
-    stream_consume<DT, OP, VPT, TREES>(a, sm, threadIdx.x - 32 * kStreamLead);
+    uint32_t tstack = 0;
+    if constexpr (TM) {
+        // this warp's quarter of the lanes; the two consumer warps on a
+        // quarter split its columns
+        const uint32_t base = *reinterpret_cast<volatile uint32_t*>(smem + kTmemAddrOffset);
+        tstack = base + ((32u * (warp & 3)) << 16) + (warp >= kStreamLead + 4 ? kTmemCols / 2 : 0u);
+    }
+    stream_consume<DT, OP, VPT, TREES, TM>(a, sm, threadIdx.x - 32 * kStreamLead, tstack);
+    if constexpr (TM) {
+        tmem_wait_st();
+        tmem_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumerWarps) : "memory");
+        if (warp == kStreamLead) {
+            tmem_fence_after();
+            tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(smem + kTmemAddrOffset), kTmemCols);
+        }
+    }
 }
 
 // --------------------------------------------------------- element kernel
@@ -544,19 +594,102 @@ __global__ void wait_selftest_kernel(int* status, uint64_t ns) {
     if (threadIdx.x == 0 && !mbar_wait_for(b, 0, ns)) atomicOr(status, kStatusWaitFull);
 }
 
+// ------------------------------------------------------- chain word kernel
+//
+// Chains (the ring's and the pipelined chain's programs) over passes too small
+// to fill the GPU with rank tiles.  A thread takes 32-bit words at the same
+// offset of every input buffer: k = kChainWordMaxIn / n_in word positions per
+// round (every input of each), so it has kChainWordMaxIn loads in flight
+// whatever P is, held in a register array indexed only by unrolled constants.
+// It folds each position's words in the program's order and stores the result
+// word to every output.  An item's buffer addresses are resolved once, into
+// shared memory, by the whole CTA.  Plain (cached) loads and stores: these
+// passes are small enough that their data may stay in L2 between calls.
+__device__ __forceinline__ uint32_t ld32(const char* p) {
+    uint32_t v;
+    asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st32(char* p, uint32_t v) {
+    asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+template <int DT, int OP, int M>
+__global__ void __launch_bounds__(kChainWordThreads) chain_word_kernel(const __grid_constant__ KernelArgs a) {
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    constexpr int K = kChainWordMaxIn / M;  // word positions per thread per round
+    __shared__ const char* src[M];
+    __shared__ char* dst[kChainWordMaxIn];
+    griddep_wait();
+    griddep_launch_dependents();
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        if ((pg.kind != PK_CHAIN_R && pg.kind != PK_CHAIN_L) || pg.n_in < 1 || pg.n_in > M ||
+            pg.n_out > kChainWordMaxIn) {
+            if (threadIdx.x == 0) atomicOr(a.status, kStatusBadProgram);
+            return;  // every thread alike, before any barrier of this item
+        }
+        const int64_t off = w.elem * ES;
+        __syncthreads();  // the previous item's addresses are read no more
+        for (uint32_t i = threadIdx.x; i < pg.n_in; i += blockDim.x) src[i] = buf_addr(a, a.refs[pg.in_off + i]) + off;
+        for (uint32_t o = threadIdx.x; o < pg.n_out; o += blockDim.x) dst[o] = out_addr(a, pg, o) + off;
+        __syncthreads();
+        const uint32_t n = pg.n_in;
+        const uint32_t nw = (w.count * ES) >> 2;
+        const bool right = pg.kind == PK_CHAIN_R;
+        const float div = avg_div(a, pg);
+        for (uint32_t base = threadIdx.x; base < nw; base += K * blockDim.x) {
+            uint32_t x[K][M];
+#pragma unroll
+            for (int i = 0; i < M; ++i)
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const uint32_t pos = base + j * blockDim.x;
+                    if (i < n && pos < nw) x[j][i] = ld32(src[i] + 4 * pos);
+                }
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const uint32_t pos = base + j * blockDim.x;
+                if (pos >= nw) break;
+                uint32_t acc = x[j][0];
+#pragma unroll
+                for (int i = 1; i < M; ++i)
+                    if (i < n) acc = right ? wop<DT, OP>(x[j][i], acc) : wop<DT, OP>(acc, x[j][i]);
+                if (div != 0.f) acc = wdiv<DT>(acc, div);
+                for (uint32_t o = 0; o < pg.n_out; ++o) st32(dst[o] + 4 * pos, acc);
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------- dispatch
 
 using KernelFn = void (*)(KernelArgs);
 
-enum Which { K_STAGED = 0, K_STREAM = 1, K_STREAM_NARROW = 2, K_ELEM = 3, K_STREAM_TREE = 4, K_STREAM_TREE_WIDE = 5 };
+enum Which {
+    K_STAGED = 0, K_STREAM = 1, K_ELEM = 3, K_STREAM_TREE = 4, K_STREAM_TREE_WIDE = 5, K_STREAM_MID = 6,
+    K_CHAIN_WORD = 7, K_CHAIN_WORD8 = 8, K_CHAIN_WORD16 = 9, K_STREAM_TREE_TMEM = 10
+};
+constexpr int kWhich[] = {K_STAGED,     K_STREAM,     K_ELEM,        K_STREAM_TREE,  K_STREAM_TREE_WIDE,
+                          K_STREAM_MID, K_CHAIN_WORD, K_CHAIN_WORD8, K_CHAIN_WORD16, K_STREAM_TREE_TMEM};
 
 template <int DT, int OP>
 KernelFn table(int which) {
     if (which == K_STAGED) return staged_kernel<DT, OP>;
     if (which == K_STREAM) return stream_kernel<DT, OP, kStreamVpt, false>;
-    if (which == K_STREAM_NARROW) return stream_kernel<DT, OP, kStreamVptNarrow, false>;
+    // bf16 fp32 accumulation on 24 KB tiles: 48 accumulators per thread stay
+    // in registers (with 64, the 32 KB tile's kernel spills)
+    if constexpr (DT == AR_BFLOAT16)
+        if (which == K_STREAM_MID) return stream_kernel<DT, OP, kStreamVptTree, false>;
+    if (which == K_STREAM_MID) return nullptr;
+    if (which == K_CHAIN_WORD8) return chain_word_kernel<DT, OP, 8>;
+    if (which == K_CHAIN_WORD16) return chain_word_kernel<DT, OP, 16>;
+    if (which == K_CHAIN_WORD) return chain_word_kernel<DT, OP, kChainWordMaxIn>;
     if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptTree, true>;
     if (which == K_STREAM_TREE_WIDE) return stream_kernel<DT, OP, kStreamVpt, true>;
+    if (which == K_STREAM_TREE_TMEM) return stream_kernel<DT, OP, kStreamVpt, true, true>;
     return elementwise_kernel<DT, OP>;
 }
 
@@ -608,9 +741,12 @@ cudaError_t prepare_kernels(int dtype, int op) {
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    for (int which : {K_STAGED, K_STREAM, K_STREAM_NARROW, K_ELEM, K_STREAM_TREE, K_STREAM_TREE_WIDE}) {
-        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel_for(dtype, op, which)),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    for (int which : kWhich) {
+        KernelFn f = kernel_for(dtype, op, which);
+        // (the chain word kernel has static shared memory only)
+        if (!f || which == K_CHAIN_WORD || which == K_CHAIN_WORD8 || which == K_CHAIN_WORD16) continue;
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -625,15 +761,23 @@ cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int 
     // the rank tile fixes the vectors per consumer thread
     const int which = (a.flags & kArgTrees)
                           ? (a.tile_bytes == kStreamTileTree    ? K_STREAM_TREE
+                             : a.tile_bytes == kStreamTileBytes && (a.flags & kArgTmemStack) ? K_STREAM_TREE_TMEM
                              : a.tile_bytes == kStreamTileBytes ? K_STREAM_TREE_WIDE
                                                                 : -1)
                       : a.tile_bytes == kStreamTileBytes  ? K_STREAM
-                      : a.tile_bytes == kStreamTileNarrow ? K_STREAM_NARROW
+                      : a.tile_bytes == kStreamTileTree   ? K_STREAM_MID
                                                           : -1;
     if (which < 0) return cudaErrorInvalidValue;
+    if (!kernel_for(dtype, op, which)) return cudaErrorInvalidValue;
     if (a.stages < 1 || a.stages > 32 || 24 * a.stages > kBarrierBytes) return cudaErrorInvalidValue;
+    return launch_dependent(reinterpret_cast<const void*>(kernel_for(dtype, op, which)), grid, kStreamThreads, smem,
+                            st, a);
+}
+
+cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_in, int grid, cudaStream_t st) {
+    const int which = max_in <= 8 ? K_CHAIN_WORD8 : max_in <= 16 ? K_CHAIN_WORD16 : K_CHAIN_WORD;
     KernelFn f = kernel_for(dtype, op, which);
-    return launch_dependent(reinterpret_cast<const void*>(f), grid, kStreamThreads, smem, st, a);
+    return launch_dependent(reinterpret_cast<const void*>(f), grid, kChainWordThreads, 0, st, a);
 }
 
 cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem, cudaStream_t st) {

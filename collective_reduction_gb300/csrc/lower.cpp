@@ -39,8 +39,33 @@
 #define AR_ACC_STAGES_4B 5
 #endif
 // ... and for bf16 chains (one bf16x2 instruction per element pair)
+#ifndef AR_TMEM_TREES
+#define AR_TMEM_TREES 0
+#endif
+#ifndef AR_TMEM_TREE_STAGES
+#define AR_TMEM_TREE_STAGES 7
+#endif
+#ifndef AR_JIT_GEOMETRY
+#define AR_JIT_GEOMETRY 1
+#endif
+#ifndef AR_JIT_WORD_STAGES
+#define AR_JIT_WORD_STAGES 3
+#endif
+constexpr int kStagesWord = 8;
 #ifndef AR_CHAIN_STAGES_BF16
 #define AR_CHAIN_STAGES_BF16 4
+#endif
+// bf16 fp32 accumulation: rank tile (bytes: 24 KB or 32 KB), pipeline depth
+// and TMA-store epilogue
+#ifndef AR_BF16_ACC_TILE
+#define AR_BF16_ACC_TILE 24576
+#endif
+#ifndef AR_ACC_STAGES_BF16
+#define AR_ACC_STAGES_BF16 7
+#endif
+static_assert(AR_BF16_ACC_TILE == 24576 || AR_BF16_ACC_TILE == 32768, "a rank tile some instantiation runs");
+#ifndef AR_BF16_ACC_TMA
+#define AR_BF16_ACC_TMA 1
 #endif
 
 namespace ar {
@@ -470,6 +495,13 @@ int64_t item_elems(const std::vector<Range>& rs, int64_t tile_elems, int64_t V) 
     return std::min(tile_elems, std::max(1024 / (16 / V), (want + V - 1) / V * V));
 }
 
+// Most inputs of a program of a set.
+int set_max_in(const Lowered& lw, const std::vector<Range>& rs) {
+    int m = 1;
+    for (const Range& r : rs) m = std::max<int>(m, lw.progs[r.prog].n_in);
+    return m;
+}
+
 // Mean elements per range (segment) of a set.
 int64_t mean_range(const std::vector<Range>& rs) {
     int64_t n = 0;
@@ -597,10 +629,10 @@ int staged_smem_bytes(const Lowered& lw) {
 }
 
 int stream_smem_bytes(const Lowered& lw) {
-    return kBarrierBytes + lw.stream_tile * (lw.stream_stages + lw.stream_slots);
+    return kBarrierBytes + lw.stream_tile * (lw.stream_stages + (lw.stream_tmem ? 0 : lw.stream_slots));
 }
 
-void lower(const Schedule& S, Lowered& lw) {
+void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
     lw = Lowered();
     const int es = esize_of(S.dtype);
     const int V = 16 / es;  // elements per 16-byte vector
@@ -617,12 +649,25 @@ void lower(const Schedule& S, Lowered& lw) {
             // wider tiles.
             const bool acc = S.params.order == AR_ORDER_FP32ACC &&
                              !(S.P == 2 && (S.dtype == AR_INT32 || S.op == AR_SUM || S.op == AR_PROD));
+            std::vector<std::pair<int, Prog>> progs;
+            bool any_dag = false;
             for (int s = 0; s < S.nseg(); ++s) {
                 if (S.bounds[s + 1] <= S.bounds[s]) continue;
                 const std::vector<int> ranks = defined_ranks(S, s);
                 if (ranks.empty()) continue;  // (an all-gather owner-only segment)
-                const Prog p = acc ? acc_program(S.P, ranks, S.op == AR_AVG) : fused_program(cn, S, s, ranks);
-                push_range(rs, b.add(p), S.bounds[s], S.bounds[s + 1]);
+                progs.push_back({s, acc ? acc_program(S.P, ranks, S.op == AR_AVG) : fused_program(cn, S, s, ranks)});
+                any_dag |= progs.back().second.kind == PK_DAG;
+            }
+            for (auto& sp : progs) {
+                // a pass with DAG programs does not stream: its single trees
+                // become DAG programs too (the staged and word kernels run
+                // chains and DAGs, not tree stacks)
+                if (any_dag && sp.second.kind == PK_TREE) {
+                    std::vector<std::pair<int, int32_t>> outs;
+                    for (int r : defined_ranks(S, sp.first)) outs.push_back({r, cn.get(S.final_at(r, sp.first))});
+                    sp.second = dag_program(cn.c, outs, S.op == AR_AVG);
+                }
+                push_range(rs, b.add(sp.second), S.bounds[sp.first], S.bounds[sp.first + 1]);
             }
             sets.push_back(rs);
         } else {
@@ -654,6 +699,55 @@ void lower(const Schedule& S, Lowered& lw) {
         small[k] = !sets[k].empty() && bytes <= (256u << 10);
         if (stream[k] && !small[k] && !trees && mean_range(sets[k]) * es < 4096) stream[k] = false;
     }
+    // Sets with DAG programs of many inputs run on the word kernel when it is
+    // available: its threads keep one 32-bit word of every input in registers,
+    // where the staged kernel's shared memory holds ever smaller tiles as the
+    // input count grows.
+    std::vector<bool> words(sets.size(), false);
+    for (size_t k = 0; k < sets.size(); ++k) {
+        if (!opt.word_dag || stream[k] || small[k]) continue;
+        int dag_in = 0;
+        uint64_t bytes = 0;
+        for (auto& r : sets[k]) {
+            const DevProg& d = lw.progs[r.prog];
+            if (d.kind == PK_DAG) dag_in = std::max<int>(dag_in, d.n_in);
+            bytes += static_cast<uint64_t>(d.n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
+        }
+        words[k] = dag_in >= opt.word_min_in && dag_in > 0 && bytes >= opt.word_min_bytes;
+    }
+    // Fused chain passes of up to AR_CHAIN_WORD_MAX_BYTES of traffic run on
+    // the chain word kernel when their chains are long: its small items
+    // spread the pass over every SM and each thread has 64 loads in flight,
+    // where the rank-streaming kernel takes one item (a chunk tile) per CTA
+    // and its P tiles one after another, and the element-wise kernel folds a
+    // chain in few threads.  Measured (fused ring, µs per call in a CUDA
+    // graph, against the previous kernels): P = 64 at 1-64 KiB per rank
+    // 5.4-5.6 against 7.2-19, 256 KiB 22.5 against 33; P = 16 at 4-64 KiB
+    // 3.2-4.7 against 5.1-11.7, 1 MiB 11.1 against 18.2; P = 8 at 64 KiB-1
+    // MiB 5-12% faster, at <= 16 KiB slower (the element-wise kernel's one
+    // launch is near the launch floor there) and at 4 MiB (64 MiB of
+    // traffic: the rank-streaming kernel fills the GPU), P = 2 slower at every
+    // size; the step form's rounds (P chains of two inputs each) slower at
+    // every size.
+    std::vector<bool> cwords(sets.size(), false);
+    for (size_t k = 0; k < sets.size(); ++k) {
+        if (sets[k].empty() || S.params.form != AR_FORM_FUSED) continue;
+        bool chains = true;
+        int max_in = 0;
+        uint64_t bytes = 0;
+        for (auto& r : sets[k]) {
+            const DevProg& d = lw.progs[r.prog];
+            chains = chains && (d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L) && d.n_in <= kChainWordMaxIn &&
+                     d.n_out <= kChainWordMaxIn;
+            max_in = std::max<int>(max_in, d.n_in);
+            bytes += static_cast<uint64_t>(d.n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
+        }
+        const bool long_chains = max_in >= 16 || (max_in >= 8 && !small[k]);
+        if (chains && long_chains && bytes <= AR_CHAIN_WORD_MAX_BYTES) {
+            cwords[k] = true;
+            stream[k] = small[k] = false;
+        }
+    }
     bool stream_trees = false;
     lw.stream_slots = 0;  // shared-memory tiles for the deepest tree stack
     for (size_t k = 0; k < sets.size(); ++k)
@@ -671,9 +765,9 @@ void lower(const Schedule& S, Lowered& lw) {
             lw.max_in_all = std::max<int>(lw.max_in_all, d.n_in);
             lw.max_tmp_all = std::max<int>(lw.max_tmp_all, d.n_tmp);
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
-            if (a < e && !stream[k] && !small[k]) {
+            if (a < e && !stream[k] && !small[k] && !words[k] && !cwords[k]) {
                 lw.max_in = std::max<int>(lw.max_in, d.n_in);
-                lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
+                if (!(opt.jit_dag && AR_JIT_GEOMETRY)) lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
             }
         }
     // deepest pipeline (up to kStages) that keeps tiles >= 6 KB, else 2 stages
@@ -688,8 +782,27 @@ void lower(const Schedule& S, Lowered& lw) {
     t = std::min<int64_t>(t, kMaxTileBytes);
     t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
     lw.tile_bytes = static_cast<int>(t);
-    // bf16 fp32 accumulation programs hold 16 fp32 per vector: 16 KB rank
-    // tiles (4 vectors per thread).  A tree keeps depth - 1 stack tiles in shared
+    // compiled programs of many inputs: tiles of 4, 2 or 1 KB (whole words
+    // for every consumer thread), the largest that keeps AR_JIT_WORD_STAGES
+    // stages, with as many stages as fit (at most kStagesWord)
+    if (opt.jit_dag && AR_JIT_GEOMETRY && lw.max_in > kWordConsumerMinIn) {
+        const int64_t room = kSmemBudget - kBarrierBytes;
+        int64_t wt = kWordTileUnit;
+        for (int64_t c = 4 * kWordTileUnit; c > kWordTileUnit; c /= 2)
+            if (room / (c * lw.max_in) >= AR_JIT_WORD_STAGES) {
+                wt = c;
+                break;
+            }
+        lw.tile_bytes = static_cast<int>(wt);
+        lw.stages = static_cast<int>(std::min<int64_t>(kStagesWord, room / (wt * lw.max_in)));
+        if (lw.stages < 2) throw std::length_error("staged kernel: too many inputs per program");
+    }
+    // bf16 fp32 accumulation keeps 8 fp32 per 16-byte vector: 24 KB rank
+    // tiles (6 vectors per thread: with 32 KB tiles the 64 accumulators and
+    // the tile loads exceed the 168 registers a 320-thread CTA gets, and the
+    // kernel spills; measured 24 KB with 7 stages against 32 KB with 7,
+    // 24 KB with 9 and 16 KB with 14: +2-4% at P = 4 ... 64 over 32 KB, e.g.
+    // P = 64 95.2% against 92.5% of the copy peak).  A tree keeps depth - 1 stack tiles in shared
     // memory next to the stages: 32 KB tiles while that leaves a pipeline of
     // at least 3 stages (trees of up to 16 leaves; measured +6% at P = 16 over
     // 16 KB tiles), 24 KB tiles for deeper trees (3 stages at 64 leaves, 4 at
@@ -699,12 +812,16 @@ void lower(const Schedule& S, Lowered& lw) {
     for (size_t k = 0; k < sets.size(); ++k)
         if (stream[k] && !small[k])
             for (auto& r : sets[k]) acc_streamed |= lw.progs[r.prog].kind == PK_ACC;
-    const bool narrow = S.dtype == AR_BFLOAT16 && acc_streamed;
+    const bool bf16_acc = S.dtype == AR_BFLOAT16 && acc_streamed;
     const bool deep = stream_trees && lw.stream_slots > AR_TREE_WIDE_SLOTS;
     lw.stream_trees = stream_trees;
-    lw.stream_tile = narrow ? kStreamTileNarrow : deep ? kStreamTileTree : kStreamTileBytes;
-    lw.stream_stages =
-        std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile - lw.stream_slots);
+    // deep trees with AR_TMEM_TREES: the stack in tensor memory, so 32 KB
+    // tiles and shared memory for stages only
+    lw.stream_tmem = deep && AR_TMEM_TREES && lw.stream_slots <= 8;
+    lw.stream_tile = bf16_acc ? AR_BF16_ACC_TILE : (deep && !lw.stream_tmem) ? kStreamTileTree : kStreamTileBytes;
+    lw.stream_stages = std::min(kMaxStages, (kStreamSmemBudget - kBarrierBytes) / lw.stream_tile -
+                                                (lw.stream_tmem ? 0 : lw.stream_slots));
+    if (lw.stream_tmem) lw.stream_stages = std::min(lw.stream_stages, AR_TMEM_TREE_STAGES);
     // Chains over 4-byte elements stream best with a short pipeline: with 7
     // stages in flight per SM the reads crowd out the writes.  Measured at
     // 256 MiB per rank, 3 stages against 7: fused ring +4% at P = 4 and 8,
@@ -714,10 +831,12 @@ void lower(const Schedule& S, Lowered& lw) {
     // bf16 chains, one bf16x2 instruction (or compare) per element pair,
     // peak at 4: against 7, sum fused ring +1% at P = 8, +3% at P = 16 and
     // 64, step rounds +1%, the reduce-scatter +5%; max / min +3-4%.  bf16
-    // fp32 accumulation keeps the full pipeline.
+    // fp32 accumulation on 24 KB tiles: 7 stages (9 fit) measured +2-3% at
+    // P = 4 ... 16, within 1% at 32 and 64.
     if (!stream_trees && es == 4)
         lw.stream_stages = std::min(lw.stream_stages, acc_streamed ? AR_ACC_STAGES_4B : AR_CHAIN_STAGES_4B);
     if (!stream_trees && es == 2 && !acc_streamed) lw.stream_stages = std::min(lw.stream_stages, AR_CHAIN_STAGES_BF16);
+    if (!stream_trees && es == 2 && acc_streamed) lw.stream_stages = std::min(lw.stream_stages, AR_ACC_STAGES_BF16);
     // The TMA-store epilogue holds an item's last stage until its outputs are
     // copied out.  Measured at the bench size with the pipelines above: in a
     // fused pass it wins for copies (one input, many outputs: the all-gather,
@@ -732,7 +851,7 @@ void lower(const Schedule& S, Lowered& lw) {
     // (recursive doubling's exchanges: TMA stores +3.5%, as for P = 2).
     const bool rounds = sets.size() > 1 || S.params.form == AR_FORM_STEP;
     auto tma_store = [&](const std::vector<Range>& set) {
-        if (S.dtype == AR_BFLOAT16 && acc_streamed) return true;
+        if (S.dtype == AR_BFLOAT16 && acc_streamed) return AR_BF16_ACC_TMA != 0;
         int max_out = 0, max_in = 0;
         for (auto& r : set) {
             max_out = std::max<int>(max_out, lw.progs[r.prog].n_out);
@@ -746,7 +865,20 @@ void lower(const Schedule& S, Lowered& lw) {
         LaunchSet ls;
         ls.stream = stream[k];
         ls.tma_store = stream[k] && tma_store(sets[k]);
-        const int64_t tile_elems = item_elems(sets[k], (stream[k] ? lw.stream_tile : lw.tile_bytes) / es, V);
+        int64_t tile_bytes = cwords[k]   ? chain_word_item_bytes(set_max_in(lw, sets[k]))
+                             : words[k]  ? kWordItemBytes
+                             : stream[k] ? lw.stream_tile
+                                         : lw.tile_bytes;
+        if (cwords[k]) {
+            // a small pass: items of down to 512 B so that there are about two
+            // per SM (each thread then has fewer positions, but the pass runs
+            // on more SMs at once)
+            int64_t rank_bytes = 0;
+            for (auto& r : sets[k]) rank_bytes += (r.hi - r.lo) * es;
+            const int64_t want = (rank_bytes / (2 * kSpreadItems) + 511) / 512 * 512;
+            tile_bytes = std::max<int64_t>(4 * kChainWordThreads, std::min(tile_bytes, want));
+        }
+        const int64_t tile_elems = item_elems(sets[k], tile_bytes / es, V);
         for (auto& r : sets[k]) {
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
             if (a < e) {
@@ -766,6 +898,15 @@ void lower(const Schedule& S, Lowered& lw) {
             ls.bytes += static_cast<uint64_t>(d.n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
         }
         ls.small = small[k];
+        ls.words = words[k];
+        ls.chain_words = cwords[k];
+        ls.max_in = set_max_in(lw, sets[k]);
+        ls.chains = !sets[k].empty();
+        for (auto& r : sets[k]) {
+            const DevProg& d = lw.progs[r.prog];
+            ls.chains = ls.chains && (d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L) && d.n_in <= kChainWordMaxIn &&
+                        d.n_out <= kChainWordMaxIn;
+        }
         lw.hbm_bytes += ls.bytes;
         lw.n_items += ls.small ? ls.fallback.size() : ls.bulk.size() + ls.edge.size();
         lw.launches += ls.small ? 1 : (!ls.bulk.empty()) + (!ls.edge.empty());

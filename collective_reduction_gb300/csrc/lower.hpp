@@ -1,6 +1,7 @@
 // Lowering of a compiled schedule to tile programs and work items.
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
 #include <vector>
 
@@ -18,6 +19,10 @@ struct LaunchSet {
     bool stream = false;             // bulk items run on the rank-streaming kernel
     bool tma_store = false;          // ... with the TMA bulk-store epilogue (else 128-bit stores)
     bool small = false;              // small set (<= 256 KB): one element-wise launch over fallback
+    bool words = false;              // bulk items run on the run-time compiled word kernel
+    bool chain_words = false;        // bulk items run on the chain word kernel
+    int max_in = 0;                  // most inputs of a program of the set
+    bool chains = false;             // every program is a chain the chain word kernel runs
 };
 
 struct Lowered {
@@ -30,6 +35,7 @@ struct Lowered {
     int stream_tile = 0;  // bytes per rank tile of the rank-streaming kernel
     int stream_stages = 0;
     bool stream_trees = false;      // rank-streaming kernel: the instantiation that runs TREE programs
+    bool stream_tmem = false;       // ... with the tree stack in tensor memory (no stack tiles)
     int stream_slots = 0;           // rank-streaming kernel: shared-memory tiles of the tree stack
     int max_in = 0;       // largest n_in of a program used by bulk items
     int max_tmp = 0;      // largest n_tmp of such a program
@@ -65,8 +71,42 @@ static_assert(kMaxTileBytes <= kMaxStagedTile, "staged tiles beyond what the con
 // full, empty and ready barriers (8 bytes each) per stage in the barrier area
 constexpr int kMaxStages = kBarrierBytes / 24;
 
+// The word kernel (run-time compiled): one thread per 32-bit word of every
+// rank, threads per CTA, rank bytes per work item.
+constexpr int kWordThreads = 256;
+constexpr int kWordItemBytes = 16384;
+// The chain word kernel: rank bytes per work item for programs of n_in
+// inputs (one round of its threads: kChainWordMaxIn / n_in words each), and
+// the largest set (bytes of traffic) it takes.
+inline int chain_word_item_bytes(int n_in) {
+    return 4 * kChainWordThreads * (n_in <= 8 ? 8 : n_in <= 16 ? 4 : 1);
+}
+#ifndef AR_CHAIN_WORD_MAX_BYTES
+#define AR_CHAIN_WORD_MAX_BYTES (32ull << 20)
+#endif
+
+struct LowerOptions {
+    // The staged launches' DAG programs will run as run-time compiled code:
+    // the staged kernel's geometry then reserves no shared-memory
+    // temporaries (the interpreter's), and programs of many inputs get
+    // tiles of whole 1 KB units (their compiled consumers take one 32-bit
+    // word per thread).
+    bool jit_dag = false;
+    // Sets with DAG programs of at least word_min_in inputs and at least
+    // word_min_bytes of traffic run on the word kernel (needs the run-time
+    // compiler); the others on the staged kernel.
+    bool word_dag = false;
+    int word_min_in = 1;
+    uint64_t word_min_bytes = 0;
+};
+
+// Compiled staged consumers take one 32-bit word of every input per thread
+// (rather than 16-byte vectors) for programs of more than this many inputs.
+constexpr int kWordConsumerMinIn = 16;
+constexpr int kWordTileUnit = 4 * 32 * kConsumerWarps;  // one word per consumer thread
+
 // Builds the fused pass (one set) or the rounds (one set per round).
-void lower(const Schedule& S, Lowered& out);
+void lower(const Schedule& S, Lowered& out, const LowerOptions& opt = LowerOptions());
 
 // Element window of a fused pass for the pipelined host path: elements
 // [lo, hi) of every rank, bulk items [b0, b1) and edge items [e0, e1).

@@ -168,10 +168,14 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
                     a.items = bulk;
                     a.n_items = static_cast<uint32_t>(s.bulk.size());
                     const int grid = static_cast<int>(std::min<size_t>(s.bulk.size(), d->num_sms));
-                    if (s.stream) {
+                    if (s.chain_words) {
+                        const int cgrid = static_cast<int>(std::min<size_t>(s.bulk.size(), 4 * d->num_sms));
+                        e = ar::launch_chain_words(dtype, op, a, s.max_in, cgrid, cs);
+                    } else if (s.stream) {
                         a.tile_bytes = L.stream_tile;
                         a.stages = L.stream_stages;
-                        a.flags = (s.tma_store ? ar::kArgTmaStore : 0) | (L.stream_trees ? ar::kArgTrees : 0);
+                        a.flags = (s.tma_store ? ar::kArgTmaStore : 0) | (L.stream_trees ? ar::kArgTrees : 0) |
+                                  (L.stream_tmem ? ar::kArgTmemStack : 0);
                         a.max_in = 1;
                         a.max_tmp = L.stream_slots;  // tree stack tiles after the stages
                         e = ar::launch_stream(dtype, op, a, grid, smem_stream, cs);

@@ -174,9 +174,14 @@ typedef struct {
 
 /* ar_plan_info.kernels bits: the rank-streaming kernel (chains, single trees,
  * fp32 accumulation), the staged kernel (DAG programs), the element-wise
- * kernel (unaligned edges and tiny passes), and DAG_JIT when the staged
- * launches run the plan's run-time compiled DAG kernel. */
-enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4, AR_KERNEL_DAG_JIT = 8 };
+ * kernel (unaligned edges and tiny passes), DAG_JIT when the staged
+ * launches run the plan's run-time compiled DAG kernel, WORD_JIT for the
+ * run-time compiled word kernel (launches whose DAG programs it runs with
+ * one 32-bit word of every input buffer per thread in registers), and
+ * CHAIN_WORD for the chain word kernel (chains of small and mid-sized
+ * passes, the same way). */
+enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4, AR_KERNEL_DAG_JIT = 8,
+       AR_KERNEL_WORD_JIT = 16, AR_KERNEL_CHAIN_WORD = 32 };
 
 typedef struct ar_schedule_s* ar_schedule_t;
 typedef struct ar_plan_s* ar_plan_t;
@@ -286,6 +291,10 @@ typedef struct {
     uint64_t dag_words;      /* instruction words of the staged launches' DAG
                                 programs (what a run-time compiled DAG kernel
                                 holds)                                          */
+    int word_sets;           /* launch sets on the run-time compiled word kernel
+                                (as a plan with params.jit would lower them
+                                here, NVRTC permitting)                         */
+    uint64_t word_kernel_words; /* instruction words of their programs           */
 } ar_lowering_info;
 ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out);
 

@@ -289,12 +289,29 @@ def test_unaligned_buffers_take_elementwise_path():
             assert_bit_equal(got[r], want[r], "float32", f"unaligned {form} rank {r}")
 
 
+@pytest.mark.parametrize("dtype", ["float32", "int32"])
+@pytest.mark.parametrize("P,algo,kw", [(3, "ring", {}), (8, "ring", {}), (20, "ring", {}),
+                                       (8, "pipeline", {"blocks": 3}), (8, "ring", {"form": "step"})])
+def test_unaligned_chains_of_4_byte_elements(P, algo, kw, dtype):
+    """Buffers one element off a 16-byte boundary: a pass of chains over
+    4-byte elements (every element on a 32-bit word) runs on the chain word
+    kernel, every other pass element by element; bit for bit the oracle,
+    the skipped leading element inside the guard band."""
+    n = 100_003
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 55)
+    want = oracle.run(algo, bufs, Arith("sum", dtype), **{k: v for k, v in kw.items() if k != "form"}).bufs
+    got = engine(bufs, dtype, "sum", algo, offset=1, **kw)
+    for r in range(P):
+        assert_bit_equal(got[r], want[r], dtype, f"unaligned {algo} {kw} rank {r}")
+
+
 @pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
 @pytest.mark.parametrize("P,algo,kw", [(5, "ring", {}), (8, "ring", {}), (64, "ring", {}),
                                        (5, "ahc", {"group_sizes": [2, 3]})])
 def test_fp32acc_same_bits_in_every_kernel(P, algo, kw, dtype):
     """The fp32-accumulate order is the engine's own and the same in every
-    kernel: the rank-streaming kernel (bf16 on 16 KB tiles, fp32 on 32 KB)
+    kernel: the rank-streaming kernel (bf16 on 24 KB tiles, fp32 on 32 KB)
     must give exactly the bits of the element-wise kernel, which unaligned
     buffers take."""
     n = 300_007
@@ -700,7 +717,39 @@ def test_dag_kernel_jit_auto_threshold():
     small = ar.Plan(7, 7 * 1024, "float32", "sum", "generalized", r=3).info()["kernels"]
     large = ar.Plan(7, 1 << 22, "float32", "sum", "generalized", r=3).info()["kernels"]
     assert small & ar.KERNEL_STAGED and not small & ar.KERNEL_DAG_JIT
-    assert large & ar.KERNEL_DAG_JIT
+    assert large & ar.KERNEL_STAGED and large & ar.KERNEL_DAG_JIT
+    off = ar.Plan(7, 1 << 22, "float32", "sum", "generalized", r=3, jit="off").info()["kernels"]
+    assert off & ar.KERNEL_STAGED and not off & ar.KERNEL_DAG_JIT
+
+
+WORD_CASES = [(31, "generalized", "sum", {"r": 5}, "float32"), (31, "generalized", "max", {"r": 5}, "float32"),
+              (31, "generalized", "avg", {"r": 5}, "bfloat16"), (31, "generalized", "min", {"r": 5}, "int32"),
+              (63, "generalized", "max", {"r": 6}, "float32"), (64, "rd", "max", {}, "float32"),
+              (64, "rd", "max", {}, "bfloat16"), (31, "generalized", "sum", {"r": 3}, "float32"),
+              (12, "generalized", "prod", {"r": 2}, "float32")]
+
+
+@pytest.mark.parametrize("P,algo,op,kw,dtype", WORD_CASES)
+def test_compiled_dag_programs_of_many_inputs_bit_exact(P, algo, op, kw, dtype):
+    """Rank-specific DAG programs at large P, compiled at run time: 17 to 32
+    inputs on the staged kernel with consumers that take one 32-bit word of
+    every staged tile per thread, more on the word kernel (one word of every
+    rank buffer per thread, no staging), both evaluating the program level by
+    level in registers (P = 12 keeps the 16-byte consumer): bit for bit the
+    oracle's literal schedule, the ragged length's edges on the element-wise
+    kernel, guard bands intact."""
+    import collective_reduction_gb300 as ar
+    n = 40_009 if P > 16 else 100_003
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 101)
+    plan = ar.Plan(P, n, dtype, op, algo, jit="on", **kw)
+    k = plan.info()["kernels"]
+    assert k & (ar.KERNEL_WORD_JIT if P > 32 else ar.KERNEL_DAG_JIT), k
+    plan.close()
+    want = oracle.run(algo, bufs, Arith(op, dtype), **kw).bufs
+    got = engine(bufs, dtype, op, algo, jit="on", **kw)
+    for r in range(P):
+        assert_bit_equal(got[r], want[r], dtype, f"{algo} {op} {kw} rank {r}")
 
 
 @pytest.mark.parametrize("algo,kw", [("ring", {}), ("rh", {"form": "step"}), ("generalized", {"r": 3, "jit": "on"}),

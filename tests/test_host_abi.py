@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert lib.ar_status_string(s).decode().startswith(ar.STATUS[s])
     assert lib.ar_status_string(99)
 
@@ -332,8 +332,8 @@ def test_wave_balance_closed_form(lib):
 def test_stream_geometry_follows_the_programs(lib):
     """Pipeline depth and rank tile as the lowering picks them: 3 stages of
     32 KB for chains over 4-byte elements, 5 for their fp32 accumulation, 4
-    for bf16 chains, 24 KB tiles for trees deeper than 16 leaves, 16 KB tiles
-    (14 stages) for bf16 fp32 accumulation."""
+    for bf16 chains, 24 KB tiles for trees deeper than 16 leaves and 7
+    stages of 24 KB for bf16 fp32 accumulation."""
     def geo(P, dtype, algo, op="sum", **kw):
         low = ar.Schedule(P, P * (1 << 16), dtype, op, algo, **kw).lowering()
         return low["stream_tile_bytes"], low["stream_stages"]
@@ -344,10 +344,35 @@ def test_stream_geometry_follows_the_programs(lib):
     assert geo(8, "float32", "rh") == (32768, 4)        # 3 stack tiles + 4 stages
     assert geo(64, "float32", "rh") == (24576, 3)       # 6 stack tiles + 3 stages
     assert geo(32, "bfloat16", "binomial") == (24576, 4)
-    assert geo(8, "bfloat16", "ring", order="fp32acc") == (16384, 14)
+    assert geo(8, "bfloat16", "ring", order="fp32acc") == (24576, 7)
+    assert geo(64, "bfloat16", "ring", order="fp32acc") == (24576, 7)
     # P = 2: the fp32 accumulation of a sum is the one faithful combine
     assert geo(2, "bfloat16", "ring", order="fp32acc") == (32768, 4)
     assert geo(8, "float32", "ring", order="fp32acc") == (32768, 5)
+
+
+@pytest.mark.parametrize("P,algo,kw", [(31, "generalized", {"r": 5}), (64, "rd", {}), (13, "generalized", {"r": 2})])
+def test_compiled_dag_lowering(lib, P, algo, kw):
+    """Plans whose DAG programs will be compiled (NVRTC present, jit on) are
+    lowered without the interpreter's shared-memory temporaries; programs of
+    17 to 32 inputs get tiles of whole 1 KB units (one 32-bit word per
+    consumer thread), programs of more go to the word kernel.  The items tile
+    every range either way, and the generated kernel compiles."""
+    n = (1 << 20) + 37
+    s = ar.Schedule(P, n, "float32", "max", algo, jit="on", **kw)
+    low = s.lowering()
+    off = ar.Schedule(P, n, "float32", "max", algo, jit="off", **kw).lowering()
+    assert low["tiling_ok"] == 1 and off["tiling_ok"] == 1
+    assert off["dag_words"] > 0 and off["word_sets"] == 0
+    if s.dag_kernel_bytes() == 0:
+        pytest.skip("NVRTC is not available on this host")
+    if P > 32:  # the word kernel: every input word of a position in registers
+        assert low["word_sets"] == 1 and low["word_kernel_words"] > 0 and low["dag_words"] == 0
+        return
+    assert low["dag_words"] > 0 and low["word_sets"] == 0
+    if P > 16:
+        assert low["staged_tile_bytes"] % 1024 == 0 and low["staged_stages"] >= 3
+    assert low["staged_tile_bytes"] * low["staged_stages"] >= off["staged_tile_bytes"] * off["staged_stages"]
 
 
 def test_lowering_null_checks(lib):
