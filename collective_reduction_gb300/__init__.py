@@ -65,7 +65,7 @@ class LoweringInfo(ctypes.Structure):
                 ("tiling_ok", ctypes.c_int), ("windows_ok", ctypes.c_int), ("wave_balance", ctypes.c_double),
                 ("stream_tile_bytes", ctypes.c_int), ("stream_stages", ctypes.c_int),
                 ("staged_tile_bytes", ctypes.c_int), ("staged_stages", ctypes.c_int), ("dag_words", ctypes.c_uint64),
-                ("word_sets", ctypes.c_int), ("word_kernel_words", ctypes.c_uint64)]
+                ("word_sets", ctypes.c_int), ("word_kernel_words", ctypes.c_uint64), ("stream_tmem", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -368,6 +368,7 @@ ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
         out->staged_stages = L.stages;
         out->dag_words = ar::dag_kernel_words(L);
         out->word_kernel_words = ar::word_kernel_words(L);
+        out->stream_tmem = L.stream_tmem ? 1 : 0;
         for (const ar::LaunchSet& ls : L.sets) out->word_sets += ls.words;
         return AR_OK;
     } catch (const std::bad_alloc&) {

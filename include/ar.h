@@ -295,6 +295,7 @@ typedef struct {
                                 (as a plan with params.jit would lower them
                                 here, NVRTC permitting)                         */
     uint64_t word_kernel_words; /* instruction words of their programs           */
+    int stream_tmem;         /* 1: the tree stack lives in tensor memory        */
 } ar_lowering_info;
 ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out);
 

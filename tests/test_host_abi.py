@@ -332,8 +332,9 @@ def test_wave_balance_closed_form(lib):
 def test_stream_geometry_follows_the_programs(lib):
     """Pipeline depth and rank tile as the lowering picks them: 3 stages of
     32 KB for chains over 4-byte elements, 5 for their fp32 accumulation, 4
-    for bf16 chains, 24 KB tiles for trees deeper than 16 leaves and 7
-    stages of 24 KB for bf16 fp32 accumulation."""
+    for bf16 chains, trees of more than 8 leaves with their stack in tensor
+    memory on 4 stages of 32 KB, and 7 stages of 24 KB for bf16 fp32
+    accumulation."""
     def geo(P, dtype, algo, op="sum", **kw):
         low = ar.Schedule(P, P * (1 << 16), dtype, op, algo, **kw).lowering()
         return low["stream_tile_bytes"], low["stream_stages"]
@@ -342,8 +343,11 @@ def test_stream_geometry_follows_the_programs(lib):
     assert geo(8, "bfloat16", "ring") == (32768, 4)
     assert geo(8, "bfloat16", "ring", op="max") == (32768, 4)
     assert geo(8, "float32", "rh") == (32768, 4)        # 3 stack tiles + 4 stages
-    assert geo(64, "float32", "rh") == (24576, 3)       # 6 stack tiles + 3 stages
-    assert geo(32, "bfloat16", "binomial") == (24576, 4)
+    assert geo(64, "float32", "rh") == (32768, 4)       # 6 stack entries in tensor memory
+    assert geo(32, "bfloat16", "binomial") == (32768, 4)
+    tm = lambda P, algo: ar.Schedule(P, P * (1 << 16), "float32", "sum", algo).lowering()["stream_tmem"]
+    assert tm(64, "rh") == 1 and tm(32, "binomial") == 1 and tm(16, "rh") == 1
+    assert tm(8, "rh") == 0 and tm(8, "ring") == 0
     assert geo(8, "bfloat16", "ring", order="fp32acc") == (24576, 7)
     assert geo(64, "bfloat16", "ring", order="fp32acc") == (24576, 7)
     # P = 2: the fp32 accumulation of a sum is the one faithful combine
