@@ -673,6 +673,49 @@ def test_streamed_trees_many_items(algo, kw, dtype):
             assert_bit_equal(got[r], res.bufs[r], dtype, f"{algo} {kw} rank {r}")
 
 
+@pytest.mark.parametrize("P", [16, 32, 64])
+@pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "sum"), ("int32", "max")])
+def test_trees_with_the_stack_in_tensor_memory(P, dtype, op):
+    """Single trees of more than 8 leaves keep their stack in tensor memory
+    (the lowering reports it): RH, binomial, AHC over two groups and RH's
+    reduce-scatter, several items per CTA with a ragged tail, bit for bit the
+    oracle; guard bands and the status word clean."""
+    import collective_reduction_gb300 as ar
+    n = (1 << 21) + 13 if P < 64 else (1 << 20) + 13
+    assert ar.Schedule(P, n, dtype, op, "rh").lowering()["stream_tmem"] == 1
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1e-2, seed=P + 303)
+    for algo, kw in (("rh", {}), ("binomial", {}), ("ahc", {"group_sizes": [P // 2, P - P // 2]}),
+                     ("rh", {"phase": "reduce_scatter"})):
+        res = oracle.run(algo, bufs, Arith(op, dtype), **kw)
+        got = engine(bufs, dtype, op, algo, **kw)
+        if kw.get("phase") == "reduce_scatter":
+            for r, lo, hi in res.info["owner"]:
+                assert_bit_equal(got[r][lo:hi], res.bufs[r][lo:hi], dtype, f"{algo} {kw} rank {r}")
+        else:
+            for r in range(P):
+                assert_bit_equal(got[r], res.bufs[r], dtype, f"{algo} {kw} rank {r}")
+
+
+@pytest.mark.parametrize("P,n,dtype,op,algo,kw", [
+    (16, 1 << 18, "float32", "avg", "ring", {}),              # 1 MiB per rank, the avg division
+    (64, 4096 + 64, "bfloat16", "sum", "ring", {}),           # 8 KiB per rank, ragged chunk edges
+    (16, 257 * 16, "int32", "prod", "ring", {}),
+    (16, 1 << 16, "float32", "max", "pipeline", {"blocks": 5}),
+    (12, (1 << 18) + 3, "bfloat16", "min", "ring", {}),
+])
+def test_chain_word_passes(P, n, dtype, op, algo, kw):
+    """Small and mid-sized fused chain passes on the chain word kernel (the
+    plan reports it): every op, bf16 pairs in one word, the avg division, a
+    pipelined chain, ragged edges on the element-wise kernel; bit for bit the
+    oracle."""
+    import collective_reduction_gb300 as ar
+    assert ar.Plan(P, n, dtype, op, algo, **kw).info()["kernels"] & ar.KERNEL_CHAIN_WORD
+    dist = "small_int" if (dtype == "int32" and op == "prod") else ("uniform_int" if dtype == "int32" else "normal")
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 404)
+    check_faithful(bufs, dtype, op, algo, "fused", **kw)
+
+
 # ---- run-time compiled DAG kernels --------------------------------------------------------
 
 JIT_CASES = [("generalized", 7, "sum", {"r": 1}), ("generalized", 7, "sum", {"r": 3}), ("rd", 8, "max", {}),
