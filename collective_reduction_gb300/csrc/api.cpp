@@ -378,6 +378,7 @@ ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
 
 ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo, const ar_params* params,
                          ar_plan_t* out) {
+    ar::TraceRange trace("ar_plan_create");
     if (!out) return AR_ERR_INVALID_ARG;
     *out = nullptr;
     if (n > (uint64_t(1) << 40)) return AR_ERR_UNSUPPORTED;
@@ -554,6 +555,7 @@ ar_status ar_plan_check_buffers(ar_plan_t plan, void* const* rank_bufs) {
 }
 
 ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
+    ar::TraceRange trace("ar_execute");
     if (!plan || !rank_bufs) return AR_ERR_INVALID_ARG;
     const ar::Schedule& S = plan->S;
     if (S.n == 0) return AR_OK;  // nothing to touch: any pointers are accepted
@@ -590,6 +592,7 @@ ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
 }
 
 ar_status ar_execute_host(ar_plan_t plan, void* const* host_bufs, void* const* dev_bufs, void* stream) {
+    ar::TraceRange trace("ar_execute_host");
     if (!plan || !host_bufs || !dev_bufs) return AR_ERR_INVALID_ARG;
     const ar::Schedule& S = plan->S;
     const int P = S.P;

@@ -1,11 +1,23 @@
-// Checks of the caller's rank buffers before any kernel may touch them.
+// Checks of the caller's rank buffers before any kernel may touch them, and
+// the trace range every launching entry point opens.
 #pragma once
+
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 
 #include "ar.h"
 
 namespace ar {
+
+// An NVTX range over one C-ABI call, seen by profilers that attach an NVTX
+// tool (a no-op function call otherwise).
+struct TraceRange {
+    explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange&) = delete;
+    TraceRange& operator=(const TraceRange&) = delete;
+};
 
 // P pointers to n elements of es bytes each.  Always checked: non-null,
 // aligned to the element size, pairwise disjoint address ranges.  With

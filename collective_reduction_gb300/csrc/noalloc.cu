@@ -91,6 +91,7 @@ size_t put(std::vector<char>& blob, const std::vector<T>& v) {
 
 extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo algo,
                                          const ar_params* params, void* const* rank_bufs, void* stream) {
+    ar::TraceRange trace("ar_allreduce_static");
     if (!rank_bufs) return AR_ERR_INVALID_ARG;
     if (n > (uint64_t(1) << 40)) return AR_ERR_UNSUPPORTED;
     try {
