@@ -62,6 +62,7 @@ struct ar_plan_s {
     const void* dag_fn = nullptr;   // run-time compiled staged kernel, or null: interpret
     const void* word_fn = nullptr;  // run-time compiled word kernel (word sets need it)
     int word_grid = 0;              // its persistent grid: SMs x resident CTAs
+    int smem_word = 0;              // its dynamic shared memory (prefetch stages)
     struct Set {
         const ar::WorkItem* bulk;
         const ar::WorkItem* edge;
@@ -184,7 +185,7 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
         const int grid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms));
         if (s.words) {
             const int wgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->word_grid));
-            e = ar::launch_dependent(plan->word_fn, wgrid, ar::kWordThreads, 0, st, a);
+            e = ar::launch_dependent(plan->word_fn, wgrid, ar::kWordThreads, plan->smem_word, st, a);
         } else if (s.chain_words) {
             const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * kChainWordCtasPerSm));
             e = ar::launch_chain_words(S.dtype, S.op, a, s.max_in, cgrid, st);
@@ -411,11 +412,13 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
         // plan is lowered again with those sets on the staged kernel
         const size_t wwords = ar::word_kernel_words(p->L);
         if (wwords > 0) {
-            if (wwords <= kJitMaxWords)
+            p->smem_word = ar::word_kernel_prefetch(p->L) ? ar::word_kernel_smem(ar::word_kernel_max_in(p->L)) : 0;
+            if (wwords <= kJitMaxWords && p->smem_word <= optin)
                 p->word_fn = ar::load_dag_kernel(ar::word_kernel_source(p->S, p->L), "ar_word_kernel");
             int nb = 0;
             if (p->word_fn &&
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, p->word_fn, ar::kWordThreads, 0) == cudaSuccess &&
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, p->word_fn, ar::kWordThreads, p->smem_word) ==
+                    cudaSuccess &&
                 nb > 0) {
                 p->word_grid = p->num_sms * nb;
             } else {

@@ -260,6 +260,18 @@ __device__ __forceinline__ void stg32(char* p, uint32_t v) {
     asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// 4-byte asynchronous global -> shared copies of this thread (the word
+// kernel's prefetch), grouped; wait_group<N> returns once at most N of this
+// thread's groups are still in flight, their data visible to the thread.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const char* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

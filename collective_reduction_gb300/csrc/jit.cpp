@@ -7,6 +7,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <functional>
 #include <map>
 #include <mutex>
 #include <set>
@@ -16,16 +17,6 @@
 #include <vector>
 
 #include "kargs.hpp"
-
-// Word kernel code generation: prefetch the next position's input words
-// (1) or load each position's words when it is reached (0); CTAs per SM the
-// launch bounds ask registers for.
-#ifndef AR_WORD_PIPE
-#define AR_WORD_PIPE 0
-#endif
-#ifndef AR_WORD_MIN_BLOCKS
-#define AR_WORD_MIN_BLOCKS 1
-#endif
 
 namespace ar {
 namespace {
@@ -121,54 +112,23 @@ std::string word_addr(uint32_t id, int P, bool out, const char* pos) {
     return o.str();
 }
 
-// One program over 32-bit words.  Each thread takes word t, t + kWordThreads,
-// ... of the item; it holds every input word of the current position in
-// registers (x*) and, with `pipe`, has the next position's words in flight
-// (y*) while it combines and stores the current one, so a warp's loads stay
-// outstanding through its arithmetic.  The combines follow the program's
-// order (chains: the fold; DAG: the instruction list).  Loads of the next
-// position never touch an address the current stores write (positions
-// differ), and every word of a position is loaded before any is stored.
-void emit_word_program(std::ostringstream& o, const Lowered& L, uint32_t id, int P, int threads, bool pipe) {
-    const DevProg& d = L.progs[id];
-    auto loads = [&](const char* var, const char* pos, const char* indent) {
-        for (uint32_t i = 0; i < d.n_in; ++i)
-            o << indent << var << i << " = ldg32(" << word_addr(L.refs[d.in_off + i], P, false, pos) << ");\n";
-    };
-    o << "__device__ __forceinline__ void wp_" << id << "(const KernelArgs& a, int64_t off, uint32_t nw) {\n";
-    o << "    uint32_t t = threadIdx.x;\n    if (t >= nw) return;\n";
-    o << "    uint32_t";
-    for (uint32_t i = 0; i < d.n_in; ++i) o << (i ? ", x" : " x") << i;
-    o << ";\n";
-    if (pipe) {
-        o << "    {\n        const int64_t pos = off + 4 * static_cast<int64_t>(t);\n";
-        loads("x", "pos", "        ");
-        o << "    }\n";
-    }
-    o << "#pragma unroll 1\n"
-         "    for (; t < nw; t += "
-      << threads
-      << "u) {\n"
-         "        const int64_t pos = off + 4 * static_cast<int64_t>(t);\n";
-    if (pipe) {
-        o << "        const uint32_t tn = t + " << threads << "u;\n";
-        o << "        const int64_t npos = off + 4 * static_cast<int64_t>(tn < nw ? tn : t);\n";
-        o << "        uint32_t";
-        for (uint32_t i = 0; i < d.n_in; ++i) o << (i ? ", y" : " y") << i;
-        o << ";\n";
-        loads("y", "npos", "        ");
-    } else {
-        loads("x", "pos", "        ");
-    }
+// The combines and stores of one program over 32-bit words, at byte
+// position `pos` of every buffer: input(i) names input word i (emitting its
+// load when the variant loads at first use).  Chains fold in their order; a
+// DAG program runs in SSA form level by level (each combine after the
+// combines it reads, by its depth above the inputs: the same combines of the
+// same values as the instruction list, with fewer values live at once).
+void emit_word_body(std::ostringstream& o, const Lowered& L, const DevProg& d, int P,
+                    const std::function<std::string(uint32_t)>& input) {
     auto store = [&](uint32_t buf, const std::string& v, bool avg) {
         o << "        stg32(" << word_addr(buf, P, true, "pos") << ", "
           << (avg ? "wdiv<DT>(" + v + ", " + std::to_string(P) + ".0f)" : v) << ");\n";
     };
     if (d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L) {
-        std::string acc = "x0";
+        std::string acc = input(0);
         for (uint32_t i = 1; i < d.n_in; ++i) {
+            const std::string x = input(i);
             const std::string t = "c" + std::to_string(i);
-            const std::string x = "x" + std::to_string(i);
             o << "        const uint32_t " << t << " = wop<DT, OP>(" << (d.kind == PK_CHAIN_R ? x + ", " + acc : acc + ", " + x)
               << ");\n";
             acc = t;
@@ -176,71 +136,128 @@ void emit_word_program(std::ostringstream& o, const Lowered& L, uint32_t id, int
         const bool avg = (d.flags & PF_AVG) != 0;
         for (uint32_t q = 0; q < d.n_out; ++q)
             store((d.flags & PF_OUT_ALL) ? buf_id(0, static_cast<int>(q)) : L.refs[d.out_off + q], acc, avg);
-    } else if (d.kind == PK_DAG) {
-        // The instruction list in SSA form (ops name fresh values; the
-        // temporaries and the accumulator of the list are reused slots),
-        // then emitted level by level: an op after the ops it reads, in
-        // order of its depth above the inputs.  Every combine reads the same
-        // two values in any such order, so the results are the list's bits,
-        // and a level's values die once the next level has read them (a
-        // butterfly keeps about 2 P values live, not the post-order's many).
-        struct Op {
-            int a, b, level;
-        };
-        std::vector<Op> ops;                          // value n_in + k is ops[k]
-        std::vector<std::pair<uint32_t, std::pair<int, bool>>> stores;  // (buffer, (value, avg))
-        std::map<uint32_t, int> tmp;
-        int acc = -1;
-        auto value = [&](uint32_t r) -> int {
-            if (r == REF_ACC) return acc;
-            if (r & REF_TMP) return tmp.at(r & 0x1FFu);
-            if (r >= d.n_in) throw std::logic_error("dag program reads a missing input");
-            return static_cast<int>(r);
-        };
-        auto level = [&](int v) { return v < static_cast<int>(d.n_in) ? 0 : ops[v - d.n_in].level; };
-        for (uint32_t q = 0; q < d.n_ins; ++q) {
-            const uint32_t w = L.ins[d.ins_off + q];
-            if ((w >> 30) == INS_OP) {
-                const int x = value(w & 0x3FFu), y = value((w >> 10) & 0x3FFu);
-                if (x < 0 || y < 0) throw std::logic_error("dag program reads an unset accumulator");
-                ops.push_back({x, y, std::max(level(x), level(y)) + 1});
-                const int v = static_cast<int>(d.n_in + ops.size() - 1);
-                const uint32_t rd = (w >> 20) & 0x3FFu;
-                if (rd == REF_ACC)
-                    acc = v;
-                else
-                    tmp[rd & 0x1FFu] = v;
-            } else {
-                const int v = value(w & 0x3FFu);
-                if (v < 0) throw std::logic_error("dag program stores an unset accumulator");
-                stores.push_back({(w >> 10) & 0xFFFFu, {v, (w >> 30) == INS_STORE_AVG}});
-            }
-        }
-        std::vector<int> order(ops.size());
-        for (size_t k = 0; k < ops.size(); ++k) order[k] = static_cast<int>(k);
-        std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return ops[x].level < ops[y].level; });
-        auto name = [&](int v) {
-            return v < static_cast<int>(d.n_in) ? "x" + std::to_string(v) : "t" + std::to_string(v - d.n_in);
-        };
-        std::map<int, std::vector<size_t>> stores_of;
-        for (size_t k = 0; k < stores.size(); ++k) stores_of[stores[k].second.first].push_back(k);
-        auto emit_stores = [&](int v) {
-            auto it = stores_of.find(v);
-            if (it == stores_of.end()) return;
-            for (size_t k : it->second) store(stores[k].first, name(v), stores[k].second.second);
-        };
-        for (uint32_t i = 0; i < d.n_in; ++i) emit_stores(static_cast<int>(i));
-        for (int k : order) {
-            o << "        const uint32_t t" << k << " = wop<DT, OP>(" << name(ops[k].a) << ", " << name(ops[k].b)
-              << ");\n";
-            emit_stores(static_cast<int>(d.n_in) + k);
-        }
-    } else {
-        throw std::logic_error("word kernel: a program kind it does not run");
+        return;
     }
-    if (pipe)
-        for (uint32_t i = 0; i < d.n_in; ++i) o << "        x" << i << " = y" << i << ";\n";
-    o << "    }\n}\n\n";
+    if (d.kind != PK_DAG) throw std::logic_error("word kernel: a program kind it does not run");
+    struct Op {
+        int a, b, level;
+    };
+    std::vector<Op> ops;  // value n_in + k is ops[k]
+    std::vector<std::pair<uint32_t, std::pair<int, bool>>> stores;  // (buffer, (value, avg))
+    std::map<uint32_t, int> tmp;
+    int acc = -1;
+    auto value = [&](uint32_t r) -> int {
+        if (r == REF_ACC) return acc;
+        if (r & REF_TMP) return tmp.at(r & 0x1FFu);
+        if (r >= d.n_in) throw std::logic_error("dag program reads a missing input");
+        return static_cast<int>(r);
+    };
+    auto level = [&](int v) { return v < static_cast<int>(d.n_in) ? 0 : ops[v - d.n_in].level; };
+    for (uint32_t q = 0; q < d.n_ins; ++q) {
+        const uint32_t w = L.ins[d.ins_off + q];
+        if ((w >> 30) == INS_OP) {
+            const int x = value(w & 0x3FFu), y = value((w >> 10) & 0x3FFu);
+            if (x < 0 || y < 0) throw std::logic_error("dag program reads an unset accumulator");
+            ops.push_back({x, y, std::max(level(x), level(y)) + 1});
+            const int v = static_cast<int>(d.n_in + ops.size() - 1);
+            const uint32_t rd = (w >> 20) & 0x3FFu;
+            if (rd == REF_ACC)
+                acc = v;
+            else
+                tmp[rd & 0x1FFu] = v;
+        } else {
+            const int v = value(w & 0x3FFu);
+            if (v < 0) throw std::logic_error("dag program stores an unset accumulator");
+            stores.push_back({(w >> 10) & 0xFFFFu, {v, (w >> 30) == INS_STORE_AVG}});
+        }
+    }
+    std::vector<int> order(ops.size());
+    for (size_t k = 0; k < ops.size(); ++k) order[k] = static_cast<int>(k);
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return ops[x].level < ops[y].level; });
+    auto name = [&](int v) -> std::string {
+        return v < static_cast<int>(d.n_in) ? input(static_cast<uint32_t>(v)) : "t" + std::to_string(v - d.n_in);
+    };
+    std::map<int, std::vector<size_t>> stores_of;
+    for (size_t k = 0; k < stores.size(); ++k) stores_of[stores[k].second.first].push_back(k);
+    auto emit_stores = [&](int v) {
+        auto it = stores_of.find(v);
+        if (it == stores_of.end()) return;
+        const std::string x = name(v);
+        for (size_t k : it->second) store(stores[k].first, x, stores[k].second.second);
+    };
+    for (uint32_t i = 0; i < d.n_in; ++i) emit_stores(static_cast<int>(i));
+    for (int k : order) {
+        const std::string x = name(ops[k].a), y = name(ops[k].b);
+        o << "        const uint32_t t" << k << " = wop<DT, OP>(" << x << ", " << y << ");\n";
+        emit_stores(static_cast<int>(d.n_in) + k);
+    }
+}
+
+// Address expression of input word i of program d at byte position q.
+std::string word_src(const Lowered& L, const DevProg& d, uint32_t i, int P, const char* q) {
+    return word_addr(L.refs[d.in_off + i], P, false, q);
+}
+
+// One program over 32-bit words, each thread taking word positions t,
+// t + kWordThreads, ... of the item.  Direct (stages = 0): every input word of
+// a position is loaded into registers before any store (a program may store
+// to a buffer it reads).  Prefetching (stages = S >= 2): the thread copies the
+// input words of the position S - 1 ahead with 4-byte asynchronous copies
+// (no registers held while they are in flight) into its own slots of stage
+// (position mod S) — [stage][input][thread], so a warp's copies and reads are
+// 128 contiguous bytes — waits for the current position's group and reads each
+// word at its first use; the prefetched positions are never the ones being
+// stored, and a stage is refilled only after its words were read.
+void emit_word_program(std::ostringstream& o, const Lowered& L, uint32_t id, int P, int threads, int S) {
+    const DevProg& d = L.progs[id];
+    o << "__device__ __forceinline__ void wp_" << id
+      << "(const KernelArgs& a, int64_t off, uint32_t nw, uint32_t sbase) {\n";
+    if (S == 0) {
+        o << "#pragma unroll 1\n"
+             "    for (uint32_t t = threadIdx.x; t < nw; t += "
+          << threads << "u) {\n        const int64_t pos = off + 4 * static_cast<int64_t>(t);\n";
+        for (uint32_t i = 0; i < d.n_in; ++i)
+            o << "        const uint32_t x" << i << " = ldg32(" << word_src(L, d, i, P, "pos") << ");\n";
+        emit_word_body(o, L, d, P, [](uint32_t i) { return "x" + std::to_string(i); });
+        o << "    }\n}\n\n";
+        return;
+    }
+    const uint64_t islot = 4ull * threads;  // bytes between inputs in a stage
+    const uint64_t sstage = islot * d.n_in;  // bytes of one stage of this program
+    auto prefetch = [&](const char* tvar, const char* kvar, const char* indent) {
+        o << indent << "if (" << tvar << " < nw) {\n";
+        o << indent << "    const int64_t q = off + 4 * static_cast<int64_t>(" << tvar << ");\n";
+        o << indent << "    const uint32_t d = sb + " << kvar << " * " << sstage << "u;\n";
+        for (uint32_t i = 0; i < d.n_in; ++i)
+            o << indent << "    cp_async4(d + " << i * islot << "u, " << word_src(L, d, i, P, "q") << ");\n";
+        o << indent << "}\n" << indent << "cp_async_commit();\n";
+    };
+    o << "    const uint32_t sb = sbase + 4u * threadIdx.x;\n";
+    for (int k = 0; k + 1 < S; ++k) {
+        o << "    {\n        const uint32_t tp = threadIdx.x + " << k * threads << "u;\n        const uint32_t kp = " << k
+          << "u;\n";
+        prefetch("tp", "kp", "        ");
+        o << "    }\n";
+    }
+    o << "    uint32_t k = 0;\n"
+         "#pragma unroll 1\n"
+         "    for (uint32_t t = threadIdx.x; t < nw; t += "
+      << threads << "u, k = (k + 1 == " << S << "u ? 0u : k + 1)) {\n";
+    o << "        {\n            const uint32_t tn = t + " << (S - 1) * threads << "u;\n"
+      << "            const uint32_t kn = (k + " << (S - 1) << "u) % " << S << "u;\n";
+    prefetch("tn", "kn", "            ");
+    o << "        }\n        cp_async_wait<" << S - 1 << ">();\n        const uint32_t s = sb + k * " << sstage
+      << "u;\n        const int64_t pos = off + 4 * static_cast<int64_t>(t);\n";
+    std::vector<char> loaded(d.n_in, 0);
+    emit_word_body(o, L, d, P, [&](uint32_t i) -> std::string {
+        if (i >= d.n_in) throw std::logic_error("word program reads a missing input");
+        if (!loaded[i]) {
+            o << "        const uint32_t x" << i << " = lds32(s + " << i * islot << "u);\n";
+            loaded[i] = 1;
+        }
+        return "x" + std::to_string(i);
+    });
+    o << "    }\n    cp_async_wait<0>();\n}\n\n";
 }
 
 // A DAG program of the staged kernel over 32-bit words (programs of many
@@ -333,6 +350,26 @@ void emit_program_words(std::ostringstream& o, const Lowered& L, uint32_t id, in
 
 }  // namespace
 
+bool word_kernel_prefetch(const Lowered& L) {
+    uint64_t ins = 0, combines = 0;
+    for (uint32_t id : word_programs(L)) {
+        const DevProg& d = L.progs[id];
+        ins += d.n_in;
+        if (d.kind == PK_DAG) {
+            for (uint32_t q = 0; q < d.n_ins; ++q) combines += (L.ins[d.ins_off + q] >> 30) == INS_OP;
+        } else {
+            combines += d.n_in - 1;
+        }
+    }
+    return ins > 0 && combines >= kWordPrefetchCombinesPerInput * ins;
+}
+
+int word_kernel_max_in(const Lowered& L) {
+    int m = 0;
+    for (uint32_t id : word_programs(L)) m = std::max<int>(m, L.progs[id].n_in);
+    return m;
+}
+
 size_t word_kernel_words(const Lowered& L) {
     size_t n = 0;
     for (uint32_t id : word_programs(L)) n += L.progs[id].kind == PK_DAG ? L.progs[id].n_ins : L.progs[id].n_in;
@@ -353,12 +390,15 @@ std::string word_kernel_source(const Schedule& S, const Lowered& L) {
          "#include \"device.cuh\"\n"
          "namespace ar {\nnamespace {\n"
       << "constexpr int DT = " << S.dtype << ";\nconstexpr int OP = " << op << ";\n\n";
-    for (uint32_t id : ids) emit_word_program(o, L, id, S.P, kWordThreads, AR_WORD_PIPE != 0);
+    const int stages = word_kernel_prefetch(L) ? word_kernel_stages(word_kernel_max_in(L)) : 0;
+    for (uint32_t id : ids) emit_word_program(o, L, id, S.P, kWordThreads, stages);
     o << "}  // namespace\n}  // namespace ar\n\n"
          "extern \"C\" __global__ void __launch_bounds__("
-      << kWordThreads << ", " << AR_WORD_MIN_BLOCKS
-      << ")\n"
+      << kWordThreads
+      << ", 1)\n"
          "ar_word_kernel(const __grid_constant__ ar::KernelArgs a) {\n"
+         "    extern __shared__ __align__(128) uint8_t smem[];\n"
+         "    const uint32_t sbase = ar::smem_addr(smem);\n"
          "    ar::griddep_wait();\n"
          "    ar::griddep_launch_dependents();\n"
          "    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {\n"
@@ -370,7 +410,7 @@ std::string word_kernel_source(const Schedule& S, const Lowered& L) {
       << es
       << ") >> 2);\n"
          "        switch (w.prog) {\n";
-    for (uint32_t id : ids) o << "            case " << id << "u: ar::wp_" << id << "(a, off, nw); break;\n";
+    for (uint32_t id : ids) o << "            case " << id << "u: ar::wp_" << id << "(a, off, nw, sbase); break;\n";
     o << "            default:\n"
          "                if (threadIdx.x == 0) atomicOr(a.status, ar::kStatusBadProgram);\n"
          "                return;\n"

@@ -43,6 +43,18 @@ int compile_dag_kernel(const std::string& src, std::string& cubin, std::string* 
 // (0: no word-kernel launch).
 size_t word_kernel_words(const Lowered& L);
 
+// Most inputs of a program of the plan's word-kernel launches (0: none).
+int word_kernel_max_in(const Lowered& L);
+
+// Whether the plan's word kernel prefetches input words through shared
+// memory (its programs average at least kWordPrefetchCombinesPerInput
+// combines per input: long enough evaluations to hide the next position's
+// loads behind; measured 3-9 points faster at P = 63 / 64 with 6-10 per input,
+// 3-9 points slower at P = 48 / 63 with 1-4 per input).  Its dynamic shared
+// memory is then word_kernel_smem(word_kernel_max_in(L)), else none.
+constexpr uint64_t kWordPrefetchCombinesPerInput = 5;
+bool word_kernel_prefetch(const Lowered& L);
+
 // CUDA C source of the plan's word kernel (its entry point is
 // ar_word_kernel); empty when word_kernel_words(L) is 0.
 std::string word_kernel_source(const Schedule& S, const Lowered& L);

@@ -72,9 +72,16 @@ static_assert(kMaxTileBytes <= kMaxStagedTile, "staged tiles beyond what the con
 constexpr int kMaxStages = kBarrierBytes / 24;
 
 // The word kernel (run-time compiled): one thread per 32-bit word of every
-// rank, threads per CTA, rank bytes per work item.
+// rank, threads per CTA, rank bytes per work item, and its prefetch depth:
+// stages of kWordThreads words of every input in shared memory (as many as
+// fit in about 220 KB, at most 4).
 constexpr int kWordThreads = 256;
-constexpr int kWordItemBytes = 16384;
+constexpr int kWordItemBytes = 32768;
+inline int word_kernel_stages(int max_in) {
+    const int fit = (220 * 1024) / (4 * kWordThreads * std::max(max_in, 1));
+    return std::min(4, fit);
+}
+inline int word_kernel_smem(int max_in) { return word_kernel_stages(max_in) * max_in * 4 * kWordThreads; }
 // The chain word kernel: rank bytes per work item for programs of n_in
 // inputs (one round of its threads: kChainWordMaxIn / n_in words each), and
 // the largest set (bytes of traffic) it takes.

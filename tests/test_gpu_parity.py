@@ -205,6 +205,35 @@ def test_bench_workload_at_full_size_sampled(dtype, form):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("algo,kw", [("ring", {}), ("ring", {"form": "step"}), ("rh", {}),
+                                     ("generalized", {"r": 1, "op": "max", "jit": "on"})])
+def test_rank_buffers_beyond_4_gib(algo, kw):
+    """Rank buffers of 5 GiB + 12 bytes (byte offsets beyond 32 bits in every
+    kernel's address arithmetic, a ragged tail): P = 2 (3 for the DAG plan),
+    checked on 4096 sampled elements of every chunk, bit for bit the oracle."""
+    import torch
+    import bench
+    import collective_reduction_gb300 as ar
+    kw = dict(kw)
+    op = kw.pop("op", "sum")
+    P = 3 if algo == "generalized" else 2
+    n = (5 << 30) // 4 + 3
+    if torch.cuda.mem_get_info()[0] < P * n * 4 * 1.2:
+        pytest.skip("not enough device memory")
+    dev = ar_synth.device_inputs(P, n, "float32", sigma=1.0, seed=P)
+    sample_in, idx = bench.gather_sample(dev, P, n, 4096, P)
+    plan = ar.Plan(P, n, "float32", op, algo, **kw)
+    plan.execute(dev)
+    plan.check()
+    want = oracle.run(algo, sample_in, Arith(op, "float32"),
+                      **{k: v for k, v in kw.items() if k not in ("form", "jit")}).bufs
+    for r in range(P):
+        assert_bit_equal(to_host(dev[r].index_select(0, idx), "float32"), want[r], "float32", f"{algo} rank {r}")
+    plan.close()
+    del dev
+    torch.cuda.empty_cache()
+
+
 # ---- every (dtype, op) through a chain and a DAG program -------------------------------
 
 @pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
