@@ -257,11 +257,11 @@ ar_status ar_cost_optimal_r(int P, uint64_t bytes_per_rank, const ar_cost_model*
 ar_status ar_cost_select(int P, uint64_t n, ar_dtype dtype, ar_op op, const ar_cost_model* model,
                          ar_algo* algo, ar_params* params, double* us);
 
-/* Host only: compiles, without a GPU, the run-time DAG kernel a plan with
- * these parameters would use (params.jit ignored); *cubin_bytes receives the
- * code size, 0 when the plan has no DAG program on the staged kernel.
- * AR_ERR_UNSUPPORTED when NVRTC cannot be loaded, AR_ERR_CUDA when the
- * compilation fails. */
+/* Host only: compiles, without a GPU, the run-time compiled kernels a plan
+ * with these parameters would use with params.jit = AR_JIT_ON (the staged DAG
+ * kernel and the word kernel); *cubin_bytes receives their total code size, 0
+ * when the plan has no DAG program.  AR_ERR_UNSUPPORTED when NVRTC cannot be
+ * loaded, AR_ERR_CUDA when a compilation fails. */
 ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes);
 
 /* Host only: the work a plan with these parameters would launch, lowered as
