@@ -31,8 +31,6 @@ constexpr size_t kJitMaxWords = 4096;
 #define AR_WORD_MIN_IN 33
 #endif
 constexpr int kWordMinIn = AR_WORD_MIN_IN;
-// Persistent grid of the chain word kernel: CTAs per SM (16 warps).
-constexpr int kChainWordCtasPerSm = 4;
 // Guard bands around the step form's scratch: written with kGuardByte when
 // the plan is created and compared by ar_plan_check, so a kernel that writes
 // past either end of the scratch is reported rather than silently
@@ -187,7 +185,7 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
             const int wgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->word_grid));
             e = ar::launch_dependent(plan->word_fn, wgrid, ar::kWordThreads, plan->smem_word, st, a);
         } else if (s.chain_words) {
-            const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * kChainWordCtasPerSm));
+            const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * ar::kChainWordCtasPerSm));
             e = ar::launch_chain_words(S.dtype, S.op, a, s.max_in, cgrid, st);
         } else if (s.stream) {
             a.tile_bytes = plan->L.stream_tile;
@@ -580,7 +578,7 @@ ar_status ar_execute(ar_plan_t plan, void* const* rank_bufs, void* stream) {
         } else if (s.n_fallback && !aligned && !s.small && words_ok && s.chains) {
             a.items = s.fallback;
             a.n_items = s.n_fallback;
-            const int cgrid = static_cast<int>(std::min<uint32_t>(s.n_fallback, plan->num_sms * kChainWordCtasPerSm));
+            const int cgrid = static_cast<int>(std::min<uint32_t>(s.n_fallback, plan->num_sms * ar::kChainWordCtasPerSm));
             e = ar::launch_chain_words(S.dtype, S.op, a, s.max_in, cgrid, st);
         } else if (s.n_fallback) {
             a.items = s.fallback;

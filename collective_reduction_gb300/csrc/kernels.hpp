@@ -21,7 +21,9 @@ cudaError_t launch_staged(int dtype, int op, const KernelArgs& a, int grid, int 
 // Persistent rank-streaming kernel over a.items (chain / FP32ACC programs only).
 cudaError_t launch_stream(int dtype, int op, const KernelArgs& a, int grid, int smem, cudaStream_t st);
 // Chain programs of at most max_in inputs, 32-bit words of every input in
-// registers (kChainWordThreads per CTA, grid CTAs over a.items).
+// registers (kChainWordThreads per CTA, grid CTAs over a.items; a persistent
+// grid is kChainWordCtasPerSm CTAs per SM).
+constexpr int kChainWordCtasPerSm = 4;
 cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_in, int grid, cudaStream_t st);
 // One CTA per item, one element per thread.
 cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem, cudaStream_t st);

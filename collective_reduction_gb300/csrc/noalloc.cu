@@ -170,7 +170,8 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
                     a.n_items = static_cast<uint32_t>(s.bulk.size());
                     const int grid = static_cast<int>(std::min<size_t>(s.bulk.size(), d->num_sms));
                     if (s.chain_words) {
-                        const int cgrid = static_cast<int>(std::min<size_t>(s.bulk.size(), 4 * d->num_sms));
+                        const int cgrid =
+                            static_cast<int>(std::min<size_t>(s.bulk.size(), ar::kChainWordCtasPerSm * d->num_sms));
                         e = ar::launch_chain_words(dtype, op, a, s.max_in, cgrid, cs);
                     } else if (s.stream) {
                         a.tile_bytes = L.stream_tile;
