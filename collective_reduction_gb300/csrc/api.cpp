@@ -31,6 +31,14 @@ constexpr size_t kJitMaxWords = 4096;
 #define AR_WORD_MIN_IN 33
 #endif
 constexpr int kWordMinIn = AR_WORD_MIN_IN;
+// bf16 max / min programs, whose compare-and-selects make the evaluation
+// ALU-heavy, go to the word kernel from this many inputs (its consumers read
+// no staged tiles): measured at 64 MiB per rank, the word kernel 50-66% of
+// the copy against 23-32% for the staged one at P = 28 ... 32, the staged
+// one 72-77% against 53-57% at P = 20 / 24.
+#ifndef AR_WORD_MIN_IN_SELECT
+#define AR_WORD_MIN_IN_SELECT 25
+#endif
 // Guard bands around the step form's scratch: written with kGuardByte when
 // the plan is created and compared by ar_plan_check, so a kernel that writes
 // past either end of the scratch is reported rather than silently
@@ -219,11 +227,14 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
 
 // How a plan with this jit setting lowers: the word kernel for DAG sets when
 // the run-time compiler is there (AUTO: for sets of at least kJitMinBytes).
-ar::LowerOptions lower_options(int jit) {
+// bf16 max / min programs from AR_WORD_MIN_IN_SELECT inputs on.
+ar::LowerOptions lower_options(const ar::Schedule& S) {
+    const int jit = S.params.jit;
     ar::LowerOptions lo;
     lo.jit_dag = jit != AR_JIT_OFF && ar::jit_available();
     lo.word_dag = lo.jit_dag;
-    lo.word_min_in = kWordMinIn;
+    const bool selects = S.dtype == AR_BFLOAT16 && (S.op == AR_MAX || S.op == AR_MIN);
+    lo.word_min_in = selects ? AR_WORD_MIN_IN_SELECT : kWordMinIn;
     lo.word_min_bytes = jit == AR_JIT_ON ? 0 : kJitMinBytes;
     return lo;
 }
@@ -325,8 +336,9 @@ ar_status ar_schedule_dag_kernel(ar_schedule_t s, size_t* cubin_bytes) {
     *cubin_bytes = 0;
     try {
         ar::Lowered L;
-        ar::LowerOptions lo = lower_options(AR_JIT_ON);
-        lo.word_dag = true;  // compile the word kernel too (a missing NVRTC is reported below)
+        ar::LowerOptions lo = lower_options(s->S);
+        lo.jit_dag = lo.word_dag = true;  // both run-time kernels (a missing NVRTC is reported below)
+        lo.word_min_bytes = 0;
         ar::lower(s->S, L, lo);
         for (const std::string& src : {ar::dag_kernel_source(s->S, L), ar::word_kernel_source(s->S, L)}) {
             if (src.empty()) continue;
@@ -349,7 +361,7 @@ ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
     *out = ar_lowering_info{};
     try {
         ar::Lowered L;
-        ar::lower(s->S, L, lower_options(s->S.params.jit));
+        ar::lower(s->S, L, lower_options(s->S));
         const int es = ar::esize_of(s->S.dtype);
         std::vector<ar::Window> W;
         if (L.sets.size() == 1)
@@ -389,7 +401,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             delete p;
             return st;
         }
-        ar::LowerOptions lo = lower_options(p->S.params.jit);
+        ar::LowerOptions lo = lower_options(p->S);
         try {
             ar::lower(p->S, p->L, lo);
         } catch (const std::length_error&) {

@@ -622,8 +622,12 @@ __device__ __forceinline__ void dag_item(const KernelArgs& a, const DevProg& pg,
 
 // Dag: how the launch evaluates DAG programs, called as
 // dag(pg, prog_index, stage_tiles, nvec, byte_offset, consumer_thread).
+// Forced inline like everything between the kernel and the programs: a
+// called function reaches the kernel parameters through a pointer, and then
+// every store may overwrite them, so buffer addresses are reloaded from
+// memory after each store.
 template <int DT, int OP, class Dag>
-__device__ void consume(const KernelArgs& a, const Stage& sm, int ct, Dag dag) {
+__device__ __forceinline__ void consume(const KernelArgs& a, const Stage& sm, int ct, Dag dag) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
     const int lane = ct & 31;
     uint32_t k = 0;
@@ -652,6 +656,18 @@ __device__ void consume(const KernelArgs& a, const Stage& sm, int ct, Dag dag) {
         if (lane == 0) mbar_arrive(sm.empty + 8 * s);
     }
 }
+
+// Binds the stage layout to a launch's DAG evaluator (a functor, not a
+// lambda, so that its call can be forced inline).
+template <class Dag>
+struct StagedDag {
+    const Stage& sm;
+    const Dag& dag;
+    __device__ __forceinline__ void operator()(const DevProg& pg, uint32_t prog, uint32_t st, uint32_t nvec,
+                                               int64_t off, int ct) const {
+        dag(sm, pg, prog, st, nvec, off, ct);
+    }
+};
 
 // The staged kernel: barrier setup, one producer thread, eight consumer
 // warps.  smem is the dynamic shared memory; dag evaluates DAG programs.
@@ -684,8 +700,7 @@ __device__ __forceinline__ void staged_body(const KernelArgs& a, uint8_t* smem, 
             produce1<ES>(a, sm);
         return;
     }
-    consume<DT, OP>(a, sm, threadIdx.x - 32, [&](const DevProg& pg, uint32_t prog, uint32_t st, uint32_t nvec,
-                                                  int64_t off, int ct) { dag(sm, pg, prog, st, nvec, off, ct); });
+    consume<DT, OP>(a, sm, threadIdx.x - 32, StagedDag<Dag>{sm, dag});
 }
 
 }  // namespace

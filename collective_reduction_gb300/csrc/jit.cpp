@@ -445,17 +445,25 @@ std::string dag_kernel_source(const Schedule& S, const Lowered& L) {
         else
             emit_program(o, L, id, S.P);
     }
-    o << "}  // namespace\n}  // namespace ar\n\n"
+    // The dispatch is a functor whose call operator is forced inline: as a
+    // lambda, a dispatch over many programs was compiled as a called
+    // function, which reached the kernel parameters through a pointer and
+    // reloaded an output's buffer address from memory after every store.
+    o << "struct Dispatch {\n"
+         "    const KernelArgs& a;\n"
+         "    __device__ __forceinline__ void operator()(const Stage& sm, const DevProg& pg, uint32_t prog,\n"
+         "                                               uint32_t st, uint32_t nvec, int64_t off, int ct) const {\n"
+         "        switch (prog) {\n";
+    for (uint32_t id : ids) o << "            case " << id << "u: dag_" << id << "(a, st, nvec, off, ct); break;\n";
+    o << "            default: dag_item<DT, OP>(a, pg, st, sm.tmps, nvec, off, ct);\n"
+         "        }\n"
+         "    }\n"
+         "};\n\n"
+         "}  // namespace\n}  // namespace ar\n\n"
          "extern \"C\" __global__ void __launch_bounds__(ar::kStagedThreads, 1)\n"
          "ar_dag_kernel(const __grid_constant__ ar::KernelArgs a) {\n"
          "    extern __shared__ __align__(128) uint8_t smem[];\n"
-         "    ar::staged_body<ar::DT, ar::OP>(a, smem, [&](const ar::Stage& sm, const ar::DevProg& pg, uint32_t prog,\n"
-         "                                              uint32_t st, uint32_t nvec, int64_t off, int ct) {\n"
-         "        switch (prog) {\n";
-    for (uint32_t id : ids) o << "            case " << id << "u: ar::dag_" << id << "(a, st, nvec, off, ct); break;\n";
-    o << "            default: ar::dag_item<ar::DT, ar::OP>(a, pg, st, sm.tmps, nvec, off, ct);\n"
-         "        }\n"
-         "    });\n"
+         "    ar::staged_body<ar::DT, ar::OP>(a, smem, ar::Dispatch{a});\n"
          "}\n";
     return o.str();
 }

@@ -788,13 +788,15 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
     t = std::min<int64_t>(t, kMaxTileBytes);
     t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
     lw.tile_bytes = static_cast<int>(t);
-    // compiled programs of many inputs: tiles of 4, 2 or 1 KB (whole words
-    // for every consumer thread), the largest that keeps AR_JIT_WORD_STAGES
-    // stages, with as many stages as fit (at most kStagesWord)
+    // compiled programs of many inputs: tiles of 2 or 1 KB (whole words for
+    // every consumer thread), the larger that keeps AR_JIT_WORD_STAGES
+    // stages, with as many stages as fit (at most kStagesWord).  4 KB tiles
+    // (3 stages at P = 17 / 18) measured 45% of the copy peak against 73-75%
+    // with 2 KB and 6 stages (fp32 sum / max, P = 17, 64 MiB per rank).
     if (opt.jit_dag && AR_JIT_GEOMETRY && lw.max_in > kWordConsumerMinIn) {
         const int64_t room = kSmemBudget - kBarrierBytes;
         int64_t wt = kWordTileUnit;
-        for (int64_t c = 4 * kWordTileUnit; c > kWordTileUnit; c /= 2)
+        for (int64_t c = 2 * kWordTileUnit; c > kWordTileUnit; c /= 2)
             if (room / (c * lw.max_in) >= AR_JIT_WORD_STAGES) {
                 wt = c;
                 break;

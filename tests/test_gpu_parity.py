@@ -798,7 +798,9 @@ WORD_CASES = [(31, "generalized", "sum", {"r": 5}, "float32"), (31, "generalized
               (31, "generalized", "avg", {"r": 5}, "bfloat16"), (31, "generalized", "min", {"r": 5}, "int32"),
               (63, "generalized", "max", {"r": 6}, "float32"), (64, "rd", "max", {}, "float32"),
               (64, "rd", "max", {}, "bfloat16"), (31, "generalized", "sum", {"r": 3}, "float32"),
-              (12, "generalized", "prod", {"r": 2}, "float32")]
+              (12, "generalized", "prod", {"r": 2}, "float32"), (31, "generalized", "max", {"r": 5}, "bfloat16"),
+              (24, "generalized", "min", {"r": 4}, "bfloat16"),
+              (17, "generalized", "sum", {"r": 2}, "float32")]
 
 
 @pytest.mark.parametrize("P,algo,op,kw,dtype", WORD_CASES)
@@ -807,7 +809,8 @@ def test_compiled_dag_programs_of_many_inputs_bit_exact(P, algo, op, kw, dtype):
     inputs on the staged kernel with consumers that take one 32-bit word of
     every staged tile per thread, more on the word kernel (one word of every
     rank buffer per thread, no staging), both evaluating the program level by
-    level in registers (P = 12 keeps the 16-byte consumer): bit for bit the
+    level in registers (P = 12 keeps the 16-byte consumer; bf16 max / min go
+    to the word kernel from 25 inputs): bit for bit the
     oracle's literal schedule, the ragged length's edges on the element-wise
     kernel, guard bands intact."""
     import collective_reduction_gb300 as ar
@@ -816,7 +819,8 @@ def test_compiled_dag_programs_of_many_inputs_bit_exact(P, algo, op, kw, dtype):
     bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 101)
     plan = ar.Plan(P, n, dtype, op, algo, jit="on", **kw)
     k = plan.info()["kernels"]
-    assert k & (ar.KERNEL_WORD_JIT if P > 32 else ar.KERNEL_DAG_JIT), k
+    selects = dtype == "bfloat16" and op in ("max", "min")
+    assert k & (ar.KERNEL_WORD_JIT if P > 32 or (selects and P >= 25) else ar.KERNEL_DAG_JIT), k
     plan.close()
     want = oracle.run(algo, bufs, Arith(op, dtype), **kw).bufs
     got = engine(bufs, dtype, op, algo, jit="on", **kw)

@@ -379,5 +379,36 @@ def test_compiled_dag_lowering(lib, P, algo, kw):
     assert low["staged_tile_bytes"] * low["staged_stages"] >= off["staged_tile_bytes"] * off["staged_stages"]
 
 
+@pytest.mark.parametrize("op,dtype,word", [("max", "bfloat16", True), ("min", "bfloat16", True),
+                                           ("sum", "bfloat16", False), ("max", "float32", False)])
+def test_bf16_select_programs_go_to_the_word_kernel_from_25_inputs(lib, op, dtype, word):
+    """bf16 max / min programs of 25 to 32 inputs (P = 31, r = 5) are lowered
+    to the word kernel, whose consumers read no staged tiles; the other
+    operations and types of that size keep the staged word consumer.  At
+    P = 24 (24 inputs) none of them does."""
+    n = (1 << 20) + 37
+    s = ar.Schedule(31, n, dtype, op, "generalized", jit="on", r=5)
+    if s.dag_kernel_bytes() == 0:
+        pytest.skip("NVRTC is not available on this host")
+    low = s.lowering()
+    assert low["tiling_ok"] == 1
+    assert (low["word_sets"] > 0) == word and (low["dag_words"] == 0) == word, low
+    small = ar.Schedule(24, n, dtype, op, "generalized", jit="on", r=4).lowering()
+    assert small["word_sets"] == 0 and small["dag_words"] > 0
+
+
+@pytest.mark.parametrize("P", [17, 18, 19, 24, 31])
+def test_word_consumer_tiles_are_at_most_2_kib(lib, P):
+    """Compiled programs of 17 to 32 inputs on the staged kernel take 2 KB
+    tiles with as many stages as fit in the shared memory (at least 3, at
+    most 8): at P = 17 six stages, not three of 4 KB."""
+    low = ar.Schedule(P, (1 << 22) + 5, "float32", "sum", "generalized", jit="on", r=2).lowering()
+    if low["dag_words"] == 0:
+        pytest.skip("NVRTC is not available on this host")
+    budget = 227 * 1024
+    assert low["staged_tile_bytes"] == 2048
+    assert low["staged_stages"] == min(8, (budget - 512) // (2048 * P)) >= 3
+
+
 def test_lowering_null_checks(lib):
     assert lib.ar_schedule_lowering(None, None) == 1
