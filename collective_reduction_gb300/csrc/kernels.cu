@@ -664,6 +664,75 @@ __global__ void __launch_bounds__(kChainWordThreads) chain_word_kernel(const __g
     }
 }
 
+// ------------------------------------------------------------- copy kernel
+//
+// Fused passes that only copy (all-gathers: one input chunk, written to every
+// other rank) move (P - 1) bytes out for each byte in, and what bounds them is
+// how many stores the SMs keep in flight.  The rank-streaming kernel, one CTA
+// of 10 warps per SM with TMA bulk stores, reached 90% of the copy peak on
+// them.  Here a CTA of 256 threads takes one 16 KB item: each thread loads
+// its AR_COPY_UNROLL 16-byte vectors (4 of them) before it stores them to
+// every output, and the grid has a CTA per item, so that the hardware keeps
+// every SM full of CTAs (64 registers: 4 resident per SM) as earlier ones
+// finish.  Measured at 256 MiB per rank (P = 2 ... 16, 32 MiB at P = 64):
+// a persistent grid of 8 CTAs per SM over 32 KB items 90-94% of the copy
+// peak, 32 CTAs per SM 97-99%, a CTA per 32 KB item 98-100%, per 16 KB item
+// 99.5-102% (above 1: the peak is a 1 : 1 copy, these passes mostly write);
+// 8 KB items 80% at P = 2.  A CTA's threads share the item's addresses
+// through shared memory.
+#ifndef AR_COPY_UNROLL
+#define AR_COPY_UNROLL 8
+#endif
+
+__device__ __forceinline__ uint4 ldg128_cs(const char* p) {
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kCopyThreads) copy_kernel(const __grid_constant__ KernelArgs a) {
+    constexpr int U = AR_COPY_UNROLL;
+    __shared__ const char* src;
+    __shared__ char* dst[AR_MAX_RANKS];
+    griddep_wait();
+    griddep_launch_dependents();
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        if ((pg.kind != PK_CHAIN_R && pg.kind != PK_CHAIN_L) || pg.n_in != 1 || pg.n_out > AR_MAX_RANKS ||
+            (pg.flags & PF_AVG)) {
+            if (threadIdx.x == 0) atomicOr(a.status, kStatusBadProgram);
+            return;  // every thread alike, before any barrier of this item
+        }
+        const int64_t off = w.elem * ES;
+        __syncthreads();  // the previous item's addresses are read no more
+        if (threadIdx.x == 0) src = buf_addr(a, a.refs[pg.in_off]) + off;
+        for (uint32_t o = threadIdx.x; o < pg.n_out; o += blockDim.x) dst[o] = out_addr(a, pg, o) + off;
+        __syncthreads();
+        const char* s = src;
+        const uint32_t nv = (w.count * ES) >> 4;  // bulk items are whole 16-byte vectors
+        for (uint32_t base = threadIdx.x; base < nv; base += U * blockDim.x) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t q = base + u * blockDim.x;
+                if (q < nv) v[u] = ldg128_cs(s + 16ull * q);
+            }
+            for (uint32_t o = 0; o < pg.n_out; ++o) {
+                char* d = dst[o];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t q = base + u * blockDim.x;
+                    if (q < nv) stg128(d + 16ull * q, v[u]);
+                }
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------- dispatch
 
 using KernelFn = void (*)(KernelArgs);
@@ -778,6 +847,12 @@ cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_i
     const int which = max_in <= 8 ? K_CHAIN_WORD8 : max_in <= 16 ? K_CHAIN_WORD16 : K_CHAIN_WORD;
     KernelFn f = kernel_for(dtype, op, which);
     return launch_dependent(reinterpret_cast<const void*>(f), grid, kChainWordThreads, 0, st, a);
+}
+
+cudaError_t launch_copies(int dtype, const KernelArgs& a, int grid, cudaStream_t st) {
+    const void* f = dtype == AR_BFLOAT16 ? reinterpret_cast<const void*>(copy_kernel<2>)
+                                         : reinterpret_cast<const void*>(copy_kernel<4>);
+    return launch_dependent(f, grid, kCopyThreads, 0, st, a);
 }
 
 cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem, cudaStream_t st) {

@@ -27,5 +27,15 @@ constexpr int kChainWordCtasPerSm = 4;
 cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_in, int grid, cudaStream_t st);
 // One CTA per item, one element per thread.
 cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem, cudaStream_t st);
+// The copy kernel over a.items (programs of one input: copies to every
+// output), kCopyThreads per CTA, grid CTAs (a CTA takes items blockIdx.x,
+// + grid, ...); any dtype and op (nothing is combined).  Launched with up to
+// kCopyCtasPerSm CTAs per SM, in practice one per item: the hardware deals
+// them to the SMs as earlier ones finish.
+#ifndef AR_COPY_CTAS_PER_SM
+#define AR_COPY_CTAS_PER_SM 1024
+#endif
+constexpr int kCopyCtasPerSm = AR_COPY_CTAS_PER_SM;
+cudaError_t launch_copies(int dtype, const KernelArgs& a, int grid, cudaStream_t st);
 
 }  // namespace ar

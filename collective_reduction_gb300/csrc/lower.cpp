@@ -51,6 +51,9 @@
 #ifndef AR_TMEM_TREE_STAGES
 #define AR_TMEM_TREE_STAGES 4
 #endif
+#ifndef AR_COPY_KERNEL
+#define AR_COPY_KERNEL 1
+#endif
 #ifndef AR_JIT_GEOMETRY
 #define AR_JIT_GEOMETRY 1
 #endif
@@ -754,6 +757,25 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
             stream[k] = small[k] = false;
         }
     }
+    // Fused passes whose programs all copy one input to their outputs (the
+    // all-gathers) run on the copy kernel: a CTA per 16 KB item, its loads
+    // in flight before its stores, where the rank-streaming kernel keeps one
+    // CTA per SM and its TMA stores (90% of the copy peak against 99.5-102%;
+    // the kernel has the measurements).
+    std::vector<bool> copies(sets.size(), false);
+    for (size_t k = 0; k < sets.size(); ++k) {
+        if (sets[k].empty() || small[k] || cwords[k] || S.params.form != AR_FORM_FUSED) continue;
+        bool copy = AR_COPY_KERNEL != 0;
+        for (auto& r : sets[k]) {
+            const DevProg& d = lw.progs[r.prog];
+            copy = copy && (d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L) && d.n_in == 1 && d.n_out >= 1 &&
+                   !(d.flags & PF_AVG);
+        }
+        if (copy) {
+            copies[k] = true;
+            stream[k] = false;
+        }
+    }
     bool stream_trees = false;
     lw.stream_slots = 0;  // shared-memory tiles for the deepest tree stack
     for (size_t k = 0; k < sets.size(); ++k)
@@ -771,7 +793,7 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
             lw.max_in_all = std::max<int>(lw.max_in_all, d.n_in);
             lw.max_tmp_all = std::max<int>(lw.max_tmp_all, d.n_tmp);
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
-            if (a < e && !stream[k] && !small[k] && !words[k] && !cwords[k]) {
+            if (a < e && !stream[k] && !small[k] && !words[k] && !cwords[k] && !copies[k]) {
                 lw.max_in = std::max<int>(lw.max_in, d.n_in);
                 if (!(opt.jit_dag && AR_JIT_GEOMETRY)) lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
             }
@@ -879,6 +901,7 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         ls.stream = stream[k];
         ls.tma_store = stream[k] && tma_store(sets[k]);
         int64_t tile_bytes = cwords[k]   ? chain_word_item_bytes(set_max_in(lw, sets[k]))
+                             : copies[k] ? kCopyItemBytes
                              : words[k]  ? kWordItemBytes
                              : stream[k] ? lw.stream_tile
                                          : lw.tile_bytes;
@@ -913,6 +936,7 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         ls.small = small[k];
         ls.words = words[k];
         ls.chain_words = cwords[k];
+        ls.copies = copies[k];
         ls.max_in = set_max_in(lw, sets[k]);
         ls.chains = !sets[k].empty();
         for (auto& r : sets[k]) {

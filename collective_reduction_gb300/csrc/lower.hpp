@@ -21,6 +21,7 @@ struct LaunchSet {
     bool small = false;              // small set (<= 256 KB): one element-wise launch over fallback
     bool words = false;              // bulk items run on the run-time compiled word kernel
     bool chain_words = false;        // bulk items run on the chain word kernel
+    bool copies = false;             // bulk items run on the copy kernel (one input, many outputs)
     int max_in = 0;                  // most inputs of a program of the set
     bool chains = false;             // every program is a chain the chain word kernel runs
 };
@@ -82,6 +83,11 @@ inline int word_kernel_stages(int max_in) {
     return std::min(4, fit);
 }
 inline int word_kernel_smem(int max_in) { return word_kernel_stages(max_in) * max_in * 4 * kWordThreads; }
+// The copy kernel: rank bytes per work item (one item per CTA).
+#ifndef AR_COPY_ITEM_BYTES
+#define AR_COPY_ITEM_BYTES 16384
+#endif
+constexpr int kCopyItemBytes = AR_COPY_ITEM_BYTES;
 // The chain word kernel: rank bytes per work item for programs of n_in
 // inputs (one round of its threads: kChainWordMaxIn / n_in words each), and
 // the largest set (bytes of traffic) it takes.

@@ -177,11 +177,12 @@ typedef struct {
  * kernel (unaligned edges and tiny passes), DAG_JIT when the staged
  * launches run the plan's run-time compiled DAG kernel, WORD_JIT for the
  * run-time compiled word kernel (launches whose DAG programs it runs with
- * one 32-bit word of every input buffer per thread in registers), and
+ * one 32-bit word of every input buffer per thread in registers),
  * CHAIN_WORD for the chain word kernel (chains of small and mid-sized
- * passes, the same way). */
+ * passes, the same way), and COPY for the copy kernel (fused passes whose
+ * programs copy one input to their outputs: the all-gathers). */
 enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4, AR_KERNEL_DAG_JIT = 8,
-       AR_KERNEL_WORD_JIT = 16, AR_KERNEL_CHAIN_WORD = 32 };
+       AR_KERNEL_WORD_JIT = 16, AR_KERNEL_CHAIN_WORD = 32, AR_KERNEL_COPY = 64 };
 
 typedef struct ar_schedule_s* ar_schedule_t;
 typedef struct ar_plan_s* ar_plan_t;
@@ -296,6 +297,7 @@ typedef struct {
                                 here, NVRTC permitting)                         */
     uint64_t word_kernel_words; /* instruction words of their programs           */
     int stream_tmem;         /* 1: the tree stack lives in tensor memory        */
+    int copy_sets;           /* launch sets on the copy kernel                  */
 } ar_lowering_info;
 ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out);
 

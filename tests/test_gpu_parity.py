@@ -617,6 +617,28 @@ def test_all_gather_spreads_owned_chunks(P, dtype, form):
             assert_bit_equal(got[r], want[r], dtype, f"{algo} {kw} rank {r}")
 
 
+@pytest.mark.parametrize("P,algo,kw,dtype,offset", [(64, "ring", {}, "float32", 0), (33, "rh", {}, "bfloat16", 0),
+                                                     (8, "generalized", {"group": "xor"}, "float32", 0),
+                                                     (8, "ring", {}, "bfloat16", 1), (3, "ring", {}, "int32", 0)])
+def test_fused_all_gathers_run_on_the_copy_kernel(P, algo, kw, dtype, offset):
+    """Fused all-gathers run on the copy kernel (one input chunk stored to
+    every other rank, 2048 threads per SM): bit for bit the oracle's result
+    at a length of several 32 KB items with a ragged tail, 63 outputs per
+    item at P = 64, guard bands intact; with buffers one element off the
+    16-byte grid the plan takes the element-wise fallback instead."""
+    import collective_reduction_gb300 as ar
+    n = (3 << 16) + 7 if P <= 8 else (1 << 14) + 3
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    src = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 41)
+    plan = ar.Plan(P, n, dtype, "sum", algo, phase="all_gather", **kw)
+    assert plan.info()["kernels"] & ar.KERNEL_COPY, plan.info()["kernels"]
+    plan.close()
+    want = oracle.run(algo, src, Arith("sum", dtype), phase="all_gather", **kw).bufs
+    got = engine(src, dtype, "sum", algo, offset=offset, phase="all_gather", **kw)
+    for r in range(P):
+        assert_bit_equal(got[r], want[r], dtype, f"{algo} {kw} rank {r}")
+
+
 # ---- avg: the sum divided by P where it completes ---------------------------------------
 
 AVG_CASES = [("ring", {}), ("binomial", {}), ("rd", {}), ("rh", {}), ("hybrid", {"k1": 1}),

@@ -410,5 +410,21 @@ def test_word_consumer_tiles_are_at_most_2_kib(lib, P):
     assert low["staged_stages"] == min(8, (budget - 512) // (2048 * P)) >= 3
 
 
+@pytest.mark.parametrize("algo,kw", [("ring", {}), ("rh", {}), ("rh", {"P": 7}), ("generalized", {}),
+                                     ("generalized", {"group": "xor"})])
+def test_fused_all_gathers_lower_to_the_copy_kernel(lib, algo, kw):
+    """A fused all-gather's programs each copy one owner's chunk: one launch
+    set on the copy kernel, whole 16-byte items that tile every chunk; the
+    step form's rounds, the allreduce and the reduce-scatter keep their
+    kernels."""
+    kw = dict(kw)
+    P = kw.pop("P", 8)
+    n = (1 << 22) + 3
+    low = ar.Schedule(P, n, "float32", "sum", algo, phase="all_gather", **kw).lowering()
+    assert low["copy_sets"] == 1 and low["launch_sets"] == 1 and low["tiling_ok"] == 1
+    for other in ({"phase": "all_gather", "form": "step"}, {"phase": "reduce_scatter"}, {}):
+        assert ar.Schedule(P, n, "float32", "sum", algo, **other, **kw).lowering()["copy_sets"] == 0
+
+
 def test_lowering_null_checks(lib):
     assert lib.ar_schedule_lowering(None, None) == 1
