@@ -51,6 +51,9 @@
 #ifndef AR_TMEM_TREE_STAGES
 #define AR_TMEM_TREE_STAGES 4
 #endif
+#ifndef AR_MIN_TILE
+#define AR_MIN_TILE 6144
+#endif
 #ifndef AR_COPY_KERNEL
 #define AR_COPY_KERNEL 1
 #endif
@@ -798,13 +801,13 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
                 if (!(opt.jit_dag && AR_JIT_GEOMETRY)) lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
             }
         }
-    // deepest pipeline (up to kStages) that keeps tiles >= 6 KB, else 2 stages
+    // deepest pipeline (up to kStages) that keeps tiles >= AR_MIN_TILE, else 2 stages
     int64_t t = 0;
     lw.stages = 2;
     for (int st = std::max(kStages, 2); st >= 2; --st) {
         t = (kSmemBudget - kBarrierBytes) / (st * lw.max_in + lw.max_tmp);
         lw.stages = st;
-        if (t >= 6144) break;
+        if (t >= AR_MIN_TILE) break;
     }
     t = (kSmemBudget - kBarrierBytes) / (lw.stages * lw.max_in + lw.max_tmp);
     t = std::min<int64_t>(t, kMaxTileBytes);

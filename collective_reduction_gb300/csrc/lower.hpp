@@ -49,10 +49,14 @@ struct Lowered {
 };
 
 // Staged-kernel geometry shared by lowering and launch: shared-memory budget
-// per CTA (the GB300 opt-in maximum), largest input tile, pipeline depth.
-// Measured on the run-time compiled DAG kernels at 256 MiB per rank, 4
-// stages in 227 KB against 3 in 200 KB: P = 7 generalized r = 1 / r = 3
-// +3% / +4% fp32, r = 1 bf16 and RD max bf16 at P = 8 +2%.
+// per CTA (the GB300 opt-in maximum), largest input tile, pipeline depth
+// (the deepest up to AR_STAGES whose tiles stay >= 6 KB).  Measured on the
+// run-time compiled DAG kernels at 256 MiB per rank: 4 stages in 227 KB
+// against 3 in 200 KB, P = 7 generalized r = 1 / r = 3 +3% / +4% fp32, r = 1
+// bf16 and RD max bf16 at P = 8 +2%; 5 stages against 4 (P <= 7 only: 6 KB
+// tiles) +3-4 points of the copy peak at P = 6 and 7, +0.5 at P = 5.  Deeper
+// pipelines of 4-5 KB tiles measured -12 ... +7 points plan by plan (P = 5 ...
+// 16) and are not taken.
 #ifndef AR_SMEM_BUDGET
 #define AR_SMEM_BUDGET (227 * 1024)
 #endif
@@ -60,7 +64,7 @@ struct Lowered {
 #define AR_MAX_TILE kMaxStagedTile
 #endif
 #ifndef AR_STAGES
-#define AR_STAGES 4
+#define AR_STAGES 5
 #endif
 constexpr int kSmemBudget = AR_SMEM_BUDGET;
 constexpr int kMaxTileBytes = AR_MAX_TILE;
