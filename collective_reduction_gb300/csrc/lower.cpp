@@ -54,6 +54,9 @@
 #ifndef AR_MIN_TILE
 #define AR_MIN_TILE 6144
 #endif
+#ifndef AR_JIT_STAGE_TABLE
+#define AR_JIT_STAGE_TABLE 1
+#endif
 #ifndef AR_COPY_KERNEL
 #define AR_COPY_KERNEL 1
 #endif
@@ -809,6 +812,15 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         lw.stages = st;
         if (t >= AR_MIN_TILE) break;
     }
+    // compiled programs of 5 ... 16 inputs (the 16-byte consumers, no
+    // temporaries): the depth measured best for that input count.  Forced
+    // depths 2 ... 7 at 64-128 MiB per rank, fp32 and bf16, generalized and
+    // RD max / min plans: against the rule above +1 point at P = 5, +2 ... +5 at
+    // P = 8 and 10 ... 14 (-1.6 for bf16 RD max at P = 8), the same elsewhere.
+    static const int kStagesByInputs[17] = {0, 0, 0, 0, 0, 6, 5, 5, 5, 4, 4, 4, 4, 3, 3, 2, 2};
+    if (opt.jit_dag && AR_JIT_GEOMETRY && AR_JIT_STAGE_TABLE && lw.max_in >= 5 && lw.max_in <= kWordConsumerMinIn &&
+        lw.max_tmp == 0)
+        lw.stages = kStagesByInputs[lw.max_in];
     t = (kSmemBudget - kBarrierBytes) / (lw.stages * lw.max_in + lw.max_tmp);
     t = std::min<int64_t>(t, kMaxTileBytes);
     t = t >= 512 ? t / 512 * 512 : std::max<int64_t>(16, t / 16 * 16);
