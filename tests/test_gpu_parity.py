@@ -851,16 +851,20 @@ def test_compiled_dag_programs_of_many_inputs_bit_exact(P, algo, op, kw, dtype):
 
 
 @pytest.mark.parametrize("algo,kw", [("ring", {}), ("rh", {"form": "step"}), ("generalized", {"r": 3, "jit": "on"}),
-                                     ("ring", {"order": "fp32acc"})])
+                                     ("ring", {"order": "fp32acc"}), ("ring", {"phase": "all_gather"}),
+                                     ("generalized", {"r": 3, "jit": "on", "P": 31}), ("rd", {"op": "max", "P": 40})])
 def test_execute_captures_in_a_cuda_graph(algo, kw):
     """ar_execute only enqueues kernels: it can be captured in a CUDA graph
-    whose replays give the same results as direct calls."""
+    whose replays give the same results as direct calls (the rank-streaming,
+    step, compiled DAG, fp32-accumulate, copy, word-consumer and word
+    kernels)."""
     import torch
 
     import collective_reduction_gb300 as ar
-    P, n = 7, (1 << 18) + 13
+    kw = dict(kw)
+    P, n, op = kw.pop("P", 7), (1 << 18) + 13, kw.pop("op", "sum")
     bufs = ar_synth.rank_inputs(P, n, "float32", "normal", sigma=1e-2, seed=23)
-    plan = ar.Plan(P, n, "float32", "sum", algo, **kw)
+    plan = ar.Plan(P, n, "float32", op, algo, **kw)
     rd = RankBufs.from_host(bufs, "float32")
     direct = rd.views
     plan.execute(direct)

@@ -62,8 +62,14 @@ CASES = [
     dict(P=8, n=(1 << 20) + 3, dtype="float32", op="sum", algo="ring", params={}),
     # step form of a schedule that keeps a second partial per chunk in scratch
     dict(P=7, n=100003, dtype="float32", op="sum", algo="generalized", params={"form": "step", "r": 1}),
-    # fused DAG programs (staged kernel), bf16
+    # fused chains and trees over unequal groups, bf16
     dict(P=5, n=65536 + 17, dtype="bfloat16", op="sum", algo="ahc", params={"group_sizes": [2, 3]}),
+    # fused DAG programs (the interpreting staged kernel)
+    dict(P=7, n=200003, dtype="float32", op="max", algo="rd", params={}),
+    # a fused all-gather (copy kernel), bf16
+    dict(P=8, n=(1 << 18) + 5, dtype="bfloat16", op="sum", algo="ring", params={"phase": "all_gather"}),
+    # a mid-sized pass of long chains (chain word kernel)
+    dict(P=16, n=(1 << 18) + 1, dtype="float32", op="sum", algo="ring", params={}),
 ]
 
 
