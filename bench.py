@@ -70,6 +70,7 @@ def parse():
     ap.add_argument("--no-floor", action="store_true",
                     help="skip the config5_floor points timed after the headline")
     ap.add_argument("--sweep", default=None, help="write the size sweep as JSON lines to this file")
+    ap.add_argument("--sweep-ps", default="2,8,16,64", help="rank counts of the size sweep (comma-separated)")
     ap.add_argument("--rows", default=None,
                     help="time every schedule at the bench size (fused and step), JSON lines to this file")
     ap.add_argument("--costmodel", default=None,
@@ -706,7 +707,7 @@ def run_sweep(a, path):
     peak, _ = measured_peak()
     with open(path, "w") as out:
         for dtype in ("float32", "bfloat16"):
-            for P in (2, 8, 16, 64):
+            for P in [int(p) for p in a.sweep_ps.split(",")]:
                 for lg in range(10, 29):
                     S = 1 << lg
                     if P * S * 1.2 > free:

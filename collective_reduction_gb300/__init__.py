@@ -24,7 +24,7 @@ PHASES = {"allreduce": 0, "reduce_scatter": 1, "all_gather": 2}
 JIT = {"auto": 0, "on": 1, "off": -1}
 ESIZE = {"int32": 4, "float32": 4, "bfloat16": 2}
 KERNEL_STREAM, KERNEL_STAGED, KERNEL_ELEMENTWISE, KERNEL_DAG_JIT, KERNEL_WORD_JIT, KERNEL_CHAIN_WORD = 1, 2, 4, 8, 16, 32
-KERNEL_COPY = 64
+KERNEL_COPY, KERNEL_FEW = 64, 128
 MAX_RANKS = 64
 
 STATUS = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_UNSUPPORTED", 3: "AR_ERR_CUDA",
@@ -67,7 +67,7 @@ class LoweringInfo(ctypes.Structure):
                 ("stream_tile_bytes", ctypes.c_int), ("stream_stages", ctypes.c_int),
                 ("staged_tile_bytes", ctypes.c_int), ("staged_stages", ctypes.c_int), ("dag_words", ctypes.c_uint64),
                 ("word_sets", ctypes.c_int), ("word_kernel_words", ctypes.c_uint64), ("stream_tmem", ctypes.c_int),
-                ("copy_sets", ctypes.c_int)]
+                ("copy_sets", ctypes.c_int), ("few_sets", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

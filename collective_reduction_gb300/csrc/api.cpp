@@ -80,6 +80,7 @@ struct ar_plan_s {
         bool words;
         bool chain_words;
         bool copies;
+        bool few;
         bool chains;
         int max_in;
     };
@@ -199,6 +200,9 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
         } else if (s.copies) {
             const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * ar::kCopyCtasPerSm));
             e = ar::launch_copies(S.dtype, a, cgrid, st);
+        } else if (s.few) {
+            const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * ar::kCopyCtasPerSm));
+            e = ar::launch_few(S.dtype, S.op, a, cgrid, st);
         } else if (s.stream) {
             a.tile_bytes = plan->L.stream_tile;
             a.stages = plan->L.stream_stages;
@@ -387,6 +391,7 @@ ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out) {
         for (const ar::LaunchSet& ls : L.sets) {
             out->word_sets += ls.words;
             out->copy_sets += ls.copies;
+            out->few_sets += ls.few;
         }
         return AR_OK;
     } catch (const std::bad_alloc&) {
@@ -460,7 +465,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
         if (words > 0 && words <= kJitMaxWords && p->S.params.jit != AR_JIT_OFF) {
             uint64_t dag_bytes = 0;
             for (const ar::LaunchSet& s : L.sets)
-                if (!s.stream && !s.small && !s.words && !s.chain_words && !s.copies && !s.bulk.empty())
+                if (!s.stream && !s.small && !s.words && !s.chain_words && !s.copies && !s.few && !s.bulk.empty())
                     dag_bytes += s.bytes;
             if (p->S.params.jit == AR_JIT_ON || dag_bytes >= kJitMinBytes)
                 p->dag_fn = ar::load_dag_kernel(ar::dag_kernel_source(p->S, L));
@@ -522,6 +527,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             s.words = L.sets[i].words;
             s.chain_words = L.sets[i].chain_words;
             s.copies = L.sets[i].copies;
+            s.few = L.sets[i].few;
             s.max_in = L.sets[i].max_in;
             s.chains = L.sets[i].chains;
             p->sets.push_back(s);
@@ -560,9 +566,10 @@ ar_status ar_plan_query(ar_plan_t plan, ar_plan_info* info) {
             info->kernels |= s.words         ? AR_KERNEL_WORD_JIT
                              : s.chain_words ? AR_KERNEL_CHAIN_WORD
                              : s.copies      ? AR_KERNEL_COPY
+                             : s.few         ? AR_KERNEL_FEW
                              : s.stream      ? AR_KERNEL_STREAM
                                              : AR_KERNEL_STAGED;
-        if (!s.bulk.empty() && !s.stream && !s.words && !s.chain_words && !s.copies && plan->dag_fn)
+        if (!s.bulk.empty() && !s.stream && !s.words && !s.chain_words && !s.copies && !s.few && plan->dag_fn)
             info->kernels |= AR_KERNEL_DAG_JIT;
         if (!s.edge.empty()) info->kernels |= AR_KERNEL_ELEMENTWISE;
     }

@@ -98,12 +98,22 @@ __device__ __forceinline__ uint4 vop(uint4 a, uint4 b) {
                       wop<DT, OP>(a.w, b.w));
 }
 
+// x / d, rounded to nearest even, for d the rank count (a positive integer).
+// When d is a power of two its reciprocal is exact, and x * (1 / d) is the
+// same real number as x / d, so rounding it once gives the same bits,
+// subnormal results included: one multiply instead of a division.
+__device__ __forceinline__ float div_rank_count(float x, float d) {
+    const uint32_t b = __float_as_uint(d);
+    if ((b & 0x7FFFFFu) == 0u) return __fmul_rn(x, __uint_as_float((254u - (b >> 23)) << 23));
+    return __fdiv_rn(x, d);
+}
+
 // AR_AVG: a complete sum divided by the rank count d (IEEE division, round to
 // nearest even; bf16 values divided in fp32 and rounded back to bf16).
 template <int DT>
 __device__ __forceinline__ uint32_t wdiv(uint32_t w, float d) {
-    if (DT == AR_FLOAT32) return __float_as_uint(__fdiv_rn(__uint_as_float(w), d));
-    if (DT == AR_BFLOAT16) return pack_bf16x2(__fdiv_rn(bf_lo(w), d), __fdiv_rn(bf_hi(w), d));
+    if (DT == AR_FLOAT32) return __float_as_uint(div_rank_count(__uint_as_float(w), d));
+    if (DT == AR_BFLOAT16) return pack_bf16x2(div_rank_count(bf_lo(w), d), div_rank_count(bf_hi(w), d));
     return w;  // int32 has no average (refused when the plan is made)
 }
 

@@ -733,16 +733,95 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(const __grid_constan
     }
 }
 
+// ------------------------------------------------------- few-input chains
+//
+// Fused passes of chains or fp32 accumulations of at most kFewMaxIn inputs
+// (the ring's fused pass at P <= 4) on the copy kernel's grid shape: a CTA
+// per 16 KB item, each thread loading its AR_FEW_UNROLL 16-byte vectors of
+// every input before it folds them in the program's order (a chain: a2's
+// element op; an accumulation: the fp32 order of the other kernels; avg
+// divided where the program says) and stores the result to every output.
+#ifndef AR_FEW_UNROLL
+#define AR_FEW_UNROLL 2
+#endif
+
+template <int DT, int OP>
+__global__ void __launch_bounds__(kCopyThreads) few_kernel(const __grid_constant__ KernelArgs a) {
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    constexpr int M = kFewMaxIn;
+    constexpr int U = AR_FEW_UNROLL;
+    __shared__ const char* src[M];
+    __shared__ char* dst[AR_MAX_RANKS];
+    griddep_wait();
+    griddep_launch_dependents();
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        if ((pg.kind != PK_CHAIN_R && pg.kind != PK_CHAIN_L && pg.kind != PK_ACC) || pg.n_in < 1 || pg.n_in > M ||
+            pg.n_out > AR_MAX_RANKS) {
+            if (threadIdx.x == 0) atomicOr(a.status, kStatusBadProgram);
+            return;  // every thread alike, before any barrier of this item
+        }
+        const int64_t off = w.elem * ES;
+        __syncthreads();  // the previous item's addresses are read no more
+        for (uint32_t i = threadIdx.x; i < pg.n_in; i += blockDim.x) src[i] = buf_addr(a, a.refs[pg.in_off + i]) + off;
+        for (uint32_t o = threadIdx.x; o < pg.n_out; o += blockDim.x) dst[o] = out_addr(a, pg, o) + off;
+        __syncthreads();
+        const uint32_t n = pg.n_in;
+        const bool right = pg.kind == PK_CHAIN_R;
+        const float div = avg_div(a, pg);
+        const uint32_t nv = (w.count * ES) >> 4;  // bulk items are whole 16-byte vectors
+        for (uint32_t base = threadIdx.x; base < nv; base += U * blockDim.x) {
+            uint4 x[M][U];
+#pragma unroll
+            for (int i = 0; i < M; ++i)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t q = base + u * blockDim.x;
+                    if (i < static_cast<int>(n) && q < nv) x[i][u] = ldg128_cs(src[i] + 16ull * q);
+                }
+            if (pg.kind == PK_ACC) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    AccStream<DT, OP> s;
+#pragma unroll
+                    for (int i = 0; i < M; ++i)
+                        if (i < static_cast<int>(n)) s.feed(i, x[i][u]);
+                    x[0][u] = s.finish(n, div);
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    uint4 acc = x[0][u];
+#pragma unroll
+                    for (int i = 1; i < M; ++i)
+                        if (i < static_cast<int>(n)) acc = right ? vop<DT, OP>(x[i][u], acc) : vop<DT, OP>(acc, x[i][u]);
+                    x[0][u] = div != 0.f ? vdiv<DT>(acc, div) : acc;
+                }
+            }
+            for (uint32_t o = 0; o < pg.n_out; ++o) {
+                char* d = dst[o];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t q = base + u * blockDim.x;
+                    if (q < nv) stg128(d + 16ull * q, x[0][u]);
+                }
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------- dispatch
 
 using KernelFn = void (*)(KernelArgs);
 
 enum Which {
     K_STAGED = 0, K_STREAM = 1, K_ELEM = 3, K_STREAM_TREE = 4, K_STREAM_TREE_WIDE = 5, K_STREAM_MID = 6,
-    K_CHAIN_WORD = 7, K_CHAIN_WORD8 = 8, K_CHAIN_WORD16 = 9, K_STREAM_TREE_TMEM = 10
+    K_CHAIN_WORD = 7, K_CHAIN_WORD8 = 8, K_CHAIN_WORD16 = 9, K_STREAM_TREE_TMEM = 10, K_FEW = 11
 };
 constexpr int kWhich[] = {K_STAGED,     K_STREAM,     K_ELEM,        K_STREAM_TREE,  K_STREAM_TREE_WIDE,
-                          K_STREAM_MID, K_CHAIN_WORD, K_CHAIN_WORD8, K_CHAIN_WORD16, K_STREAM_TREE_TMEM};
+                          K_STREAM_MID, K_CHAIN_WORD, K_CHAIN_WORD8, K_CHAIN_WORD16, K_STREAM_TREE_TMEM,
+                          K_FEW};
 
 template <int DT, int OP>
 KernelFn table(int which) {
@@ -756,6 +835,7 @@ KernelFn table(int which) {
     if (which == K_CHAIN_WORD8) return chain_word_kernel<DT, OP, 8>;
     if (which == K_CHAIN_WORD16) return chain_word_kernel<DT, OP, 16>;
     if (which == K_CHAIN_WORD) return chain_word_kernel<DT, OP, kChainWordMaxIn>;
+    if (which == K_FEW) return few_kernel<DT, OP>;
     if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptTree, true>;
     if (which == K_STREAM_TREE_WIDE) return stream_kernel<DT, OP, kStreamVpt, true>;
     if (which == K_STREAM_TREE_TMEM) return stream_kernel<DT, OP, kStreamVpt, true, true>;
@@ -812,8 +892,9 @@ cudaError_t prepare_kernels(int dtype, int op) {
     if (e != cudaSuccess) return e;
     for (int which : kWhich) {
         KernelFn f = kernel_for(dtype, op, which);
-        // (the chain word kernel has static shared memory only)
-        if (!f || which == K_CHAIN_WORD || which == K_CHAIN_WORD8 || which == K_CHAIN_WORD16) continue;
+        // (the chain word and few-input kernels have static shared memory only)
+        if (!f || which == K_CHAIN_WORD || which == K_CHAIN_WORD8 || which == K_CHAIN_WORD16 || which == K_FEW)
+            continue;
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin);
         if (e != cudaSuccess) return e;
@@ -847,6 +928,11 @@ cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_i
     const int which = max_in <= 8 ? K_CHAIN_WORD8 : max_in <= 16 ? K_CHAIN_WORD16 : K_CHAIN_WORD;
     KernelFn f = kernel_for(dtype, op, which);
     return launch_dependent(reinterpret_cast<const void*>(f), grid, kChainWordThreads, 0, st, a);
+}
+
+cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int grid, cudaStream_t st) {
+    KernelFn f = kernel_for(dtype, op, K_FEW);
+    return launch_dependent(reinterpret_cast<const void*>(f), grid, kCopyThreads, 0, st, a);
 }
 
 cudaError_t launch_copies(int dtype, const KernelArgs& a, int grid, cudaStream_t st) {

@@ -60,6 +60,9 @@
 #ifndef AR_COPY_KERNEL
 #define AR_COPY_KERNEL 1
 #endif
+#ifndef AR_FEW_KERNEL
+#define AR_FEW_KERNEL 1
+#endif
 #ifndef AR_JIT_GEOMETRY
 #define AR_JIT_GEOMETRY 1
 #endif
@@ -782,6 +785,23 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
             stream[k] = false;
         }
     }
+    // Fused passes of short chains or fp32 accumulations (2 ... kFewMaxIn
+    // inputs: the ring's at P <= 4) run on the few-input chain kernel, the
+    // copy kernel's grid shape.
+    std::vector<bool> few(sets.size(), false);
+    for (size_t k = 0; k < sets.size(); ++k) {
+        if (sets[k].empty() || small[k] || cwords[k] || copies[k] || S.params.form != AR_FORM_FUSED) continue;
+        bool ok = AR_FEW_KERNEL != 0;
+        for (auto& r : sets[k]) {
+            const DevProg& d = lw.progs[r.prog];
+            ok = ok && (d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L || d.kind == PK_ACC) && d.n_in >= 2 &&
+                 d.n_in <= kFewMaxIn;
+        }
+        if (ok) {
+            few[k] = true;
+            stream[k] = false;
+        }
+    }
     bool stream_trees = false;
     lw.stream_slots = 0;  // shared-memory tiles for the deepest tree stack
     for (size_t k = 0; k < sets.size(); ++k)
@@ -799,7 +819,7 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
             lw.max_in_all = std::max<int>(lw.max_in_all, d.n_in);
             lw.max_tmp_all = std::max<int>(lw.max_tmp_all, d.n_tmp);
             int64_t a = (r.lo + V - 1) / V * V, e = r.hi / V * V;
-            if (a < e && !stream[k] && !small[k] && !words[k] && !cwords[k] && !copies[k]) {
+            if (a < e && !stream[k] && !small[k] && !words[k] && !cwords[k] && !copies[k] && !few[k]) {
                 lw.max_in = std::max<int>(lw.max_in, d.n_in);
                 if (!(opt.jit_dag && AR_JIT_GEOMETRY)) lw.max_tmp = std::max<int>(lw.max_tmp, d.n_tmp);
             }
@@ -916,7 +936,7 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         ls.stream = stream[k];
         ls.tma_store = stream[k] && tma_store(sets[k]);
         int64_t tile_bytes = cwords[k]   ? chain_word_item_bytes(set_max_in(lw, sets[k]))
-                             : copies[k] ? kCopyItemBytes
+                             : copies[k] || few[k] ? kCopyItemBytes
                              : words[k]  ? kWordItemBytes
                              : stream[k] ? lw.stream_tile
                                          : lw.tile_bytes;
@@ -952,6 +972,7 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         ls.words = words[k];
         ls.chain_words = cwords[k];
         ls.copies = copies[k];
+        ls.few = few[k];
         ls.max_in = set_max_in(lw, sets[k]);
         ls.chains = !sets[k].empty();
         for (auto& r : sets[k]) {

@@ -179,10 +179,12 @@ typedef struct {
  * run-time compiled word kernel (launches whose DAG programs it runs with
  * one 32-bit word of every input buffer per thread in registers),
  * CHAIN_WORD for the chain word kernel (chains of small and mid-sized
- * passes, the same way), and COPY for the copy kernel (fused passes whose
- * programs copy one input to their outputs: the all-gathers). */
+ * passes, the same way), COPY for the copy kernel (fused passes whose
+ * programs copy one input to their outputs: the all-gathers), and FEW for the
+ * few-input chain kernel (fused passes of chains of 2 to 4 inputs: the ring's
+ * at P <= 4). */
 enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4, AR_KERNEL_DAG_JIT = 8,
-       AR_KERNEL_WORD_JIT = 16, AR_KERNEL_CHAIN_WORD = 32, AR_KERNEL_COPY = 64 };
+       AR_KERNEL_WORD_JIT = 16, AR_KERNEL_CHAIN_WORD = 32, AR_KERNEL_COPY = 64, AR_KERNEL_FEW = 128 };
 
 typedef struct ar_schedule_s* ar_schedule_t;
 typedef struct ar_plan_s* ar_plan_t;
@@ -298,6 +300,7 @@ typedef struct {
     uint64_t word_kernel_words; /* instruction words of their programs           */
     int stream_tmem;         /* 1: the tree stack lives in tensor memory        */
     int copy_sets;           /* launch sets on the copy kernel                  */
+    int few_sets;            /* launch sets on the few-input chain kernel       */
 } ar_lowering_info;
 ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out);
 

@@ -337,12 +337,12 @@ def test_unaligned_chains_of_4_byte_elements(P, algo, kw, dtype):
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
 @pytest.mark.parametrize("P,algo,kw", [(5, "ring", {}), (8, "ring", {}), (64, "ring", {}),
-                                       (5, "ahc", {"group_sizes": [2, 3]})])
+                                       (5, "ahc", {"group_sizes": [2, 3]}), (3, "ring", {}), (4, "ring", {})])
 def test_fp32acc_same_bits_in_every_kernel(P, algo, kw, dtype):
     """The fp32-accumulate order is the engine's own and the same in every
     kernel: the rank-streaming kernel (bf16 on 24 KB tiles, fp32 on 32 KB)
-    must give exactly the bits of the element-wise kernel, which unaligned
-    buffers take."""
+    and the few-input chain kernel (P = 3, 4) must give exactly the bits of
+    the element-wise kernel, which unaligned buffers take."""
     n = 300_007
     bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=P + 3)
     fast = engine(bufs, dtype, "sum", algo, order="fp32acc", **kw)
@@ -639,6 +639,30 @@ def test_fused_all_gathers_run_on_the_copy_kernel(P, algo, kw, dtype, offset):
         assert_bit_equal(got[r], want[r], dtype, f"{algo} {kw} rank {r}")
 
 
+@pytest.mark.parametrize("P,algo,op,dtype,offset", [(2, "ring", "sum", "float32", 0), (3, "ring", "max", "bfloat16", 0),
+                                                     (4, "ring", "avg", "float32", 0), (4, "ring", "prod", "int32", 0),
+                                                     (2, "rd", "sum", "bfloat16", 0), (3, "pipeline", "min", "float32", 0),
+                                                     (4, "ring", "sum", "bfloat16", 1), (4, "ring", "avg", "bfloat16", 0)])
+def test_short_chains_run_on_the_few_input_kernel(P, algo, op, dtype, offset):
+    """Fused passes of chains of 2 to 4 inputs run on the few-input chain
+    kernel (a CTA per 16 KB item, every input's vectors loaded before the
+    fold): bit for bit the oracle's chains, avg divided where they complete,
+    over several items and a ragged tail, guard bands intact; one element off
+    the 16-byte grid the plan takes the element-wise fallback instead."""
+    import collective_reduction_gb300 as ar
+    n = (5 << 15) + 11
+    kw = {"blocks": 3} if algo == "pipeline" else {}
+    dist = "uniform_int" if dtype == "int32" else "normal"
+    bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 77)
+    plan = ar.Plan(P, n, dtype, op, algo, **kw)
+    assert plan.info()["kernels"] & ar.KERNEL_FEW, plan.info()["kernels"]
+    plan.close()
+    want = oracle.run(algo, bufs, Arith(op, dtype), **kw).bufs
+    got = engine(bufs, dtype, op, algo, offset=offset, **kw)
+    for r in range(P):
+        assert_bit_equal(got[r], want[r], dtype, f"{algo} {op} rank {r}")
+
+
 # ---- avg: the sum divided by P where it completes ---------------------------------------
 
 AVG_CASES = [("ring", {}), ("binomial", {}), ("rd", {}), ("rh", {}), ("hybrid", {"k1": 1}),
@@ -672,6 +696,28 @@ def test_avg_fp32acc_and_halves(dtype):
             got = engine(bufs, dtype, "avg", algo, form=form, phase="reduce_scatter", **kw)
             for rank, lo, hi in res.info["owner"]:
                 assert_bit_equal(got[rank][lo:hi], res.bufs[rank][lo:hi], dtype, f"{algo} {form} rank {rank}")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("P,algo,form", [(2, "ring", "fused"), (4, "ring", "fused"), (8, "ring", "fused"),
+                                         (8, "rh", "step"), (16, "binomial", "fused"), (3, "ring", "fused")])
+def test_avg_special_values_and_subnormal_quotients(P, algo, form, dtype):
+    """avg over random bit patterns (normal, subnormal, zero, infinite and NaN
+    values of both signs) and over tiny sums whose quotient is subnormal and
+    sits on or beside a rounding tie: at P = 2^k the kernels multiply by the
+    exact reciprocal, which must give the IEEE quotient's bits everywhere; at
+    P = 3 they divide."""
+    n = 200_003
+    rng = np.random.default_rng(31 * P + len(dtype))
+    if dtype == "float32":
+        rand = [rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32).view(np.float32) for _ in range(P)]
+        tiny = [(rng.integers(-64, 64, n) * np.float32(2.0 ** -149)).astype(np.float32) for _ in range(P)]
+    else:
+        rand = [rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16) for _ in range(P)]
+        tiny = [(rng.integers(0, 64, n, dtype=np.uint32) | (rng.integers(0, 2, n, dtype=np.uint32) << 15))
+                .astype(np.uint16) for _ in range(P)]
+    for bufs in (rand, tiny):
+        check_faithful([b.copy() for b in bufs], dtype, "avg", algo, form)
 
 
 def test_avg_unaligned_and_int32_refused():

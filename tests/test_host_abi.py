@@ -426,5 +426,17 @@ def test_fused_all_gathers_lower_to_the_copy_kernel(lib, algo, kw):
         assert ar.Schedule(P, n, "float32", "sum", algo, **other, **kw).lowering()["copy_sets"] == 0
 
 
+@pytest.mark.parametrize("P,algo,kw,few", [(2, "ring", {}, 1), (3, "ring", {}, 1), (4, "ring", {}, 1), (5, "ring", {}, 0),
+                                           (2, "rd", {}, 1), (3, "pipeline", {"blocks": 3}, 1),
+                                           (2, "ring", {"form": "step"}, 0), (4, "ring", {"order": "fp32acc"}, 1),
+                                           (5, "ring", {"order": "fp32acc"}, 0), (4, "binomial", {}, 0)])
+def test_short_fused_chains_lower_to_the_few_input_kernel(lib, P, algo, kw, few):
+    """Fused passes whose programs are all chains or fp32 accumulations of 2
+    to 4 inputs take the few-input chain kernel; longer ones, trees and the
+    step form's rounds keep theirs.  The items tile every range."""
+    low = ar.Schedule(P, (1 << 22) + 3, "float32", "sum", algo, **kw).lowering()
+    assert low["few_sets"] == few and low["tiling_ok"] == 1
+
+
 def test_lowering_null_checks(lib):
     assert lib.ar_schedule_lowering(None, None) == 1
