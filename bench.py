@@ -122,6 +122,15 @@ def kernel_hash():
     return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
+def bulk_kernel_name(bits):
+    """The kernel that runs a plan's aligned bulk items, from ar_plan_info.kernels."""
+    for bit, name in ((16, "ar_word_kernel"), (32, "chain_word_kernel"), (64, "copy_kernel"), (128, "few_kernel"),
+                      (1, "stream_kernel"), (8, "ar_dag_kernel"), (2, "staged_kernel")):
+        if bits & bit:
+            return name
+    return "elementwise_kernel"
+
+
 def recorded_traffic(P, mib, dtype, algo, form, order):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     summary is missing, is for another workload, or predates the kernel."""
@@ -571,8 +580,7 @@ def run_ours(a):
                      "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": alg_bytes,
                      "kernel_ms": round(kernel_ms, 6),
-                     "kernel": ("stream_kernel" if info["kernels"] & 1
-                                else "ar_dag_kernel" if info["kernels"] & 8 else "staged_kernel")},
+                     "kernel": bulk_kernel_name(info["kernels"])},
         "cpu_baseline": cpu,
         "e2e": {"value": round(whole_job_gbps(bytes_per_call, 1, world, e2e_s * 1e3), 3), "unit": "GB/s",
                 "h2d_bytes_per_step": bytes_per_call, "d2h_bytes_per_step": bytes_per_call},

@@ -202,7 +202,7 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
             e = ar::launch_copies(S.dtype, a, cgrid, st);
         } else if (s.few) {
             const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * ar::kCopyCtasPerSm));
-            e = ar::launch_few(S.dtype, S.op, a, cgrid, st);
+            e = ar::launch_few(S.dtype, S.op, a, s.max_in, cgrid, st);
         } else if (s.stream) {
             a.tile_bytes = plan->L.stream_tile;
             a.stages = plan->L.stream_stages;

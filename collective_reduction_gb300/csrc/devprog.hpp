@@ -56,7 +56,7 @@ constexpr int kMaxStagedTile = 32 * kConsumerWarps * 16 * kStagedVpt;          /
 // most inputs / outputs of a program it runs
 constexpr int kChainWordThreads = 128;
 constexpr int kCopyThreads = 256;  // the copy kernel (one input, many outputs)
-constexpr int kFewMaxIn = 4;       // the few-input chain kernel: most inputs of a chain
+constexpr int kFewMaxIn = 16;  // the few-input kernel: most inputs of a program
 constexpr int kChainWordMaxIn = 64;
 constexpr int kStreamTileBytes = 32 * kConsumerWarps * 16 * kStreamVpt;        // 32 KB
 constexpr int kStreamTileTree = 32 * kConsumerWarps * 16 * kStreamVptTree;     // 24 KB

@@ -736,20 +736,20 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(const __grid_constan
 // ------------------------------------------------------- few-input chains
 //
 // Fused passes of chains or fp32 accumulations of at most kFewMaxIn inputs
-// (the ring's fused pass at P <= 4) on the copy kernel's grid shape: a CTA
-// per 16 KB item, each thread loading its AR_FEW_UNROLL 16-byte vectors of
-// every input before it folds them in the program's order (a chain: a2's
-// element op; an accumulation: the fp32 order of the other kernels; avg
-// divided where the program says) and stores the result to every output.
-#ifndef AR_FEW_UNROLL
-#define AR_FEW_UNROLL 2
-#endif
+// (the ring's fused pass at P <= 16) on the copy kernel's grid shape: a CTA
+// per 16 KB item, each thread loading its U 16-byte vectors of every input
+// before it folds them in the program's order (a chain: a2's element op; an
+// accumulation: the fp32 order of the other kernels; avg divided where the
+// program says) and stores the result to every output.  Three
+// instantiations, every load of a thread in flight at once: up to 4 inputs
+// with two vectors per thread (64 registers, four CTAs per SM), up to 8 with
+// two (102 registers, two CTAs per SM), up to 16 with one (110 registers).
+// (The 8-input one at P = 2 held too few loads in flight per SM: 77% of the
+// copy peak against 100.5%.)
 
-template <int DT, int OP>
+template <int DT, int OP, int M, int U>
 __global__ void __launch_bounds__(kCopyThreads) few_kernel(const __grid_constant__ KernelArgs a) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
-    constexpr int M = kFewMaxIn;
-    constexpr int U = AR_FEW_UNROLL;
     __shared__ const char* src[M];
     __shared__ char* dst[AR_MAX_RANKS];
     griddep_wait();
@@ -817,11 +817,12 @@ using KernelFn = void (*)(KernelArgs);
 
 enum Which {
     K_STAGED = 0, K_STREAM = 1, K_ELEM = 3, K_STREAM_TREE = 4, K_STREAM_TREE_WIDE = 5, K_STREAM_MID = 6,
-    K_CHAIN_WORD = 7, K_CHAIN_WORD8 = 8, K_CHAIN_WORD16 = 9, K_STREAM_TREE_TMEM = 10, K_FEW = 11
+    K_CHAIN_WORD = 7, K_CHAIN_WORD8 = 8, K_CHAIN_WORD16 = 9, K_STREAM_TREE_TMEM = 10, K_FEW8 = 11, K_FEW16 = 12,
+    K_FEW4 = 13
 };
 constexpr int kWhich[] = {K_STAGED,     K_STREAM,     K_ELEM,        K_STREAM_TREE,  K_STREAM_TREE_WIDE,
                           K_STREAM_MID, K_CHAIN_WORD, K_CHAIN_WORD8, K_CHAIN_WORD16, K_STREAM_TREE_TMEM,
-                          K_FEW};
+                          K_FEW8,       K_FEW16,      K_FEW4};
 
 template <int DT, int OP>
 KernelFn table(int which) {
@@ -835,7 +836,9 @@ KernelFn table(int which) {
     if (which == K_CHAIN_WORD8) return chain_word_kernel<DT, OP, 8>;
     if (which == K_CHAIN_WORD16) return chain_word_kernel<DT, OP, 16>;
     if (which == K_CHAIN_WORD) return chain_word_kernel<DT, OP, kChainWordMaxIn>;
-    if (which == K_FEW) return few_kernel<DT, OP>;
+    if (which == K_FEW4) return few_kernel<DT, OP, 4, 2>;
+    if (which == K_FEW8) return few_kernel<DT, OP, 8, 2>;
+    if (which == K_FEW16) return few_kernel<DT, OP, kFewMaxIn, 1>;
     if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptTree, true>;
     if (which == K_STREAM_TREE_WIDE) return stream_kernel<DT, OP, kStreamVpt, true>;
     if (which == K_STREAM_TREE_TMEM) return stream_kernel<DT, OP, kStreamVpt, true, true>;
@@ -893,7 +896,8 @@ cudaError_t prepare_kernels(int dtype, int op) {
     for (int which : kWhich) {
         KernelFn f = kernel_for(dtype, op, which);
         // (the chain word and few-input kernels have static shared memory only)
-        if (!f || which == K_CHAIN_WORD || which == K_CHAIN_WORD8 || which == K_CHAIN_WORD16 || which == K_FEW)
+        if (!f || which == K_CHAIN_WORD || which == K_CHAIN_WORD8 || which == K_CHAIN_WORD16 || which == K_FEW4 ||
+            which == K_FEW8 || which == K_FEW16)
             continue;
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin);
@@ -930,8 +934,8 @@ cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_i
     return launch_dependent(reinterpret_cast<const void*>(f), grid, kChainWordThreads, 0, st, a);
 }
 
-cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int grid, cudaStream_t st) {
-    KernelFn f = kernel_for(dtype, op, K_FEW);
+cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int max_in, int grid, cudaStream_t st) {
+    KernelFn f = kernel_for(dtype, op, max_in <= 4 ? K_FEW4 : max_in <= 8 ? K_FEW8 : K_FEW16);
     return launch_dependent(reinterpret_cast<const void*>(f), grid, kCopyThreads, 0, st, a);
 }
 

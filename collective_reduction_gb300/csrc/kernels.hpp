@@ -37,8 +37,9 @@ cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem,
 #endif
 constexpr int kCopyCtasPerSm = AR_COPY_CTAS_PER_SM;
 cudaError_t launch_copies(int dtype, const KernelArgs& a, int grid, cudaStream_t st);
-// The few-input chain kernel over a.items (chains of at most kFewMaxIn
-// inputs), the copy kernel's grid shape.
-cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int grid, cudaStream_t st);
+// The few-input kernel over a.items (chains and fp32 accumulations of at
+// most kFewMaxIn inputs; max_in: the most of the launch's programs), the
+// copy kernel's grid shape.
+cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int max_in, int grid, cudaStream_t st);
 
 }  // namespace ar

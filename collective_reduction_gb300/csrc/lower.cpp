@@ -786,8 +786,8 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         }
     }
     // Fused passes of short chains or fp32 accumulations (2 ... kFewMaxIn
-    // inputs: the ring's at P <= 4) run on the few-input chain kernel, the
-    // copy kernel's grid shape.
+    // inputs: the ring's at P <= 16) run on the few-input kernel, the copy
+    // kernel's grid shape (measured at 128-256 MiB per rank: see the kernel).
     std::vector<bool> few(sets.size(), false);
     for (size_t k = 0; k < sets.size(); ++k) {
         if (sets[k].empty() || small[k] || cwords[k] || copies[k] || S.params.form != AR_FORM_FUSED) continue;

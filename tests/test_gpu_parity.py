@@ -733,12 +733,14 @@ def test_avg_unaligned_and_int32_refused():
 
 
 def test_kernel_choice_per_program_kind():
-    """Chains and single trees stream rank tiles (rank-streaming kernel);
-    rank-specific DAGs stage an item's tiles (staged kernel); tiny or
-    unaligned ranges go element by element."""
+    """Single trees stream rank tiles (rank-streaming kernel); chains of up
+    to 16 inputs take a CTA per item (few-input kernel); rank-specific DAGs
+    stage an item's tiles (staged kernel); tiny or unaligned ranges go
+    element by element."""
     import collective_reduction_gb300 as ar
     n = 1 << 20
-    for algo, kw in (("ring", {}), ("rh", {}), ("binomial", {}), ("rd", {}), ("ahc", {"group_sizes": [4, 4]})):
+    assert ar.Plan(8, n, "float32", "sum", "ring").info()["kernels"] == ar.KERNEL_FEW
+    for algo, kw in (("rh", {}), ("binomial", {}), ("rd", {}), ("ahc", {"group_sizes": [4, 4]})):
         k = ar.Plan(8, n, "float32", "sum", algo, **kw).info()["kernels"]
         assert k == ar.KERNEL_STREAM, (algo, k)
     # 30 chunks of 2^20 elements: unaligned chunk edges go element-wise

@@ -319,14 +319,17 @@ def test_wave_balance_closed_form(lib):
     """Round robin over 152 CTAs: P = 64 x 2^23 fp32 ring has 64 chunks of
     2^17 elements, 16 whole 32 KB tiles each, 1024 equal items: 112 CTAs take
     7 and 40 take 6, so the largest share over the mean is 7 / (1024 / 152).
-    P = 8 x 2^26 has 8192 items: 54 / (8192 / 152).  Windows: 2 GiB of rank
-    data makes 16 windows of 128 MB."""
+    P = 8 x 2^26 RH (single trees) has 8192 items: 54 / (8192 / 152); the
+    ring there runs on the few-input kernel, a CTA per 16 KB item (16384).
+    Windows: 2 GiB of rank data makes 16 windows of 128 MB."""
     low = ar.Schedule(64, 1 << 23, "float32", "sum", "ring").lowering()
     assert low["items"] == 1024 and low["windows"] == 16
     assert abs(low["wave_balance"] - 7 / (1024 / 152)) < 1e-9
-    low = ar.Schedule(8, 1 << 26, "float32", "sum", "ring").lowering()
+    low = ar.Schedule(8, 1 << 26, "float32", "sum", "rh").lowering()
     assert low["items"] == 8192 and low["windows"] == 16
     assert abs(low["wave_balance"] - 54 / (8192 / 152)) < 1e-9
+    low = ar.Schedule(8, 1 << 26, "float32", "sum", "ring").lowering()
+    assert low["items"] == 16384 and low["few_sets"] == 1 and low["windows"] == 16
 
 
 def test_stream_geometry_follows_the_programs(lib):
@@ -334,25 +337,24 @@ def test_stream_geometry_follows_the_programs(lib):
     32 KB for chains over 4-byte elements, 5 for their fp32 accumulation, 4
     for bf16 chains, trees of more than 8 leaves with their stack in tensor
     memory on 4 stages of 32 KB, and 7 stages of 24 KB for bf16 fp32
-    accumulation."""
+    accumulation.  (Chains and accumulations of up to 16 inputs run on the
+    few-input kernel instead.)"""
     def geo(P, dtype, algo, op="sum", **kw):
         low = ar.Schedule(P, P * (1 << 16), dtype, op, algo, **kw).lowering()
         return low["stream_tile_bytes"], low["stream_stages"]
-    assert geo(8, "float32", "ring") == (32768, 3)
-    assert geo(8, "int32", "ring") == (32768, 3)
-    assert geo(8, "bfloat16", "ring") == (32768, 4)
-    assert geo(8, "bfloat16", "ring", op="max") == (32768, 4)
+    assert geo(32, "float32", "ring") == (32768, 3)
+    assert geo(32, "int32", "ring") == (32768, 3)
+    assert geo(32, "bfloat16", "ring") == (32768, 4)
+    assert geo(32, "bfloat16", "ring", op="max") == (32768, 4)
     assert geo(8, "float32", "rh") == (32768, 4)        # 3 stack tiles + 4 stages
     assert geo(64, "float32", "rh") == (32768, 4)       # 6 stack entries in tensor memory
     assert geo(32, "bfloat16", "binomial") == (32768, 4)
     tm = lambda P, algo: ar.Schedule(P, P * (1 << 16), "float32", "sum", algo).lowering()["stream_tmem"]
     assert tm(64, "rh") == 1 and tm(32, "binomial") == 1 and tm(16, "rh") == 1
     assert tm(8, "rh") == 0 and tm(8, "ring") == 0
-    assert geo(8, "bfloat16", "ring", order="fp32acc") == (24576, 7)
+    assert geo(32, "bfloat16", "ring", order="fp32acc") == (24576, 7)
     assert geo(64, "bfloat16", "ring", order="fp32acc") == (24576, 7)
-    # P = 2: the fp32 accumulation of a sum is the one faithful combine
-    assert geo(2, "bfloat16", "ring", order="fp32acc") == (32768, 4)
-    assert geo(8, "float32", "ring", order="fp32acc") == (32768, 5)
+    assert geo(32, "float32", "ring", order="fp32acc") == (32768, 5)
 
 
 @pytest.mark.parametrize("P,algo,kw", [(31, "generalized", {"r": 5}), (64, "rd", {}), (13, "generalized", {"r": 2})])
@@ -426,15 +428,17 @@ def test_fused_all_gathers_lower_to_the_copy_kernel(lib, algo, kw):
         assert ar.Schedule(P, n, "float32", "sum", algo, **other, **kw).lowering()["copy_sets"] == 0
 
 
-@pytest.mark.parametrize("P,algo,kw,few", [(2, "ring", {}, 1), (3, "ring", {}, 1), (4, "ring", {}, 1), (5, "ring", {}, 0),
-                                           (2, "rd", {}, 1), (3, "pipeline", {"blocks": 3}, 1),
+@pytest.mark.parametrize("P,algo,kw,few", [(2, "ring", {}, 1), (3, "ring", {}, 1), (8, "ring", {}, 1), (16, "ring", {}, 1),
+                                           (17, "ring", {}, 0), (2, "rd", {}, 1), (8, "pipeline", {"blocks": 4}, 1),
                                            (2, "ring", {"form": "step"}, 0), (4, "ring", {"order": "fp32acc"}, 1),
-                                           (5, "ring", {"order": "fp32acc"}, 0), (4, "binomial", {}, 0)])
+                                           (16, "ring", {"order": "fp32acc"}, 1), (17, "ring", {"order": "fp32acc"}, 0),
+                                           (4, "binomial", {}, 0), (8, "rh", {}, 0)])
 def test_short_fused_chains_lower_to_the_few_input_kernel(lib, P, algo, kw, few):
     """Fused passes whose programs are all chains or fp32 accumulations of 2
-    to 4 inputs take the few-input chain kernel; longer ones, trees and the
-    step form's rounds keep theirs.  The items tile every range."""
-    low = ar.Schedule(P, (1 << 22) + 3, "float32", "sum", algo, **kw).lowering()
+    to 16 inputs, and too large for the chain word kernel, take the
+    few-input kernel; longer ones, trees and the step form's rounds keep
+    theirs.  The items tile every range."""
+    low = ar.Schedule(P, (1 << 24) + 3, "float32", "sum", algo, **kw).lowering()
     assert low["few_sets"] == few and low["tiling_ok"] == 1
 
 
