@@ -81,6 +81,7 @@ struct ar_plan_s {
         bool chain_words;
         bool copies;
         bool few;
+        bool few_trees;
         bool chains;
         int max_in;
     };
@@ -202,7 +203,7 @@ cudaError_t launch_range(const ar_plan_s* plan, ar::KernelArgs& a, const ar_plan
             e = ar::launch_copies(S.dtype, a, cgrid, st);
         } else if (s.few) {
             const int cgrid = static_cast<int>(std::min<uint32_t>(b1 - b0, plan->num_sms * ar::kCopyCtasPerSm));
-            e = ar::launch_few(S.dtype, S.op, a, s.max_in, cgrid, st);
+            e = ar::launch_few(S.dtype, S.op, a, s.max_in, s.few_trees, cgrid, st);
         } else if (s.stream) {
             a.tile_bytes = plan->L.stream_tile;
             a.stages = plan->L.stream_stages;
@@ -528,6 +529,7 @@ ar_status ar_plan_create(int P, uint64_t n, ar_dtype dtype, ar_op op, ar_algo al
             s.chain_words = L.sets[i].chain_words;
             s.copies = L.sets[i].copies;
             s.few = L.sets[i].few;
+            s.few_trees = L.sets[i].few_trees;
             s.max_in = L.sets[i].max_in;
             s.chains = L.sets[i].chains;
             p->sets.push_back(s);

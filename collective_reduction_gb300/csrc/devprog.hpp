@@ -56,7 +56,11 @@ constexpr int kMaxStagedTile = 32 * kConsumerWarps * 16 * kStagedVpt;          /
 // most inputs / outputs of a program it runs
 constexpr int kChainWordThreads = 128;
 constexpr int kCopyThreads = 256;  // the copy kernel (one input, many outputs)
-constexpr int kFewMaxIn = 16;  // the few-input kernel: most inputs of a program
+constexpr int kFewMaxIn = 16;        // the few-input kernel: most inputs of a program
+constexpr int kFewTreeMaxIn = 8;     // ... of a single tree
+// ... and the stack entries below the top of a tree its instantiation for
+// trees of up to m leaves holds
+AR_HD constexpr int few_tree_stack(int m) { return m <= 4 ? 2 : 4; }
 constexpr int kChainWordMaxIn = 64;
 constexpr int kStreamTileBytes = 32 * kConsumerWarps * 16 * kStreamVpt;        // 32 KB
 constexpr int kStreamTileTree = 32 * kConsumerWarps * 16 * kStreamVptTree;     // 24 KB

@@ -746,19 +746,30 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(const __grid_constan
 // two (102 registers, two CTAs per SM), up to 16 with one (110 registers).
 // (The 8-input one at P = 2 held too few loads in flight per SM: 77% of the
 // copy peak against 100.5%.)
+#ifndef AR_FEW_TREE_UNROLL
+#define AR_FEW_TREE_UNROLL 1
+#endif
 
-template <int DT, int OP, int M, int U>
+// The TREES instantiations run single trees too (with chains): the program's
+// leaves in post-order with the combines that follow each (4 bits a leaf, as
+// the rank-streaming kernel reads them), the top of the stack in registers
+// and at most kFewTreeStack deeper entries in registers indexed by unrolled
+// selects (the stack pointer is the same in every thread).
+template <int DT, int OP, int M, int U, bool TREES>
 __global__ void __launch_bounds__(kCopyThreads) few_kernel(const __grid_constant__ KernelArgs a) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    constexpr int S = few_tree_stack(M);
     __shared__ const char* src[M];
     __shared__ char* dst[AR_MAX_RANKS];
+    __shared__ uint32_t counts[(M + 7) / 8];
     griddep_wait();
     griddep_launch_dependents();
     for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
         const WorkItem w = a.items[it];
         const DevProg pg = a.progs[w.prog];
-        if ((pg.kind != PK_CHAIN_R && pg.kind != PK_CHAIN_L && pg.kind != PK_ACC) || pg.n_in < 1 || pg.n_in > M ||
-            pg.n_out > AR_MAX_RANKS) {
+        const bool kind_ok = pg.kind == PK_CHAIN_R || pg.kind == PK_CHAIN_L ||
+                             (TREES ? pg.kind == PK_TREE && pg.n_tmp <= S : pg.kind == PK_ACC);
+        if (!kind_ok || pg.n_in < 1 || pg.n_in > M || pg.n_out > AR_MAX_RANKS) {
             if (threadIdx.x == 0) atomicOr(a.status, kStatusBadProgram);
             return;  // every thread alike, before any barrier of this item
         }
@@ -766,6 +777,7 @@ __global__ void __launch_bounds__(kCopyThreads) few_kernel(const __grid_constant
         __syncthreads();  // the previous item's addresses are read no more
         for (uint32_t i = threadIdx.x; i < pg.n_in; i += blockDim.x) src[i] = buf_addr(a, a.refs[pg.in_off + i]) + off;
         for (uint32_t o = threadIdx.x; o < pg.n_out; o += blockDim.x) dst[o] = out_addr(a, pg, o) + off;
+        if (TREES && pg.kind == PK_TREE && threadIdx.x < (pg.n_in + 7) / 8) counts[threadIdx.x] = a.ins[pg.ins_off + threadIdx.x];
         __syncthreads();
         const uint32_t n = pg.n_in;
         const bool right = pg.kind == PK_CHAIN_R;
@@ -780,7 +792,39 @@ __global__ void __launch_bounds__(kCopyThreads) few_kernel(const __grid_constant
                     const uint32_t q = base + u * blockDim.x;
                     if (i < static_cast<int>(n) && q < nv) x[i][u] = ldg128_cs(src[i] + 16ull * q);
                 }
-            if (pg.kind == PK_ACC) {
+            if (TREES && pg.kind == PK_TREE) {
+                uint4 acc[U], st[S][U];
+                uint32_t sp = 0;  // stack entries, the top one in acc
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    if (i < static_cast<int>(n)) {
+                        uint32_t c = (counts[i >> 3] >> (4 * (i & 7))) & 15u;
+                        if (sp == 0 || c == 0) {
+#pragma unroll
+                            for (int d = 0; d < S; ++d)
+                                if (d + 1 == static_cast<int>(sp))
+#pragma unroll
+                                    for (int u = 0; u < U; ++u) st[d][u] = acc[u];
+#pragma unroll
+                            for (int u = 0; u < U; ++u) acc[u] = x[i][u];
+                            ++sp;
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < U; ++u) acc[u] = vop<DT, OP>(acc[u], x[i][u]);
+                            --c;
+                        }
+                        for (; c > 0; --c, --sp) {
+#pragma unroll
+                            for (int d = 0; d < S; ++d)
+                                if (d + 2 == static_cast<int>(sp))
+#pragma unroll
+                                    for (int u = 0; u < U; ++u) acc[u] = vop<DT, OP>(st[d][u], acc[u]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) x[0][u] = div != 0.f ? vdiv<DT>(acc[u], div) : acc[u];
+            } else if (pg.kind == PK_ACC) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     AccStream<DT, OP> s;
@@ -818,11 +862,11 @@ using KernelFn = void (*)(KernelArgs);
 enum Which {
     K_STAGED = 0, K_STREAM = 1, K_ELEM = 3, K_STREAM_TREE = 4, K_STREAM_TREE_WIDE = 5, K_STREAM_MID = 6,
     K_CHAIN_WORD = 7, K_CHAIN_WORD8 = 8, K_CHAIN_WORD16 = 9, K_STREAM_TREE_TMEM = 10, K_FEW8 = 11, K_FEW16 = 12,
-    K_FEW4 = 13
+    K_FEW4 = 13, K_FEW_TREE8 = 14, K_FEW_TREE4 = 15
 };
 constexpr int kWhich[] = {K_STAGED,     K_STREAM,     K_ELEM,        K_STREAM_TREE,  K_STREAM_TREE_WIDE,
                           K_STREAM_MID, K_CHAIN_WORD, K_CHAIN_WORD8, K_CHAIN_WORD16, K_STREAM_TREE_TMEM,
-                          K_FEW8,       K_FEW16,      K_FEW4};
+                          K_FEW8,       K_FEW16,      K_FEW4,        K_FEW_TREE8,    K_FEW_TREE4};
 
 template <int DT, int OP>
 KernelFn table(int which) {
@@ -836,9 +880,11 @@ KernelFn table(int which) {
     if (which == K_CHAIN_WORD8) return chain_word_kernel<DT, OP, 8>;
     if (which == K_CHAIN_WORD16) return chain_word_kernel<DT, OP, 16>;
     if (which == K_CHAIN_WORD) return chain_word_kernel<DT, OP, kChainWordMaxIn>;
-    if (which == K_FEW4) return few_kernel<DT, OP, 4, 2>;
-    if (which == K_FEW8) return few_kernel<DT, OP, 8, 2>;
-    if (which == K_FEW16) return few_kernel<DT, OP, kFewMaxIn, 1>;
+    if (which == K_FEW4) return few_kernel<DT, OP, 4, 2, false>;
+    if (which == K_FEW8) return few_kernel<DT, OP, 8, 2, false>;
+    if (which == K_FEW16) return few_kernel<DT, OP, kFewMaxIn, 1, false>;
+    if (which == K_FEW_TREE4) return few_kernel<DT, OP, 4, 2, true>;
+    if (which == K_FEW_TREE8) return few_kernel<DT, OP, 8, AR_FEW_TREE_UNROLL, true>;
     if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptTree, true>;
     if (which == K_STREAM_TREE_WIDE) return stream_kernel<DT, OP, kStreamVpt, true>;
     if (which == K_STREAM_TREE_TMEM) return stream_kernel<DT, OP, kStreamVpt, true, true>;
@@ -897,7 +943,7 @@ cudaError_t prepare_kernels(int dtype, int op) {
         KernelFn f = kernel_for(dtype, op, which);
         // (the chain word and few-input kernels have static shared memory only)
         if (!f || which == K_CHAIN_WORD || which == K_CHAIN_WORD8 || which == K_CHAIN_WORD16 || which == K_FEW4 ||
-            which == K_FEW8 || which == K_FEW16)
+            which == K_FEW8 || which == K_FEW16 || which == K_FEW_TREE8 || which == K_FEW_TREE4)
             continue;
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin);
@@ -934,8 +980,10 @@ cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_i
     return launch_dependent(reinterpret_cast<const void*>(f), grid, kChainWordThreads, 0, st, a);
 }
 
-cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int max_in, int grid, cudaStream_t st) {
-    KernelFn f = kernel_for(dtype, op, max_in <= 4 ? K_FEW4 : max_in <= 8 ? K_FEW8 : K_FEW16);
+cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int max_in, bool trees, int grid, cudaStream_t st) {
+    KernelFn f = kernel_for(dtype, op,
+                            trees ? (max_in <= 4 ? K_FEW_TREE4 : K_FEW_TREE8)
+                                  : (max_in <= 4 ? K_FEW4 : max_in <= 8 ? K_FEW8 : K_FEW16));
     return launch_dependent(reinterpret_cast<const void*>(f), grid, kCopyThreads, 0, st, a);
 }
 

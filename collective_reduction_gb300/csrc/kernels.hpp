@@ -38,8 +38,9 @@ cudaError_t launch_elementwise(int dtype, int op, const KernelArgs& a, int smem,
 constexpr int kCopyCtasPerSm = AR_COPY_CTAS_PER_SM;
 cudaError_t launch_copies(int dtype, const KernelArgs& a, int grid, cudaStream_t st);
 // The few-input kernel over a.items (chains and fp32 accumulations of at
-// most kFewMaxIn inputs; max_in: the most of the launch's programs), the
-// copy kernel's grid shape.
-cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int max_in, int grid, cudaStream_t st);
+// most kFewMaxIn inputs, or with `trees` chains and single trees of at most
+// kFewTreeMaxIn; max_in: the most of the launch's programs), the copy
+// kernel's grid shape.
+cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int max_in, bool trees, int grid, cudaStream_t st);
 
 }  // namespace ar

@@ -63,6 +63,10 @@
 #ifndef AR_FEW_KERNEL
 #define AR_FEW_KERNEL 1
 #endif
+#ifndef AR_FEW_TREES
+#define AR_FEW_TREES 1
+#endif
+
 #ifndef AR_JIT_GEOMETRY
 #define AR_JIT_GEOMETRY 1
 #endif
@@ -788,17 +792,27 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
     // Fused passes of short chains or fp32 accumulations (2 ... kFewMaxIn
     // inputs: the ring's at P <= 16) run on the few-input kernel, the copy
     // kernel's grid shape (measured at 128-256 MiB per rank: see the kernel).
-    std::vector<bool> few(sets.size(), false);
+    // Sets of single trees (with chains) of up to kFewTreeMaxIn leaves that
+    // write every rank (the allreduce's trees, not a reduce-scatter's, which
+    // measured 2 points slower there) take its tree instantiation, when
+    // their stacks fit the registers it keeps for them.
+    std::vector<bool> few(sets.size(), false), few_trees(sets.size(), false);
     for (size_t k = 0; k < sets.size(); ++k) {
         if (sets[k].empty() || small[k] || cwords[k] || copies[k] || S.params.form != AR_FORM_FUSED) continue;
-        bool ok = AR_FEW_KERNEL != 0;
+        bool flat = AR_FEW_KERNEL != 0, tree = AR_FEW_KERNEL != 0 && AR_FEW_TREES != 0, any_tree = false;
+        const int stack = few_tree_stack(set_max_in(lw, sets[k]));
         for (auto& r : sets[k]) {
             const DevProg& d = lw.progs[r.prog];
-            ok = ok && (d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L || d.kind == PK_ACC) && d.n_in >= 2 &&
-                 d.n_in <= kFewMaxIn;
+            const bool size_ok = d.n_in >= 2 && d.n_in <= kFewMaxIn;
+            const bool chain = d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L;
+            flat = flat && size_ok && (chain || d.kind == PK_ACC);
+            tree = tree && size_ok && d.n_in <= kFewTreeMaxIn &&
+                   (chain || (d.kind == PK_TREE && d.n_tmp <= stack && d.n_out >= 2));
+            any_tree = any_tree || d.kind == PK_TREE;
         }
-        if (ok) {
+        if (flat || (tree && any_tree)) {
             few[k] = true;
+            few_trees[k] = !flat;
             stream[k] = false;
         }
     }
@@ -973,6 +987,7 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         ls.chain_words = cwords[k];
         ls.copies = copies[k];
         ls.few = few[k];
+        ls.few_trees = few_trees[k];
         ls.max_in = set_max_in(lw, sets[k]);
         ls.chains = !sets[k].empty();
         for (auto& r : sets[k]) {

@@ -22,7 +22,8 @@ struct LaunchSet {
     bool words = false;              // bulk items run on the run-time compiled word kernel
     bool chain_words = false;        // bulk items run on the chain word kernel
     bool copies = false;             // bulk items run on the copy kernel (one input, many outputs)
-    bool few = false;                // bulk items run on the few-input chain kernel
+    bool few = false;                // bulk items run on the few-input kernel
+    bool few_trees = false;          // ... its instantiation for single trees (and chains)
     int max_in = 0;                  // most inputs of a program of the set
     bool chains = false;             // every program is a chain the chain word kernel runs
 };

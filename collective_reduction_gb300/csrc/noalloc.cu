@@ -180,7 +180,7 @@ extern "C" ar_status ar_allreduce_static(int P, uint64_t n, ar_dtype dtype, ar_o
                     } else if (s.few) {
                         const int cgrid =
                             static_cast<int>(std::min<size_t>(s.bulk.size(), ar::kCopyCtasPerSm * d->num_sms));
-                        e = ar::launch_few(dtype, op, a, s.max_in, cgrid, cs);
+                        e = ar::launch_few(dtype, op, a, s.max_in, s.few_trees, cgrid, cs);
                     } else if (s.stream) {
                         a.tile_bytes = L.stream_tile;
                         a.stages = L.stream_stages;

@@ -642,16 +642,21 @@ def test_fused_all_gathers_run_on_the_copy_kernel(P, algo, kw, dtype, offset):
 @pytest.mark.parametrize("P,algo,op,dtype,offset", [(2, "ring", "sum", "float32", 0), (3, "ring", "max", "bfloat16", 0),
                                                      (4, "ring", "avg", "float32", 0), (4, "ring", "prod", "int32", 0),
                                                      (2, "rd", "sum", "bfloat16", 0), (3, "pipeline", "min", "float32", 0),
-                                                     (4, "ring", "sum", "bfloat16", 1), (4, "ring", "avg", "bfloat16", 0)])
+                                                     (4, "ring", "sum", "bfloat16", 1), (4, "ring", "avg", "bfloat16", 0),
+                                                     (8, "rh", "sum", "float32", 0), (8, "binomial", "max", "bfloat16", 0),
+                                                     (7, "rh", "avg", "float32", 0), (8, "rd", "prod", "int32", 0),
+                                                     (6, "ahc", "sum", "bfloat16", 0), (5, "generalized", "min", "float32", 0),
+                                                     (8, "hybrid", "sum", "bfloat16", 1)])
 def test_short_chains_run_on_the_few_input_kernel(P, algo, op, dtype, offset):
-    """Fused passes of chains of 2 to 4 inputs run on the few-input chain
-    kernel (a CTA per 16 KB item, every input's vectors loaded before the
-    fold): bit for bit the oracle's chains, avg divided where they complete,
+    """Fused passes of chains of up to 16 inputs and single trees of up to 8
+    leaves run on the few-input kernel (a CTA per 16 KB item, every input's
+    vectors loaded before the fold; a tree's stack in registers): bit for
+    bit the oracle's chains and trees, avg divided where they complete,
     over several items and a ragged tail, guard bands intact; one element off
     the 16-byte grid the plan takes the element-wise fallback instead."""
     import collective_reduction_gb300 as ar
     n = (5 << 15) + 11
-    kw = {"blocks": 3} if algo == "pipeline" else {}
+    kw = {"pipeline": {"blocks": 3}, "ahc": {"group_sizes": [2, 4]}, "hybrid": {"k1": 1}}.get(algo, {})
     dist = "uniform_int" if dtype == "int32" else "normal"
     bufs = ar_synth.rank_inputs(P, n, dtype, dist, sigma=1.0, seed=P + 77)
     plan = ar.Plan(P, n, dtype, op, algo, **kw)
@@ -733,20 +738,22 @@ def test_avg_unaligned_and_int32_refused():
 
 
 def test_kernel_choice_per_program_kind():
-    """Single trees stream rank tiles (rank-streaming kernel); chains of up
-    to 16 inputs take a CTA per item (few-input kernel); rank-specific DAGs
-    stage an item's tiles (staged kernel); tiny or unaligned ranges go
-    element by element."""
+    """Chains of up to 16 inputs and single trees of up to 8 leaves take a
+    CTA per item (few-input kernel); larger single trees stream rank tiles
+    (rank-streaming kernel); rank-specific DAGs stage an item's tiles
+    (staged kernel); tiny or unaligned ranges go element by element."""
     import collective_reduction_gb300 as ar
     n = 1 << 20
-    assert ar.Plan(8, n, "float32", "sum", "ring").info()["kernels"] == ar.KERNEL_FEW
-    for algo, kw in (("rh", {}), ("binomial", {}), ("rd", {}), ("ahc", {"group_sizes": [4, 4]})):
+    for algo, kw in (("ring", {}), ("rh", {}), ("binomial", {}), ("rd", {}), ("ahc", {"group_sizes": [4, 4]})):
         k = ar.Plan(8, n, "float32", "sum", algo, **kw).info()["kernels"]
+        assert k == ar.KERNEL_FEW, (algo, k)
+    for algo, kw in (("rh", {}), ("binomial", {}), ("ahc", {"group_sizes": [8, 8]})):
+        k = ar.Plan(16, n, "float32", "sum", algo, **kw).info()["kernels"]
         assert k == ar.KERNEL_STREAM, (algo, k)
     # 30 chunks of 2^20 elements: unaligned chunk edges go element-wise
     k = ar.Plan(8, n, "float32", "sum", "ahc", group_sizes=[3, 5]).info()["kernels"]
-    assert k == ar.KERNEL_STREAM | ar.KERNEL_ELEMENTWISE, k
-    assert ar.Plan(8, n, "bfloat16", "sum", "rh").info()["kernels"] == ar.KERNEL_STREAM
+    assert k == ar.KERNEL_FEW | ar.KERNEL_ELEMENTWISE, k
+    assert ar.Plan(8, n, "bfloat16", "sum", "rh").info()["kernels"] == ar.KERNEL_FEW
     assert ar.Plan(7, 7 * 4096, "float32", "max", "generalized", r=3).info()["kernels"] & ar.KERNEL_STAGED
     assert ar.Plan(3, 5, "float32", "sum", "ring").info()["kernels"] == ar.KERNEL_ELEMENTWISE
 
