@@ -855,6 +855,71 @@ __global__ void __launch_bounds__(kCopyThreads) few_kernel(const __grid_constant
     }
 }
 
+// Chains and fp32 accumulations of more than kFewMaxIn inputs (up to
+// AR_MAX_RANKS) on the same grid shape: a thread folds its vector of each
+// item in groups of AR_FEW_LONG_GROUP inputs, every load of a group in
+// flight at once, in the program's order across the groups; registers
+// capped for AR_FEW_LONG_MIN_CTAS CTAs per SM.  Measured at 64-256 MiB per
+// rank, P = 32 / 64, fp32 / bf16, faithful / fp32-accumulate: groups of 8
+// with three CTAs per SM (80 registers) 98.5-100.8% of the copy peak,
+// groups of 16 with two (128) within a point of it, groups of 16 with one
+// (142 registers) 91-95%, the rank-streaming kernel 89.6-96.8%.
+#ifndef AR_FEW_LONG_GROUP
+#define AR_FEW_LONG_GROUP 8
+#endif
+#ifndef AR_FEW_LONG_MIN_CTAS
+#define AR_FEW_LONG_MIN_CTAS 3
+#endif
+template <int DT, int OP>
+__global__ void __launch_bounds__(kCopyThreads, AR_FEW_LONG_MIN_CTAS) few_long_kernel(const __grid_constant__ KernelArgs a) {
+    constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;
+    constexpr int G = AR_FEW_LONG_GROUP;
+    __shared__ const char* src[AR_MAX_RANKS];
+    __shared__ char* dst[AR_MAX_RANKS];
+    griddep_wait();
+    griddep_launch_dependents();
+    for (uint32_t it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+        const WorkItem w = a.items[it];
+        const DevProg pg = a.progs[w.prog];
+        if ((pg.kind != PK_CHAIN_R && pg.kind != PK_CHAIN_L && pg.kind != PK_ACC) || pg.n_in < 1 ||
+            pg.n_in > AR_MAX_RANKS || pg.n_out > AR_MAX_RANKS) {
+            if (threadIdx.x == 0) atomicOr(a.status, kStatusBadProgram);
+            return;  // every thread alike, before any barrier of this item
+        }
+        const int64_t off = w.elem * ES;
+        __syncthreads();  // the previous item's addresses are read no more
+        for (uint32_t i = threadIdx.x; i < pg.n_in; i += blockDim.x) src[i] = buf_addr(a, a.refs[pg.in_off + i]) + off;
+        for (uint32_t o = threadIdx.x; o < pg.n_out; o += blockDim.x) dst[o] = out_addr(a, pg, o) + off;
+        __syncthreads();
+        const uint32_t n = pg.n_in;
+        const bool right = pg.kind == PK_CHAIN_R, accumulate = pg.kind == PK_ACC;
+        const float div = avg_div(a, pg);
+        const uint32_t nv = (w.count * ES) >> 4;  // bulk items are whole 16-byte vectors
+        for (uint32_t q = threadIdx.x; q < nv; q += blockDim.x) {
+            AccStream<DT, OP> s;
+            uint4 acc;
+            for (uint32_t g0 = 0; g0 < n; g0 += G) {
+                uint4 x[G];
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if (g0 + i < n) x[i] = ldg128_cs(src[g0 + i] + 16ull * q);
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (g0 + i >= n) break;
+                    if (accumulate)
+                        s.feed(g0 + i, x[i]);
+                    else if (g0 + i == 0)
+                        acc = x[i];
+                    else
+                        acc = right ? vop<DT, OP>(x[i], acc) : vop<DT, OP>(acc, x[i]);
+                }
+            }
+            const uint4 r = accumulate ? s.finish(n, div) : (div != 0.f ? vdiv<DT>(acc, div) : acc);
+            for (uint32_t o = 0; o < pg.n_out; ++o) stg128(dst[o] + 16ull * q, r);
+        }
+    }
+}
+
 // ----------------------------------------------------------------- dispatch
 
 using KernelFn = void (*)(KernelArgs);
@@ -862,11 +927,12 @@ using KernelFn = void (*)(KernelArgs);
 enum Which {
     K_STAGED = 0, K_STREAM = 1, K_ELEM = 3, K_STREAM_TREE = 4, K_STREAM_TREE_WIDE = 5, K_STREAM_MID = 6,
     K_CHAIN_WORD = 7, K_CHAIN_WORD8 = 8, K_CHAIN_WORD16 = 9, K_STREAM_TREE_TMEM = 10, K_FEW8 = 11, K_FEW16 = 12,
-    K_FEW4 = 13, K_FEW_TREE8 = 14, K_FEW_TREE4 = 15
+    K_FEW4 = 13, K_FEW_TREE8 = 14, K_FEW_TREE4 = 15, K_FEW_LONG = 16
 };
 constexpr int kWhich[] = {K_STAGED,     K_STREAM,     K_ELEM,        K_STREAM_TREE,  K_STREAM_TREE_WIDE,
                           K_STREAM_MID, K_CHAIN_WORD, K_CHAIN_WORD8, K_CHAIN_WORD16, K_STREAM_TREE_TMEM,
-                          K_FEW8,       K_FEW16,      K_FEW4,        K_FEW_TREE8,    K_FEW_TREE4};
+                          K_FEW8,       K_FEW16,      K_FEW4,        K_FEW_TREE8,    K_FEW_TREE4,
+                          K_FEW_LONG};
 
 template <int DT, int OP>
 KernelFn table(int which) {
@@ -884,6 +950,7 @@ KernelFn table(int which) {
     if (which == K_FEW8) return few_kernel<DT, OP, 8, 2, false>;
     if (which == K_FEW16) return few_kernel<DT, OP, kFewMaxIn, 1, false>;
     if (which == K_FEW_TREE4) return few_kernel<DT, OP, 4, 2, true>;
+    if (which == K_FEW_LONG) return few_long_kernel<DT, OP>;
     if (which == K_FEW_TREE8) return few_kernel<DT, OP, 8, AR_FEW_TREE_UNROLL, true>;
     if (which == K_STREAM_TREE) return stream_kernel<DT, OP, kStreamVptTree, true>;
     if (which == K_STREAM_TREE_WIDE) return stream_kernel<DT, OP, kStreamVpt, true>;
@@ -943,7 +1010,8 @@ cudaError_t prepare_kernels(int dtype, int op) {
         KernelFn f = kernel_for(dtype, op, which);
         // (the chain word and few-input kernels have static shared memory only)
         if (!f || which == K_CHAIN_WORD || which == K_CHAIN_WORD8 || which == K_CHAIN_WORD16 || which == K_FEW4 ||
-            which == K_FEW8 || which == K_FEW16 || which == K_FEW_TREE8 || which == K_FEW_TREE4)
+            which == K_FEW8 || which == K_FEW16 || which == K_FEW_TREE8 || which == K_FEW_TREE4 ||
+            which == K_FEW_LONG)
             continue;
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin);
@@ -983,7 +1051,10 @@ cudaError_t launch_chain_words(int dtype, int op, const KernelArgs& a, int max_i
 cudaError_t launch_few(int dtype, int op, const KernelArgs& a, int max_in, bool trees, int grid, cudaStream_t st) {
     KernelFn f = kernel_for(dtype, op,
                             trees ? (max_in <= 4 ? K_FEW_TREE4 : K_FEW_TREE8)
-                                  : (max_in <= 4 ? K_FEW4 : max_in <= 8 ? K_FEW8 : K_FEW16));
+                                  : (max_in <= 4   ? K_FEW4
+                                     : max_in <= 8 ? K_FEW8
+                                     : max_in <= kFewMaxIn ? K_FEW16
+                                                           : K_FEW_LONG));
     return launch_dependent(reinterpret_cast<const void*>(f), grid, kCopyThreads, 0, st, a);
 }
 

@@ -66,6 +66,12 @@
 #ifndef AR_FEW_TREES
 #define AR_FEW_TREES 1
 #endif
+#ifndef AR_FEW_LONG
+#define AR_FEW_LONG 1
+#endif
+#ifndef AR_FEW_LONG_MIN_BYTES
+#define AR_FEW_LONG_MIN_BYTES (1536ull << 20)
+#endif
 
 #ifndef AR_JIT_GEOMETRY
 #define AR_JIT_GEOMETRY 1
@@ -801,11 +807,19 @@ void lower(const Schedule& S, Lowered& lw, const LowerOptions& opt) {
         if (sets[k].empty() || small[k] || cwords[k] || copies[k] || S.params.form != AR_FORM_FUSED) continue;
         bool flat = AR_FEW_KERNEL != 0, tree = AR_FEW_KERNEL != 0 && AR_FEW_TREES != 0, any_tree = false;
         const int stack = few_tree_stack(set_max_in(lw, sets[k]));
+        // programs of more inputs than one group (the grouped variant) only
+        // in sets of at least AR_FEW_LONG_MIN_BYTES: P = 64 at 4-8 MiB per
+        // rank measured 78-85% of the copy peak there against 87-89% on the
+        // rank-streaming kernel, at 16-256 MiB 92-98% against 86-96%
+        uint64_t set_bytes = 0;
+        for (auto& r : sets[k])
+            set_bytes += static_cast<uint64_t>(lw.progs[r.prog].n_in + b.stores(r.prog)) * (r.hi - r.lo) * es;
+        const int flat_max = AR_FEW_LONG && set_bytes >= AR_FEW_LONG_MIN_BYTES ? AR_MAX_RANKS : kFewMaxIn;
         for (auto& r : sets[k]) {
             const DevProg& d = lw.progs[r.prog];
             const bool size_ok = d.n_in >= 2 && d.n_in <= kFewMaxIn;
             const bool chain = d.kind == PK_CHAIN_R || d.kind == PK_CHAIN_L;
-            flat = flat && size_ok && (chain || d.kind == PK_ACC);
+            flat = flat && d.n_in >= 2 && d.n_in <= flat_max && (chain || d.kind == PK_ACC);
             tree = tree && size_ok && d.n_in <= kFewTreeMaxIn &&
                    (chain || (d.kind == PK_TREE && d.n_tmp <= stack && d.n_out >= 2));
             any_tree = any_tree || d.kind == PK_TREE;

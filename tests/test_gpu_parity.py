@@ -340,15 +340,50 @@ def test_unaligned_chains_of_4_byte_elements(P, algo, kw, dtype):
                                        (5, "ahc", {"group_sizes": [2, 3]}), (3, "ring", {}), (4, "ring", {})])
 def test_fp32acc_same_bits_in_every_kernel(P, algo, kw, dtype):
     """The fp32-accumulate order is the engine's own and the same in every
-    kernel: the rank-streaming kernel (bf16 on 24 KB tiles, fp32 on 32 KB)
-    and the few-input chain kernel (P = 3, 4) must give exactly the bits of
-    the element-wise kernel, which unaligned buffers take."""
+    kernel: the few-input kernel (P = 3 ... 8) and the rank-streaming kernel
+    (P = 64 at this size; bf16 on 24 KB tiles, fp32 on 32 KB) must give
+    exactly the bits of the element-wise kernel, which unaligned buffers
+    take.  test_fp32acc_grouped_on_the_few_input_kernel covers the grouped
+    variant."""
     n = 300_007
     bufs = ar_synth.rank_inputs(P, n, dtype, "normal", sigma=1e-2, seed=P + 3)
     fast = engine(bufs, dtype, "sum", algo, order="fp32acc", **kw)
     slow = engine(bufs, dtype, "sum", algo, offset=1, order="fp32acc", **kw)  # not 16-byte aligned
     for r in range(P):
         assert_bit_equal(slow[r], fast[r], dtype, f"{algo} P={P} rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+@pytest.mark.parametrize("order", ["fp32acc", "faithful"])
+def test_fp32acc_grouped_on_the_few_input_kernel(order, dtype):
+    """Chains and fp32 accumulations of 64 inputs in a set of at least 1.5
+    GiB run on the few-input kernel's grouped variant (8 inputs' loads in
+    flight at a time, folded in the program's order across the groups): bit
+    for bit the element-wise kernel, which the same plan takes for buffers
+    one element off the 16-byte grid (itself checked against the oracle in
+    the other tests), every element of every rank, guard bands intact."""
+    import torch
+    import collective_reduction_gb300 as ar
+    P, n = 64, ((3 << 21) + 64) * (2 if dtype == "bfloat16" else 1)  # 24 MiB per rank
+    plan = ar.Plan(P, n, dtype, "sum", "ring", order=order)
+    assert plan.info()["kernels"] & ar.KERNEL_FEW, plan.info()["kernels"]
+    tdt = torch.bfloat16 if dtype == "bfloat16" else torch.float32
+    itype = torch.int16 if dtype == "bfloat16" else torch.int32
+    fast, slow = RankBufs(P, n, dtype), RankBufs(P, n, dtype, offset=1)
+    gen = torch.Generator(device="cuda").manual_seed(64)
+    for r in range(P):
+        x = (torch.randn(n, device="cuda", generator=gen) * 1e-2).to(tdt)
+        fast.views[r].copy_(x)
+        slow.views[r].copy_(x)
+    plan.execute(fast.views)
+    plan.execute(slow.views)
+    torch.cuda.synchronize()
+    plan.check()
+    plan.close()
+    fast.check_guards("grouped")
+    slow.check_guards("element-wise")
+    for r in range(P):
+        assert torch.equal(fast.views[r].view(itype), slow.views[r].view(itype)), f"{order} {dtype} rank {r}"
 
 
 @pytest.mark.parametrize("form", FORMS)

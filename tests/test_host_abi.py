@@ -316,14 +316,15 @@ def test_lowering_tiles_every_range_and_windows_hold_their_items(lib):
 
 
 def test_wave_balance_closed_form(lib):
-    """Round robin over 152 CTAs: P = 64 x 2^23 fp32 ring has 64 chunks of
-    2^17 elements, 16 whole 32 KB tiles each, 1024 equal items: 112 CTAs take
-    7 and 40 take 6, so the largest share over the mean is 7 / (1024 / 152).
+    """Round robin over 152 CTAs: P = 64 x 2^23 fp32 RH (single trees of 64
+    leaves, rank-streaming kernel) has 64 chunks of 2^17 elements, 16 whole
+    32 KB tiles each, 1024 equal items: 112 CTAs take 7 and 40 take 6, so the
+    largest share over the mean is 7 / (1024 / 152).
     P = 16 x 2^25 RH (single trees of 16 leaves) has 4096 items: 27 / (4096 /
     152).  P = 8 x 2^26 runs on the few-input kernel, a CTA per 16 KB item
     (16384), for the ring's chains and RH's trees alike.  Windows: 2 GiB of
     rank data makes 16 windows of 128 MB."""
-    low = ar.Schedule(64, 1 << 23, "float32", "sum", "ring").lowering()
+    low = ar.Schedule(64, 1 << 23, "float32", "sum", "rh").lowering()
     assert low["items"] == 1024 and low["windows"] == 16
     assert abs(low["wave_balance"] - 7 / (1024 / 152)) < 1e-9
     low = ar.Schedule(16, 1 << 25, "float32", "sum", "rh").lowering()
@@ -335,28 +336,34 @@ def test_wave_balance_closed_form(lib):
 
 
 def test_stream_geometry_follows_the_programs(lib):
-    """Pipeline depth and rank tile as the lowering picks them: 3 stages of
-    32 KB for chains over 4-byte elements, 5 for their fp32 accumulation, 4
-    for bf16 chains, trees of more than 8 leaves with their stack in tensor
-    memory on 4 stages of 32 KB, and 7 stages of 24 KB for bf16 fp32
-    accumulation.  (Chains and accumulations of up to 16 inputs, and trees of
-    up to 8 leaves, run on the few-input kernel instead.)"""
-    def geo(P, dtype, algo, op="sum", **kw):
-        low = ar.Schedule(P, P * (1 << 16), dtype, op, algo, **kw).lowering()
-        return low["stream_tile_bytes"], low["stream_stages"]
-    assert geo(32, "float32", "ring") == (32768, 3)
-    assert geo(32, "int32", "ring") == (32768, 3)
-    assert geo(32, "bfloat16", "ring") == (32768, 4)
-    assert geo(32, "bfloat16", "ring", op="max") == (32768, 4)
+    """Pipeline depth and rank tile of the rank-streaming kernel as the
+    lowering picks them: 3 stages of 32 KB for chains over 4-byte elements
+    (the step form's rounds), 4 for bf16 chains, trees of more than 8 leaves
+    with their stack in tensor memory on 4 stages of 32 KB, bf16 fp32
+    accumulation on 7 of 24 KB.  Fused chains and fp32 accumulations of up to
+    16 inputs, of more in sets of at least 1.5 GiB, and trees of up to 8
+    leaves run on the few-input kernel instead."""
+    def low(P, dtype, algo, op="sum", **kw):
+        return ar.Schedule(P, P * (1 << 16), dtype, op, algo, **kw).lowering()
+    geo = lambda *x, **kw: (low(*x, **kw)["stream_tile_bytes"], low(*x, **kw)["stream_stages"])
+    assert geo(32, "float32", "ring", form="step") == (32768, 3)
+    assert geo(32, "int32", "ring", form="step") == (32768, 3)
+    assert geo(32, "bfloat16", "ring", form="step") == (32768, 4)
     assert geo(16, "float32", "rh") == (32768, 4)       # 4 stack entries in tensor memory
     assert geo(64, "float32", "rh") == (32768, 4)       # 6 stack entries in tensor memory
     assert geo(32, "bfloat16", "binomial") == (32768, 4)
-    tm = lambda P, algo: ar.Schedule(P, P * (1 << 16), "float32", "sum", algo).lowering()["stream_tmem"]
+    tm = lambda P, algo: low(P, "float32", algo)["stream_tmem"]
     assert tm(64, "rh") == 1 and tm(32, "binomial") == 1 and tm(16, "rh") == 1
     assert tm(8, "rh") == 0 and tm(8, "ring") == 0
-    assert geo(32, "bfloat16", "ring", order="fp32acc") == (24576, 7)
+    for P, dtype in ((8, "bfloat16"), (16, "float32"), (2, "bfloat16")):
+        assert low(P, dtype, "ring", order="fp32acc")["few_sets"] == 1
+    # 64 inputs below 1.5 GiB of traffic (8 MiB of bf16 per rank): the
+    # rank-streaming kernel, fp32 accumulation on 7 stages of 24 KB, chains
+    # on 4 of 32 KB
     assert geo(64, "bfloat16", "ring", order="fp32acc") == (24576, 7)
-    assert geo(32, "float32", "ring", order="fp32acc") == (32768, 5)
+    assert geo(64, "bfloat16", "ring") == (32768, 4)
+    big = ar.Schedule(64, 1 << 24, "float32", "sum", "ring").lowering()
+    assert big["few_sets"] == 1 and big["tiling_ok"] == 1
 
 
 @pytest.mark.parametrize("P,algo,kw", [(31, "generalized", {"r": 5}), (64, "rd", {}), (13, "generalized", {"r": 2})])
@@ -431,17 +438,18 @@ def test_fused_all_gathers_lower_to_the_copy_kernel(lib, algo, kw):
 
 
 @pytest.mark.parametrize("P,algo,kw,few", [(2, "ring", {}, 1), (3, "ring", {}, 1), (8, "ring", {}, 1), (16, "ring", {}, 1),
-                                           (17, "ring", {}, 0), (2, "rd", {}, 1), (8, "pipeline", {"blocks": 4}, 1),
+                                           (17, "ring", {}, 1), (64, "ring", {}, 1), (2, "rd", {}, 1),
+                                           (8, "pipeline", {"blocks": 4}, 1),
                                            (2, "ring", {"form": "step"}, 0), (4, "ring", {"order": "fp32acc"}, 1),
-                                           (16, "ring", {"order": "fp32acc"}, 1), (17, "ring", {"order": "fp32acc"}, 0),
+                                           (16, "ring", {"order": "fp32acc"}, 1), (64, "ring", {"order": "fp32acc"}, 1),
                                            (4, "binomial", {}, 1), (8, "rh", {}, 1), (16, "rh", {}, 0),
                                            (8, "rh", {"form": "step"}, 0)])
 def test_short_fused_chains_lower_to_the_few_input_kernel(lib, P, algo, kw, few):
-    """Fused passes whose programs are all chains or fp32 accumulations of 2
-    to 16 inputs, or single trees (with chains) of up to 8, and too large
-    for the chain word kernel, take the few-input kernel; longer ones,
-    larger trees and the step form's rounds keep theirs.  The items tile
-    every range."""
+    """Fused passes whose programs are all chains or fp32 accumulations (of
+    up to 16 inputs at once, more in groups), or single trees (with chains)
+    of up to 8, and too large for the chain word kernel, take the few-input
+    kernel; larger trees and the step form's rounds keep theirs.  The items
+    tile every range."""
     low = ar.Schedule(P, (1 << 24) + 3, "float32", "sum", algo, **kw).lowering()
     assert low["few_sets"] == few and low["tiling_ok"] == 1
 
