@@ -733,28 +733,30 @@ __global__ void __launch_bounds__(kCopyThreads) copy_kernel(const __grid_constan
     }
 }
 
-// ------------------------------------------------------- few-input chains
+// ------------------------------------------------------- few-input kernel
 //
 // Fused passes of chains or fp32 accumulations of at most kFewMaxIn inputs
 // (the ring's fused pass at P <= 16) on the copy kernel's grid shape: a CTA
 // per 16 KB item, each thread loading its U 16-byte vectors of every input
 // before it folds them in the program's order (a chain: a2's element op; an
 // accumulation: the fp32 order of the other kernels; avg divided where the
-// program says) and stores the result to every output.  Three
-// instantiations, every load of a thread in flight at once: up to 4 inputs
-// with two vectors per thread (64 registers, four CTAs per SM), up to 8 with
-// two (102 registers, two CTAs per SM), up to 16 with one (110 registers).
-// (The 8-input one at P = 2 held too few loads in flight per SM: 77% of the
-// copy peak against 100.5%.)
+// program says) and stores the result to every output.  Instantiations,
+// every load of a thread in flight at once: up to 4 inputs with two vectors
+// per thread (64 registers, four CTAs per SM), up to 8 with two (102
+// registers, two CTAs per SM), up to 16 with one (110 registers).  (The
+// 8-input one at P = 2 held too few loads in flight per SM: 77% of the copy
+// peak against 100.5%.)
+//
+// The TREES instantiations (up to 4 leaves with two vectors per thread, 90
+// registers; up to kFewTreeMaxIn with one, 80) run single trees too, with
+// chains: the program's leaves in post-order with the combines that follow
+// each (4 bits a leaf, as the rank-streaming kernel reads them), the top of
+// the stack in registers and at most few_tree_stack(M) deeper entries in
+// registers indexed by unrolled selects (the stack pointer is the same in
+// every thread).
 #ifndef AR_FEW_TREE_UNROLL
 #define AR_FEW_TREE_UNROLL 1
 #endif
-
-// The TREES instantiations run single trees too (with chains): the program's
-// leaves in post-order with the combines that follow each (4 bits a leaf, as
-// the rank-streaming kernel reads them), the top of the stack in registers
-// and at most kFewTreeStack deeper entries in registers indexed by unrolled
-// selects (the stack pointer is the same in every thread).
 template <int DT, int OP, int M, int U, bool TREES>
 __global__ void __launch_bounds__(kCopyThreads) few_kernel(const __grid_constant__ KernelArgs a) {
     constexpr int ES = DT == AR_BFLOAT16 ? 2 : 4;

@@ -181,8 +181,9 @@ typedef struct {
  * CHAIN_WORD for the chain word kernel (chains of small and mid-sized
  * passes, the same way), COPY for the copy kernel (fused passes whose
  * programs copy one input to their outputs: the all-gathers), and FEW for the
- * few-input chain kernel (fused passes of chains of 2 to 4 inputs: the ring's
- * at P <= 4). */
+ * few-input kernel (a CTA per 16 KB item: fused passes of chains and fp32
+ * accumulations of 2 to 16 inputs, of more in passes of at least 1.5 GiB,
+ * and of single trees of up to 8 leaves that write every rank). */
 enum { AR_KERNEL_STREAM = 1, AR_KERNEL_STAGED = 2, AR_KERNEL_ELEMENTWISE = 4, AR_KERNEL_DAG_JIT = 8,
        AR_KERNEL_WORD_JIT = 16, AR_KERNEL_CHAIN_WORD = 32, AR_KERNEL_COPY = 64, AR_KERNEL_FEW = 128 };
 
@@ -300,7 +301,7 @@ typedef struct {
     uint64_t word_kernel_words; /* instruction words of their programs           */
     int stream_tmem;         /* 1: the tree stack lives in tensor memory        */
     int copy_sets;           /* launch sets on the copy kernel                  */
-    int few_sets;            /* launch sets on the few-input chain kernel       */
+    int few_sets;            /* launch sets on the few-input kernel             */
 } ar_lowering_info;
 ar_status ar_schedule_lowering(ar_schedule_t s, ar_lowering_info* out);
 
