@@ -79,3 +79,20 @@ def test_phase_option_reaches_the_oracle_and_the_workload_name():
         sys.argv = argv
     assert a.phase == "allreduce" and bench.oracle_kw(a) == {}
     assert "phase" not in bench.workload_name(a)
+
+
+def test_bulk_kernel_name_follows_the_plan_kernel_bits():
+    """The bench line names the kernel that runs a plan's aligned bulk items
+    from ar_plan_info.kernels: the launch-set kernels before the staged ones,
+    the element-wise kernel only when nothing else runs."""
+    import bench
+    import collective_reduction_gb300 as ar
+    assert bench.bulk_kernel_name(ar.KERNEL_FEW) == "few_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_FEW | ar.KERNEL_ELEMENTWISE) == "few_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_STREAM) == "stream_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_COPY) == "copy_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_WORD_JIT | ar.KERNEL_ELEMENTWISE) == "ar_word_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_STAGED | ar.KERNEL_DAG_JIT) == "ar_dag_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_STAGED) == "staged_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_CHAIN_WORD) == "chain_word_kernel"
+    assert bench.bulk_kernel_name(ar.KERNEL_ELEMENTWISE) == "elementwise_kernel"
